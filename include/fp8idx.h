@@ -1,0 +1,222 @@
+/*
+ * fp8idx -- FP8 "lightning indexer" logits on NVIDIA GB300 (sm_103a).
+ *
+ * The operation (aiter PR 5047 "[HIP] [JIT] fp8_paged_mqa_logits:
+ * hand-written gfx950 decode indexer kernel", section Motivation; aiter PR
+ * 5046 "[HIP] [JIT] fp8_mqa_logits: hand-written gfx950 prefill indexer
+ * kernel", section Motivation):
+ *
+ *     logits[m, n] = sum_h relu(<Q[m,h,:], K[n,:]>) * kv_scale[n] * weights[m,h]
+ *
+ * Q and K are e4m3 (OCP FP8, "e4m3fn": bias 7, no infinities, S.1111.111 =
+ * NaN); kv_scale, weights and logits are IEEE f32.  Products are formed on
+ * the tensor cores with f32 accumulation; the ReLU, weight, head sum and scale
+ * run in f32 on the CUDA cores.
+ *
+ * Conventions for every entry point:
+ *  - All tensor data pointers are DEVICE pointers on the current device,
+ *    owned by the caller; the library keeps no reference after the call
+ *    returns and allocates no memory.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Work is enqueued asynchronously; no call synchronises the
+ *    host, so the compute calls can be captured in a CUDA graph.
+ *  - Shapes, dtypes, strides and alignment are checked on the host before
+ *    anything is launched.  A non-OK status launches nothing (except
+ *    FP8IDX_ERR_CUDA, returned when the launch itself failed); the message
+ *    for the last non-OK status on the calling thread is available from
+ *    fp8idx_last_error().
+ *  - Values are not checked (they live on the device).  Preconditions:
+ *    kv_scale >= 0 (the hoist of the scale out of the ReLU relies on it);
+ *    no NaN in owned Q/K/scales/weights; block ids in range.  Indices read
+ *    from the device are clamped so that bad values cannot fault, but the
+ *    results for inputs that break a precondition are unspecified.
+ *  - Every in-kernel pipeline wait is bounded (about 2 s).  A wait that runs
+ *    out abandons the call's remaining work, records the failure on the
+ *    device, and the kernel exits normally; fp8idx_device_status() reports
+ *    it.
+ */
+#ifndef FP8IDX_H_
+#define FP8IDX_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FP8IDX_OK = 0,
+  FP8IDX_ERR_INVALID = 1,     /* null pointer, bad shape/dtype/stride/alignment */
+  FP8IDX_ERR_UNSUPPORTED = 2, /* legal input this build does not implement    */
+  FP8IDX_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed          */
+  FP8IDX_ERR_TIMEOUT = 4      /* a device pipeline wait ran out (watchdog)     */
+} fp8idx_status;
+
+typedef enum {
+  FP8IDX_U8 = 0,  /* e4m3 codes or raw bytes */
+  FP8IDX_F32 = 1,
+  FP8IDX_I32 = 2
+} fp8idx_dtype;
+
+/* A strided view of caller-owned device memory.  Strides are in elements.
+ * Only dimensions 0..ndim-1 are read. */
+typedef struct {
+  void* data;
+  int32_t dtype; /* fp8idx_dtype */
+  int32_t ndim;  /* 1..4 */
+  int64_t shape[4];
+  int64_t stride[4];
+} fp8idx_tensor;
+
+/* Tunables; 0 (or -1 for reverse_rows) means "let the host planner decide",
+ * after the pages' "zero means use the host heuristic" (aiter PR 5047,
+ * Technical Details; aiter PR 5046, Technical Details). */
+typedef struct {
+  int32_t num_ctas;     /* decode: persistent CTAs (<= SMs)                  */
+  int32_t stages;       /* K-tile pipeline depth in shared memory             */
+  int32_t split_n;      /* prefill: column-tile splits per row block          */
+  int32_t reverse_rows; /* prefill: -1 planner, 0 natural, 1 longest-first    */
+  int32_t block_m;      /* prefill: query rows per CTA (block_m*heads <= 256) */
+} fp8idx_options;
+
+/* The launch the planner chose (filled by the fp8idx_plan_* queries). */
+typedef struct {
+  int32_t grid;        /* CTAs launched                                  */
+  int32_t threads;     /* threads per CTA                                */
+  int32_t smem_bytes;  /* dynamic shared memory per CTA                  */
+  int32_t stages;      /* K-tile pipeline depth                          */
+  int32_t tile_n;      /* MMA N: next_n*heads (decode), block_m*heads    */
+  int32_t block_m;     /* prefill query rows per CTA; decode: next_n     */
+  int32_t split_n;     /* prefill column splits; decode: 1               */
+  int32_t reverse_rows;/* prefill dispatch order; decode: 0              */
+  int32_t tmem_cols;   /* tensor-memory columns allocated per CTA        */
+  int32_t gather;      /* decode: 1 = per-token gather (block size 1)    */
+} fp8idx_plan;
+
+/*
+ * Decode: fp8_paged_mqa_logits.
+ * Defined by aiter PR 5047, sections Motivation and Technical Details: K and
+ * its per-token f32 dequant scale are read from a paged cache through a block
+ * table; row r = b*next_n + n of the output receives, at column p, the logit
+ * of query row (b, n) against token p of request b, for
+ *     0 <= p <= context_lens[b] - next_n + n   (and p < max_model_len);
+ * positions outside that causal window are NOT written -- pre-filling them
+ * (with -inf) is the caller's job (same PR, section "GLM-5.2-MXFP4 E2E":
+ * the caller pre-fills -inf; aiter issue 5477, section "The ask": the causal
+ * bound context_length - next_n + pid_next_n, one output row per token).
+ *
+ *  q_fp8        [batch, next_n, heads, head_dim] U8 (e4m3), contiguous,
+ *               16-byte aligned.
+ *  kv_cache     [num_blocks, block_size*(head_dim+4)] U8, contiguous,
+ *               16-byte aligned.  Block i holds block_size K rows of head_dim
+ *               e4m3 bytes followed by block_size f32 scales (little endian).
+ *               block_size is shape[1]/(head_dim+4).  block_size 1 is the
+ *               plain co-packed cache (128 K bytes then a 4-byte scale per
+ *               token).
+ *  weights      [batch*next_n, heads] F32, contiguous, 16-byte aligned.
+ *  context_lens [batch] I32 (device).  Must satisfy context_lens[b] <=
+ *               min(max_model_len, max_blocks*block_size).
+ *  block_tables [batch, max_blocks] I32, contiguous rows (stride[0] >=
+ *               max_blocks, stride[1] == 1); entry j of row b is the physical
+ *               block holding tokens [j*block_size, (j+1)*block_size).
+ *  max_model_len  output width.
+ *  out          [batch*next_n, >= max_model_len] F32, stride[1] == 1,
+ *               stride[0] >= max_model_len.
+ * Supported (fp8idx_paged_is_supported): head_dim 128; heads 32 or 64;
+ * next_n*heads in {32, 64, ..., 256} (a multiple of 32); block_size in
+ * {1, 16, 32, 64, 128}; batch <= 4096.
+ * Returns FP8IDX_OK, FP8IDX_ERR_INVALID, FP8IDX_ERR_UNSUPPORTED or
+ * FP8IDX_ERR_CUDA.
+ */
+fp8idx_status fp8_paged_mqa_logits(const fp8idx_tensor* q_fp8,
+                                   const fp8idx_tensor* kv_cache,
+                                   const fp8idx_tensor* weights,
+                                   const fp8idx_tensor* context_lens,
+                                   const fp8idx_tensor* block_tables,
+                                   int32_t max_model_len,
+                                   const fp8idx_tensor* out, void* stream);
+
+/* As fp8_paged_mqa_logits, with tunables (NULL = all heuristic). */
+fp8idx_status fp8_paged_mqa_logits_ex(const fp8idx_tensor* q_fp8,
+                                      const fp8idx_tensor* kv_cache,
+                                      const fp8idx_tensor* weights,
+                                      const fp8idx_tensor* context_lens,
+                                      const fp8idx_tensor* block_tables,
+                                      int32_t max_model_len,
+                                      const fp8idx_tensor* out,
+                                      const fp8idx_options* opts, void* stream);
+
+/*
+ * Prefill: fp8_mqa_logits.
+ * Defined by aiter PR 5046, section Motivation: K is a contiguous [N, 128]
+ * e4m3 buffer with a separate [N] f32 scale; row m is defined for n in
+ * [cu_seqlen_ks[m], cu_seqlen_ke[m]) and is -inf elsewhere.  Every element of
+ * out is written (the "clean_logits" semantics, same PR, Technical Details:
+ * the -inf fill is fused into the kernel).  Windows are clamped to [0, N);
+ * ke <= ks, or ke <= 0, gives an all -inf row (same PR, Test Plan: empty and
+ * past_end windows are legal input).
+ *
+ *  q_fp8        [M, heads, head_dim] U8 (e4m3), contiguous, 16-byte aligned.
+ *  k_fp8        [N, head_dim] U8 (e4m3), contiguous, 16-byte aligned.
+ *  kv_scale     [N] F32, contiguous, 16-byte aligned, values >= 0.
+ *  weights      [M, heads] F32, contiguous.
+ *  cu_seqlen_ks, cu_seqlen_ke  [M] I32, contiguous.
+ *  out          [M, >= N] F32, stride[1] == 1, stride[0] >= N.
+ * Supported (fp8idx_prefill_is_supported): head_dim 128; heads 32 or 64;
+ * M, N >= 0 with M*heads and N below 2^31.
+ */
+fp8idx_status fp8_mqa_logits(const fp8idx_tensor* q_fp8,
+                             const fp8idx_tensor* k_fp8,
+                             const fp8idx_tensor* kv_scale,
+                             const fp8idx_tensor* weights,
+                             const fp8idx_tensor* cu_seqlen_ks,
+                             const fp8idx_tensor* cu_seqlen_ke,
+                             const fp8idx_tensor* out, void* stream);
+
+fp8idx_status fp8_mqa_logits_ex(const fp8idx_tensor* q_fp8,
+                                const fp8idx_tensor* k_fp8,
+                                const fp8idx_tensor* kv_scale,
+                                const fp8idx_tensor* weights,
+                                const fp8idx_tensor* cu_seqlen_ks,
+                                const fp8idx_tensor* cu_seqlen_ke,
+                                const fp8idx_tensor* out,
+                                const fp8idx_options* opts, void* stream);
+
+/* Support gates, after the pages' is_supported(num_heads, head_dim,
+ * kv_block_size) (aiter PR 5047, Technical Details) and is_supported(
+ * num_heads, head_dim) (aiter PR 5046, Technical Details): 1 if the shape is
+ * implemented, else 0.  Pure host functions; no device needed. */
+int fp8idx_paged_is_supported(int32_t heads, int32_t head_dim,
+                              int32_t block_size, int32_t next_n);
+int fp8idx_prefill_is_supported(int32_t heads, int32_t head_dim);
+
+/* The launch the planner would choose for a shape, for `num_sms` SMs (pass 0
+ * to query the current device).  After the pages' host heuristics that pick
+ * the split and tile from the problem size (aiter PR 5047, Technical
+ * Details: from batch * max_model_len; aiter PR 5046, Technical Details:
+ * BlockM, SplitN, reverse_rows).  Pure host functions when num_sms > 0. */
+fp8idx_status fp8idx_plan_paged(int32_t batch, int32_t next_n, int32_t heads,
+                                int32_t head_dim, int32_t block_size,
+                                int32_t max_model_len, int32_t num_sms,
+                                const fp8idx_options* opts, fp8idx_plan* plan);
+fp8idx_status fp8idx_plan_prefill(int64_t rows, int64_t cols, int32_t heads,
+                                  int32_t head_dim, int32_t num_sms,
+                                  const fp8idx_options* opts, fp8idx_plan* plan);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char* fp8idx_last_error(void);
+
+/* Reads and optionally clears the device watchdog word of the current
+ * device.  FP8IDX_OK if no in-kernel wait has run out since the last clear,
+ * FP8IDX_ERR_TIMEOUT if one has.  This call synchronises with the device
+ * (it copies the word back), so it does not belong inside a captured graph. */
+fp8idx_status fp8idx_device_status(int32_t clear);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int32_t fp8idx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8IDX_H_ */

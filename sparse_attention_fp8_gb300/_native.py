@@ -1,0 +1,226 @@
+"""ctypes binding of libfp8idx (argument marshalling only)."""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+import re
+import threading
+
+from . import _build
+
+FP8IDX_OK = 0
+FP8IDX_ERR_INVALID = 1
+FP8IDX_ERR_UNSUPPORTED = 2
+FP8IDX_ERR_CUDA = 3
+FP8IDX_ERR_TIMEOUT = 4
+_STATUS_NAMES = {0: "OK", 1: "INVALID", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT"}
+
+_U8, _F32, _I32 = 0, 1, 2
+
+
+class Fp8IdxError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"fp8idx {_STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class _Tensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class _Options(ctypes.Structure):
+    _fields_ = [("num_ctas", ctypes.c_int32), ("stages", ctypes.c_int32), ("split_n", ctypes.c_int32),
+                ("reverse_rows", ctypes.c_int32), ("block_m", ctypes.c_int32)]
+
+
+class _Plan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("grid", "threads", "smem_bytes", "stages", "tile_n", "block_m",
+                                               "split_n", "reverse_rows", "tmem_cols", "gather")]
+
+
+@dataclasses.dataclass
+class Options:
+    """Tunables; 0 (or -1 for reverse_rows) = host heuristic."""
+    num_ctas: int = 0
+    stages: int = 0
+    split_n: int = 0
+    reverse_rows: int = -1
+    block_m: int = 0
+
+    def _c(self):
+        return _Options(self.num_ctas, self.stages, self.split_n, self.reverse_rows, self.block_m)
+
+
+@dataclasses.dataclass
+class Plan:
+    grid: int
+    threads: int
+    smem_bytes: int
+    stages: int
+    tile_n: int
+    block_m: int
+    split_n: int
+    reverse_rows: int
+    tmem_cols: int
+    gather: int
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def library():
+    """The loaded libfp8idx; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise ImportError(f"libfp8idx.so not built ({path}); run __graft_entry__.build() "
+                                  "or python sparse_attention_fp8_gb300/_build.py")
+            lib = ctypes.CDLL(path)
+            P = ctypes.POINTER
+            T = P(_Tensor)
+            V = ctypes.c_void_p
+            lib.fp8_paged_mqa_logits.argtypes = [T, T, T, T, T, ctypes.c_int32, T, V]
+            lib.fp8_paged_mqa_logits_ex.argtypes = [T, T, T, T, T, ctypes.c_int32, T, P(_Options), V]
+            lib.fp8_mqa_logits.argtypes = [T, T, T, T, T, T, T, V]
+            lib.fp8_mqa_logits_ex.argtypes = [T, T, T, T, T, T, T, P(_Options), V]
+            for f in ("fp8_paged_mqa_logits", "fp8_paged_mqa_logits_ex", "fp8_mqa_logits", "fp8_mqa_logits_ex"):
+                getattr(lib, f).restype = ctypes.c_int
+            lib.fp8idx_paged_is_supported.argtypes = [ctypes.c_int32] * 4
+            lib.fp8idx_paged_is_supported.restype = ctypes.c_int
+            lib.fp8idx_prefill_is_supported.argtypes = [ctypes.c_int32] * 2
+            lib.fp8idx_prefill_is_supported.restype = ctypes.c_int
+            lib.fp8idx_plan_paged.argtypes = [ctypes.c_int32] * 7 + [P(_Options), P(_Plan)]
+            lib.fp8idx_plan_paged.restype = ctypes.c_int
+            lib.fp8idx_plan_prefill.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                                ctypes.c_int32, P(_Options), P(_Plan)]
+            lib.fp8idx_plan_prefill.restype = ctypes.c_int
+            lib.fp8idx_last_error.restype = ctypes.c_char_p
+            lib.fp8idx_device_status.argtypes = [ctypes.c_int32]
+            lib.fp8idx_device_status.restype = ctypes.c_int
+            lib.fp8idx_version.restype = ctypes.c_int32
+            _lib = lib
+    return _lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions declared in include/fp8idx.h."""
+    path = os.path.join(_build.ROOT, "include", "fp8idx.h")
+    with open(path) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return re.findall(r"^[A-Za-z_][\w \*]*?\b(\w+)\s*\(", src, flags=re.M)
+
+
+def _check(status: int):
+    if status != FP8IDX_OK:
+        msg = library().fp8idx_last_error()
+        raise Fp8IdxError(status, msg.decode() if msg else "")
+
+
+def _desc(t) -> _Tensor:
+    """torch tensor -> descriptor (no copy; the tensor must outlive the call)."""
+    import torch
+    dt = {torch.uint8: _U8, torch.float8_e4m3fn: _U8, torch.float32: _F32, torch.int32: _I32}.get(t.dtype)
+    if dt is None:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    if t.dim() > 4:
+        raise ValueError("at most 4 dimensions")
+    d = _Tensor()
+    d.data = t.data_ptr()
+    d.dtype = dt
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _stream(stream, like):
+    import torch
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream(like.device).cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def fp8_paged_mqa_logits(q_fp8, kv_cache, weights, context_lens, block_tables, max_model_len, out,
+                         stream=None, options: Options | None = None):
+    """Decode logits into ``out`` (only the causal windows are written)."""
+    lib = library()
+    args = [_desc(q_fp8), _desc(kv_cache), _desc(weights), _desc(context_lens), _desc(block_tables)]
+    o = _desc(out)
+    s = _stream(stream, q_fp8)
+    refs = [ctypes.byref(a) for a in args]
+    if options is None:
+        st = lib.fp8_paged_mqa_logits(*refs, int(max_model_len), ctypes.byref(o), s)
+    else:
+        oc = options._c()
+        st = lib.fp8_paged_mqa_logits_ex(*refs, int(max_model_len), ctypes.byref(o), ctypes.byref(oc), s)
+    _check(st)
+    return out
+
+
+def fp8_mqa_logits(q_fp8, k_fp8, kv_scale, weights, cu_seqlen_ks, cu_seqlen_ke, out, stream=None,
+                   options: Options | None = None):
+    """Prefill logits into ``out`` (every element written, -inf outside windows)."""
+    lib = library()
+    args = [_desc(q_fp8), _desc(k_fp8), _desc(kv_scale), _desc(weights), _desc(cu_seqlen_ks),
+            _desc(cu_seqlen_ke)]
+    o = _desc(out)
+    s = _stream(stream, q_fp8)
+    refs = [ctypes.byref(a) for a in args]
+    if options is None:
+        st = lib.fp8_mqa_logits(*refs, ctypes.byref(o), s)
+    else:
+        oc = options._c()
+        st = lib.fp8_mqa_logits_ex(*refs, ctypes.byref(o), ctypes.byref(oc), s)
+    _check(st)
+    return out
+
+
+def paged_is_supported(heads, head_dim, block_size, next_n) -> bool:
+    return bool(library().fp8idx_paged_is_supported(heads, head_dim, block_size, next_n))
+
+
+def prefill_is_supported(heads, head_dim) -> bool:
+    return bool(library().fp8idx_prefill_is_supported(heads, head_dim))
+
+
+def _plan(pc: _Plan) -> Plan:
+    return Plan(**{n: getattr(pc, n) for n, _ in _Plan._fields_})
+
+
+def plan_paged(batch, next_n, heads, head_dim, block_size, max_model_len, num_sms=0,
+               options: Options | None = None) -> Plan:
+    pc = _Plan()
+    oc = options._c() if options else None
+    _check(library().fp8idx_plan_paged(batch, next_n, heads, head_dim, block_size, max_model_len, num_sms,
+                                       ctypes.byref(oc) if oc else None, ctypes.byref(pc)))
+    return _plan(pc)
+
+
+def plan_prefill(rows, cols, heads, head_dim, num_sms=0, options: Options | None = None) -> Plan:
+    pc = _Plan()
+    oc = options._c() if options else None
+    _check(library().fp8idx_plan_prefill(rows, cols, heads, head_dim, num_sms,
+                                         ctypes.byref(oc) if oc else None, ctypes.byref(pc)))
+    return _plan(pc)
+
+
+def device_status(clear: bool = True) -> int:
+    """FP8IDX_OK, or FP8IDX_ERR_TIMEOUT if an in-kernel wait ran out (synchronises)."""
+    return int(library().fp8idx_device_status(1 if clear else 0))
+
+
+def version() -> int:
+    return int(library().fp8idx_version())

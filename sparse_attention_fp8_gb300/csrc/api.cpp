@@ -1,0 +1,455 @@
+// C-ABI entry points of libfp8idx: argument validation, the host planner,
+// TMA tensor-map encoding and kernel launch.  No allocation, no host
+// synchronisation on the compute paths (both are graph-capturable).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/fp8idx.h"
+#include "kernels.h"
+
+namespace {
+
+using namespace fp8idx;
+
+thread_local std::string g_last_error;
+
+fp8idx_status fail(fp8idx_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+fp8idx_status ok() { return FP8IDX_OK; }
+
+// ---------------------------------------------------------- device facts
+struct DeviceInfo {
+  int sms = 0;
+  int smem_optin = 0;
+  bool valid = false;
+};
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+fp8idx_status device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "cudaGetDevice failed");
+  if (dev < 0 || dev >= kMaxDevices) return fail(FP8IDX_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.valid) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return fail(FP8IDX_ERR_CUDA, "cudaDeviceGetAttribute failed");
+    if (major != 10 || minor != 3)
+      return fail(FP8IDX_ERR_UNSUPPORTED, "built for sm_103a; device is sm_%d%d", major, minor);
+    d.valid = true;
+  }
+  *out = d;
+  return FP8IDX_OK;
+}
+
+// ---------------------------------------------------- tensor-map encoding
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+fp8idx_status encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
+                     const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz, const char* what) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(FP8IDX_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t gd[5], gs[5];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i < rank - 1) gs[i] = strides_bytes[i];
+  }
+  CUresult r = fn(m, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), gd, gs, bx, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FP8IDX_ERR_CUDA, "tensor map for %s: cuTensorMapEncodeTiled error %d", what, (int)r);
+  return FP8IDX_OK;
+}
+
+// ------------------------------------------------------------ validation
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fp8idx_status check_tensor(const fp8idx_tensor* t, const char* name, int dtype, int ndim) {
+  if (!t) return fail(FP8IDX_ERR_INVALID, "%s: null descriptor", name);
+  if (t->ndim != ndim) return fail(FP8IDX_ERR_INVALID, "%s: ndim %d, expected %d", name, t->ndim, ndim);
+  if (t->dtype != dtype) return fail(FP8IDX_ERR_INVALID, "%s: wrong dtype %d", name, t->dtype);
+  int64_t numel = 1;
+  for (int i = 0; i < ndim; ++i) {
+    if (t->shape[i] < 0) return fail(FP8IDX_ERR_INVALID, "%s: negative extent", name);
+    numel *= t->shape[i];
+  }
+  if (numel > 0 && !t->data) return fail(FP8IDX_ERR_INVALID, "%s: null data pointer", name);
+  return FP8IDX_OK;
+}
+
+bool contiguous(const fp8idx_tensor* t) {
+  int64_t expect = 1;
+  for (int i = t->ndim - 1; i >= 0; --i) {
+    if (t->shape[i] != 1 && t->stride[i] != expect) return false;
+    expect *= t->shape[i];
+  }
+  return true;
+}
+
+#define TRY(expr)                          \
+  do {                                     \
+    fp8idx_status _st = (expr);            \
+    if (_st != FP8IDX_OK) return _st;      \
+  } while (0)
+
+// ---------------------------------------------------------------- planner
+
+bool paged_supported(int heads, int head_dim, int block_size, int next_n) {
+  if (head_dim != kHeadDim) return false;
+  if (heads != 32 && heads != 64) return false;
+  if (next_n < 1 || next_n * heads > 256) return false;
+  return block_size == 1 || block_size == 16 || block_size == 32 || block_size == 64 || block_size == 128;
+}
+
+bool prefill_supported(int heads, int head_dim) { return head_dim == kHeadDim && (heads == 32 || heads == 64); }
+
+fp8idx_status plan_paged(int32_t batch, int32_t next_n, int32_t heads, int32_t head_dim, int32_t block_size,
+                         int32_t max_model_len, int32_t num_sms, int32_t smem_limit, const fp8idx_options* o,
+                         fp8idx_plan* plan) {
+  if (!paged_supported(heads, head_dim, block_size, next_n))
+    return fail(FP8IDX_ERR_UNSUPPORTED, "decode: heads=%d head_dim=%d block_size=%d next_n=%d not supported", heads,
+                head_dim, block_size, next_n);
+  if (batch < 0 || batch > kMaxBatch) return fail(FP8IDX_ERR_UNSUPPORTED, "decode: batch %d > %d", batch, kMaxBatch);
+  if (num_sms <= 0) return fail(FP8IDX_ERR_INVALID, "num_sms must be positive");
+  const bool gather = block_size == 1;
+  const int n_cols = next_n * heads;
+  int stages = (o && o->stages > 0) ? o->stages : 12;
+  const int min_stages = gather ? 6 : 2;
+  while (stages > min_stages && (int)paged_smem_layout(n_cols, stages, batch).total > smem_limit) --stages;
+  if (stages < min_stages || (int)paged_smem_layout(n_cols, stages, batch).total > smem_limit)
+    return fail(FP8IDX_ERR_UNSUPPORTED, "decode: shared memory too small for %d stages", stages);
+  // Upper bound on work items without reading context_lens: every request
+  // full to max_model_len.  The persistent grid never exceeds the SM count.
+  const int64_t tiles_per_req = (static_cast<int64_t>(std::max(max_model_len, 0)) + kTileTokens - 1) / kTileTokens;
+  const int64_t items_ub = static_cast<int64_t>(batch) * tiles_per_req;
+  int grid = static_cast<int>(std::min<int64_t>(num_sms, std::max<int64_t>(items_ub, 1)));
+  if (o && o->num_ctas > 0) grid = std::min(o->num_ctas, num_sms);
+  std::memset(plan, 0, sizeof(*plan));
+  plan->grid = grid;
+  plan->threads = paged_threads(gather);
+  plan->smem_bytes = (int)paged_smem_layout(n_cols, stages, batch).total;
+  plan->stages = stages;
+  plan->tile_n = n_cols;
+  plan->block_m = next_n;
+  plan->split_n = 1;
+  plan->reverse_rows = 0;
+  plan->tmem_cols = 512;
+  plan->gather = gather ? 1 : 0;
+  return FP8IDX_OK;
+}
+
+fp8idx_status plan_prefill(int64_t rows, int64_t cols, int32_t heads, int32_t head_dim, int32_t num_sms,
+                           int32_t smem_limit, const fp8idx_options* o, fp8idx_plan* plan) {
+  if (!prefill_supported(heads, head_dim))
+    return fail(FP8IDX_ERR_UNSUPPORTED, "prefill: heads=%d head_dim=%d not supported", heads, head_dim);
+  if (rows < 0 || cols < 0 || rows * heads >= (1ll << 31) || cols >= (1ll << 31))
+    return fail(FP8IDX_ERR_UNSUPPORTED, "prefill: M=%lld N=%lld out of range", (long long)rows, (long long)cols);
+  if (num_sms <= 0) return fail(FP8IDX_ERR_INVALID, "num_sms must be positive");
+  int block_m = (o && o->block_m > 0) ? o->block_m : 256 / heads;
+  if (block_m * heads > 256 || block_m > 32)
+    return fail(FP8IDX_ERR_UNSUPPORTED, "prefill: block_m %d too large for %d heads", block_m, heads);
+  const int n_cols = block_m * heads;
+  // Two CTAs per SM: keep each at or below half of the shared memory.
+  const int per_cta = std::min(smem_limit, 232448 / 2 - 1024);
+  int stages = (o && o->stages > 0) ? o->stages : 4;
+  while (stages > 2 && (int)prefill_smem_layout(n_cols, stages, block_m).total > per_cta) --stages;
+  if ((int)prefill_smem_layout(n_cols, stages, block_m).total > smem_limit)
+    return fail(FP8IDX_ERR_UNSUPPORTED, "prefill: shared memory too small");
+  const int64_t num_rb = (rows + block_m - 1) / block_m;
+  const int64_t n_tiles = (cols + kTileTokens - 1) / kTileTokens;
+  int64_t split = 1;
+  if (o && o->split_n > 0) {
+    split = o->split_n;
+  } else if (num_rb > 0) {
+    // aim for at least four waves of two CTAs per SM
+    split = (8ll * num_sms + num_rb - 1) / num_rb;
+  }
+  split = std::max<int64_t>(1, std::min<int64_t>(split, std::max<int64_t>(n_tiles, 1)));
+  int reverse = (cols > 2048) ? 1 : 0;  // longest-first pays off only for long rows
+  if (o && o->reverse_rows >= 0 && o->reverse_rows <= 1) reverse = o->reverse_rows;
+  if (num_rb * split > 0x7fffffffll) return fail(FP8IDX_ERR_UNSUPPORTED, "prefill: grid too large");
+  std::memset(plan, 0, sizeof(*plan));
+  plan->grid = static_cast<int32_t>(num_rb * split);
+  plan->threads = prefill_threads();
+  plan->smem_bytes = (int)prefill_smem_layout(n_cols, stages, block_m).total;
+  plan->stages = stages;
+  plan->tile_n = n_cols;
+  plan->block_m = block_m;
+  plan->split_n = static_cast<int32_t>(split);
+  plan->reverse_rows = reverse;
+  plan->tmem_cols = n_cols > 128 ? 256 : 128;
+  plan->gather = 0;
+  return FP8IDX_OK;
+}
+
+// ----------------------------------------------------------------- decode
+fp8idx_status paged_impl(const fp8idx_tensor* q, const fp8idx_tensor* kv, const fp8idx_tensor* w,
+                         const fp8idx_tensor* cl, const fp8idx_tensor* bt, int32_t max_model_len,
+                         const fp8idx_tensor* out, const fp8idx_options* opts, void* stream) {
+  g_last_error.clear();
+  TRY(check_tensor(q, "q_fp8", FP8IDX_U8, 4));
+  TRY(check_tensor(kv, "kv_cache", FP8IDX_U8, 2));
+  TRY(check_tensor(w, "weights", FP8IDX_F32, 2));
+  TRY(check_tensor(cl, "context_lens", FP8IDX_I32, 1));
+  TRY(check_tensor(bt, "block_tables", FP8IDX_I32, 2));
+  TRY(check_tensor(out, "out", FP8IDX_F32, 2));
+  const int64_t B = q->shape[0], next_n = q->shape[1], H = q->shape[2], D = q->shape[3];
+  if (max_model_len < 0) return fail(FP8IDX_ERR_INVALID, "max_model_len < 0");
+  if (!contiguous(q)) return fail(FP8IDX_ERR_INVALID, "q_fp8 must be contiguous");
+  if (!contiguous(kv)) return fail(FP8IDX_ERR_INVALID, "kv_cache must be contiguous");
+  if (!contiguous(w)) return fail(FP8IDX_ERR_INVALID, "weights must be contiguous");
+  if (cl->shape[0] != B || (B > 1 && cl->stride[0] != 1)) return fail(FP8IDX_ERR_INVALID, "context_lens must be [batch] contiguous");
+  if (w->shape[0] != B * next_n || w->shape[1] != H) return fail(FP8IDX_ERR_INVALID, "weights must be [batch*next_n, heads]");
+  if (bt->shape[0] != B || (bt->shape[1] > 1 && bt->stride[1] != 1) || (B > 1 && bt->stride[0] < bt->shape[1]))
+    return fail(FP8IDX_ERR_INVALID, "block_tables must be [batch, max_blocks] with unit inner stride");
+  if (out->shape[0] != B * next_n || out->shape[1] < max_model_len ||
+      (out->shape[1] > 1 && out->stride[1] != 1) || (out->shape[0] > 1 && out->stride[0] < out->shape[1]))
+    return fail(FP8IDX_ERR_INVALID, "out must be [batch*next_n, >=max_model_len] with unit inner stride");
+  if (D <= 0 || kv->shape[1] % (D + 4) != 0) return fail(FP8IDX_ERR_INVALID, "kv_cache row is not block_size*(head_dim+4) bytes");
+  const int64_t blk = kv->shape[1] / (D + 4);
+  if (next_n <= 0 || H <= 0 || blk <= 0) return fail(FP8IDX_ERR_INVALID, "empty next_n/heads/block_size");
+  if (!paged_supported((int)H, (int)D, (int)blk, (int)next_n))
+    return fail(FP8IDX_ERR_UNSUPPORTED, "decode: heads=%lld head_dim=%lld block_size=%lld next_n=%lld not supported",
+                (long long)H, (long long)D, (long long)blk, (long long)next_n);
+  if (B == 0 || max_model_len == 0) return ok();
+  if (kv->shape[0] < 1) return fail(FP8IDX_ERR_INVALID, "kv_cache has no blocks");
+  if (bt->shape[1] < 1) return fail(FP8IDX_ERR_INVALID, "block_tables has no columns");
+  if (!aligned16(q->data) || !aligned16(kv->data) || !aligned16(w->data))
+    return fail(FP8IDX_ERR_INVALID, "q_fp8, kv_cache and weights must be 16-byte aligned");
+  if (B * next_n * H >= (1ll << 31) || kv->shape[0] >= (1ll << 31) || bt->shape[1] >= (1ll << 31))
+    return fail(FP8IDX_ERR_UNSUPPORTED, "decode: extents too large");
+
+  DeviceInfo dev;
+  TRY(device_info(&dev));
+  fp8idx_plan plan;
+  TRY(plan_paged((int)B, (int)next_n, (int)H, (int)D, (int)blk, max_model_len, dev.sms, dev.smem_optin, opts, &plan));
+
+  const int n_cols = (int)(next_n * H);
+  CUtensorMap tm_q, tm_kv;
+  {
+    const uint64_t dims[2] = {(uint64_t)D, (uint64_t)(B * n_cols)};
+    const uint64_t strides[1] = {(uint64_t)D};
+    const uint32_t box[2] = {(uint32_t)D, (uint32_t)n_cols};
+    TRY(encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q->data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "q"));
+  }
+  if (!plan.gather) {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)blk, (uint64_t)kv->shape[0]};
+    const uint64_t strides[2] = {(uint64_t)D, (uint64_t)kv->shape[1]};
+    const uint32_t box[3] = {(uint32_t)D, (uint32_t)blk, 1u};
+    TRY(encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, kv->data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+               "kv_cache"));
+  } else {
+    tm_kv = tm_q;  // unused by the gather kernel
+  }
+  PagedParams p;
+  p.kv_cache = static_cast<const uint8_t*>(kv->data);
+  p.weights = static_cast<const float*>(w->data);
+  p.context_lens = static_cast<const int32_t*>(cl->data);
+  p.block_tables = static_cast<const int32_t*>(bt->data);
+  p.out = static_cast<float*>(out->data);
+  p.out_stride = out->shape[0] > 1 ? out->stride[0] : out->shape[1];
+  p.bt_stride = B > 1 ? bt->stride[0] : bt->shape[1];
+  p.num_blocks = kv->shape[0];
+  p.batch = (int32_t)B;
+  p.next_n = (int32_t)next_n;
+  p.max_blocks = (int32_t)bt->shape[1];
+  p.max_model_len = max_model_len;
+  p.block_size = (int32_t)blk;
+  p.n_cols = n_cols;
+  p.stages = plan.stages;
+  p.acc_cols = n_cols > 128 ? 256 : 128;
+  cudaError_t e = launch_paged(tm_q, tm_kv, p, (int)H, plan.gather != 0, plan.grid, plan.smem_bytes,
+                               static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+// ---------------------------------------------------------------- prefill
+fp8idx_status prefill_impl(const fp8idx_tensor* q, const fp8idx_tensor* k, const fp8idx_tensor* s,
+                           const fp8idx_tensor* w, const fp8idx_tensor* ks, const fp8idx_tensor* ke,
+                           const fp8idx_tensor* out, const fp8idx_options* opts, void* stream) {
+  g_last_error.clear();
+  TRY(check_tensor(q, "q_fp8", FP8IDX_U8, 3));
+  TRY(check_tensor(k, "k_fp8", FP8IDX_U8, 2));
+  TRY(check_tensor(s, "kv_scale", FP8IDX_F32, 1));
+  TRY(check_tensor(w, "weights", FP8IDX_F32, 2));
+  TRY(check_tensor(ks, "cu_seqlen_ks", FP8IDX_I32, 1));
+  TRY(check_tensor(ke, "cu_seqlen_ke", FP8IDX_I32, 1));
+  TRY(check_tensor(out, "out", FP8IDX_F32, 2));
+  const int64_t M = q->shape[0], H = q->shape[1], D = q->shape[2], N = k->shape[0];
+  if (!contiguous(q) || !contiguous(k) || !contiguous(s) || !contiguous(w) || !contiguous(ks) || !contiguous(ke))
+    return fail(FP8IDX_ERR_INVALID, "prefill inputs must be contiguous");
+  if (k->shape[1] != D || s->shape[0] != N) return fail(FP8IDX_ERR_INVALID, "k_fp8 must be [N, head_dim], kv_scale [N]");
+  if (w->shape[0] != M || w->shape[1] != H) return fail(FP8IDX_ERR_INVALID, "weights must be [M, heads]");
+  if (ks->shape[0] != M || ke->shape[0] != M) return fail(FP8IDX_ERR_INVALID, "cu_seqlen_ks/ke must be [M]");
+  if (out->shape[0] != M || out->shape[1] != N || (N > 1 && out->stride[1] != 1) || (M > 1 && out->stride[0] < N))
+    return fail(FP8IDX_ERR_INVALID, "out must be [M, N] with unit inner stride");
+  if (!prefill_supported((int)H, (int)D))
+    return fail(FP8IDX_ERR_UNSUPPORTED, "prefill: heads=%lld head_dim=%lld not supported", (long long)H, (long long)D);
+  if (M == 0 || N == 0) return ok();
+  if (!aligned16(q->data) || !aligned16(k->data) || !aligned16(s->data))
+    return fail(FP8IDX_ERR_INVALID, "q_fp8, k_fp8 and kv_scale must be 16-byte aligned");
+  DeviceInfo dev;
+  TRY(device_info(&dev));
+  fp8idx_plan plan;
+  TRY(plan_prefill(M, N, (int)H, (int)D, dev.sms, dev.smem_optin, opts, &plan));
+  CUtensorMap tm_q, tm_k, tm_s;
+  {
+    const uint64_t dims[2] = {(uint64_t)D, (uint64_t)(M * H)};
+    const uint64_t strides[1] = {(uint64_t)D};
+    const uint32_t box[2] = {(uint32_t)D, (uint32_t)plan.tile_n};
+    TRY(encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q->data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "q"));
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)D, (uint64_t)N};
+    const uint64_t strides[1] = {(uint64_t)D};
+    const uint32_t box[2] = {(uint32_t)D, (uint32_t)kTileTokens};
+    TRY(encode(&tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, k->data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "k"));
+  }
+  {
+    const uint64_t dims[1] = {(uint64_t)N};
+    const uint32_t box[1] = {(uint32_t)kTileTokens};
+    TRY(encode(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, s->data, dims, nullptr, box, CU_TENSOR_MAP_SWIZZLE_NONE,
+               "kv_scale"));
+  }
+  PrefillParams p;
+  p.weights = static_cast<const float*>(w->data);
+  p.ks = static_cast<const int32_t*>(ks->data);
+  p.ke = static_cast<const int32_t*>(ke->data);
+  p.out = static_cast<float*>(out->data);
+  p.out_stride = M > 1 ? out->stride[0] : N;
+  p.rows = (int32_t)M;
+  p.cols = (int32_t)N;
+  p.block_m = plan.block_m;
+  p.n_cols = plan.tile_n;
+  p.stages = plan.stages;
+  p.acc_cols = plan.tmem_cols;
+  p.split = plan.split_n;
+  p.reverse = plan.reverse_rows;
+  p.vec_ok = (aligned16(out->data) && (p.out_stride % 4) == 0) ? 1 : 0;
+  cudaError_t e = launch_prefill(tm_q, tm_k, tm_s, p, (int)H, plan.grid, plan.smem_bytes,
+                                 static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+fp8idx_status fp8_paged_mqa_logits(const fp8idx_tensor* q_fp8, const fp8idx_tensor* kv_cache,
+                                   const fp8idx_tensor* weights, const fp8idx_tensor* context_lens,
+                                   const fp8idx_tensor* block_tables, int32_t max_model_len,
+                                   const fp8idx_tensor* out, void* stream) {
+  return paged_impl(q_fp8, kv_cache, weights, context_lens, block_tables, max_model_len, out, nullptr, stream);
+}
+
+fp8idx_status fp8_paged_mqa_logits_ex(const fp8idx_tensor* q_fp8, const fp8idx_tensor* kv_cache,
+                                      const fp8idx_tensor* weights, const fp8idx_tensor* context_lens,
+                                      const fp8idx_tensor* block_tables, int32_t max_model_len,
+                                      const fp8idx_tensor* out, const fp8idx_options* opts, void* stream) {
+  return paged_impl(q_fp8, kv_cache, weights, context_lens, block_tables, max_model_len, out, opts, stream);
+}
+
+fp8idx_status fp8_mqa_logits(const fp8idx_tensor* q_fp8, const fp8idx_tensor* k_fp8, const fp8idx_tensor* kv_scale,
+                             const fp8idx_tensor* weights, const fp8idx_tensor* cu_seqlen_ks,
+                             const fp8idx_tensor* cu_seqlen_ke, const fp8idx_tensor* out, void* stream) {
+  return prefill_impl(q_fp8, k_fp8, kv_scale, weights, cu_seqlen_ks, cu_seqlen_ke, out, nullptr, stream);
+}
+
+fp8idx_status fp8_mqa_logits_ex(const fp8idx_tensor* q_fp8, const fp8idx_tensor* k_fp8,
+                                const fp8idx_tensor* kv_scale, const fp8idx_tensor* weights,
+                                const fp8idx_tensor* cu_seqlen_ks, const fp8idx_tensor* cu_seqlen_ke,
+                                const fp8idx_tensor* out, const fp8idx_options* opts, void* stream) {
+  return prefill_impl(q_fp8, k_fp8, kv_scale, weights, cu_seqlen_ks, cu_seqlen_ke, out, opts, stream);
+}
+
+int fp8idx_paged_is_supported(int32_t heads, int32_t head_dim, int32_t block_size, int32_t next_n) {
+  return paged_supported(heads, head_dim, block_size, next_n) ? 1 : 0;
+}
+
+int fp8idx_prefill_is_supported(int32_t heads, int32_t head_dim) { return prefill_supported(heads, head_dim) ? 1 : 0; }
+
+fp8idx_status fp8idx_plan_paged(int32_t batch, int32_t next_n, int32_t heads, int32_t head_dim, int32_t block_size,
+                                int32_t max_model_len, int32_t num_sms, const fp8idx_options* opts,
+                                fp8idx_plan* plan) {
+  g_last_error.clear();
+  if (!plan) return fail(FP8IDX_ERR_INVALID, "plan: null output");
+  int smem = kMaxSmem;
+  if (num_sms <= 0) {
+    DeviceInfo dev;
+    TRY(device_info(&dev));
+    num_sms = dev.sms;
+    smem = dev.smem_optin;
+  }
+  return plan_paged(batch, next_n, heads, head_dim, block_size, max_model_len, num_sms, smem, opts, plan);
+}
+
+fp8idx_status fp8idx_plan_prefill(int64_t rows, int64_t cols, int32_t heads, int32_t head_dim, int32_t num_sms,
+                                  const fp8idx_options* opts, fp8idx_plan* plan) {
+  g_last_error.clear();
+  if (!plan) return fail(FP8IDX_ERR_INVALID, "plan: null output");
+  int smem = kMaxSmem;
+  if (num_sms <= 0) {
+    DeviceInfo dev;
+    TRY(device_info(&dev));
+    num_sms = dev.sms;
+    smem = dev.smem_optin;
+  }
+  return plan_prefill(rows, cols, heads, head_dim, num_sms, smem, opts, plan);
+}
+
+const char* fp8idx_last_error(void) { return g_last_error.c_str(); }
+
+fp8idx_status fp8idx_device_status(int32_t clear) {
+  g_last_error.clear();
+  unsigned int a = 0, b = 0;
+  if (read_paged_watchdog(&a, clear != 0) != cudaSuccess || read_prefill_watchdog(&b, clear != 0) != cudaSuccess)
+    return fail(FP8IDX_ERR_CUDA, "reading the device watchdog failed");
+  if (a | b) return fail(FP8IDX_ERR_TIMEOUT, "device wait timed out (decode sites 0x%x, prefill sites 0x%x)", a, b);
+  return FP8IDX_OK;
+}
+
+int32_t fp8idx_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,87 @@
+// Device-side pieces shared by the decode and prefill kernels: bounded
+// mbarrier waits (every pipeline wait gives up after kWaitTimeoutNs, sets the
+// CTA's abort flag and a bit in the translation unit's watchdog word, so a
+// broken pipeline ends the kernel instead of hanging the GPU), and the
+// ReLU * weight head-reduction over one 32-column TMEM chunk.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+
+namespace fp8idx {
+
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s: no legitimate wait comes close
+constexpr uint64_t kDrainTimeoutNs = 200000000ull;  // 0.2 s: waiting out in-flight copies after an abort
+
+// Watchdog bit per wait site (reported through fp8idx_device_status).
+enum WaitSite : uint32_t {
+  kSiteQEmpty = 1u << 0,
+  kSiteStageEmpty = 1u << 1,
+  kSiteQFull = 1u << 2,
+  kSiteStageFull = 1u << 3,
+  kSiteAccEmpty = 1u << 4,
+  kSiteAccFull = 1u << 5,
+  kSiteDrain = 1u << 6,
+};
+
+// Polls `bar` for the phase with parity `parity`.  Returns false if the CTA
+// has aborted or the wait ran out (then it aborts the CTA and flags `wd`).
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                             unsigned int* wd, uint32_t site) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (ptx::globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      *abort_flag = 1u;
+      atomicOr(wd, site);
+      return false;
+    }
+  }
+}
+
+// Waits out a phase after an abort (copies already issued must land before
+// the CTA's shared memory is released).  Ignores the abort flag.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned int* wd) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer_ns() - t0 > kDrainTimeoutNs) {
+      atomicOr(wd, static_cast<uint32_t>(kSiteDrain));
+      return;
+    }
+  }
+}
+
+// One warp-collective bounded wait: lane 0 polls, the verdict is broadcast.
+__device__ __forceinline__ bool warp_wait_bounded(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                                  unsigned int* wd, uint32_t site) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, abort_flag, wd, site) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// acc0 + acc1 += sum_{j<32} relu(x_j) * w_j for one 32-column TMEM chunk in
+// registers; w points at 32 f32 weights in shared memory (16-byte aligned,
+// read as broadcast float4).  Two packed f32x2 accumulators.
+__device__ __forceinline__ void relu_dot32(const uint32_t (&r)[32], const float* w, float2& acc0, float2& acc1) {
+  const float4* w4 = reinterpret_cast<const float4*>(w);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float4 ww = w4[j];
+    const float2 x01 = make_float2(fmaxf(__uint_as_float(r[4 * j + 0]), 0.f), fmaxf(__uint_as_float(r[4 * j + 1]), 0.f));
+    const float2 x23 = make_float2(fmaxf(__uint_as_float(r[4 * j + 2]), 0.f), fmaxf(__uint_as_float(r[4 * j + 3]), 0.f));
+    acc0 = __ffma2_rn(x01, make_float2(ww.x, ww.y), acc0);
+    acc1 = __ffma2_rn(x23, make_float2(ww.z, ww.w), acc1);
+  }
+}
+
+__device__ __forceinline__ uint8_t* align_up_1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+}  // namespace fp8idx

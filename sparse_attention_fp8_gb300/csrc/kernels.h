@@ -1,0 +1,111 @@
+// Kernel parameter blocks, shared-memory layouts and launchers shared by the
+// host API (api.cpp) and the kernel translation units.  Host and device both
+// size shared memory with the functions below, so they cannot disagree.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fp8idx {
+
+constexpr int kHeadDim = 128;     // bytes per e4m3 K/Q row
+constexpr int kTileTokens = 128;  // KV tokens per MMA tile (MMA M)
+constexpr int kKTileBytes = kTileTokens * kHeadDim;  // 16 KB
+constexpr int kMaxBatch = 4096;   // decode requests per call (tile prefix lives in smem)
+constexpr int kMaxSmem = 232448;  // 227 KB opt-in per CTA on sm_100-family parts
+
+// ---------------------------------------------------------------- decode
+struct PagedParams {
+  const uint8_t* kv_cache;
+  const float* weights;
+  const int32_t* context_lens;
+  const int32_t* block_tables;
+  float* out;
+  int64_t out_stride;  // elements between output rows
+  int64_t bt_stride;   // elements between block-table rows
+  int64_t num_blocks;
+  int32_t batch;
+  int32_t next_n;
+  int32_t max_blocks;
+  int32_t max_model_len;
+  int32_t block_size;
+  int32_t n_cols;    // next_n * heads = MMA N
+  int32_t stages;
+  int32_t acc_cols;  // TMEM columns per accumulator buffer
+};
+
+// Roles: producer warp(s), one MMA warp, two epilogue warpgroups.
+__host__ __device__ constexpr int paged_producer_warps(bool gather) { return gather ? 4 : 1; }
+__host__ __device__ constexpr int paged_threads(bool gather) { return 32 * (paged_producer_warps(gather) + 1 + 8); }
+
+struct PagedSmem {
+  uint32_t q, k, scale, w, tp, bars, misc, total;
+};
+__host__ __device__ inline PagedSmem paged_smem_layout(int n_cols, int stages, int batch) {
+  PagedSmem L;
+  uint32_t off = 0;
+  L.q = off;     off += 2u * n_cols * kHeadDim;          // two Q buffers (1024-aligned: n_cols % 8 == 0)
+  L.k = off;     off += (uint32_t)stages * kKTileBytes;   // K tile ring
+  L.scale = off; off += (uint32_t)stages * kTileTokens * 4;
+  L.w = off;     off += 2u * n_cols * 4;                  // two weight rows
+  L.tp = off;    off += (uint32_t)(batch + 1) * 4;        // per-request tile prefix
+  off = (off + 7u) & ~7u;
+  L.bars = off;  off += 8u * (2u * stages + 9u);          // full/empty per stage, accf/acce/qf/qe x2, drain
+  L.misc = off;  off += 32u;
+  L.total = off + 1024u;                                  // slack for 1024-byte alignment
+  return L;
+}
+
+// --------------------------------------------------------------- prefill
+struct PrefillParams {
+  const float* weights;
+  const int32_t* ks;
+  const int32_t* ke;
+  float* out;
+  int64_t out_stride;
+  int32_t rows;     // M
+  int32_t cols;     // N
+  int32_t block_m;  // query rows per CTA
+  int32_t n_cols;   // block_m * heads = MMA N
+  int32_t stages;
+  int32_t acc_cols;
+  int32_t split;    // column-tile splits per row block (strided)
+  int32_t reverse;  // 1: row blocks dispatched from the last one
+  int32_t vec_ok;   // out rows are 16-byte aligned: float4 -inf fill
+};
+
+__host__ __device__ constexpr int prefill_threads() { return 32 * (1 + 1 + 4); }
+
+struct PrefillSmem {
+  uint32_t q, k, scale, w, rows, bars, misc, total;
+};
+__host__ __device__ inline PrefillSmem prefill_smem_layout(int n_cols, int stages, int block_m) {
+  PrefillSmem L;
+  uint32_t off = 0;
+  L.q = off;     off += (uint32_t)n_cols * kHeadDim;
+  L.k = off;     off += (uint32_t)stages * kKTileBytes;
+  L.scale = off; off += (uint32_t)stages * kTileTokens * 4;
+  L.w = off;     off += (uint32_t)n_cols * 4;
+  L.rows = off;  off += 2u * 4u * (uint32_t)block_m;     // per-row [lo, hi)
+  off = (off + 7u) & ~7u;
+  L.bars = off;  off += 8u * (2u * stages + 3u);         // full/empty per stage, accf, acce, drain
+  L.misc = off;  off += 32u;
+  L.total = off + 1024u;
+  return L;
+}
+
+// ------------------------------------------------------------- launchers
+// Each returns cudaSuccess or the launch error.  The tensor maps are encoded
+// by the caller; `heads` selects the template instance.
+cudaError_t launch_paged(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const PagedParams& p, int heads,
+                         bool gather, int grid, int smem_bytes, cudaStream_t stream);
+cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_s,
+                           const PrefillParams& p, int heads, int grid, int smem_bytes, cudaStream_t stream);
+
+// Watchdog words of the two translation units (synchronous read, optional clear).
+cudaError_t read_paged_watchdog(unsigned int* value, bool clear);
+cudaError_t read_prefill_watchdog(unsigned int* value, bool clear);
+
+}  // namespace fp8idx

@@ -1,0 +1,437 @@
+// Decode indexer logits (fp8_paged_mqa_logits) for sm_103a.
+//
+// Defined by aiter PR 5047 "[HIP] [JIT] fp8_paged_mqa_logits: hand-written
+// gfx950 decode indexer kernel" (Motivation; Technical Details) and aiter
+// issue 5477 "gfx950 paged MQA logits: next_n spends the tile on program
+// count ..." (The ask):
+//   out[b*next_n + n, p] = sum_h relu(<Q[b,n,h,:], K_b[p,:]>) * w[b*next_n+n, h]
+//                          * kv_scale_b[p]       for p <= ctx_b - next_n + n,
+// with K_b[p] and its scale read from the paged cache through block_tables.
+//
+// Design (one persistent CTA per SM, warp-specialised):
+//  * Work items are (request b, 128-token tile t) for t < ceil(ctx_b / 128);
+//    each CTA takes one contiguous range of the flattened item list, found
+//    on the device from context_lens (a prefix sum in shared memory), so no
+//    host synchronisation is needed and every CTA gets the same number of
+//    tiles (+-1).
+//  * Producer warp: one TMA per cache block (3-D view [block][row][128 B],
+//    128-byte swizzle) and one bulk copy of the block's scales into a ring of
+//    `stages` shared-memory slots; block-table entries are prefetched 32
+//    blocks ahead.  For block size 1 (co-packed 132-byte tokens, only 4-byte
+//    aligned) four producer warps gather each token with 4-byte cp.async in
+//    the same swizzled layout instead.
+//  * MMA warp: the K tile is the A operand (M = 128 tokens) and the request's
+//    whole Q block [next_n*heads, 128] is the B operand, so N = next_n*heads:
+//    one K tile feeds every speculative row in one tcgen05.mma chain (the fold
+//    of next_n into the MMA asked for in aiter issue 5477, The ask).  Four
+//    K=32 e4m3 MMAs accumulate in f32 in tensor memory.  Q and the weights of
+//    the current and the next request are double-buffered.
+//  * Two epilogue warpgroups alternate over tiles (double-buffered TMEM
+//    accumulators).  Thread = token: tcgen05.ld a row of 32 head scores,
+//    ReLU, multiply by the weights, sum the heads, then multiply once by the
+//    token's kv_scale (the hoist of aiter PR 5047, Technical Details: scale
+//    >= 0 and ReLU is positive-homogeneous) and store if inside the causal
+//    window.  A warp stores 32 consecutive floats per row: coalesced 128 B.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fp8idx {
+
+static __device__ unsigned int g_paged_watchdog;
+
+namespace {
+
+// Cursor over a CTA's contiguous range of (request, tile) items.
+struct ItemCursor {
+  const int32_t* tp;  // tile prefix in smem, tp[b] = first item of request b
+  int batch;
+  int b, t, tiles_b;
+
+  __device__ void start(int begin) {
+    int lo = 0, hi = batch;  // largest b with tp[b] <= begin
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (tp[mid] <= begin) lo = mid; else hi = mid;
+    }
+    b = lo;
+    t = begin - tp[lo];
+    tiles_b = tp[lo + 1] - tp[lo];
+  }
+  // Moves to the next item; returns true if it belongs to a new request.
+  __device__ bool advance() {
+    if (++t < tiles_b) return false;
+    do { ++b; } while (b < batch && tp[b + 1] == tp[b]);
+    t = 0;
+    tiles_b = (b < batch) ? tp[b + 1] - tp[b] : 0;
+    return true;
+  }
+};
+
+__device__ __forceinline__ int64_t clamp_ctx(int32_t ctx, const PagedParams& p) {
+  int64_t c = ctx < 0 ? 0 : ctx;
+  const int64_t cap_table = static_cast<int64_t>(p.max_blocks) * p.block_size;
+  if (c > p.max_model_len) c = p.max_model_len;
+  if (c > cap_table) c = cap_table;
+  return c;
+}
+
+__device__ __forceinline__ int32_t load_table(const PagedParams& p, int b, int64_t idx, int64_t limit) {
+  if (idx < 0 || idx >= limit) return 0;
+  return __ldg(p.block_tables + static_cast<int64_t>(b) * p.bt_stride + idx);
+}
+
+__device__ __forceinline__ int64_t clamp_block(int32_t v, int64_t num_blocks) {
+  int64_t x = v < 0 ? 0 : v;
+  return x >= num_blocks ? num_blocks - 1 : x;
+}
+
+}  // namespace
+
+template <int HEADS, bool GATHER>
+__global__ void __launch_bounds__(paged_threads(GATHER), 1)
+    paged_logits_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
+                        const PagedParams p) {
+  constexpr int kProdWarps = paged_producer_warps(GATHER);
+  constexpr int kMmaWarp = kProdWarps;
+  constexpr int kEpiWarp0 = kMmaWarp + 1;
+  constexpr uint32_t kTmemCols = 512;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_up_1024(smem_raw);
+  const int N = p.n_cols;
+  const int S = p.stages;
+  const int B = p.batch;
+  const PagedSmem L = paged_smem_layout(N, S, B);
+  uint8_t* q_s = smem + L.q;
+  uint8_t* k_s = smem + L.k;
+  float* sc_s = reinterpret_cast<float*>(smem + L.scale);
+  float* w_s = reinterpret_cast<float*>(smem + L.w);
+  int32_t* tp = reinterpret_cast<int32_t*>(smem + L.tp);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L.misc);
+  volatile uint32_t* abort_flag = misc + 1;
+
+  const uint32_t full0 = ptx::smem_u32(bars);
+  const uint32_t empty0 = full0 + 8u * S;
+  const uint32_t accf0 = empty0 + 8u * S;
+  const uint32_t acce0 = accf0 + 16u;
+  const uint32_t qf0 = acce0 + 16u;
+  const uint32_t qe0 = qf0 + 16u;
+  const uint32_t drain_bar = qe0 + 16u;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- prologue: per-request tile counts, barriers, tensor memory --------
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    const int64_t c = clamp_ctx(__ldg(p.context_lens + b), p);
+    tp[b + 1] = static_cast<int32_t>((c + kTileTokens - 1) / kTileTokens);
+  }
+  if (threadIdx.x == 0) {
+    tp[0] = 0;
+    misc[1] = 0u;
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(full0 + 8u * s, GATHER ? 32u * kProdWarps : 1u);
+      ptx::mbar_init(empty0 + 8u * s, 1u + 4u);  // MMA commit + the 4 warps that read the scales
+    }
+    for (int g = 0; g < 2; ++g) {
+      ptx::mbar_init(accf0 + 8u * g, 1u);
+      ptx::mbar_init(acce0 + 8u * g, 4u);
+      ptx::mbar_init(qf0 + 8u * g, 1u);
+      ptx::mbar_init(qe0 + 8u * g, 1u + 8u);  // MMA commit + all 8 epilogue warps
+    }
+    ptx::mbar_init(drain_bar, 1u);
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tm_q);
+    if (!GATHER) ptx::prefetch_tmap(&tm_kv);
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(misc), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  __syncthreads();
+  if (warp == 0) {  // inclusive scan of the tile counts
+    int running = 0;
+    for (int base = 0; base < B; base += 32) {
+      const int idx = base + lane;
+      int v = idx < B ? tp[idx + 1] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+      }
+      if (idx < B) tp[idx + 1] = running + v;
+      running += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = misc[0];
+
+  const int total = tp[B];
+  const int begin = static_cast<int>(static_cast<int64_t>(total) * blockIdx.x / gridDim.x);
+  const int end = static_cast<int>(static_cast<int64_t>(total) * (blockIdx.x + 1) / gridDim.x);
+  const int n_items = end - begin;
+  ItemCursor cur{tp, B, 0, 0, 0};
+  if (n_items > 0) cur.start(begin);
+
+  if (warp < kProdWarps) {
+    // =========================== producer ===============================
+    int seg = -1;
+    int issued = 0;
+    int64_t ctx_eff = 0;
+    if constexpr (!GATHER) {
+      const int blk = p.block_size;             // 16, 32, 64 or 128
+      const int P = kTileTokens / blk;          // cache blocks per tile
+      const uint32_t blk_bytes = blk * (kHeadDim + 4);
+      int64_t chunk = 0, need_blocks = 0;
+      int32_t tbl_cur = 0, tbl_nxt = 0;
+      for (int it = 0; it < n_items; ++it) {
+        const bool new_seg = (it == 0) || (cur.t == 0);
+        if (new_seg) {
+          ++seg;
+          if (!warp_wait_bounded(qe0 + 8u * (seg & 1), ((seg >> 1) & 1) ^ 1, abort_flag, &g_paged_watchdog,
+                                 kSiteQEmpty))
+            break;
+          if (lane == 0) {
+            const uint32_t qf = qf0 + 8u * (seg & 1);
+            ptx::mbar_arrive_expect_tx(qf, N * (kHeadDim + 4));
+            ptx::tma_load_2d(ptx::smem_u32(q_s + (seg & 1) * N * kHeadDim), &tm_q, qf, 0, cur.b * N);
+            ptx::bulk_g2s(ptx::smem_u32(w_s + (seg & 1) * N), p.weights + static_cast<int64_t>(cur.b) * N, N * 4,
+                          qf);
+          }
+          ctx_eff = clamp_ctx(__ldg(p.context_lens + cur.b), p);
+          need_blocks = (ctx_eff + blk - 1) / blk;
+          chunk = (static_cast<int64_t>(cur.t) * P) & ~31ll;
+          tbl_cur = load_table(p, cur.b, chunk + lane, need_blocks);
+          tbl_nxt = load_table(p, cur.b, chunk + 32 + lane, need_blocks);
+        }
+        const int s = it % S;
+        if (!warp_wait_bounded(empty0 + 8u * s, ((it / S) & 1) ^ 1, abort_flag, &g_paged_watchdog,
+                               kSiteStageEmpty))
+          break;
+        const int64_t first_tok = static_cast<int64_t>(cur.t) * kTileTokens;
+        const int64_t first_blk = static_cast<int64_t>(cur.t) * P;
+        const int valid = static_cast<int>(ctx_eff - first_tok < kTileTokens ? ctx_eff - first_tok : kTileTokens);
+        const int nblk = (valid + blk - 1) / blk;
+        const uint32_t full = full0 + 8u * s;
+        if (lane == 0) ptx::mbar_arrive_expect_tx(full, nblk * blk_bytes);
+        __syncwarp();
+        const int32_t id = __shfl_sync(0xffffffffu, tbl_cur, static_cast<int>(first_blk - chunk + lane) & 31);
+        if (lane < nblk) {
+          const int64_t page = clamp_block(id, p.num_blocks);
+          ptx::tma_load_3d(ptx::smem_u32(k_s + s * kKTileBytes + lane * blk * kHeadDim), &tm_kv, full, 0, 0,
+                           static_cast<int32_t>(page));
+          ptx::bulk_g2s(ptx::smem_u32(sc_s + s * kTileTokens + lane * blk),
+                        p.kv_cache + page * blk_bytes + static_cast<int64_t>(blk) * kHeadDim, blk * 4, full);
+        }
+        issued = it + 1;
+        if (first_blk + P >= chunk + 32) {  // next tile starts a new 32-block chunk
+          chunk += 32;
+          tbl_cur = tbl_nxt;
+          tbl_nxt = load_table(p, cur.b, chunk + 32 + lane, need_blocks);
+        }
+        cur.advance();
+      }
+      if (*abort_flag && lane == 0) {  // let issued copies land before the CTA exits
+        for (int it = max(0, issued - S); it < issued; ++it)
+          wait_drain(full0 + 8u * (it % S), (it / S) & 1, &g_paged_watchdog);
+        for (int sg = max(0, seg - 1); sg <= seg; ++sg) wait_drain(qf0 + 8u * (sg & 1), (sg >> 1) & 1, &g_paged_watchdog);
+      }
+    } else {
+      // Block size 1: token p of request b is the 132-byte cache row
+      // block_tables[b][p].  Warp w gathers tokens [32w, 32w+32) of a tile:
+      // one token per instruction, lane l copying bytes [4l, 4l+4) into the
+      // 128-byte-swizzled row; lane l also copies token 32w+l's scale.
+      constexpr int kLag = 4;  // tiles in flight per thread before arriving
+      const int pw = warp;     // 0..3
+      int32_t slot_cur = 0, slot_nxt = 0;
+      int pending = 0;
+      for (int it = 0; it < n_items; ++it) {
+        const bool new_seg = (it == 0) || (cur.t == 0);
+        if (new_seg) {
+          ++seg;
+          if (!warp_wait_bounded(qe0 + 8u * (seg & 1), ((seg >> 1) & 1) ^ 1, abort_flag, &g_paged_watchdog,
+                                 kSiteQEmpty))
+            break;
+          if (pw == 0 && lane == 0) {
+            const uint32_t qf = qf0 + 8u * (seg & 1);
+            ptx::mbar_arrive_expect_tx(qf, N * (kHeadDim + 4));
+            ptx::tma_load_2d(ptx::smem_u32(q_s + (seg & 1) * N * kHeadDim), &tm_q, qf, 0, cur.b * N);
+            ptx::bulk_g2s(ptx::smem_u32(w_s + (seg & 1) * N), p.weights + static_cast<int64_t>(cur.b) * N, N * 4,
+                          qf);
+          }
+          ctx_eff = clamp_ctx(__ldg(p.context_lens + cur.b), p);
+          slot_cur = load_table(p, cur.b, static_cast<int64_t>(cur.t) * kTileTokens + pw * 32 + lane, ctx_eff);
+        }
+        // prefetch the next tile's slots (same request only)
+        const bool next_same = (cur.t + 1 < cur.tiles_b);
+        slot_nxt = next_same ? load_table(p, cur.b, static_cast<int64_t>(cur.t + 1) * kTileTokens + pw * 32 + lane,
+                                          ctx_eff)
+                             : 0;
+        const int s = it % S;
+        if (!warp_wait_bounded(empty0 + 8u * s, ((it / S) & 1) ^ 1, abort_flag, &g_paged_watchdog,
+                               kSiteStageEmpty))
+          break;
+        const int64_t first_tok = static_cast<int64_t>(cur.t) * kTileTokens;
+        const int valid = static_cast<int>(ctx_eff - first_tok < kTileTokens ? ctx_eff - first_tok : kTileTokens);
+        const uint32_t tile_s = ptx::smem_u32(k_s + s * kKTileBytes);
+        const uint32_t chunk_in_row = static_cast<uint32_t>(lane >> 2);
+        const uint32_t byte_in_chunk = static_cast<uint32_t>(lane & 3) * 4u;
+#pragma unroll 4
+        for (int j = 0; j < 32; ++j) {
+          const int tok = pw * 32 + j;
+          const int32_t sid = __shfl_sync(0xffffffffu, slot_cur, j);
+          if (tok < valid) {
+            const int64_t row = clamp_block(sid, p.num_blocks);
+            const uint32_t dst = tile_s + tok * kHeadDim + (((chunk_in_row ^ (tok & 7)) << 4) | byte_in_chunk);
+            ptx::cp_async_4(dst, p.kv_cache + row * (kHeadDim + 4) + lane * 4);
+          }
+        }
+        {
+          const int tok = pw * 32 + lane;
+          if (tok < valid) {
+            const int64_t row = clamp_block(slot_cur, p.num_blocks);
+            ptx::cp_async_4(ptx::smem_u32(sc_s + s * kTileTokens + tok), p.kv_cache + row * (kHeadDim + 4) + kHeadDim);
+          }
+        }
+        ptx::cp_async_commit();
+        ++pending;
+        issued = it + 1;
+        if (pending > kLag) {  // the tile issued kLag tiles ago has landed
+          ptx::cp_async_wait<kLag>();
+          ptx::fence_proxy_async_smem();
+          const int done = it - kLag;
+          ptx::mbar_arrive(full0 + 8u * (done % S));
+          --pending;
+        }
+        slot_cur = slot_nxt;
+        cur.advance();
+      }
+      ptx::cp_async_wait<0>();
+      ptx::fence_proxy_async_smem();
+      for (int done = issued - pending; done < issued; ++done) ptx::mbar_arrive(full0 + 8u * (done % S));
+      if (*abort_flag && pw == 0 && lane == 0)
+        for (int sg = max(0, seg - 1); sg <= seg; ++sg) wait_drain(qf0 + 8u * (sg & 1), (sg >> 1) & 1, &g_paged_watchdog);
+    }
+  } else if (warp == kMmaWarp) {
+    // ============================= MMA ==================================
+    if (lane == 0) {
+      const uint32_t idesc = ptx::idesc_e4m3_f32(kTileTokens, N);
+      int seg = -1;
+      bool ok = true;
+      for (int it = 0; it < n_items && ok; ++it) {
+        if (it == 0 || cur.t == 0) {
+          ++seg;
+          if (!(ok = wait_bounded(qf0 + 8u * (seg & 1), (seg >> 1) & 1, abort_flag, &g_paged_watchdog, kSiteQFull)))
+            break;
+        }
+        const int s = it % S;
+        const int g = it & 1;
+        if (!(ok = wait_bounded(full0 + 8u * s, (it / S) & 1, abort_flag, &g_paged_watchdog, kSiteStageFull))) break;
+        if (!(ok = wait_bounded(acce0 + 8u * g, ((it >> 1) & 1) ^ 1, abort_flag, &g_paged_watchdog, kSiteAccEmpty)))
+          break;
+        ptx::tc_fence_after();
+        const uint64_t a_desc = ptx::smem_desc_sw128(ptx::smem_u32(k_s + s * kKTileBytes));
+        const uint64_t b_desc = ptx::smem_desc_sw128(ptx::smem_u32(q_s + (seg & 1) * N * kHeadDim));
+        const uint32_t d_tmem = tmem + g * p.acc_cols;
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 32; ++kk)  // K = 32 e4m3 per MMA: advance 32 bytes in the swizzled row
+          ptx::mma_f8f6f4(d_tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, kk > 0 ? 1u : 0u);
+        ptx::mma_commit(empty0 + 8u * s);
+        ptx::mma_commit(accf0 + 8u * g);
+        const bool seg_end = cur.advance() || (it + 1 == n_items);
+        if (seg_end) ptx::mma_commit(qe0 + 8u * (seg & 1));
+      }
+      if (*abort_flag) {
+        ptx::mma_commit(drain_bar);
+        wait_drain(drain_bar, 0, &g_paged_watchdog);
+      }
+    }
+  } else {
+    // =========================== epilogue ===============================
+    const int ew = warp - kEpiWarp0;  // 0..7
+    const int grp = ew >> 2;          // accumulator buffer this warpgroup owns
+    const int quad = warp & 3;        // TMEM lane quadrant this warp may access
+    const int row = quad * 32 + lane; // token within the tile
+    const int next_n = p.next_n;
+    int seg = -1;
+    int32_t ctx = 0;
+    for (int it = 0; it < n_items; ++it) {
+      if (it == 0 || cur.t == 0) {
+        ++seg;
+        if (!warp_wait_bounded(qf0 + 8u * (seg & 1), (seg >> 1) & 1, abort_flag, &g_paged_watchdog, kSiteQFull)) break;
+        ctx = __ldg(p.context_lens + cur.b);
+      }
+      if ((it & 1) == grp) {
+        const int s = it % S;
+        if (!warp_wait_bounded(accf0 + 8u * grp, (it >> 1) & 1, abort_flag, &g_paged_watchdog, kSiteAccFull)) break;
+        ptx::tc_fence_after();
+        if (!warp_wait_bounded(full0 + 8u * s, (it / S) & 1, abort_flag, &g_paged_watchdog, kSiteStageFull)) break;
+        const float scale = sc_s[s * kTileTokens + row];
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(empty0 + 8u * s);
+
+        const float* w = w_s + (seg & 1) * N;
+        const uint32_t tbase = tmem + grp * p.acc_cols + (static_cast<uint32_t>(quad * 32) << 16);
+        const int64_t pos = static_cast<int64_t>(cur.t) * kTileTokens + row;
+        float* out_col = p.out + static_cast<int64_t>(cur.b) * next_n * p.out_stride + pos;
+        for (int n = 0; n < next_n; ++n) {
+          float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int hc = 0; hc < HEADS / 32; ++hc) {
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(tbase + n * HEADS + hc * 32, r);
+            ptx::tmem_wait_ld();
+            relu_dot32(r, w + n * HEADS + hc * 32, a0, a1);
+          }
+          const float logit = ((a0.x + a0.y) + (a1.x + a1.y)) * scale;
+          if (pos <= static_cast<int64_t>(ctx) - next_n + n && pos < p.max_model_len)
+            __stcs(out_col + static_cast<int64_t>(n) * p.out_stride, logit);
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(acce0 + 8u * grp);
+      }
+      const bool seg_end = cur.advance() || (it + 1 == n_items);
+      if (seg_end) {
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(qe0 + 8u * (seg & 1));
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+cudaError_t launch_paged(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const PagedParams& p, int heads,
+                         bool gather, int grid, int smem_bytes, cudaStream_t stream) {
+  void (*kern)(CUtensorMap, CUtensorMap, PagedParams) = nullptr;
+  if (heads == 32) kern = gather ? paged_logits_kernel<32, true> : paged_logits_kernel<32, false>;
+  else if (heads == 64) kern = gather ? paged_logits_kernel<64, true> : paged_logits_kernel<64, false>;
+  else return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, paged_threads(gather), smem_bytes, stream>>>(tm_q, tm_kv, p);
+  return cudaGetLastError();
+}
+
+cudaError_t read_paged_watchdog(unsigned int* value, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_paged_watchdog, sizeof(unsigned int));
+  if (e != cudaSuccess || !clear) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_paged_watchdog, &zero, sizeof(unsigned int));
+}
+
+}  // namespace fp8idx

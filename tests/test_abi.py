@@ -1,0 +1,119 @@
+"""The C-ABI library on the host (CPU only; nothing is launched).
+
+Checks that libfp8idx.so loads, exports every function include/fp8idx.h
+declares, and that the host-side logic (support gates, planner, argument
+validation) behaves as documented.
+"""
+import ctypes
+
+import pytest
+
+import sparse_attention_fp8_gb300 as fp8idx
+from sparse_attention_fp8_gb300 import _native
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_attention_fp8_gb300 import _build
+    _build.build()
+    return fp8idx.library()
+
+
+def test_exports_every_declared_function(lib):
+    names = _native.header_functions()
+    expected = {"fp8_paged_mqa_logits", "fp8_paged_mqa_logits_ex", "fp8_mqa_logits", "fp8_mqa_logits_ex",
+                "fp8idx_paged_is_supported", "fp8idx_prefill_is_supported", "fp8idx_plan_paged",
+                "fp8idx_plan_prefill", "fp8idx_last_error", "fp8idx_device_status", "fp8idx_version"}
+    assert expected <= set(names), set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared but not exported"
+
+
+def test_version(lib):
+    assert fp8idx.version() >= 100
+
+
+def test_support_gates(lib):
+    assert fp8idx.paged_is_supported(32, 128, 64, 6)
+    assert fp8idx.paged_is_supported(32, 128, 1, 1)
+    assert fp8idx.paged_is_supported(64, 128, 16, 4)
+    assert not fp8idx.paged_is_supported(64, 128, 64, 5)   # next_n*heads > 256
+    assert not fp8idx.paged_is_supported(32, 64, 64, 1)    # head_dim 64
+    assert not fp8idx.paged_is_supported(16, 128, 64, 1)
+    assert not fp8idx.paged_is_supported(32, 128, 8, 1)    # block size 8
+    assert fp8idx.prefill_is_supported(32, 128) and fp8idx.prefill_is_supported(64, 128)
+    assert not fp8idx.prefill_is_supported(128, 128)
+
+
+def test_planner_decode(lib):
+    p = fp8idx.plan_paged(16, 6, 32, 128, 64, 1048576, num_sms=148)
+    assert p.grid == 148 and p.tile_n == 192 and p.gather == 0
+    assert p.smem_bytes <= 232448 and p.stages >= 4
+    small = fp8idx.plan_paged(1, 1, 32, 128, 64, 1024, num_sms=148)
+    assert small.grid == 8  # one CTA per 128-token tile when there are fewer tiles than SMs
+    g = fp8idx.plan_paged(64, 4, 64, 128, 1, 32768, num_sms=148)
+    assert g.gather == 1 and g.tile_n == 256 and g.stages >= 6
+    o = fp8idx.plan_paged(16, 6, 32, 128, 64, 1048576, num_sms=148, options=fp8idx.Options(num_ctas=7, stages=3))
+    assert o.grid == 7 and o.stages == 3
+
+
+def test_planner_prefill(lib):
+    p = fp8idx.plan_prefill(4096, 32768, 32, 128, num_sms=148)
+    assert p.block_m == 8 and p.tile_n == 256 and p.reverse_rows == 1
+    assert p.grid == 512 * p.split_n and p.split_n >= 2
+    assert 2 * p.smem_bytes <= 232448  # two CTAs per SM
+    p64 = fp8idx.plan_prefill(1000, 1000, 64, 128, num_sms=148)
+    assert p64.block_m == 4 and p64.reverse_rows == 0
+    o = fp8idx.plan_prefill(4096, 32768, 32, 128, num_sms=148,
+                            options=fp8idx.Options(split_n=3, reverse_rows=0, block_m=2))
+    assert o.split_n == 3 and o.reverse_rows == 0 and o.tile_n == 64 and o.grid == 2048 * 3
+    with pytest.raises(fp8idx.Fp8IdxError) as e:
+        fp8idx.plan_prefill(10, 10, 32, 128, num_sms=148, options=fp8idx.Options(block_m=9))
+    assert e.value.status == fp8idx.FP8IDX_ERR_UNSUPPORTED
+
+
+def _t(dtype, shape, ptr=0x1000):
+    d = _native._Tensor()
+    d.data = ptr
+    d.dtype = dtype
+    d.ndim = len(shape)
+    st = 1
+    for i in reversed(range(len(shape))):
+        d.shape[i] = shape[i]
+        d.stride[i] = st
+        st *= shape[i]
+    return d
+
+
+def test_validation_rejects_before_touching_the_device(lib):
+    """Malformed descriptors return INVALID from host checks (fake pointers,
+    never dereferenced, no CUDA call reached)."""
+    B, n, H, D = 2, 2, 32, 128
+    q = _t(0, (B, n, H, D))
+    kv = _t(0, (4, 64 * (D + 4)))
+    w = _t(1, (B * n, H))
+    cl = _t(2, (B,))
+    bt = _t(2, (B, 2))
+    out = _t(1, (B * n, 128))
+    R = ctypes.byref
+    st = lib.fp8_paged_mqa_logits(R(q), R(kv), R(_t(2, (B * n, H))), R(cl), R(bt), 128, R(out), None)
+    assert st == fp8idx.FP8IDX_ERR_INVALID and b"weights" in lib.fp8idx_last_error()
+    st = lib.fp8_paged_mqa_logits(None, R(kv), R(w), R(cl), R(bt), 128, R(out), None)
+    assert st == fp8idx.FP8IDX_ERR_INVALID
+    st = lib.fp8_paged_mqa_logits(R(q), R(_t(0, (4, 100))), R(w), R(cl), R(bt), 128, R(out), None)
+    assert st == fp8idx.FP8IDX_ERR_INVALID  # cache row not block_size*(D+4)
+    st = lib.fp8_paged_mqa_logits(R(q), R(kv), R(w), R(cl), R(bt), 129, R(out), None)
+    assert st == fp8idx.FP8IDX_ERR_INVALID  # out narrower than max_model_len
+    q16 = _t(0, (B, n, 16, D))
+    st = lib.fp8_paged_mqa_logits(R(q16), R(kv), R(_t(1, (B * n, 16))), R(cl), R(bt), 128, R(out), None)
+    assert st == fp8idx.FP8IDX_ERR_UNSUPPORTED
+    qp = _t(0, (5, H, D))
+    k = _t(0, (300, D))
+    s = _t(1, (300,))
+    wp = _t(1, (5, H))
+    ks = _t(2, (5,))
+    outp = _t(1, (5, 300))
+    st = lib.fp8_mqa_logits(R(qp), R(k), R(s), R(wp), R(ks), R(_t(2, (4,))), R(outp), None)
+    assert st == fp8idx.FP8IDX_ERR_INVALID
+    st = lib.fp8_mqa_logits(R(qp), R(k), R(_t(1, (299,))), R(wp), R(ks), R(ks), R(outp), None)
+    assert st == fp8idx.FP8IDX_ERR_INVALID

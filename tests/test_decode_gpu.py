@@ -1,0 +1,194 @@
+"""GPU parity of fp8_paged_mqa_logits (decode) against the CPU oracle.
+
+Every case NaN-poisons the output, so a window position the kernel fails to
+write, or a position outside the window it writes, is caught (decode writes
+only the causal window; the -inf outside is the caller's).  Block tables
+point into a permuted pool with NaN-poisoned unowned blocks and tail slots,
+so a kernel that walks the cache linearly or reads past a context fails.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from parity import assert_rows_close, decode_window_mask, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fp8idx():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sparse_attention_fp8_gb300 as m
+    m.library()
+    return m
+
+
+def run_decode(fp8idx, case, options=None, out=None):
+    d = to_device(case)
+    rows = case.batch * case.next_n
+    if out is None:
+        out = torch.full((rows, case.max_model_len), float("nan"), dtype=torch.float32, device="cuda")
+    fp8idx.fp8_paged_mqa_logits(d["q"], d["kv_cache"], d["weights"], d["context_lens"], d["block_tables"],
+                                case.max_model_len, out, options=options)
+    torch.cuda.synchronize()
+    return out
+
+
+def oracle_decode(o, case, rows=None):
+    return o.paged_mqa_logits(case.q, case.kv_cache, case.weights, case.context_lens, case.block_tables,
+                              case.block_size, case.max_model_len, rows=rows)
+
+
+SMALL = [
+    # (name, batch, next_n, heads, max_model_len, block_size, context_lens)
+    ("b1_n1_h32_blk64_full", 1, 1, 32, 1024, 64, [1024]),
+    ("b3_n2_h32_blk64_ragged", 3, 2, 32, 700, 64, [700, 129, 1]),
+    ("b4_n6_h32_blk64_short", 4, 6, 32, 600, 64, [600, 255, 5, 6]),
+    ("b2_n8_h32_blk16", 2, 8, 32, 300, 16, [300, 77]),
+    ("b2_n4_h64_blk32", 2, 4, 64, 520, 32, [520, 300]),
+    ("b5_n3_h64_blk128", 5, 3, 64, 400, 128, None),
+    ("b3_n5_h32_blk64", 3, 5, 32, 450, 64, [450, 128, 127]),
+    ("b3_n4_h64_blk1", 3, 4, 64, 333, 1, [333, 200, 4]),
+    ("b2_n2_h32_blk1_ctx0", 2, 2, 32, 900, 1, [900, 0]),
+    ("b2_n1_h64_blk64_ctx0", 2, 1, 64, 256, 64, [0, 256]),
+    ("b6_n1_h32_blk1_ragged", 6, 1, 32, 1000, 1, None),
+]
+
+
+@pytest.mark.parametrize("name,batch,next_n,heads,mml,blk,ctx", SMALL, ids=[s[0] for s in SMALL])
+def test_decode_small(fp8idx, oracle_impl, name, batch, next_n, heads, mml, blk, ctx):
+    case = workloads.decode_case(batch, next_n, heads, max_model_len=mml, block_size=blk, context_lens=ctx,
+                                 var_ratio=0.3, seed=zlib.crc32(name.encode()) % 1000, poison=True, extra_blocks=3)
+    gpu = run_decode(fp8idx, case).cpu().numpy()
+    ref = oracle_decode(oracle_impl, case)
+    assert_rows_close(gpu, ref, written=decode_window_mask(case), what=name)
+
+
+@pytest.mark.parametrize("opts", [dict(num_ctas=1), dict(num_ctas=3), dict(stages=2), dict(stages=3, num_ctas=5),
+                                  dict(stages=6, num_ctas=2)],
+                         ids=["one_cta", "three_ctas", "two_stages", "three_stages", "gather_min_stages"])
+def test_decode_planner_overrides(fp8idx, oracle_impl, opts):
+    """One CTA crossing many requests exercises the Q/weight double buffer and
+    every ring wrap; small stage counts exercise the back-pressure paths."""
+    blk = 1 if opts.get("stages") == 6 else 64
+    case = workloads.decode_case(7, 3, 32, max_model_len=520, block_size=blk, var_ratio=0.6, seed=7,
+                                 poison=True, extra_blocks=2)
+    gpu = run_decode(fp8idx, case, options=fp8idx.Options(**opts)).cpu().numpy()
+    ref = oracle_decode(oracle_impl, case)
+    assert_rows_close(gpu, ref, written=decode_window_mask(case), what=str(opts))
+
+
+def test_decode_config0(fp8idx, oracle_impl):
+    case = workloads.make_config(0)
+    gpu = run_decode(fp8idx, case).cpu().numpy()
+    assert_rows_close(gpu, oracle_decode(oracle_impl, case), written=decode_window_mask(case), what="config0")
+
+
+def test_decode_config1(fp8idx, oracle_impl):
+    case = workloads.make_config(1)
+    gpu = run_decode(fp8idx, case).cpu().numpy()
+    assert_rows_close(gpu, oracle_decode(oracle_impl, case), written=decode_window_mask(case), what="config1")
+
+
+def _full_size_sampled(fp8idx, o, case, full_rows, n_samples=4096, seed=0):
+    """Full-size run: exact window check on every row, full oracle rows for a
+    few rows, and oracle elements at random in-window positions of all rows."""
+    out = run_decode(fp8idx, case)
+    gpu = out.cpu().numpy()
+    del out
+    nrows = case.batch * case.next_n
+    for r0 in range(0, nrows, 8):
+        r1 = min(nrows, r0 + 8)
+        win = decode_window_mask(case, rows=(r0, r1))
+        untouched = np.isnan(gpu[r0:r1])
+        assert not (untouched == win).any(), f"rows {r0}..{r1}: window written incorrectly"
+        assert np.isfinite(gpu[r0:r1][win]).all()
+    rowmax_min = np.inf
+    for r in full_rows:
+        ref = oracle_decode(o, case, rows=(r, r + 1))
+        assert_rows_close(gpu[r:r + 1], ref, written=decode_window_mask(case, rows=(r, r + 1)), what=f"row {r}")
+        rowmax_min = min(rowmax_min, np.abs(ref[np.isfinite(ref)]).max())
+    rng = np.random.default_rng(seed)
+    rows = rng.integers(0, nrows, n_samples)
+    b = rows // case.next_n
+    last = case.context_lens.astype(np.int64)[b] - case.next_n + rows % case.next_n
+    keep = last >= 0
+    rows, last = rows[keep], last[keep]
+    cols = (rng.random(rows.size) * (last + 1)).astype(np.int64)
+    ref = o.paged_mqa_logits_at(case.q, case.kv_cache, case.weights, case.context_lens, case.block_tables,
+                                case.block_size, case.max_model_len, rows, cols)
+    err = np.abs(gpu[rows, cols].astype(np.float64) - ref)
+    assert np.all(err <= 1e-3 * rowmax_min + 1e-5), f"sampled max err {err.max()}"
+
+
+@pytest.mark.slow
+def test_decode_config2_full_size(fp8idx, oracle_impl):
+    case = workloads.make_config(2)
+    _full_size_sampled(fp8idx, oracle_impl, case, full_rows=[0, 47, 95])
+
+
+@pytest.mark.slow
+def test_decode_config2_next_n1_full_size(fp8idx, oracle_impl):
+    case = workloads.make_config(2, next_n=1)
+    _full_size_sampled(fp8idx, oracle_impl, case, full_rows=[0, 15])
+
+
+@pytest.mark.slow
+def test_decode_config4_full_size(fp8idx, oracle_impl):
+    case = workloads.make_config(4)
+    _full_size_sampled(fp8idx, oracle_impl, case, full_rows=[0, 131, 255])
+
+
+def test_decode_graph_capture_replay(fp8idx, oracle_impl):
+    """Captured once, replayed with new input contents: matches the oracle."""
+    case = workloads.decode_case(4, 2, 32, max_model_len=640, block_size=64, var_ratio=0.3, seed=31,
+                                 poison=True, extra_blocks=1)
+    d = to_device(case)
+    out = torch.full((8, 640), float("nan"), device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up on the capture stream
+        fp8idx.fp8_paged_mqa_logits(d["q"], d["kv_cache"], d["weights"], d["context_lens"], d["block_tables"],
+                                    640, out, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fp8idx.fp8_paged_mqa_logits(d["q"], d["kv_cache"], d["weights"], d["context_lens"], d["block_tables"],
+                                    640, out, stream=s)
+    case2 = workloads.decode_case(4, 2, 32, max_model_len=640, block_size=64, var_ratio=0.3, seed=32,
+                                  poison=True, extra_blocks=1)
+    # same shapes; new contents copied into the captured buffers
+    case2.context_lens[:] = case.context_lens
+    case2.block_tables[:] = case.block_tables
+    case2.kv_cache = case.kv_cache
+    d["q"].copy_(torch.from_numpy(case2.q))
+    d["weights"].copy_(torch.from_numpy(case2.weights))
+    out.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    ref = oracle_decode(oracle_impl, case2)
+    assert_rows_close(out.cpu().numpy(), ref, written=decode_window_mask(case2), what="graph replay")
+
+
+def test_decode_empty_and_errors(fp8idx):
+    case = workloads.decode_case(2, 2, 32, max_model_len=128, block_size=64, context_lens=[128, 64], seed=3)
+    d = to_device(case)
+    out = torch.full((4, 128), float("nan"), device="cuda")
+    # max_model_len 0: nothing to do
+    fp8idx.fp8_paged_mqa_logits(d["q"], d["kv_cache"], d["weights"], d["context_lens"], d["block_tables"], 0, out)
+    torch.cuda.synchronize()
+    assert torch.isnan(out).all()
+    with pytest.raises(fp8idx.Fp8IdxError) as e:  # weights with the wrong dtype
+        fp8idx.fp8_paged_mqa_logits(d["q"], d["kv_cache"], d["weights"].to(torch.int32), d["context_lens"],
+                                    d["block_tables"], 128, out)
+    assert e.value.status == fp8idx.FP8IDX_ERR_INVALID
+    q16 = torch.zeros((2, 2, 16, 128), dtype=torch.uint8, device="cuda")
+    w16 = torch.zeros((4, 16), dtype=torch.float32, device="cuda")
+    with pytest.raises(fp8idx.Fp8IdxError) as e:  # 16 heads: not implemented
+        fp8idx.fp8_paged_mqa_logits(q16, d["kv_cache"], w16, d["context_lens"], d["block_tables"], 128, out)
+    assert e.value.status == fp8idx.FP8IDX_ERR_UNSUPPORTED
+    assert fp8idx.device_status() == fp8idx.FP8IDX_OK

@@ -1,0 +1,130 @@
+"""GPU parity of fp8_mqa_logits (prefill) against the CPU oracle.
+
+The output is NaN-poisoned before every call; prefill writes every element
+(-inf outside the windows), so any position left unwritten fails the -inf
+mask check.  The window modes are the ones the prefill pages grade: causal,
+multi-request packing, a misaligned start, empty rows, windows past the end
+(and before the start), and a context-parallel split.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from parity import assert_rows_close, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fp8idx():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sparse_attention_fp8_gb300 as m
+    m.library()
+    return m
+
+
+def run_prefill(fp8idx, case, options=None):
+    d = to_device(case)
+    out = torch.full((case.rows, case.cols), float("nan"), dtype=torch.float32, device="cuda")
+    fp8idx.fp8_mqa_logits(d["q"], d["k"], d["kv_scale"], d["weights"], d["ks"], d["ke"], out, options=options)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def oracle_prefill(o, case, rows=None):
+    return o.mqa_logits(case.q, case.k, case.kv_scale, case.weights, case.ks, case.ke, rows=rows)
+
+
+MODES = ["causal", "multi_req", "misaligned", "empty", "past_end", "cp"]
+
+
+@pytest.mark.parametrize("heads", [32, 64])
+@pytest.mark.parametrize("mode", MODES)
+def test_prefill_window_modes(fp8idx, oracle_impl, mode, heads):
+    # M not a multiple of the row block, N not a multiple of the 128-token tile
+    case = workloads.prefill_case(45, 700, heads, mode=mode, seed=100 + MODES.index(mode))
+    gpu = run_prefill(fp8idx, case)
+    assert_rows_close(gpu, oracle_prefill(oracle_impl, case), what=f"{mode}/h{heads}")
+
+
+@pytest.mark.parametrize("shape", [(1, 1), (3, 128), (8, 129), (17, 256), (64, 1000), (200, 520)])
+def test_prefill_shapes(fp8idx, oracle_impl, shape):
+    m, n = shape
+    case = workloads.prefill_case(m, n, 32, mode="causal" if m <= n else "past_end", seed=m * 7 + n)
+    gpu = run_prefill(fp8idx, case)
+    assert_rows_close(gpu, oracle_prefill(oracle_impl, case), what=str(shape))
+
+
+@pytest.mark.parametrize("opts", [dict(split_n=1), dict(split_n=5), dict(reverse_rows=0), dict(reverse_rows=1),
+                                  dict(block_m=3), dict(stages=2), dict(block_m=1, split_n=2)],
+                         ids=["split1", "split5", "natural", "reverse", "block_m3", "stages2", "block_m1"])
+def test_prefill_planner_overrides(fp8idx, oracle_impl, opts):
+    case = workloads.prefill_case(70, 900, 32, mode="multi_req", seed=9)
+    gpu = run_prefill(fp8idx, case, options=fp8idx.Options(**opts))
+    assert_rows_close(gpu, oracle_prefill(oracle_impl, case), what=str(opts))
+
+
+@pytest.mark.slow
+def test_prefill_config3_full_size(fp8idx, oracle_impl):
+    """Full 4096 x 32768 run: -inf mask of every row, full oracle rows at the
+    request boundaries, and random sampled in-window elements."""
+    case = workloads.make_config(3)
+    gpu = run_prefill(fp8idx, case)
+    n = np.arange(case.cols)[None, :]
+    for r0 in range(0, case.rows, 256):
+        r1 = r0 + 256
+        lo = np.maximum(case.ks[r0:r1].astype(np.int64), 0)[:, None]
+        hi = np.minimum(case.ke[r0:r1].astype(np.int64), case.cols)[:, None]
+        inside = (n >= lo) & (n < hi)
+        g = gpu[r0:r1]
+        assert np.array_equal(np.isneginf(g), ~inside), f"rows {r0}..{r1}: -inf mask"
+        assert np.isfinite(g[inside]).all()
+    rowmax_min = np.inf
+    for r in (0, 1023, 1024, 2047, 4095):
+        ref = oracle_prefill(oracle_impl, case, rows=(r, r + 1))
+        assert_rows_close(gpu[r:r + 1], ref, what=f"row {r}")
+        rowmax_min = min(rowmax_min, np.abs(ref[np.isfinite(ref)]).max())
+    rng = np.random.default_rng(1)
+    rows = rng.integers(0, case.rows, 4096)
+    lo = case.ks[rows].astype(np.int64)
+    hi = case.ke[rows].astype(np.int64)
+    cols = lo + (rng.random(rows.size) * (hi - lo)).astype(np.int64)
+    ref = oracle_impl.mqa_logits_at(case.q, case.k, case.kv_scale, case.weights, case.ks, case.ke, rows, cols)
+    err = np.abs(gpu[rows, cols].astype(np.float64) - ref)
+    assert np.all(err <= 1e-3 * rowmax_min + 1e-5), f"sampled max err {err.max()}"
+
+
+def test_prefill_graph_capture_replay(fp8idx, oracle_impl):
+    case = workloads.prefill_case(40, 600, 32, mode="multi_req", seed=41)
+    d = to_device(case)
+    out = torch.full((40, 600), float("nan"), device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fp8idx.fp8_mqa_logits(d["q"], d["k"], d["kv_scale"], d["weights"], d["ks"], d["ke"], out, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fp8idx.fp8_mqa_logits(d["q"], d["k"], d["kv_scale"], d["weights"], d["ks"], d["ke"], out, stream=s)
+    case2 = workloads.prefill_case(40, 600, 32, mode="multi_req", seed=42)
+    for key in ("q", "k", "kv_scale", "weights", "ks", "ke"):
+        d[key].copy_(torch.from_numpy(getattr(case2, key)))
+    out.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert_rows_close(out.cpu().numpy(), oracle_prefill(oracle_impl, case2), what="graph replay")
+
+
+def test_prefill_empty_and_errors(fp8idx):
+    case = workloads.prefill_case(4, 64, 32, seed=5)
+    d = to_device(case)
+    empty = torch.empty((0, 64), device="cuda")
+    fp8idx.fp8_mqa_logits(d["q"][:0], d["k"], d["kv_scale"], d["weights"][:0], d["ks"][:0], d["ke"][:0], empty)
+    out = torch.full((4, 64), float("nan"), device="cuda")
+    with pytest.raises(fp8idx.Fp8IdxError) as e:
+        fp8idx.fp8_mqa_logits(d["q"], d["k"], d["kv_scale"], d["weights"], d["ks"], d["ke"][:3], out)
+    assert e.value.status == fp8idx.FP8IDX_ERR_INVALID
+    torch.cuda.synchronize()
+    assert fp8idx.device_status() == fp8idx.FP8IDX_OK
