@@ -257,6 +257,15 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
         const bool new_seg = (it == 0) || (cur.t == 0);
         if (new_seg) {
           ++seg;
+          if (seg >= 2 && pending > 0) {
+            // The Q buffer is freed only once the consumers finish request
+            // seg-2, whose last tiles may still be among the deferred
+            // arrivals: publish every tile in flight before waiting on it.
+            ptx::cp_async_wait<0>();
+            ptx::fence_proxy_async_smem();
+            for (int done = issued - pending; done < issued; ++done) ptx::mbar_arrive(full0 + 8u * (done % S));
+            pending = 0;
+          }
           if (!warp_wait_bounded(qe0 + 8u * (seg & 1), ((seg >> 1) & 1) ^ 1, abort_flag, &g_paged_watchdog,
                                  kSiteQEmpty))
             break;
