@@ -1,0 +1,488 @@
+#!/usr/bin/env python
+"""Benchmark of the FP8 indexer logits on GB300.
+
+One step = one call of the hot path on one batch of synthetic input.  The
+default workload is the MTP-verify decode batch (batch 16, next_n 6, 32 heads,
+131072-token contexts, max_model_len 1048576, KV block size 64) -- the shape
+the indexer pages quote their decode figure on.  Other workloads:
+--workload {decode_b1, decode_ragged, decode_mtp_verify, decode_mtp_verify_n1,
+prefill_4x1024, decode_blk1}.
+
+Prints ONE JSON line (rank 0):
+  value      = us per call (all ranks' calls / max-over-ranks device time),
+               timed with CUDA events on the launching stream around each
+               call; the L2 is flushed (512 MB write) before every call.
+  roofline   = the dominant kernel's algorithmic bytes / its mean duration
+               against the measured HBM copy bandwidth.
+  e2e        = the same call driven from pinned host memory: per-step inputs
+               copied host->device and the written logits copied back, all
+               inside the timed region.
+  cpu_baseline = the CPU oracle (fp64, OpenMP) on a bounded random sample of
+               the same workload's logits, scaled to the whole workload.
+--impl reference times that oracle alone as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "indexer logits us/call; essential GB/s and % of roofline (1 GB300)"
+UNIT = "us/call"
+HEAD_DIM = 128
+KV_TOKEN_BYTES = HEAD_DIM + 4  # 128 e4m3 bytes + f32 scale per token
+
+WORKLOADS = {
+    "decode_b1": (0, None),
+    "decode_ragged": (1, None),
+    "decode_mtp_verify": (2, None),
+    "decode_mtp_verify_n1": (2, 1),
+    "prefill_4x1024": (3, None),
+    "decode_blk1": (4, None),
+}
+DEFAULT_WORKLOAD = "decode_mtp_verify"
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------- byte model
+def decode_window_elems(context_lens, next_n, max_model_len) -> int:
+    """Written logits: sum over rows of |{p : p <= ctx - next_n + n, p < max_model_len}|."""
+    tot = 0
+    for c in np.asarray(context_lens, dtype=np.int64).tolist():
+        for n in range(next_n):
+            tot += max(0, min(c - next_n + n, max_model_len - 1) + 1)
+    return tot
+
+
+def decode_bytes(batch, next_n, heads, context_lens, max_model_len, block_size=64, k_reads=1):
+    """Essential HBM bytes of one decode call: every K token (128 B + 4 B
+    scale) read k_reads times per request (1 for a shared K walk), Q, weights,
+    and the written output.  The block table is reported separately."""
+    ctx = np.minimum(np.maximum(np.asarray(context_lens, dtype=np.int64), 0), max_model_len)
+    k = int(ctx.sum()) * KV_TOKEN_BYTES * k_reads
+    q = batch * next_n * heads * HEAD_DIM
+    w = batch * next_n * heads * 4
+    out = decode_window_elems(context_lens, next_n, max_model_len) * 4
+    table = int(np.ceil(ctx / block_size).sum()) * 4
+    return {"k": k, "q": q, "w": w, "out": out, "total": k + q + w + out, "table": table}
+
+
+def decode_flops(heads, context_lens, next_n, max_model_len) -> int:
+    return 2 * HEAD_DIM * heads * decode_window_elems(context_lens, next_n, max_model_len)
+
+
+def prefill_bytes(m, n, heads):
+    """Essential bytes of one prefill call: K + scale, Q, weights, and the full
+    [M, N] f32 output (every element is written)."""
+    k = n * KV_TOKEN_BYTES
+    q = m * heads * HEAD_DIM
+    w = m * heads * 4
+    out = m * n * 4
+    return {"k": k, "q": q, "w": w, "out": out, "total": k + q + w + out, "table": 0}
+
+
+def prefill_window_pairs(ks, ke, n) -> int:
+    lo = np.maximum(np.asarray(ks, np.int64), 0)
+    hi = np.minimum(np.asarray(ke, np.int64), n)
+    return int(np.maximum(hi - lo, 0).sum())
+
+
+def prefill_flops(heads, ks, ke, n) -> int:
+    return 2 * HEAD_DIM * heads * prefill_window_pairs(ks, ke, n)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    """Hash of the kernel sources: a recorded ncu traffic figure is reported
+    only while the kernels it was taken on are unchanged."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_attention_fp8_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """dram read+write bytes per launch from the committed ncu summary, if the
+    kernels are unchanged since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("kernel_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+        self.marks = []
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        rows = []
+        if self.path and os.path.exists(self.path):
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+            os.unlink(self.path)
+        return rows
+
+    @staticmethod
+    def summarize(rows):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------- helpers
+def make_case(workload):
+    idx, next_n = WORKLOADS[workload]
+    return idx, workloads.make_config(idx, next_n=next_n)
+
+
+def case_bytes_flops(idx, case):
+    if workloads.CONFIGS[idx]["kind"] == "decode":
+        b = decode_bytes(case.batch, case.next_n, case.heads, case.context_lens, case.max_model_len,
+                         case.block_size)
+        f = decode_flops(case.heads, case.context_lens, case.next_n, case.max_model_len)
+        units = decode_window_elems(case.context_lens, case.next_n, case.max_model_len)
+    else:
+        b = prefill_bytes(case.rows, case.cols, case.heads)
+        f = prefill_flops(case.heads, case.ks, case.ke, case.cols)
+        units = prefill_window_pairs(case.ks, case.ke, case.cols)
+    return b, f, units
+
+
+def oracle_sample_us(o, case, kind, n_elems, rng):
+    """Oracle time (s) for n_elems random in-window logits of the workload."""
+    if kind == "decode":
+        rows_total = case.batch * case.next_n
+        rows = rng.integers(0, rows_total, n_elems * 2)
+        last = np.minimum(case.context_lens.astype(np.int64)[rows // case.next_n] - case.next_n + rows % case.next_n,
+                          case.max_model_len - 1)
+        keep = last >= 0
+        rows, last = rows[keep][:n_elems], last[keep][:n_elems]
+        cols = (rng.random(rows.size) * (last + 1)).astype(np.int64)
+        t0 = time.perf_counter()
+        o.paged_mqa_logits_at(case.q, case.kv_cache, case.weights, case.context_lens, case.block_tables,
+                              case.block_size, case.max_model_len, rows, cols)
+        return time.perf_counter() - t0, rows.size
+    lo = np.maximum(case.ks.astype(np.int64), 0)
+    hi = np.minimum(case.ke.astype(np.int64), case.cols)
+    ok = np.nonzero(hi > lo)[0]
+    rows = ok[rng.integers(0, ok.size, n_elems)]
+    cols = lo[rows] + (rng.random(rows.size) * (hi[rows] - lo[rows])).astype(np.int64)
+    t0 = time.perf_counter()
+    o.mqa_logits_at(case.q, case.k, case.kv_scale, case.weights, case.ks, case.ke, rows, cols)
+    return time.perf_counter() - t0, rows.size
+
+
+def cpu_baseline(case, kind, units, budget_s=12.0, seed=0):
+    """The oracle as it stands on this host's cores, on a bounded sample."""
+    import oracle
+    o = oracle.Oracle()
+    rng = np.random.default_rng(seed)
+    t, n = oracle_sample_us(o, case, kind, 2000, rng)  # calibrate
+    rate = n / max(t, 1e-6)
+    n_elems = int(min(max(2000, rate * budget_s), 5_000_000))
+    t, n = oracle_sample_us(o, case, kind, n_elems, rng)
+    us_per_call = t / n * units * 1e6
+    return {"value": us_per_call, "unit": UNIT, "cores": o.max_threads(), "kind": "oracle",
+            "sample": f"{n} random in-window logits of {units} ({t:.1f} s), scaled to the whole workload"}
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world):
+    import torch
+    import sparse_attention_fp8_gb300 as fp8idx
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    idx, case = make_case(args.workload)
+    kind = workloads.CONFIGS[idx]["kind"]
+    nbytes, flops, units = case_bytes_flops(idx, case)
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.Stream(device=dev)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    if kind == "decode":
+        d = {k: up(getattr(case, k)) for k in ("q", "kv_cache", "weights", "context_lens", "block_tables")}
+        rows = case.batch * case.next_n
+        out = torch.full((rows, case.max_model_len), float("-inf"), device=dev)  # caller's pre-fill, once
+
+        def call(s=stream):
+            fp8idx.fp8_paged_mqa_logits(d["q"], d["kv_cache"], d["weights"], d["context_lens"], d["block_tables"],
+                                        case.max_model_len, out, stream=s)
+        step_inputs = ("q", "weights", "context_lens", "block_tables")
+        result_cols = int(min(case.max_model_len, max(int(case.context_lens.max()), 1)))
+    else:
+        d = {k: up(getattr(case, k)) for k in ("q", "k", "kv_scale", "weights", "ks", "ke")}
+        out = torch.empty((case.rows, case.cols), device=dev)
+
+        def call(s=stream):
+            fp8idx.fp8_mqa_logits(d["q"], d["k"], d["kv_scale"], d["weights"], d["ks"], d["ke"], out, stream=s)
+        step_inputs = ("q", "k", "kv_scale", "weights", "ks", "ke")
+        result_cols = case.cols
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            call()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            call()
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t_wall = time.time() - t_wall0
+    per_call_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    # clocks: if the timed region was too short for the sampler, soak the same step for ~1 s
+    soak_t0 = time.time()
+    if t_wall < 1.0:
+        with torch.cuda.stream(stream):
+            while time.time() - soak_t0 < 1.0:
+                for _ in range(50):
+                    flush.zero_()
+                    call()
+                torch.cuda.synchronize()
+    clocks = ClockSampler.summarize(sampler.stop())
+    clocks["window"] = "timed region" if t_wall >= 1.0 else "timed region + 1 s soak of the same step"
+
+    total_ms = float(sum(per_call_ms))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    us_per_call = total_ms * 1e3 / (args.steps * world)
+    mean_ms = total_ms / args.steps
+    median_us = statistics.median(per_call_ms) * 1e3
+
+    # hot back-to-back replay of a captured graph (20 calls), for reference
+    graph_us = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            call()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(20):
+                call()
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(10):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        graph_us = e0.elapsed_time(e1) * 1e3 / 200
+        del g
+    except Exception as exc:  # graph timing is informative only
+        graph_us = f"unavailable: {exc}"
+
+    # end to end from pinned host memory
+    host_in = {k: torch.from_numpy(np.ascontiguousarray(getattr(case, k))).pin_memory() for k in step_inputs}
+    host_out = torch.empty((out.shape[0], result_cols), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * 4
+    e2e_steps = max(3, min(args.steps, 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for k, t in host_in.items():
+                d[k].copy_(t, non_blocking=True)
+            call()
+            host_out.copy_(out[:, :result_cols], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_us = e2e_ms * 1e3 / (e2e_steps * world)
+
+    status = fp8idx.device_status()
+    hbm_peak = float(peaks["hbm_gbs"])
+    fp8_peak = 2.0 * float(peaks["bf16_tflops"])  # nominal fp8:bf16 dense ratio 2
+    achieved_gbs = nbytes["total"] / (mean_ms * 1e-3) / 1e9
+    tflops = flops / (mean_ms * 1e-3) / 1e12
+    roof_t_us = max(nbytes["total"] / (hbm_peak * 1e9), flops / (fp8_peak * 1e12)) * 1e6
+    line = {
+        "metric": METRIC, "value": round(us_per_call, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(mean_ms, 6), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32", "data": "synthetic",
+        "config": {"workload": args.workload, "desc": case.name, "l2": "flushed (512 MB write) before every call",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "median_us": round(median_us, 3),
+        "graph_replay_us_hot": round(graph_us, 3) if isinstance(graph_us, float) else graph_us,
+        "essential_bytes": nbytes, "fp8_flops": flops,
+        "essential_gbs": round(achieved_gbs, 1),
+        "roofline_fraction": round(roof_t_us / (mean_ms * 1e3), 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved_gbs / hbm_peak, 4), "traffic": recorded_traffic(args.workload),
+                     "peak_source": f"{peak_src} hbm_gbs"},
+        "tensor": {"achieved_tflops": round(tflops, 1), "peak_tflops": fp8_peak,
+                   "frac": round(tflops / fp8_peak, 4), "peak_source": f"{peak_src} bf16_tflops x2 (fp8:bf16)"},
+        "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "per-step inputs H2D from pinned memory, call, written logits D2H; "
+                        + ("the paged K cache stays resident" if kind == "decode" else "")},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "device_status": "ok" if status == 0 else f"watchdog {status}",
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case, kind, units)
+    return line
+
+
+# ---------------------------------------------------------- reference arm
+def run_reference(args):
+    import oracle
+    idx, case = make_case(args.workload)
+    kind = workloads.CONFIGS[idx]["kind"]
+    _, _, units = case_bytes_flops(idx, case)
+    o = oracle.Oracle()
+    rng = np.random.default_rng(1)
+    t, n = oracle_sample_us(o, case, kind, 2000, rng)
+    rate = n / max(t, 1e-6)
+    per_step_s = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    n_elems = int(min(max(2000, rate * per_step_s), 5_000_000))
+    for _ in range(args.warmup):
+        oracle_sample_us(o, case, kind, n_elems, rng)
+    vals = []
+    for _ in range(args.steps):
+        t, n = oracle_sample_us(o, case, kind, n_elems, rng)
+        vals.append(t / n * units * 1e6)
+    v = float(np.mean(vals))
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v / 1e3, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "desc": case.name},
+        "cpu_baseline": {"value": round(v, 1), "unit": UNIT, "cores": o.max_threads(), "kind": "oracle",
+                         "sample": f"{n_elems} random in-window logits per step of {units}, scaled"},
+        "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        torch.distributed.init_process_group("nccl")
+    line = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
