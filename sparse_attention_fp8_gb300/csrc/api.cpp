@@ -189,11 +189,9 @@ fp8idx_status plan_prefill(int64_t rows, int64_t cols, int32_t heads, int32_t he
   if (block_m * heads > 256 || block_m > 32)
     return fail(FP8IDX_ERR_UNSUPPORTED, "prefill: block_m %d too large for %d heads", block_m, heads);
   const int n_cols = block_m * heads;
-  // Two CTAs per SM: keep each at or below half of the shared memory.
-  const int per_cta = std::min(smem_limit, 232448 / 2 - 1024);
-  int stages = (o && o->stages > 0) ? o->stages : 4;
-  while (stages > 2 && (int)prefill_smem_layout(n_cols, stages, block_m).total > per_cta) --stages;
-  if ((int)prefill_smem_layout(n_cols, stages, block_m).total > smem_limit)
+  int stages = (o && o->stages > 0) ? o->stages : 12;
+  while (stages > 2 && (int)prefill_smem_layout(n_cols, stages).total > smem_limit) --stages;
+  if ((int)prefill_smem_layout(n_cols, stages).total > smem_limit)
     return fail(FP8IDX_ERR_UNSUPPORTED, "prefill: shared memory too small");
   const int64_t num_rb = (rows + block_m - 1) / block_m;
   const int64_t n_tiles = (cols + kTileTokens - 1) / kTileTokens;
@@ -201,23 +199,27 @@ fp8idx_status plan_prefill(int64_t rows, int64_t cols, int32_t heads, int32_t he
   if (o && o->split_n > 0) {
     split = o->split_n;
   } else if (num_rb > 0) {
-    // aim for at least four waves of two CTAs per SM
-    split = (8ll * num_sms + num_rb - 1) / num_rb;
+    // about 16 work units per persistent CTA keeps the round-robin deal
+    // within a few percent of even
+    split = (16ll * num_sms + num_rb - 1) / num_rb;
   }
   split = std::max<int64_t>(1, std::min<int64_t>(split, std::max<int64_t>(n_tiles, 1)));
   int reverse = (cols > 2048) ? 1 : 0;  // longest-first pays off only for long rows
   if (o && o->reverse_rows >= 0 && o->reverse_rows <= 1) reverse = o->reverse_rows;
-  if (num_rb * split > 0x7fffffffll) return fail(FP8IDX_ERR_UNSUPPORTED, "prefill: grid too large");
+  const int64_t units = num_rb * split;
+  if (units > 0x7fffffffll) return fail(FP8IDX_ERR_UNSUPPORTED, "prefill: too many work units");
+  int grid = (int)std::min<int64_t>(num_sms, std::max<int64_t>(units, 1));
+  if (o && o->num_ctas > 0) grid = std::min(o->num_ctas, num_sms);
   std::memset(plan, 0, sizeof(*plan));
-  plan->grid = static_cast<int32_t>(num_rb * split);
+  plan->grid = grid;
   plan->threads = prefill_threads();
-  plan->smem_bytes = (int)prefill_smem_layout(n_cols, stages, block_m).total;
+  plan->smem_bytes = (int)prefill_smem_layout(n_cols, stages).total;
   plan->stages = stages;
   plan->tile_n = n_cols;
   plan->block_m = block_m;
   plan->split_n = static_cast<int32_t>(split);
   plan->reverse_rows = reverse;
-  plan->tmem_cols = n_cols > 128 ? 256 : 128;
+  plan->tmem_cols = 512;
   plan->gather = 0;
   return FP8IDX_OK;
 }
@@ -327,8 +329,8 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const fp8idx_tensor* k, const
   if (!prefill_supported((int)H, (int)D))
     return fail(FP8IDX_ERR_UNSUPPORTED, "prefill: heads=%lld head_dim=%lld not supported", (long long)H, (long long)D);
   if (M == 0 || N == 0) return ok();
-  if (!aligned16(q->data) || !aligned16(k->data) || !aligned16(s->data))
-    return fail(FP8IDX_ERR_INVALID, "q_fp8, k_fp8 and kv_scale must be 16-byte aligned");
+  if (!aligned16(q->data) || !aligned16(k->data) || !aligned16(s->data) || !aligned16(w->data))
+    return fail(FP8IDX_ERR_INVALID, "q_fp8, k_fp8, kv_scale and weights must be 16-byte aligned");
   DeviceInfo dev;
   TRY(device_info(&dev));
   fp8idx_plan plan;
@@ -352,8 +354,14 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const fp8idx_tensor* k, const
     TRY(encode(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, s->data, dims, nullptr, box, CU_TENSOR_MAP_SWIZZLE_NONE,
                "kv_scale"));
   }
+  CUtensorMap tm_w;
+  {
+    const uint64_t dims[1] = {(uint64_t)(M * H)};
+    const uint32_t box[1] = {(uint32_t)plan.tile_n};
+    TRY(encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, w->data, dims, nullptr, box, CU_TENSOR_MAP_SWIZZLE_NONE,
+               "weights"));
+  }
   PrefillParams p;
-  p.weights = static_cast<const float*>(w->data);
   p.ks = static_cast<const int32_t*>(ks->data);
   p.ke = static_cast<const int32_t*>(ke->data);
   p.out = static_cast<float*>(out->data);
@@ -363,11 +371,10 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const fp8idx_tensor* k, const
   p.block_m = plan.block_m;
   p.n_cols = plan.tile_n;
   p.stages = plan.stages;
-  p.acc_cols = plan.tmem_cols;
   p.split = plan.split_n;
   p.reverse = plan.reverse_rows;
   p.vec_ok = (aligned16(out->data) && (p.out_stride % 4) == 0) ? 1 : 0;
-  cudaError_t e = launch_prefill(tm_q, tm_k, tm_s, p, (int)H, plan.grid, plan.smem_bytes,
+  cudaError_t e = launch_prefill(tm_q, tm_k, tm_s, tm_w, p, (int)H, plan.grid, plan.smem_bytes,
                                  static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
   return ok();

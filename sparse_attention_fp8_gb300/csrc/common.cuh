@@ -49,7 +49,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
 // the CTA's shared memory is released).  Ignores the abort flag.
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned int* wd) {
   const uint64_t t0 = ptx::globaltimer_ns();
-  while (!ptx::mbar_try_wait(bar, parity)) {
+  while (!ptx::mbar_try_wait(bar, parity, 100000u)) {
     if (ptx::globaltimer_ns() - t0 > kDrainTimeoutNs) {
       atomicOr(wd, static_cast<uint32_t>(kSiteDrain));
       return;

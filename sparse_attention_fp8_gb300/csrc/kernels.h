@@ -37,7 +37,7 @@ struct PagedParams {
 };
 
 // Roles: producer warp(s), one MMA warp, two epilogue warpgroups.
-__host__ __device__ constexpr int paged_producer_warps(bool gather) { return gather ? 4 : 1; }
+__host__ __device__ constexpr int paged_producer_warps(bool gather) { return gather ? 2 : 1; }
 __host__ __device__ constexpr int paged_threads(bool gather) { return 32 * (paged_producer_warps(gather) + 1 + 8); }
 
 struct PagedSmem {
@@ -60,37 +60,35 @@ __host__ __device__ inline PagedSmem paged_smem_layout(int n_cols, int stages, i
 
 // --------------------------------------------------------------- prefill
 struct PrefillParams {
-  const float* weights;
   const int32_t* ks;
   const int32_t* ke;
   float* out;
   int64_t out_stride;
   int32_t rows;     // M
   int32_t cols;     // N
-  int32_t block_m;  // query rows per CTA
+  int32_t block_m;  // query rows per work unit
   int32_t n_cols;   // block_m * heads = MMA N
   int32_t stages;
-  int32_t acc_cols;
   int32_t split;    // column-tile splits per row block (strided)
-  int32_t reverse;  // 1: row blocks dispatched from the last one
+  int32_t reverse;  // 1: row blocks dealt from the last one
   int32_t vec_ok;   // out rows are 16-byte aligned: float4 -inf fill
 };
 
-__host__ __device__ constexpr int prefill_threads() { return 32 * (1 + 1 + 4); }
+// Roles: producer warp, MMA warp, two epilogue warpgroups.
+__host__ __device__ constexpr int prefill_threads() { return 32 * (1 + 1 + 8); }
 
 struct PrefillSmem {
-  uint32_t q, k, scale, w, rows, bars, misc, total;
+  uint32_t q, k, scale, w, bars, misc, total;
 };
-__host__ __device__ inline PrefillSmem prefill_smem_layout(int n_cols, int stages, int block_m) {
+__host__ __device__ inline PrefillSmem prefill_smem_layout(int n_cols, int stages) {
   PrefillSmem L;
   uint32_t off = 0;
-  L.q = off;     off += (uint32_t)n_cols * kHeadDim;
+  L.q = off;     off += 2u * n_cols * kHeadDim;            // two Q blocks
   L.k = off;     off += (uint32_t)stages * kKTileBytes;
   L.scale = off; off += (uint32_t)stages * kTileTokens * 4;
-  L.w = off;     off += (uint32_t)n_cols * 4;
-  L.rows = off;  off += 2u * 4u * (uint32_t)block_m;     // per-row [lo, hi)
+  L.w = off;     off += 2u * n_cols * 4;                    // two weight blocks
   off = (off + 7u) & ~7u;
-  L.bars = off;  off += 8u * (2u * stages + 3u);         // full/empty per stage, accf, acce, drain
+  L.bars = off;  off += 8u * (2u * stages + 9u);           // full/empty per stage, accf/acce/qf/qe x2, drain
   L.misc = off;  off += 32u;
   L.total = off + 1024u;
   return L;
@@ -102,7 +100,8 @@ __host__ __device__ inline PrefillSmem prefill_smem_layout(int n_cols, int stage
 cudaError_t launch_paged(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const PagedParams& p, int heads,
                          bool gather, int grid, int smem_bytes, cudaStream_t stream);
 cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_s,
-                           const PrefillParams& p, int heads, int grid, int smem_bytes, cudaStream_t stream);
+                           const CUtensorMap& tm_w, const PrefillParams& p, int heads, int grid, int smem_bytes,
+                           cudaStream_t stream);
 
 // Watchdog words of the two translation units (synchronous read, optional clear).
 cudaError_t read_paged_watchdog(unsigned int* value, bool clear);

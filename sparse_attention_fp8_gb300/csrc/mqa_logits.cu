@@ -4,25 +4,25 @@
 // prefill indexer kernel" (Motivation; Technical Details):
 //   out[m, n] = sum_h relu(<Q[m,h,:], K[n,:]>) * kv_scale[n] * w[m,h]
 //               for n in [ks[m], ke[m]) (clamped to [0, N)), -inf elsewhere,
-// every element written (the fused -inf fill of that PR).
+// with every element written (the fused -inf fill of that PR).
 //
-// Design: one CTA per (row block, column split); two CTAs share an SM so one
-// CTA's epilogue overlaps the other's MMA and loads.
-//  * A row block is block_m query rows; its Q block [block_m*heads, 128]
-//    stays resident in shared memory as the MMA B operand (N = block_m*heads,
-//    256 at 32 heads), so one K tile feeds every row of the block.
-//  * Column tiles of 128 tokens are split across `split` CTAs in a strided
-//    way (CTA s takes tiles s, s+split, ...), which gives every CTA the same
-//    mix of computed and pure -inf tiles.
-//  * Tiles that meet the union of the block's windows are computed: TMA of
-//    the K tile (128-byte swizzle) and its 128 scales, four K=32 e4m3
-//    tcgen05.mma into a TMEM accumulator, then the epilogue (thread = token)
-//    applies ReLU * weight, sums the heads, multiplies by the token's scale
-//    and stores each row's value or -inf (outside that row's own window).
-//  * Tiles outside the union are written with -inf directly (float4 stores).
-//  * Row blocks are dispatched from the last one when `reverse` is set: under
-//    causal masking later rows have longer windows, so the long CTAs start
-//    first and short ones fill in behind (same PR, Technical Details).
+// Design: persistent, one CTA per SM, warp-specialised like the decode kernel.
+//  * A work unit is (row block, column split): block_m query rows whose Q
+//    block [block_m*heads, 128] is the MMA B operand (N = block_m*heads, 256
+//    at 32 heads), and the column tiles j = split_idx, split_idx + split, ...
+//    (strided, so every unit has the same mix of computed and -inf tiles).
+//    Units are ordered longest-first when `reverse` is set (row blocks from
+//    the last one: under causal masking later rows have longer windows, same
+//    PR, Technical Details) and dealt to CTAs round-robin.
+//  * Per unit every role derives the union of the block's windows from
+//    ks/ke; tiles meeting it are computed (TMA of K and its scales, four K=32
+//    e4m3 tcgen05.mma into a double-buffered TMEM accumulator), the others are
+//    written with -inf directly.  Q and the weights are double-buffered
+//    across units.
+//  * Two epilogue warpgroups share every tile, each owning half of the
+//    block's rows; a thread owns one token: it loads its <= 128 accumulator
+//    columns, releases TMEM, applies ReLU * weight, sums the heads, scales by
+//    the token's kv_scale and stores the value or -inf per row.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -33,201 +33,285 @@ namespace fp8idx {
 
 static __device__ unsigned int g_prefill_watchdog;
 
+namespace {
+
+struct Unit {
+  int m0;      // first query row
+  int sidx;    // column split index
+  int n_j;     // column tiles of this unit
+  int t_lo;    // union tile range [t_lo, t_hi) of computed tiles
+  int t_hi;
+  int row_lo;  // this lane's row window (lanes < block_m), clamped; empty: 0,0
+  int row_hi;
+};
+
+// Warp-collective: unit u's geometry and window union.  Every lane gets the
+// union; lane r < block_m also gets row r's window.
+__device__ __forceinline__ Unit load_unit(const PrefillParams& p, int u, int num_rb, int n_tiles) {
+  Unit U;
+  const int lane = threadIdx.x & 31;
+  const int rb_index = u / p.split;
+  U.sidx = u % p.split;
+  const int rb = p.reverse ? (num_rb - 1 - rb_index) : rb_index;
+  U.m0 = rb * p.block_m;
+  U.n_j = (U.sidx < n_tiles) ? (n_tiles - U.sidx + p.split - 1) / p.split : 0;
+  int rlo = 0, rhi = 0;
+  const int m = U.m0 + lane;
+  if (lane < p.block_m && m < p.rows) {
+    const int ks = __ldg(p.ks + m), ke = __ldg(p.ke + m);
+    rlo = ks < 0 ? 0 : ks;
+    rhi = ke > p.cols ? p.cols : ke;
+    if (rhi <= rlo) rlo = rhi = 0;
+  }
+  U.row_lo = rlo;
+  U.row_hi = rhi;
+  int lo = rhi > rlo ? rlo : p.cols;
+  int hi = rhi > rlo ? rhi : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  U.t_lo = hi > lo ? lo / kTileTokens : 0;
+  U.t_hi = hi > lo ? (hi + kTileTokens - 1) / kTileTokens : 0;
+  return U;
+}
+
+__device__ __forceinline__ bool is_compute(const Unit& U, int j) { return j >= U.t_lo && j < U.t_hi; }
+
+}  // namespace
+
 template <int HEADS>
-__global__ void __launch_bounds__(prefill_threads(), 2)
+__global__ void __launch_bounds__(prefill_threads(), 1)
     mqa_logits_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_s, const PrefillParams p) {
+                      const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_w,
+                      const PrefillParams p) {
   constexpr int kEpiWarp0 = 2;
+  constexpr uint32_t kTmemCols = 512;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_up_1024(smem_raw);
   const int N = p.n_cols;
   const int S = p.stages;
   const int BM = p.block_m;
-  const PrefillSmem L = prefill_smem_layout(N, S, BM);
+  const PrefillSmem L = prefill_smem_layout(N, S);
   uint8_t* q_s = smem + L.q;
   uint8_t* k_s = smem + L.k;
   float* sc_s = reinterpret_cast<float*>(smem + L.scale);
   float* w_s = reinterpret_cast<float*>(smem + L.w);
-  int32_t* row_lo = reinterpret_cast<int32_t*>(smem + L.rows);
-  int32_t* row_hi = row_lo + BM;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile uint32_t* abort_flag = misc + 1;
 
   const uint32_t full0 = ptx::smem_u32(bars);
   const uint32_t empty0 = full0 + 8u * S;
-  const uint32_t accf = empty0 + 8u * S;
-  const uint32_t acce = accf + 8u;
-  const uint32_t drain_bar = acce + 8u;
+  const uint32_t accf0 = empty0 + 8u * S;
+  const uint32_t acce0 = accf0 + 16u;
+  const uint32_t qf0 = acce0 + 16u;
+  const uint32_t qe0 = qf0 + 16u;
+  const uint32_t drain_bar = qe0 + 16u;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int num_rb = (p.rows + BM - 1) / BM;
-  const int rb_index = blockIdx.x / p.split;
-  const int sidx = blockIdx.x % p.split;
-  const int rb = p.reverse ? (num_rb - 1 - rb_index) : rb_index;
-  const int m0 = rb * BM;
   const int n_tiles = (p.cols + kTileTokens - 1) / kTileTokens;
-  const uint32_t tmem_cols = static_cast<uint32_t>(p.acc_cols);
+  const int n_units = num_rb * p.split;
 
-  // ---- prologue ----------------------------------------------------------
-  if (warp == 0) {
-    // per-row clamped windows [lo, hi); empty rows get lo = hi = 0
-    int lo = p.cols, hi = 0;
-    if (lane < BM) {
-      const int m = m0 + lane;
-      int rlo = 0, rhi = 0;
-      if (m < p.rows) {
-        const int ks = __ldg(p.ks + m), ke = __ldg(p.ke + m);
-        rlo = ks < 0 ? 0 : ks;
-        rhi = ke > p.cols ? p.cols : ke;
-        if (rhi <= rlo) rlo = rhi = 0;
-      }
-      row_lo[lane] = rlo;
-      row_hi[lane] = rhi;
-      if (rhi > rlo) { lo = rlo; hi = rhi; }
+  if (threadIdx.x == 0) {
+    misc[1] = 0u;
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(full0 + 8u * s, 1u);
+      ptx::mbar_init(empty0 + 8u * s, 1u + 8u);  // MMA commit + 8 epilogue warps (scales)
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    for (int g = 0; g < 2; ++g) {
+      ptx::mbar_init(accf0 + 8u * g, 1u);
+      ptx::mbar_init(acce0 + 8u * g, 8u);
+      ptx::mbar_init(qf0 + 8u * g, 1u);
+      ptx::mbar_init(qe0 + 8u * g, 1u + 8u);
     }
-    if (lane == 0) {
-      // union tile range [t_lo, t_hi) of computed tiles
-      misc[2] = hi > lo ? static_cast<uint32_t>(lo / kTileTokens) : 0u;
-      misc[3] = hi > lo ? static_cast<uint32_t>((hi + kTileTokens - 1) / kTileTokens) : 0u;
-      misc[1] = 0u;
-      for (int s = 0; s < S; ++s) {
-        ptx::mbar_init(full0 + 8u * s, 1u);
-        ptx::mbar_init(empty0 + 8u * s, 1u + 4u);
-      }
-      ptx::mbar_init(accf, 1u);
-      ptx::mbar_init(acce, 4u);
-      ptx::mbar_init(drain_bar, 1u);
-      ptx::fence_barrier_init();
-      ptx::prefetch_tmap(&tm_q);
-      ptx::prefetch_tmap(&tm_k);
-      ptx::prefetch_tmap(&tm_s);
-    }
-  } else if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(misc), tmem_cols);
+    ptx::mbar_init(drain_bar, 1u);
+    ptx::fence_barrier_init();
+    ptx::prefetch_tmap(&tm_q);
+    ptx::prefetch_tmap(&tm_k);
+    ptx::prefetch_tmap(&tm_s);
+    ptx::prefetch_tmap(&tm_w);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(misc), kTmemCols);
     ptx::tmem_relinquish();
-  } else {
-    // weights of the block's rows (zero for rows past M)
-    for (int i = threadIdx.x - 32 * kEpiWarp0; i < N; i += 128) {
-      const int m = m0 + i / HEADS;
-      w_s[i] = (m < p.rows) ? __ldg(p.weights + static_cast<int64_t>(m0) * HEADS + i) : 0.f;
-    }
   }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = misc[0];
-  const int t_lo = static_cast<int>(misc[2]);
-  const int t_hi = static_cast<int>(misc[3]);
-  // computed tiles of this CTA: j = sidx + k*split with t_lo <= j < t_hi
-  const int c_first = (t_lo <= sidx) ? sidx : sidx + ((t_lo - sidx + p.split - 1) / p.split) * p.split;
-  const int n_comp = (t_hi > c_first) ? (t_hi - c_first + p.split - 1) / p.split : 0;
 
   if (warp == 0) {
     // ============================ producer ==============================
-    if (lane == 0 && n_comp > 0) {
-      // Q block: rows [m0*HEADS, m0*HEADS + N) of the [M*heads, 128] view; counted on stage 0's barrier
-      int issued = 0;
-      for (int c = 0; c < n_comp; ++c) {
-        const int s = c % S;
-        if (!wait_bounded(empty0 + 8u * s, ((c / S) & 1) ^ 1, abort_flag, &g_prefill_watchdog, kSiteStageEmpty))
-          break;
-        const uint32_t full = full0 + 8u * s;
-        const int j = c_first + c * p.split;
-        const uint32_t bytes = kKTileBytes + kTileTokens * 4 + (c == 0 ? N * kHeadDim : 0);
-        ptx::mbar_arrive_expect_tx(full, bytes);
-        if (c == 0) ptx::tma_load_2d(ptx::smem_u32(q_s), &tm_q, full, 0, m0 * HEADS);
-        ptx::tma_load_2d(ptx::smem_u32(k_s + s * kKTileBytes), &tm_k, full, 0, j * kTileTokens);
-        ptx::tma_load_1d(ptx::smem_u32(sc_s + s * kTileTokens), &tm_s, full, j * kTileTokens);
-        issued = c + 1;
+    int seg = -1, ci = 0, q_issued = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      const Unit U = load_unit(p, u, num_rb, n_tiles);
+      ++seg;
+      if (!warp_wait_bounded(qe0 + 8u * (seg & 1), ((seg >> 1) & 1) ^ 1, abort_flag, &g_prefill_watchdog,
+                             kSiteQEmpty))
+        break;
+      if (lane == 0) {
+        const uint32_t qf = qf0 + 8u * (seg & 1);
+        ptx::mbar_arrive_expect_tx(qf, N * (kHeadDim + 4));
+        ptx::tma_load_2d(ptx::smem_u32(q_s + (seg & 1) * N * kHeadDim), &tm_q, qf, 0, U.m0 * HEADS);
+        ptx::tma_load_1d(ptx::smem_u32(w_s + (seg & 1) * N), &tm_w, qf, U.m0 * HEADS);
       }
-      if (*abort_flag)
-        for (int c = max(0, issued - S); c < issued; ++c)
-          wait_drain(full0 + 8u * (c % S), (c / S) & 1, &g_prefill_watchdog);
+      ++q_issued;
+      bool ok = true;
+      for (int k = 0; k < U.n_j; ++k) {
+        const int j = U.sidx + k * p.split;
+        if (!is_compute(U, j)) continue;
+        const int s = ci % S;
+        if (!(ok = warp_wait_bounded(empty0 + 8u * s, ((ci / S) & 1) ^ 1, abort_flag, &g_prefill_watchdog,
+                                     kSiteStageEmpty)))
+          break;
+        if (lane == 0) {
+          const uint32_t full = full0 + 8u * s;
+          ptx::mbar_arrive_expect_tx(full, kKTileBytes + kTileTokens * 4);
+          ptx::tma_load_2d(ptx::smem_u32(k_s + s * kKTileBytes), &tm_k, full, 0, j * kTileTokens);
+          ptx::tma_load_1d(ptx::smem_u32(sc_s + s * kTileTokens), &tm_s, full, j * kTileTokens);
+        }
+        ++ci;
+      }
+      if (!ok) break;
+    }
+    if (*abort_flag && lane == 0) {
+      for (int c = max(0, ci - S); c < ci; ++c) wait_drain(full0 + 8u * (c % S), (c / S) & 1, &g_prefill_watchdog);
+      for (int sg = max(0, q_issued - 2); sg < q_issued; ++sg)
+        wait_drain(qf0 + 8u * (sg & 1), (sg >> 1) & 1, &g_prefill_watchdog);
     }
   } else if (warp == 1) {
     // ============================== MMA =================================
-    if (lane == 0 && n_comp > 0) {
-      const uint32_t idesc = ptx::idesc_e4m3_f32(kTileTokens, N);
-      const uint64_t b_desc = ptx::smem_desc_sw128(ptx::smem_u32(q_s));
-      for (int c = 0; c < n_comp; ++c) {
-        const int s = c % S;
-        if (!wait_bounded(full0 + 8u * s, (c / S) & 1, abort_flag, &g_prefill_watchdog, kSiteStageFull)) break;
-        if (!wait_bounded(acce, (c & 1) ^ 1, abort_flag, &g_prefill_watchdog, kSiteAccEmpty)) break;
-        ptx::tc_fence_after();
-        const uint64_t a_desc = ptx::smem_desc_sw128(ptx::smem_u32(k_s + s * kKTileBytes));
+    const uint32_t idesc = ptx::idesc_e4m3_f32(kTileTokens, N);
+    int seg = -1, ci = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const Unit U = load_unit(p, u, num_rb, n_tiles);
+      ++seg;
+      if (lane == 0) ok = wait_bounded(qf0 + 8u * (seg & 1), (seg >> 1) & 1, abort_flag, &g_prefill_watchdog,
+                                       kSiteQFull);
+      if (lane == 0 && ok) {
+        const uint64_t b_desc = ptx::smem_desc_sw128(ptx::smem_u32(q_s + (seg & 1) * N * kHeadDim));
+        for (int k = 0; k < U.n_j; ++k) {
+          const int j = U.sidx + k * p.split;
+          if (!is_compute(U, j)) continue;
+          const int s = ci % S;
+          const int g = ci & 1;
+          if (!(ok = wait_bounded(full0 + 8u * s, (ci / S) & 1, abort_flag, &g_prefill_watchdog, kSiteStageFull)))
+            break;
+          if (!(ok = wait_bounded(acce0 + 8u * g, ((ci >> 1) & 1) ^ 1, abort_flag, &g_prefill_watchdog,
+                                  kSiteAccEmpty)))
+            break;
+          ptx::tc_fence_after();
+          const uint64_t a_desc = ptx::smem_desc_sw128(ptx::smem_u32(k_s + s * kKTileBytes));
+          const uint32_t d_tmem = tmem + g * 256u;
 #pragma unroll
-        for (int kk = 0; kk < kHeadDim / 32; ++kk)
-          ptx::mma_f8f6f4(tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, kk > 0 ? 1u : 0u);
-        ptx::mma_commit(empty0 + 8u * s);
-        ptx::mma_commit(accf);
+          for (int kk = 0; kk < kHeadDim / 32; ++kk)
+            ptx::mma_f8f6f4(d_tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, kk > 0 ? 1u : 0u);
+          ptx::mma_commit(empty0 + 8u * s);
+          ptx::mma_commit(accf0 + 8u * g);
+          ++ci;
+        }
+        ptx::mma_commit(qe0 + 8u * (seg & 1));
       }
-      if (*abort_flag) {
-        ptx::mma_commit(drain_bar);
-        wait_drain(drain_bar, 0, &g_prefill_watchdog);
-      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    }
+    if (lane == 0 && *abort_flag) {
+      ptx::mma_commit(drain_bar);
+      wait_drain(drain_bar, 0, &g_prefill_watchdog);
     }
   } else {
     // =========================== epilogue ===============================
-    const int et = threadIdx.x - 32 * kEpiWarp0;  // 0..127
-    const int quad = warp & 3;
-    const int row = quad * 32 + lane;             // token within the tile
-    const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const int ew = warp - kEpiWarp0;   // 0..7
+    const int grp = ew >> 2;           // half of the block's rows
+    const int et = threadIdx.x - 32 * (kEpiWarp0 + 4 * grp);  // 0..127 within the warpgroup
+    const int quad = warp & 3;         // TMEM lane quadrant
+    const int row = quad * 32 + lane;  // token within the tile
+    const int rows_per_grp = (BM + 1) >> 1;
+    const int r_begin = grp * rows_per_grp;
+    const int r_end = min(BM, r_begin + rows_per_grp);
+    const int nchunks = max(0, r_end - r_begin) * (HEADS / 32);  // <= 4
     const float ninf = __int_as_float(0xff800000);
-    int c = 0;  // computed-tile counter
-    for (int j = sidx; j < n_tiles; j += p.split) {
-      const int col0 = j * kTileTokens;
-      if (j >= t_lo && j < t_hi) {
-        const int s = c % S;
-        if (!warp_wait_bounded(accf, c & 1, abort_flag, &g_prefill_watchdog, kSiteAccFull)) break;
-        ptx::tc_fence_after();
-        if (!warp_wait_bounded(full0 + 8u * s, (c / S) & 1, abort_flag, &g_prefill_watchdog, kSiteStageFull)) break;
-        const float scale = sc_s[s * kTileTokens + row];
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(empty0 + 8u * s);
-        const int n = col0 + row;
-        for (int r = 0; r < BM; ++r) {
-          float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+    int seg = -1, ci = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const Unit U = load_unit(p, u, num_rb, n_tiles);
+      ++seg;
+      if (!(ok = warp_wait_bounded(qf0 + 8u * (seg & 1), (seg >> 1) & 1, abort_flag, &g_prefill_watchdog,
+                                   kSiteQFull)))
+        break;
+      const float* w = w_s + (seg & 1) * N + r_begin * HEADS;
+      for (int k = 0; k < U.n_j; ++k) {
+        const int j = U.sidx + k * p.split;
+        const int col0 = j * kTileTokens;
+        if (is_compute(U, j)) {
+          const int s = ci % S;
+          const int g = ci & 1;
+          if (!(ok = warp_wait_bounded(accf0 + 8u * g, (ci >> 1) & 1, abort_flag, &g_prefill_watchdog,
+                                       kSiteAccFull)))
+            break;
+          ptx::tc_fence_after();
+          if (!(ok = warp_wait_bounded(full0 + 8u * s, (ci / S) & 1, abort_flag, &g_prefill_watchdog,
+                                       kSiteStageFull)))
+            break;
+          const float scale = sc_s[s * kTileTokens + row];
+          const uint32_t tbase = tmem + g * 256u + (static_cast<uint32_t>(quad * 32) << 16) +
+                                 static_cast<uint32_t>(r_begin * HEADS);
+          uint32_t r[4][32];
 #pragma unroll
-          for (int hc = 0; hc < HEADS / 32; ++hc) {
-            uint32_t v[32];
-            ptx::tmem_ld_32x32b_x32(tbase + r * HEADS + hc * 32, v);
-            ptx::tmem_wait_ld();
-            relu_dot32(v, w_s + r * HEADS + hc * 32, a0, a1);
+          for (int c = 0; c < 4; ++c)
+            if (c < nchunks) ptx::tmem_ld_32x32b_x32(tbase + c * 32, r[c]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (c < nchunks) ptx::tmem_wait_ld_regs(r[c]);
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::mbar_arrive(acce0 + 8u * g);
+            ptx::mbar_arrive(empty0 + 8u * s);
           }
-          const int m = m0 + r;
-          if (m < p.rows && n < p.cols) {
-            const float logit = ((a0.x + a0.y) + (a1.x + a1.y)) * scale;
-            const bool inside = n >= row_lo[r] && n < row_hi[r];
-            __stcs(p.out + static_cast<int64_t>(m) * p.out_stride + n, inside ? logit : ninf);
+          const int n = col0 + row;
+#pragma unroll
+          for (int c0 = 0; c0 < 4; c0 += HEADS / 32) {
+            if (c0 < nchunks) {
+              float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+              for (int hc = 0; hc < HEADS / 32; ++hc) relu_dot32(r[c0 + hc], w + (c0 + hc) * 32, a0, a1);
+              const int rr = r_begin + c0 / (HEADS / 32);
+              const int lo = __shfl_sync(0xffffffffu, U.row_lo, rr);
+              const int hi = __shfl_sync(0xffffffffu, U.row_hi, rr);
+              const int m = U.m0 + rr;
+              const float logit = ((a0.x + a0.y) + (a1.x + a1.y)) * scale;
+              if (m < p.rows && n < p.cols)
+                __stcs(p.out + static_cast<int64_t>(m) * p.out_stride + n, (n >= lo && n < hi) ? logit : ninf);
+            }
           }
-        }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(acce);
-        ++c;
-      } else {
-        // pure -inf tile: rows of this block x 128 columns
-        const int ncols = min(kTileTokens, p.cols - col0);
-        if (p.vec_ok && ncols == kTileTokens) {
-          const float4 f4 = make_float4(ninf, ninf, ninf, ninf);
-          for (int e = et; e < BM * 32; e += 128) {
-            const int r = e >> 5, c4 = e & 31;
-            if (m0 + r < p.rows)
-              __stcs(reinterpret_cast<float4*>(p.out + static_cast<int64_t>(m0 + r) * p.out_stride + col0) + c4, f4);
-          }
+          ++ci;
         } else {
-          for (int r = 0; r < BM; ++r)
-            if (m0 + r < p.rows && row < ncols)
-              __stcs(p.out + static_cast<int64_t>(m0 + r) * p.out_stride + col0 + row, ninf);
+          // a tile no row of the block reaches: -inf for this warpgroup's rows
+          const int ncols = min(kTileTokens, p.cols - col0);
+          const int nr = r_end - r_begin;
+          if (p.vec_ok && ncols == kTileTokens) {
+            const float4 f4 = make_float4(ninf, ninf, ninf, ninf);
+            for (int e = et; e < nr * 32; e += 128) {
+              const int m = U.m0 + r_begin + (e >> 5);
+              if (m < p.rows)
+                __stcs(reinterpret_cast<float4*>(p.out + static_cast<int64_t>(m) * p.out_stride + col0) + (e & 31), f4);
+            }
+          } else {
+            for (int rr = r_begin; rr < r_end; ++rr) {
+              const int m = U.m0 + rr;
+              if (m < p.rows && row < ncols) __stcs(p.out + static_cast<int64_t>(m) * p.out_stride + col0 + row, ninf);
+            }
+          }
         }
       }
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(qe0 + 8u * (seg & 1));
     }
   }
 
@@ -235,19 +319,20 @@ __global__ void __launch_bounds__(prefill_threads(), 2)
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, tmem_cols);
+    ptx::tmem_dealloc(tmem, kTmemCols);
   }
 }
 
 cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_s,
-                           const PrefillParams& p, int heads, int grid, int smem_bytes, cudaStream_t stream) {
-  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, PrefillParams) = nullptr;
+                           const CUtensorMap& tm_w, const PrefillParams& p, int heads, int grid, int smem_bytes,
+                           cudaStream_t stream) {
+  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, PrefillParams) = nullptr;
   if (heads == 32) kern = mqa_logits_kernel<32>;
   else if (heads == 64) kern = mqa_logits_kernel<64>;
   else return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
-  kern<<<grid, prefill_threads(), smem_bytes, stream>>>(tm_q, tm_k, tm_s, p);
+  kern<<<grid, prefill_threads(), smem_bytes, stream>>>(tm_q, tm_k, tm_s, tm_w, p);
   return cudaGetLastError();
 }
 

@@ -26,12 +26,14 @@
 //    of next_n into the MMA asked for in aiter issue 5477, The ask).  Four
 //    K=32 e4m3 MMAs accumulate in f32 in tensor memory.  Q and the weights of
 //    the current and the next request are double-buffered.
-//  * Two epilogue warpgroups alternate over tiles (double-buffered TMEM
-//    accumulators).  Thread = token: tcgen05.ld a row of 32 head scores,
-//    ReLU, multiply by the weights, sum the heads, then multiply once by the
-//    token's kv_scale (the hoist of aiter PR 5047, Technical Details: scale
-//    >= 0 and ReLU is positive-homogeneous) and store if inside the causal
-//    window.  A warp stores 32 consecutive floats per row: coalesced 128 B.
+//  * Two epilogue warpgroups share every tile, each reducing half of the
+//    speculative rows; TMEM accumulators are double-buffered so the MMA of
+//    tile i+1 overlaps the epilogue of tile i.  Thread = token: all of its
+//    tcgen05.ld loads (<= 128 columns) are issued before one wait, then ReLU,
+//    multiply by the weights, sum the heads, multiply once by the token's
+//    kv_scale (the hoist of aiter PR 5047, Technical Details: scale >= 0 and
+//    ReLU is positive-homogeneous) and store if inside the causal window.  A
+//    warp stores 32 consecutive floats per row: coalesced 128 B.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -135,11 +137,11 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
     misc[1] = 0u;
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(full0 + 8u * s, GATHER ? 32u * kProdWarps : 1u);
-      ptx::mbar_init(empty0 + 8u * s, 1u + 4u);  // MMA commit + the 4 warps that read the scales
+      ptx::mbar_init(empty0 + 8u * s, 1u + 8u);  // MMA commit + the 8 epilogue warps (they read the scales)
     }
     for (int g = 0; g < 2; ++g) {
       ptx::mbar_init(accf0 + 8u * g, 1u);
-      ptx::mbar_init(acce0 + 8u * g, 4u);
+      ptx::mbar_init(acce0 + 8u * g, 8u);
       ptx::mbar_init(qf0 + 8u * g, 1u);
       ptx::mbar_init(qe0 + 8u * g, 1u + 8u);  // MMA commit + all 8 epilogue warps
     }
@@ -183,7 +185,7 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
 
   if (warp < kProdWarps) {
     // =========================== producer ===============================
-    int seg = -1;
+    int seg = -1, q_issued = 0;
     int issued = 0;
     int64_t ctx_eff = 0;
     if constexpr (!GATHER) {
@@ -206,6 +208,7 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
             ptx::bulk_g2s(ptx::smem_u32(w_s + (seg & 1) * N), p.weights + static_cast<int64_t>(cur.b) * N, N * 4,
                           qf);
           }
+          ++q_issued;
           ctx_eff = clamp_ctx(__ldg(p.context_lens + cur.b), p);
           need_blocks = (ctx_eff + blk - 1) / blk;
           chunk = (static_cast<int64_t>(cur.t) * P) & ~31ll;
@@ -242,16 +245,17 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
       if (*abort_flag && lane == 0) {  // let issued copies land before the CTA exits
         for (int it = max(0, issued - S); it < issued; ++it)
           wait_drain(full0 + 8u * (it % S), (it / S) & 1, &g_paged_watchdog);
-        for (int sg = max(0, seg - 1); sg <= seg; ++sg) wait_drain(qf0 + 8u * (sg & 1), (sg >> 1) & 1, &g_paged_watchdog);
+        for (int sg = max(0, q_issued - 2); sg < q_issued; ++sg) wait_drain(qf0 + 8u * (sg & 1), (sg >> 1) & 1, &g_paged_watchdog);
       }
     } else {
       // Block size 1: token p of request b is the 132-byte cache row
-      // block_tables[b][p].  Warp w gathers tokens [32w, 32w+32) of a tile:
-      // one token per instruction, lane l copying bytes [4l, 4l+4) into the
-      // 128-byte-swizzled row; lane l also copies token 32w+l's scale.
+      // block_tables[b][p].  Producer warp w gathers tokens [64w, 64w+64) of
+      // a tile, one token per instruction: lane l copies bytes [4l, 4l+4)
+      // into the 128-byte-swizzled row; lane l also copies the scales of
+      // tokens 64w+l and 64w+32+l.
       constexpr int kLag = 4;  // tiles in flight per thread before arriving
-      const int pw = warp;     // 0..3
-      int32_t slot_cur = 0, slot_nxt = 0;
+      const int pw = warp;     // 0..1
+      int32_t slot_a = 0, slot_b = 0, nxt_a = 0, nxt_b = 0;
       int pending = 0;
       for (int it = 0; it < n_items; ++it) {
         const bool new_seg = (it == 0) || (cur.t == 0);
@@ -276,14 +280,18 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
             ptx::bulk_g2s(ptx::smem_u32(w_s + (seg & 1) * N), p.weights + static_cast<int64_t>(cur.b) * N, N * 4,
                           qf);
           }
+          ++q_issued;
           ctx_eff = clamp_ctx(__ldg(p.context_lens + cur.b), p);
-          slot_cur = load_table(p, cur.b, static_cast<int64_t>(cur.t) * kTileTokens + pw * 32 + lane, ctx_eff);
+          const int64_t t0 = static_cast<int64_t>(cur.t) * kTileTokens + pw * 64 + lane;
+          slot_a = load_table(p, cur.b, t0, ctx_eff);
+          slot_b = load_table(p, cur.b, t0 + 32, ctx_eff);
         }
         // prefetch the next tile's slots (same request only)
-        const bool next_same = (cur.t + 1 < cur.tiles_b);
-        slot_nxt = next_same ? load_table(p, cur.b, static_cast<int64_t>(cur.t + 1) * kTileTokens + pw * 32 + lane,
-                                          ctx_eff)
-                             : 0;
+        if (cur.t + 1 < cur.tiles_b) {
+          const int64_t t1 = static_cast<int64_t>(cur.t + 1) * kTileTokens + pw * 64 + lane;
+          nxt_a = load_table(p, cur.b, t1, ctx_eff);
+          nxt_b = load_table(p, cur.b, t1 + 32, ctx_eff);
+        }
         const int s = it % S;
         if (!warp_wait_bounded(empty0 + 8u * s, ((it / S) & 1) ^ 1, abort_flag, &g_paged_watchdog,
                                kSiteStageEmpty))
@@ -294,19 +302,20 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
         const uint32_t chunk_in_row = static_cast<uint32_t>(lane >> 2);
         const uint32_t byte_in_chunk = static_cast<uint32_t>(lane & 3) * 4u;
 #pragma unroll 4
-        for (int j = 0; j < 32; ++j) {
-          const int tok = pw * 32 + j;
-          const int32_t sid = __shfl_sync(0xffffffffu, slot_cur, j);
+        for (int j = 0; j < 64; ++j) {
+          const int tok = pw * 64 + j;
+          const int32_t sid = __shfl_sync(0xffffffffu, j < 32 ? slot_a : slot_b, j & 31);
           if (tok < valid) {
             const int64_t row = clamp_block(sid, p.num_blocks);
             const uint32_t dst = tile_s + tok * kHeadDim + (((chunk_in_row ^ (tok & 7)) << 4) | byte_in_chunk);
             ptx::cp_async_4(dst, p.kv_cache + row * (kHeadDim + 4) + lane * 4);
           }
         }
-        {
-          const int tok = pw * 32 + lane;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int tok = pw * 64 + half * 32 + lane;
           if (tok < valid) {
-            const int64_t row = clamp_block(slot_cur, p.num_blocks);
+            const int64_t row = clamp_block(half ? slot_b : slot_a, p.num_blocks);
             ptx::cp_async_4(ptx::smem_u32(sc_s + s * kTileTokens + tok), p.kv_cache + row * (kHeadDim + 4) + kHeadDim);
           }
         }
@@ -320,14 +329,15 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
           ptx::mbar_arrive(full0 + 8u * (done % S));
           --pending;
         }
-        slot_cur = slot_nxt;
+        slot_a = nxt_a;
+        slot_b = nxt_b;
         cur.advance();
       }
       ptx::cp_async_wait<0>();
       ptx::fence_proxy_async_smem();
       for (int done = issued - pending; done < issued; ++done) ptx::mbar_arrive(full0 + 8u * (done % S));
       if (*abort_flag && pw == 0 && lane == 0)
-        for (int sg = max(0, seg - 1); sg <= seg; ++sg) wait_drain(qf0 + 8u * (sg & 1), (sg >> 1) & 1, &g_paged_watchdog);
+        for (int sg = max(0, q_issued - 2); sg < q_issued; ++sg) wait_drain(qf0 + 8u * (sg & 1), (sg >> 1) & 1, &g_paged_watchdog);
     }
   } else if (warp == kMmaWarp) {
     // ============================= MMA ==================================
@@ -365,11 +375,19 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
     }
   } else {
     // =========================== epilogue ===============================
+    // Both warpgroups work on every tile; warpgroup g reduces the speculative
+    // rows n in [n_begin, n_end).  A thread owns one token (TMEM lane): it
+    // issues all of its TMEM loads for the tile (<= 128 columns) before one
+    // wait, hands the accumulator and the stage back, then reduces.
     const int ew = warp - kEpiWarp0;  // 0..7
-    const int grp = ew >> 2;          // accumulator buffer this warpgroup owns
+    const int grp = ew >> 2;
     const int quad = warp & 3;        // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane; // token within the tile
     const int next_n = p.next_n;
+    const int rows_per_grp = (next_n + 1) >> 1;
+    const int n_begin = grp * rows_per_grp;
+    const int n_end = min(next_n, n_begin + rows_per_grp);
+    const int nchunks = max(0, n_end - n_begin) * (HEADS / 32);  // <= 4
     int seg = -1;
     int32_t ctx = 0;
     for (int it = 0; it < n_items; ++it) {
@@ -378,35 +396,42 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
         if (!warp_wait_bounded(qf0 + 8u * (seg & 1), (seg >> 1) & 1, abort_flag, &g_paged_watchdog, kSiteQFull)) break;
         ctx = __ldg(p.context_lens + cur.b);
       }
-      if ((it & 1) == grp) {
-        const int s = it % S;
-        if (!warp_wait_bounded(accf0 + 8u * grp, (it >> 1) & 1, abort_flag, &g_paged_watchdog, kSiteAccFull)) break;
-        ptx::tc_fence_after();
-        if (!warp_wait_bounded(full0 + 8u * s, (it / S) & 1, abort_flag, &g_paged_watchdog, kSiteStageFull)) break;
-        const float scale = sc_s[s * kTileTokens + row];
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(empty0 + 8u * s);
-
-        const float* w = w_s + (seg & 1) * N;
-        const uint32_t tbase = tmem + grp * p.acc_cols + (static_cast<uint32_t>(quad * 32) << 16);
-        const int64_t pos = static_cast<int64_t>(cur.t) * kTileTokens + row;
-        float* out_col = p.out + static_cast<int64_t>(cur.b) * next_n * p.out_stride + pos;
-        for (int n = 0; n < next_n; ++n) {
+      const int s = it % S;
+      const int g = it & 1;
+      if (!warp_wait_bounded(accf0 + 8u * g, (it >> 1) & 1, abort_flag, &g_paged_watchdog, kSiteAccFull)) break;
+      ptx::tc_fence_after();
+      if (!warp_wait_bounded(full0 + 8u * s, (it / S) & 1, abort_flag, &g_paged_watchdog, kSiteStageFull)) break;
+      const float scale = sc_s[s * kTileTokens + row];
+      const uint32_t tbase =
+          tmem + g * p.acc_cols + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(n_begin * HEADS);
+      uint32_t r[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (c < nchunks) ptx::tmem_ld_32x32b_x32(tbase + c * 32, r[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (c < nchunks) ptx::tmem_wait_ld_regs(r[c]);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(acce0 + 8u * g);
+        ptx::mbar_arrive(empty0 + 8u * s);
+      }
+      const float* w = w_s + (seg & 1) * N + n_begin * HEADS;
+      const int64_t pos = static_cast<int64_t>(cur.t) * kTileTokens + row;
+      const int64_t last = static_cast<int64_t>(ctx) - next_n;
+      float* out_col = p.out + (static_cast<int64_t>(cur.b) * next_n + n_begin) * p.out_stride + pos;
+#pragma unroll
+      for (int c0 = 0; c0 < 4; c0 += HEADS / 32) {
+        if (c0 < nchunks) {
           float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int hc = 0; hc < HEADS / 32; ++hc) {
-            uint32_t r[32];
-            ptx::tmem_ld_32x32b_x32(tbase + n * HEADS + hc * 32, r);
-            ptx::tmem_wait_ld();
-            relu_dot32(r, w + n * HEADS + hc * 32, a0, a1);
-          }
+          for (int hc = 0; hc < HEADS / 32; ++hc) relu_dot32(r[c0 + hc], w + (c0 + hc) * 32, a0, a1);
+          const int dn = c0 / (HEADS / 32);
           const float logit = ((a0.x + a0.y) + (a1.x + a1.y)) * scale;
-          if (pos <= static_cast<int64_t>(ctx) - next_n + n && pos < p.max_model_len)
-            __stcs(out_col + static_cast<int64_t>(n) * p.out_stride, logit);
+          if (pos <= last + n_begin + dn && pos < p.max_model_len)
+            __stcs(out_col + static_cast<int64_t>(dn) * p.out_stride, logit);
         }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(acce0 + 8u * grp);
       }
       const bool seg_end = cur.advance() || (it + 1 == n_items);
       if (seg_end) {

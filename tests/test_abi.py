@@ -60,13 +60,15 @@ def test_planner_decode(lib):
 def test_planner_prefill(lib):
     p = fp8idx.plan_prefill(4096, 32768, 32, 128, num_sms=148)
     assert p.block_m == 8 and p.tile_n == 256 and p.reverse_rows == 1
-    assert p.grid == 512 * p.split_n and p.split_n >= 2
-    assert 2 * p.smem_bytes <= 232448  # two CTAs per SM
+    assert p.grid == 148 and p.split_n >= 4  # persistent; >= 16 units per CTA
+    assert p.smem_bytes <= 232448 and p.stages >= 4
     p64 = fp8idx.plan_prefill(1000, 1000, 64, 128, num_sms=148)
     assert p64.block_m == 4 and p64.reverse_rows == 0
     o = fp8idx.plan_prefill(4096, 32768, 32, 128, num_sms=148,
                             options=fp8idx.Options(split_n=3, reverse_rows=0, block_m=2))
-    assert o.split_n == 3 and o.reverse_rows == 0 and o.tile_n == 64 and o.grid == 2048 * 3
+    assert o.split_n == 3 and o.reverse_rows == 0 and o.tile_n == 64 and o.grid == 148
+    small = fp8idx.plan_prefill(3, 100, 32, 128, num_sms=148)
+    assert small.grid == 1 and small.split_n == 1  # one row block, one column tile
     with pytest.raises(fp8idx.Fp8IdxError) as e:
         fp8idx.plan_prefill(10, 10, 32, 128, num_sms=148, options=fp8idx.Options(block_m=9))
     assert e.value.status == fp8idx.FP8IDX_ERR_UNSUPPORTED
