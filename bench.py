@@ -353,13 +353,15 @@ def run_ours(args, rank, world):
         with torch.cuda.graph(g, stream=stream):
             for _ in range(20):
                 call()
-        g.replay()
+        with torch.cuda.stream(stream):
+            g.replay()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(10):
-            g.replay()
-        e1.record(stream)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(10):
+                g.replay()
+            e1.record(stream)
         torch.cuda.synchronize()
         graph_us = e0.elapsed_time(e1) * 1e3 / 200
         del g
@@ -369,6 +371,8 @@ def run_ours(args, rank, world):
     # end to end from pinned host memory
     host_in = {k: torch.from_numpy(np.ascontiguousarray(getattr(case, k))).pin_memory() for k in step_inputs}
     host_out = torch.empty((out.shape[0], result_cols), dtype=torch.float32).pin_memory()
+    # the written columns, packed on the device, then one contiguous D2H copy
+    staging = torch.empty((out.shape[0], result_cols), dtype=torch.float32, device=dev)
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = host_out.numel() * 4
     e2e_steps = max(3, min(args.steps, 20))
@@ -381,7 +385,8 @@ def run_ours(args, rank, world):
             for k, t in host_in.items():
                 d[k].copy_(t, non_blocking=True)
             call()
-            host_out.copy_(out[:, :result_cols], non_blocking=True)
+            staging.copy_(out[:, :result_cols])
+            host_out.copy_(staging, non_blocking=True)
         e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)

@@ -11,7 +11,7 @@
 #include <mutex>
 #include <string>
 
-#include "../../include/fp8idx.h"
+#include "fp8idx.h"
 #include "kernels.h"
 
 namespace {
@@ -299,7 +299,7 @@ fp8idx_status paged_impl(const fp8idx_tensor* q, const fp8idx_tensor* kv, const 
   p.block_size = (int32_t)blk;
   p.n_cols = n_cols;
   p.stages = plan.stages;
-  p.acc_cols = n_cols > 128 ? 256 : 128;
+  p.acc_bufs = acc_buffers(n_cols);
   cudaError_t e = launch_paged(tm_q, tm_kv, p, (int)H, plan.gather != 0, plan.grid, plan.smem_bytes,
                                static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
@@ -374,6 +374,7 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const fp8idx_tensor* k, const
   p.split = plan.split_n;
   p.reverse = plan.reverse_rows;
   p.vec_ok = (aligned16(out->data) && (p.out_stride % 4) == 0) ? 1 : 0;
+  p.acc_bufs = acc_buffers(plan.tile_n);
   cudaError_t e = launch_prefill(tm_q, tm_k, tm_s, tm_w, p, (int)H, plan.grid, plan.smem_bytes,
                                  static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));

@@ -80,6 +80,42 @@ __device__ __forceinline__ void relu_dot32(const uint32_t (&r)[32], const float*
   }
 }
 
+// The epilogue's TMEM-to-register reduction for one tile and one thread's
+// token: output row k (k < nrows) is sum_h relu(acc[k*HEADS + h]) * w[k*HEADS + h]
+// over TMEM columns starting at `taddr`.  The 32-column loads are
+// double-buffered (chunk c+1 is in flight while chunk c is reduced); once the
+// last load has landed `release()` hands the accumulator back to the MMA warp,
+// and `emit(k, sum)` receives each finished row.  At most MAX_CHUNKS chunks.
+template <int HEADS, int MAX_CHUNKS, class Release, class Emit>
+__device__ __forceinline__ void reduce_rows(uint32_t taddr, const float* w, int nrows, Release release, Emit emit) {
+  constexpr int kChunksPerRow = HEADS / 32;
+  const int nchunks = nrows * kChunksPerRow;
+  uint32_t ra[32], rb[32];
+  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+  if (nchunks > 0)
+    ptx::tmem_ld_32x32b_x32(taddr, ra);
+  else
+    release();
+#pragma unroll
+  for (int c = 0; c < MAX_CHUNKS; ++c) {
+    if (c < nchunks) {
+      uint32_t(&cur)[32] = (c & 1) ? rb : ra;
+      uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
+      ptx::tmem_wait_ld_regs(cur);
+      if (c + 1 < nchunks)
+        ptx::tmem_ld_32x32b_x32(taddr + (c + 1) * 32, nxt);
+      else
+        release();
+      relu_dot32(cur, w + c * 32, a0, a1);
+      if ((c + 1) % kChunksPerRow == 0) {
+        emit(c / kChunksPerRow, (a0.x + a0.y) + (a1.x + a1.y));
+        a0 = make_float2(0.f, 0.f);
+        a1 = make_float2(0.f, 0.f);
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ uint8_t* align_up_1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
 }

@@ -33,12 +33,20 @@ struct PagedParams {
   int32_t block_size;
   int32_t n_cols;    // next_n * heads = MMA N
   int32_t stages;
-  int32_t acc_cols;  // TMEM columns per accumulator buffer
+  int32_t acc_bufs;  // TMEM accumulator buffers: 4 if n_cols <= 128, else 2
 };
 
-// Roles: producer warp(s), one MMA warp, two epilogue warpgroups.
+// Epilogue warpgroups.  Tiles are dealt round-robin to the accumulator
+// buffers; the kEpiGroups / acc_bufs warpgroups that serve one buffer split
+// the tile's output rows between them.
+constexpr int kEpiGroups = 4;
+__host__ __device__ constexpr int acc_buffers(int n_cols) { return n_cols <= 128 ? 4 : 2; }
+
+// Roles: producer warp(s), one MMA warp, kEpiGroups epilogue warpgroups.
 __host__ __device__ constexpr int paged_producer_warps(bool gather) { return gather ? 2 : 1; }
-__host__ __device__ constexpr int paged_threads(bool gather) { return 32 * (paged_producer_warps(gather) + 1 + 8); }
+__host__ __device__ constexpr int paged_threads(bool gather) {
+  return 32 * (paged_producer_warps(gather) + 1 + 4 * kEpiGroups);
+}
 
 struct PagedSmem {
   uint32_t q, k, scale, w, tp, bars, misc, total;
@@ -52,7 +60,7 @@ __host__ __device__ inline PagedSmem paged_smem_layout(int n_cols, int stages, i
   L.w = off;     off += 2u * n_cols * 4;                  // two weight rows
   L.tp = off;    off += (uint32_t)(batch + 1) * 4;        // per-request tile prefix
   off = (off + 7u) & ~7u;
-  L.bars = off;  off += 8u * (2u * stages + 9u);          // full/empty per stage, accf/acce/qf/qe x2, drain
+  L.bars = off;  off += 8u * (2u * stages + 13u);         // full/empty per stage, accf/acce x4, qf/qe x2, drain
   L.misc = off;  off += 32u;
   L.total = off + 1024u;                                  // slack for 1024-byte alignment
   return L;
@@ -72,10 +80,11 @@ struct PrefillParams {
   int32_t split;    // column-tile splits per row block (strided)
   int32_t reverse;  // 1: row blocks dealt from the last one
   int32_t vec_ok;   // out rows are 16-byte aligned: float4 -inf fill
+  int32_t acc_bufs; // TMEM accumulator buffers: 4 if n_cols <= 128, else 2
 };
 
-// Roles: producer warp, MMA warp, two epilogue warpgroups.
-__host__ __device__ constexpr int prefill_threads() { return 32 * (1 + 1 + 8); }
+// Roles: producer warp, MMA warp, kEpiGroups epilogue warpgroups.
+__host__ __device__ constexpr int prefill_threads() { return 32 * (1 + 1 + 4 * kEpiGroups); }
 
 struct PrefillSmem {
   uint32_t q, k, scale, w, bars, misc, total;
@@ -88,7 +97,7 @@ __host__ __device__ inline PrefillSmem prefill_smem_layout(int n_cols, int stage
   L.scale = off; off += (uint32_t)stages * kTileTokens * 4;
   L.w = off;     off += 2u * n_cols * 4;                    // two weight blocks
   off = (off + 7u) & ~7u;
-  L.bars = off;  off += 8u * (2u * stages + 9u);           // full/empty per stage, accf/acce/qf/qe x2, drain
+  L.bars = off;  off += 8u * (2u * stages + 13u);          // full/empty per stage, accf/acce x4, qf/qe x2, drain
   L.misc = off;  off += 32u;
   L.total = off + 1024u;
   return L;

@@ -19,10 +19,11 @@
 //    e4m3 tcgen05.mma into a double-buffered TMEM accumulator), the others are
 //    written with -inf directly.  Q and the weights are double-buffered
 //    across units.
-//  * Two epilogue warpgroups share every tile, each owning half of the
-//    block's rows; a thread owns one token: it loads its <= 128 accumulator
-//    columns, releases TMEM, applies ReLU * weight, sums the heads, scales by
-//    the token's kv_scale and stores the value or -inf per row.
+//  * Four epilogue warpgroups; computed tiles go round-robin to the TMEM
+//    accumulators (4, or 2 when block_m*heads > 128, then two warpgroups
+//    split the block's rows).  A thread owns one token: it reduces its rows
+//    out of TMEM with double-buffered loads, applies ReLU * weight, sums the
+//    heads, scales by the token's kv_scale and stores the value or -inf.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -104,11 +105,14 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
 
   const uint32_t full0 = ptx::smem_u32(bars);
   const uint32_t empty0 = full0 + 8u * S;
-  const uint32_t accf0 = empty0 + 8u * S;
-  const uint32_t acce0 = accf0 + 16u;
-  const uint32_t qf0 = acce0 + 16u;
-  const uint32_t qe0 = qf0 + 16u;
+  const uint32_t accf0 = empty0 + 8u * S;  // [4]
+  const uint32_t acce0 = accf0 + 32u;      // [4]
+  const uint32_t qf0 = acce0 + 32u;        // [2]
+  const uint32_t qe0 = qf0 + 16u;          // [2]
   const uint32_t drain_bar = qe0 + 16u;
+  const int AB = p.acc_bufs;
+  const uint32_t acc_cols = kTmemCols / AB;
+  const uint32_t epi_per_buf = 4u * kEpiGroups / AB;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -120,13 +124,15 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
     misc[1] = 0u;
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(full0 + 8u * s, 1u);
-      ptx::mbar_init(empty0 + 8u * s, 1u + 8u);  // MMA commit + 8 epilogue warps (scales)
+      ptx::mbar_init(empty0 + 8u * s, 1u + epi_per_buf);  // MMA commit + the warps that read the scales
+    }
+    for (int g = 0; g < 4; ++g) {
+      ptx::mbar_init(accf0 + 8u * g, 1u);
+      ptx::mbar_init(acce0 + 8u * g, epi_per_buf);
     }
     for (int g = 0; g < 2; ++g) {
-      ptx::mbar_init(accf0 + 8u * g, 1u);
-      ptx::mbar_init(acce0 + 8u * g, 8u);
       ptx::mbar_init(qf0 + 8u * g, 1u);
-      ptx::mbar_init(qe0 + 8u * g, 1u + 8u);
+      ptx::mbar_init(qe0 + 8u * g, 1u + 4u * kEpiGroups);
     }
     ptx::mbar_init(drain_bar, 1u);
     ptx::fence_barrier_init();
@@ -199,15 +205,15 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
           const int j = U.sidx + k * p.split;
           if (!is_compute(U, j)) continue;
           const int s = ci % S;
-          const int g = ci & 1;
+          const int g = ci % AB;
           if (!(ok = wait_bounded(full0 + 8u * s, (ci / S) & 1, abort_flag, &g_prefill_watchdog, kSiteStageFull)))
             break;
-          if (!(ok = wait_bounded(acce0 + 8u * g, ((ci >> 1) & 1) ^ 1, abort_flag, &g_prefill_watchdog,
+          if (!(ok = wait_bounded(acce0 + 8u * g, ((ci / AB) & 1) ^ 1, abort_flag, &g_prefill_watchdog,
                                   kSiteAccEmpty)))
             break;
           ptx::tc_fence_after();
           const uint64_t a_desc = ptx::smem_desc_sw128(ptx::smem_u32(k_s + s * kKTileBytes));
-          const uint32_t d_tmem = tmem + g * 256u;
+          const uint32_t d_tmem = tmem + g * acc_cols;
 #pragma unroll
           for (int kk = 0; kk < kHeadDim / 32; ++kk)
             ptx::mma_f8f6f4(d_tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, kk > 0 ? 1u : 0u);
@@ -225,17 +231,22 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
     }
   } else {
     // =========================== epilogue ===============================
-    const int ew = warp - kEpiWarp0;   // 0..7
-    const int grp = ew >> 2;           // half of the block's rows
-    const int et = threadIdx.x - 32 * (kEpiWarp0 + 4 * grp);  // 0..127 within the warpgroup
+    // Computed tile ci goes to accumulator buffer ci % AB, served by the
+    // kEpiGroups / AB warpgroups of that buffer, which split the block's
+    // rows; pure -inf tiles are dealt round-robin to the warpgroups.
+    const int ew = warp - kEpiWarp0;   // 0 .. 4*kEpiGroups-1
+    const int grp = ew >> 2;
+    const int et = (ew & 3) * 32 + lane;  // 0..127 within the warpgroup
     const int quad = warp & 3;         // TMEM lane quadrant
     const int row = quad * 32 + lane;  // token within the tile
-    const int rows_per_grp = (BM + 1) >> 1;
-    const int r_begin = grp * rows_per_grp;
-    const int r_end = min(BM, r_begin + rows_per_grp);
-    const int nchunks = max(0, r_end - r_begin) * (HEADS / 32);  // <= 4
+    const int parts = kEpiGroups / AB;
+    const int my_buf = grp / parts;
+    const int part = grp % parts;
+    const int rows_per_part = (BM + parts - 1) / parts;
+    const int r_begin = part * rows_per_part;
+    const int nrows = max(0, min(BM, r_begin + rows_per_part) - r_begin);
     const float ninf = __int_as_float(0xff800000);
-    int seg = -1, ci = 0;
+    int seg = -1, ci = 0, fi = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const Unit U = load_unit(p, u, num_rb, n_tiles);
@@ -243,66 +254,56 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
       if (!(ok = warp_wait_bounded(qf0 + 8u * (seg & 1), (seg >> 1) & 1, abort_flag, &g_prefill_watchdog,
                                    kSiteQFull)))
         break;
-      const float* w = w_s + (seg & 1) * N + r_begin * HEADS;
       for (int k = 0; k < U.n_j; ++k) {
         const int j = U.sidx + k * p.split;
         const int col0 = j * kTileTokens;
         if (is_compute(U, j)) {
-          const int s = ci % S;
-          const int g = ci & 1;
-          if (!(ok = warp_wait_bounded(accf0 + 8u * g, (ci >> 1) & 1, abort_flag, &g_prefill_watchdog,
-                                       kSiteAccFull)))
-            break;
-          ptx::tc_fence_after();
-          if (!(ok = warp_wait_bounded(full0 + 8u * s, (ci / S) & 1, abort_flag, &g_prefill_watchdog,
+          const int c = ci++;
+          if (c % AB != my_buf) continue;
+          const int s = c % S;
+          if (!(ok = warp_wait_bounded(full0 + 8u * s, (c / S) & 1, abort_flag, &g_prefill_watchdog,
                                        kSiteStageFull)))
             break;
           const float scale = sc_s[s * kTileTokens + row];
-          const uint32_t tbase = tmem + g * 256u + (static_cast<uint32_t>(quad * 32) << 16) +
-                                 static_cast<uint32_t>(r_begin * HEADS);
-          uint32_t r[4][32];
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            if (c < nchunks) ptx::tmem_ld_32x32b_x32(tbase + c * 32, r[c]);
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            if (c < nchunks) ptx::tmem_wait_ld_regs(r[c]);
-          ptx::tc_fence_before();
           __syncwarp();
-          if (lane == 0) {
-            ptx::mbar_arrive(acce0 + 8u * g);
-            ptx::mbar_arrive(empty0 + 8u * s);
-          }
+          if (lane == 0) ptx::mbar_arrive(empty0 + 8u * s);
+          if (!(ok = warp_wait_bounded(accf0 + 8u * my_buf, (c / AB) & 1, abort_flag, &g_prefill_watchdog,
+                                       kSiteAccFull)))
+            break;
+          ptx::tc_fence_after();
+          const uint32_t taddr = tmem + my_buf * acc_cols + (static_cast<uint32_t>(quad * 32) << 16) +
+                                 static_cast<uint32_t>(r_begin * HEADS);
           const int n = col0 + row;
-#pragma unroll
-          for (int c0 = 0; c0 < 4; c0 += HEADS / 32) {
-            if (c0 < nchunks) {
-              float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
-#pragma unroll
-              for (int hc = 0; hc < HEADS / 32; ++hc) relu_dot32(r[c0 + hc], w + (c0 + hc) * 32, a0, a1);
-              const int rr = r_begin + c0 / (HEADS / 32);
-              const int lo = __shfl_sync(0xffffffffu, U.row_lo, rr);
-              const int hi = __shfl_sync(0xffffffffu, U.row_hi, rr);
-              const int m = U.m0 + rr;
-              const float logit = ((a0.x + a0.y) + (a1.x + a1.y)) * scale;
-              if (m < p.rows && n < p.cols)
-                __stcs(p.out + static_cast<int64_t>(m) * p.out_stride + n, (n >= lo && n < hi) ? logit : ninf);
-            }
-          }
-          ++ci;
+          const uint32_t acce = acce0 + 8u * my_buf;
+          reduce_rows<HEADS, 4>(
+              taddr, w_s + (seg & 1) * N + r_begin * HEADS, nrows,
+              [&]() {
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(acce);
+              },
+              [&](int kr, float v) {
+                const int rr = r_begin + kr;
+                const int lo = __shfl_sync(0xffffffffu, U.row_lo, rr);
+                const int hi = __shfl_sync(0xffffffffu, U.row_hi, rr);
+                const int m = U.m0 + rr;
+                if (m < p.rows && n < p.cols)
+                  __stcs(p.out + static_cast<int64_t>(m) * p.out_stride + n, (n >= lo && n < hi) ? v * scale : ninf);
+              });
         } else {
-          // a tile no row of the block reaches: -inf for this warpgroup's rows
+          // a tile no row of the block reaches: -inf for all the block's rows
+          const int f = fi++;
+          if (f % kEpiGroups != grp) continue;
           const int ncols = min(kTileTokens, p.cols - col0);
-          const int nr = r_end - r_begin;
           if (p.vec_ok && ncols == kTileTokens) {
             const float4 f4 = make_float4(ninf, ninf, ninf, ninf);
-            for (int e = et; e < nr * 32; e += 128) {
-              const int m = U.m0 + r_begin + (e >> 5);
+            for (int e = et; e < BM * 32; e += 128) {
+              const int m = U.m0 + (e >> 5);
               if (m < p.rows)
                 __stcs(reinterpret_cast<float4*>(p.out + static_cast<int64_t>(m) * p.out_stride + col0) + (e & 31), f4);
             }
           } else {
-            for (int rr = r_begin; rr < r_end; ++rr) {
+            for (int rr = 0; rr < BM; ++rr) {
               const int m = U.m0 + rr;
               if (m < p.rows && row < ncols) __stcs(p.out + static_cast<int64_t>(m) * p.out_stride + col0 + row, ninf);
             }

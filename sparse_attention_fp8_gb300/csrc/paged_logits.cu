@@ -26,14 +26,14 @@
 //    of next_n into the MMA asked for in aiter issue 5477, The ask).  Four
 //    K=32 e4m3 MMAs accumulate in f32 in tensor memory.  Q and the weights of
 //    the current and the next request are double-buffered.
-//  * Two epilogue warpgroups share every tile, each reducing half of the
-//    speculative rows; TMEM accumulators are double-buffered so the MMA of
-//    tile i+1 overlaps the epilogue of tile i.  Thread = token: all of its
-//    tcgen05.ld loads (<= 128 columns) are issued before one wait, then ReLU,
-//    multiply by the weights, sum the heads, multiply once by the token's
-//    kv_scale (the hoist of aiter PR 5047, Technical Details: scale >= 0 and
-//    ReLU is positive-homogeneous) and store if inside the causal window.  A
-//    warp stores 32 consecutive floats per row: coalesced 128 B.
+//  * Four epilogue warpgroups.  Tensor memory holds 4 accumulators (2 when
+//    next_n*heads > 128); tiles go round-robin to them, so up to four tiles
+//    are in the epilogue at once, and the warpgroups serving one buffer split
+//    its rows.  Thread = token: 32-column tcgen05.ld loads, double-buffered,
+//    then ReLU, multiply by the weights, sum the heads, multiply once by the
+//    token's kv_scale (the hoist of aiter PR 5047, Technical Details: scale
+//    >= 0 and ReLU is positive-homogeneous) and store if inside the causal
+//    window.  A warp stores 32 consecutive floats per row: coalesced 128 B.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -118,11 +118,14 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
 
   const uint32_t full0 = ptx::smem_u32(bars);
   const uint32_t empty0 = full0 + 8u * S;
-  const uint32_t accf0 = empty0 + 8u * S;
-  const uint32_t acce0 = accf0 + 16u;
-  const uint32_t qf0 = acce0 + 16u;
-  const uint32_t qe0 = qf0 + 16u;
+  const uint32_t accf0 = empty0 + 8u * S;  // [4]
+  const uint32_t acce0 = accf0 + 32u;      // [4]
+  const uint32_t qf0 = acce0 + 32u;        // [2]
+  const uint32_t qe0 = qf0 + 16u;          // [2]
   const uint32_t drain_bar = qe0 + 16u;
+  const int AB = p.acc_bufs;                        // accumulator buffers (2 or 4)
+  const uint32_t acc_cols = kTmemCols / AB;         // columns per buffer
+  const uint32_t epi_per_buf = 4u * kEpiGroups / AB;  // epilogue warps serving one buffer
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -137,13 +140,15 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
     misc[1] = 0u;
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(full0 + 8u * s, GATHER ? 32u * kProdWarps : 1u);
-      ptx::mbar_init(empty0 + 8u * s, 1u + 8u);  // MMA commit + the 8 epilogue warps (they read the scales)
+      ptx::mbar_init(empty0 + 8u * s, 1u + epi_per_buf);  // MMA commit + the warps that read the tile's scales
+    }
+    for (int g = 0; g < 4; ++g) {
+      ptx::mbar_init(accf0 + 8u * g, 1u);
+      ptx::mbar_init(acce0 + 8u * g, epi_per_buf);
     }
     for (int g = 0; g < 2; ++g) {
-      ptx::mbar_init(accf0 + 8u * g, 1u);
-      ptx::mbar_init(acce0 + 8u * g, 8u);
       ptx::mbar_init(qf0 + 8u * g, 1u);
-      ptx::mbar_init(qe0 + 8u * g, 1u + 8u);  // MMA commit + all 8 epilogue warps
+      ptx::mbar_init(qe0 + 8u * g, 1u + 4u * kEpiGroups);  // MMA commit + every epilogue warp
     }
     ptx::mbar_init(drain_bar, 1u);
     ptx::fence_barrier_init();
@@ -352,14 +357,14 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
             break;
         }
         const int s = it % S;
-        const int g = it & 1;
+        const int g = it % AB;
         if (!(ok = wait_bounded(full0 + 8u * s, (it / S) & 1, abort_flag, &g_paged_watchdog, kSiteStageFull))) break;
-        if (!(ok = wait_bounded(acce0 + 8u * g, ((it >> 1) & 1) ^ 1, abort_flag, &g_paged_watchdog, kSiteAccEmpty)))
+        if (!(ok = wait_bounded(acce0 + 8u * g, ((it / AB) & 1) ^ 1, abort_flag, &g_paged_watchdog, kSiteAccEmpty)))
           break;
         ptx::tc_fence_after();
         const uint64_t a_desc = ptx::smem_desc_sw128(ptx::smem_u32(k_s + s * kKTileBytes));
         const uint64_t b_desc = ptx::smem_desc_sw128(ptx::smem_u32(q_s + (seg & 1) * N * kHeadDim));
-        const uint32_t d_tmem = tmem + g * p.acc_cols;
+        const uint32_t d_tmem = tmem + g * acc_cols;
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 32; ++kk)  // K = 32 e4m3 per MMA: advance 32 bytes in the swizzled row
           ptx::mma_f8f6f4(d_tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, kk > 0 ? 1u : 0u);
@@ -375,19 +380,22 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
     }
   } else {
     // =========================== epilogue ===============================
-    // Both warpgroups work on every tile; warpgroup g reduces the speculative
-    // rows n in [n_begin, n_end).  A thread owns one token (TMEM lane): it
-    // issues all of its TMEM loads for the tile (<= 128 columns) before one
-    // wait, hands the accumulator and the stage back, then reduces.
-    const int ew = warp - kEpiWarp0;  // 0..7
+    // kEpiGroups warpgroups.  Tile it goes to accumulator buffer it % AB and
+    // is served by the kEpiGroups / AB warpgroups of that buffer, which split
+    // its speculative rows.  Thread = token (TMEM lane): read the token's
+    // scale and free the stage, then reduce its rows out of TMEM with
+    // double-buffered loads, releasing the accumulator after the last load.
+    const int ew = warp - kEpiWarp0;      // 0 .. 4*kEpiGroups-1
     const int grp = ew >> 2;
-    const int quad = warp & 3;        // TMEM lane quadrant this warp may access
-    const int row = quad * 32 + lane; // token within the tile
+    const int quad = warp & 3;            // TMEM lane quadrant this warp may access
+    const int row = quad * 32 + lane;     // token within the tile
     const int next_n = p.next_n;
-    const int rows_per_grp = (next_n + 1) >> 1;
-    const int n_begin = grp * rows_per_grp;
-    const int n_end = min(next_n, n_begin + rows_per_grp);
-    const int nchunks = max(0, n_end - n_begin) * (HEADS / 32);  // <= 4
+    const int parts = kEpiGroups / AB;    // warpgroups per tile
+    const int my_buf = grp / parts;
+    const int part = grp % parts;
+    const int rows_per_part = (next_n + parts - 1) / parts;
+    const int n_begin = part * rows_per_part;
+    const int nrows = max(0, min(next_n, n_begin + rows_per_part) - n_begin);
     int seg = -1;
     int32_t ctx = 0;
     for (int it = 0; it < n_items; ++it) {
@@ -396,42 +404,32 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
         if (!warp_wait_bounded(qf0 + 8u * (seg & 1), (seg >> 1) & 1, abort_flag, &g_paged_watchdog, kSiteQFull)) break;
         ctx = __ldg(p.context_lens + cur.b);
       }
-      const int s = it % S;
-      const int g = it & 1;
-      if (!warp_wait_bounded(accf0 + 8u * g, (it >> 1) & 1, abort_flag, &g_paged_watchdog, kSiteAccFull)) break;
-      ptx::tc_fence_after();
-      if (!warp_wait_bounded(full0 + 8u * s, (it / S) & 1, abort_flag, &g_paged_watchdog, kSiteStageFull)) break;
-      const float scale = sc_s[s * kTileTokens + row];
-      const uint32_t tbase =
-          tmem + g * p.acc_cols + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(n_begin * HEADS);
-      uint32_t r[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        if (c < nchunks) ptx::tmem_ld_32x32b_x32(tbase + c * 32, r[c]);
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        if (c < nchunks) ptx::tmem_wait_ld_regs(r[c]);
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        ptx::mbar_arrive(acce0 + 8u * g);
-        ptx::mbar_arrive(empty0 + 8u * s);
-      }
-      const float* w = w_s + (seg & 1) * N + n_begin * HEADS;
-      const int64_t pos = static_cast<int64_t>(cur.t) * kTileTokens + row;
-      const int64_t last = static_cast<int64_t>(ctx) - next_n;
-      float* out_col = p.out + (static_cast<int64_t>(cur.b) * next_n + n_begin) * p.out_stride + pos;
-#pragma unroll
-      for (int c0 = 0; c0 < 4; c0 += HEADS / 32) {
-        if (c0 < nchunks) {
-          float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int hc = 0; hc < HEADS / 32; ++hc) relu_dot32(r[c0 + hc], w + (c0 + hc) * 32, a0, a1);
-          const int dn = c0 / (HEADS / 32);
-          const float logit = ((a0.x + a0.y) + (a1.x + a1.y)) * scale;
-          if (pos <= last + n_begin + dn && pos < p.max_model_len)
-            __stcs(out_col + static_cast<int64_t>(dn) * p.out_stride, logit);
-        }
+      if (it % AB == my_buf) {
+        const int s = it % S;
+        if (!warp_wait_bounded(full0 + 8u * s, (it / S) & 1, abort_flag, &g_paged_watchdog, kSiteStageFull)) break;
+        const float scale = sc_s[s * kTileTokens + row];
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(empty0 + 8u * s);
+        if (!warp_wait_bounded(accf0 + 8u * my_buf, (it / AB) & 1, abort_flag, &g_paged_watchdog, kSiteAccFull))
+          break;
+        ptx::tc_fence_after();
+        const uint32_t taddr = tmem + my_buf * acc_cols + (static_cast<uint32_t>(quad * 32) << 16) +
+                               static_cast<uint32_t>(n_begin * HEADS);
+        const int64_t pos = static_cast<int64_t>(cur.t) * kTileTokens + row;
+        const int64_t last = static_cast<int64_t>(ctx) - next_n + n_begin;
+        float* out_col = p.out + (static_cast<int64_t>(cur.b) * next_n + n_begin) * p.out_stride + pos;
+        const uint32_t acce = acce0 + 8u * my_buf;
+        reduce_rows<HEADS, 4>(
+            taddr, w_s + (seg & 1) * N + n_begin * HEADS, nrows,
+            [&]() {
+              ptx::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) ptx::mbar_arrive(acce);
+            },
+            [&](int k, float v) {
+              if (pos <= last + k && pos < p.max_model_len)
+                __stcs(out_col + static_cast<int64_t>(k) * p.out_stride, v * scale);
+            });
       }
       const bool seg_end = cur.advance() || (it + 1 == n_items);
       if (seg_end) {
