@@ -267,7 +267,7 @@ fp8idx_status paged_impl(const fp8idx_tensor* q, const fp8idx_tensor* kv, const 
   TRY(plan_paged((int)B, (int)next_n, (int)H, (int)D, (int)blk, max_model_len, dev.sms, dev.smem_optin, opts, &plan));
 
   const int n_cols = (int)(next_n * H);
-  CUtensorMap tm_q, tm_kv;
+  CUtensorMap tm_q, tm_kv, tm_sc;
   {
     const uint64_t dims[2] = {(uint64_t)D, (uint64_t)(B * n_cols)};
     const uint64_t strides[1] = {(uint64_t)D};
@@ -275,13 +275,20 @@ fp8idx_status paged_impl(const fp8idx_tensor* q, const fp8idx_tensor* kv, const 
     TRY(encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q->data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "q"));
   }
   if (!plan.gather) {
+    // K rows: [block][row][128 B]; scales: [block][blk f32], starting after the block's K rows
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)blk, (uint64_t)kv->shape[0]};
     const uint64_t strides[2] = {(uint64_t)D, (uint64_t)kv->shape[1]};
     const uint32_t box[3] = {(uint32_t)D, (uint32_t)blk, 1u};
     TRY(encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, kv->data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
                "kv_cache"));
+    const uint64_t sdims[2] = {(uint64_t)blk, (uint64_t)kv->shape[0]};
+    const uint64_t sstrides[1] = {(uint64_t)kv->shape[1]};
+    const uint32_t sbox[2] = {(uint32_t)blk, 1u};
+    TRY(encode(&tm_sc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, static_cast<const uint8_t*>(kv->data) + blk * D, sdims,
+               sstrides, sbox, CU_TENSOR_MAP_SWIZZLE_NONE, "kv_cache scales"));
   } else {
     tm_kv = tm_q;  // unused by the gather kernel
+    tm_sc = tm_q;
   }
   PagedParams p;
   p.kv_cache = static_cast<const uint8_t*>(kv->data);
@@ -299,8 +306,8 @@ fp8idx_status paged_impl(const fp8idx_tensor* q, const fp8idx_tensor* kv, const 
   p.block_size = (int32_t)blk;
   p.n_cols = n_cols;
   p.stages = plan.stages;
-  p.acc_bufs = acc_buffers(n_cols);
-  cudaError_t e = launch_paged(tm_q, tm_kv, p, (int)H, plan.gather != 0, plan.grid, plan.smem_bytes,
+  p.acc_bufs = paged_acc_buffers(n_cols);
+  cudaError_t e = launch_paged(tm_q, tm_kv, tm_sc, p, (int)H, plan.gather != 0, plan.grid, plan.smem_bytes,
                                static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
   return ok();
@@ -374,7 +381,7 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const fp8idx_tensor* k, const
   p.split = plan.split_n;
   p.reverse = plan.reverse_rows;
   p.vec_ok = (aligned16(out->data) && (p.out_stride % 4) == 0) ? 1 : 0;
-  p.acc_bufs = acc_buffers(plan.tile_n);
+  p.acc_bufs = paged_acc_buffers(plan.tile_n);
   cudaError_t e = launch_prefill(tm_q, tm_k, tm_s, tm_w, p, (int)H, plan.grid, plan.smem_bytes,
                                  static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));

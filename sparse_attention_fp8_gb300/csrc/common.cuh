@@ -65,32 +65,45 @@ __device__ __forceinline__ bool warp_wait_bounded(uint32_t bar, uint32_t parity,
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// Index and phase of a ring of `n` mbarrier-guarded slots, advanced by one
+// slot per use (no division on the per-tile path).
+struct Ring {
+  uint32_t idx, phase, n;
+  __device__ __forceinline__ void next() {
+    if (++idx == n) {
+      idx = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 // acc0 + acc1 += sum_{j<32} relu(x_j) * w_j for one 32-column TMEM chunk in
-// registers; w points at 32 f32 weights in shared memory (16-byte aligned,
-// read as broadcast float4).  Two packed f32x2 accumulators.
-__device__ __forceinline__ void relu_dot32(const uint32_t (&r)[32], const float* w, float2& acc0, float2& acc1) {
-  const float4* w4 = reinterpret_cast<const float4*>(w);
+// registers and its 32 weights in registers.  Two packed f32x2 accumulators.
+__device__ __forceinline__ void relu_dot32(const uint32_t (&r)[32], const float4 (&wv)[8], float2& acc0,
+                                           float2& acc1) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const float4 ww = w4[j];
     const float2 x01 = make_float2(fmaxf(__uint_as_float(r[4 * j + 0]), 0.f), fmaxf(__uint_as_float(r[4 * j + 1]), 0.f));
     const float2 x23 = make_float2(fmaxf(__uint_as_float(r[4 * j + 2]), 0.f), fmaxf(__uint_as_float(r[4 * j + 3]), 0.f));
-    acc0 = __ffma2_rn(x01, make_float2(ww.x, ww.y), acc0);
-    acc1 = __ffma2_rn(x23, make_float2(ww.z, ww.w), acc1);
+    acc0 = __ffma2_rn(x01, make_float2(wv[j].x, wv[j].y), acc0);
+    acc1 = __ffma2_rn(x23, make_float2(wv[j].z, wv[j].w), acc1);
   }
 }
 
 // The epilogue's TMEM-to-register reduction for one tile and one thread's
 // token: output row k (k < nrows) is sum_h relu(acc[k*HEADS + h]) * w[k*HEADS + h]
 // over TMEM columns starting at `taddr`.  The 32-column loads are
-// double-buffered (chunk c+1 is in flight while chunk c is reduced); once the
-// last load has landed `release()` hands the accumulator back to the MMA warp,
-// and `emit(k, sum)` receives each finished row.  At most MAX_CHUNKS chunks.
+// double-buffered (chunk c+1 is in flight while chunk c is reduced) and each
+// chunk's 32 weights are read from shared memory (broadcast) before waiting
+// on its data; once the last load has landed `release()` hands the
+// accumulator back to the MMA warp, and `emit(k, sum)` receives each finished
+// row.  At most MAX_CHUNKS chunks.
 template <int HEADS, int MAX_CHUNKS, class Release, class Emit>
 __device__ __forceinline__ void reduce_rows(uint32_t taddr, const float* w, int nrows, Release release, Emit emit) {
   constexpr int kChunksPerRow = HEADS / 32;
   const int nchunks = nrows * kChunksPerRow;
   uint32_t ra[32], rb[32];
+  float4 wv[8];
   float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
   if (nchunks > 0)
     ptx::tmem_ld_32x32b_x32(taddr, ra);
@@ -101,12 +114,15 @@ __device__ __forceinline__ void reduce_rows(uint32_t taddr, const float* w, int 
     if (c < nchunks) {
       uint32_t(&cur)[32] = (c & 1) ? rb : ra;
       uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
+      const float4* w4 = reinterpret_cast<const float4*>(w + c * 32);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) wv[j] = w4[j];
       ptx::tmem_wait_ld_regs(cur);
       if (c + 1 < nchunks)
         ptx::tmem_ld_32x32b_x32(taddr + (c + 1) * 32, nxt);
       else
         release();
-      relu_dot32(cur, w + c * 32, a0, a1);
+      relu_dot32(cur, wv, a0, a1);
       if ((c + 1) % kChunksPerRow == 0) {
         emit(c / kChunksPerRow, (a0.x + a0.y) + (a1.x + a1.y));
         a0 = make_float2(0.f, 0.f);

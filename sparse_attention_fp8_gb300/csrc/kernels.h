@@ -33,14 +33,17 @@ struct PagedParams {
   int32_t block_size;
   int32_t n_cols;    // next_n * heads = MMA N
   int32_t stages;
-  int32_t acc_bufs;  // TMEM accumulator buffers: 4 if n_cols <= 128, else 2
+  int32_t acc_bufs;  // TMEM accumulator buffers: paged_acc_buffers(n_cols)
 };
 
-// Epilogue warpgroups.  Tiles are dealt round-robin to the accumulator
-// buffers; the kEpiGroups / acc_bufs warpgroups that serve one buffer split
-// the tile's output rows between them.
-constexpr int kEpiGroups = 4;
-__host__ __device__ constexpr int acc_buffers(int n_cols) { return n_cols <= 128 ? 4 : 2; }
+// Two epilogue warpgroups take alternate tiles; tensor memory holds 2..16
+// accumulators (512 columns in buffers of the smallest power of two >=
+// n_cols), so the MMA warp can run that many tiles ahead of the epilogue.
+constexpr int kEpiGroups = 2;
+constexpr int kMaxAccBufs = 16;
+__host__ __device__ constexpr int paged_acc_buffers(int n_cols) {
+  return n_cols <= 32 ? 16 : n_cols <= 64 ? 8 : n_cols <= 128 ? 4 : 2;
+}
 
 // Roles: producer warp(s), one MMA warp, kEpiGroups epilogue warpgroups.
 __host__ __device__ constexpr int paged_producer_warps(bool gather) { return gather ? 2 : 1; }
@@ -60,7 +63,7 @@ __host__ __device__ inline PagedSmem paged_smem_layout(int n_cols, int stages, i
   L.w = off;     off += 2u * n_cols * 4;                  // two weight rows
   L.tp = off;    off += (uint32_t)(batch + 1) * 4;        // per-request tile prefix
   off = (off + 7u) & ~7u;
-  L.bars = off;  off += 8u * (2u * stages + 13u);         // full/empty per stage, accf/acce x4, qf/qe x2, drain
+  L.bars = off;  off += 8u * (2u * stages + 2u * kMaxAccBufs + 5u);  // full/empty per stage, accf/acce, qf/qe x2, drain
   L.misc = off;  off += 32u;
   L.total = off + 1024u;                                  // slack for 1024-byte alignment
   return L;
@@ -80,7 +83,7 @@ struct PrefillParams {
   int32_t split;    // column-tile splits per row block (strided)
   int32_t reverse;  // 1: row blocks dealt from the last one
   int32_t vec_ok;   // out rows are 16-byte aligned: float4 -inf fill
-  int32_t acc_bufs; // TMEM accumulator buffers: 4 if n_cols <= 128, else 2
+  int32_t acc_bufs; // TMEM accumulator buffers: paged_acc_buffers(n_cols)
 };
 
 // Roles: producer warp, MMA warp, kEpiGroups epilogue warpgroups.
@@ -97,7 +100,7 @@ __host__ __device__ inline PrefillSmem prefill_smem_layout(int n_cols, int stage
   L.scale = off; off += (uint32_t)stages * kTileTokens * 4;
   L.w = off;     off += 2u * n_cols * 4;                    // two weight blocks
   off = (off + 7u) & ~7u;
-  L.bars = off;  off += 8u * (2u * stages + 13u);          // full/empty per stage, accf/acce x4, qf/qe x2, drain
+  L.bars = off;  off += 8u * (2u * stages + 2u * kMaxAccBufs + 5u);  // full/empty per stage, accf/acce, qf/qe x2, drain
   L.misc = off;  off += 32u;
   L.total = off + 1024u;
   return L;
@@ -106,8 +109,8 @@ __host__ __device__ inline PrefillSmem prefill_smem_layout(int n_cols, int stage
 // ------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error.  The tensor maps are encoded
 // by the caller; `heads` selects the template instance.
-cudaError_t launch_paged(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const PagedParams& p, int heads,
-                         bool gather, int grid, int smem_bytes, cudaStream_t stream);
+cudaError_t launch_paged(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const CUtensorMap& tm_sc,
+                         const PagedParams& p, int heads, bool gather, int grid, int smem_bytes, cudaStream_t stream);
 cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_s,
                            const CUtensorMap& tm_w, const PrefillParams& p, int heads, int grid, int smem_bytes,
                            cudaStream_t stream);

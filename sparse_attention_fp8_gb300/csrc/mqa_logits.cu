@@ -16,13 +16,12 @@
 //    PR, Technical Details) and dealt to CTAs round-robin.
 //  * Per unit every role derives the union of the block's windows from
 //    ks/ke; tiles meeting it are computed (TMA of K and its scales, four K=32
-//    e4m3 tcgen05.mma into a double-buffered TMEM accumulator), the others are
+//    e4m3 tcgen05.mma into one of the TMEM accumulators), the others are
 //    written with -inf directly.  Q and the weights are double-buffered
 //    across units.
-//  * Four epilogue warpgroups; computed tiles go round-robin to the TMEM
-//    accumulators (4, or 2 when block_m*heads > 128, then two warpgroups
-//    split the block's rows).  A thread owns one token: it reduces its rows
-//    out of TMEM with double-buffered loads, applies ReLU * weight, sums the
+//  * Two epilogue warpgroups take alternate computed tiles and share the -inf
+//    tiles.  A thread owns one token: it walks the accumulator's 32-column
+//    chunks with double-buffered TMEM loads, applies ReLU * weight, sums the
 //    heads, scales by the token's kv_scale and stores the value or -inf.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -42,6 +41,8 @@ struct Unit {
   int n_j;     // column tiles of this unit
   int t_lo;    // union tile range [t_lo, t_hi) of computed tiles
   int t_hi;
+  int j0;      // first computed tile of this unit
+  int n_comp;  // computed tiles of this unit (j0, j0 + split, ...)
   int row_lo;  // this lane's row window (lanes < block_m), clamped; empty: 0,0
   int row_hi;
 };
@@ -52,7 +53,7 @@ __device__ __forceinline__ Unit load_unit(const PrefillParams& p, int u, int num
   Unit U;
   const int lane = threadIdx.x & 31;
   const int rb_index = u / p.split;
-  U.sidx = u % p.split;
+  U.sidx = u - rb_index * p.split;
   const int rb = p.reverse ? (num_rb - 1 - rb_index) : rb_index;
   U.m0 = rb * p.block_m;
   U.n_j = (U.sidx < n_tiles) ? (n_tiles - U.sidx + p.split - 1) / p.split : 0;
@@ -75,10 +76,10 @@ __device__ __forceinline__ Unit load_unit(const PrefillParams& p, int u, int num
   }
   U.t_lo = hi > lo ? lo / kTileTokens : 0;
   U.t_hi = hi > lo ? (hi + kTileTokens - 1) / kTileTokens : 0;
+  U.j0 = (U.t_lo <= U.sidx) ? U.sidx : U.sidx + ((U.t_lo - U.sidx + p.split - 1) / p.split) * p.split;
+  U.n_comp = (U.t_hi > U.j0) ? (U.t_hi - U.j0 + p.split - 1) / p.split : 0;
   return U;
 }
-
-__device__ __forceinline__ bool is_compute(const Unit& U, int j) { return j >= U.t_lo && j < U.t_hi; }
 
 }  // namespace
 
@@ -94,6 +95,8 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
   const int N = p.n_cols;
   const int S = p.stages;
   const int BM = p.block_m;
+  const int AB = p.acc_bufs;
+  const uint32_t acc_cols = kTmemCols / AB;
   const PrefillSmem L = prefill_smem_layout(N, S);
   uint8_t* q_s = smem + L.q;
   uint8_t* k_s = smem + L.k;
@@ -105,14 +108,11 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
 
   const uint32_t full0 = ptx::smem_u32(bars);
   const uint32_t empty0 = full0 + 8u * S;
-  const uint32_t accf0 = empty0 + 8u * S;  // [4]
-  const uint32_t acce0 = accf0 + 32u;      // [4]
-  const uint32_t qf0 = acce0 + 32u;        // [2]
-  const uint32_t qe0 = qf0 + 16u;          // [2]
+  const uint32_t accf0 = empty0 + 8u * S;           // [kMaxAccBufs]
+  const uint32_t acce0 = accf0 + 8u * kMaxAccBufs;  // [kMaxAccBufs]
+  const uint32_t qf0 = acce0 + 8u * kMaxAccBufs;    // [2]
+  const uint32_t qe0 = qf0 + 16u;                   // [2]
   const uint32_t drain_bar = qe0 + 16u;
-  const int AB = p.acc_bufs;
-  const uint32_t acc_cols = kTmemCols / AB;
-  const uint32_t epi_per_buf = 4u * kEpiGroups / AB;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -124,15 +124,15 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
     misc[1] = 0u;
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(full0 + 8u * s, 1u);
-      ptx::mbar_init(empty0 + 8u * s, 1u + epi_per_buf);  // MMA commit + the warps that read the scales
+      ptx::mbar_init(empty0 + 8u * s, 1u + 4u);  // MMA commit + the 4 warps that read the tile's scales
     }
-    for (int g = 0; g < 4; ++g) {
+    for (int g = 0; g < AB; ++g) {
       ptx::mbar_init(accf0 + 8u * g, 1u);
-      ptx::mbar_init(acce0 + 8u * g, epi_per_buf);
+      ptx::mbar_init(acce0 + 8u * g, 4u);
     }
     for (int g = 0; g < 2; ++g) {
       ptx::mbar_init(qf0 + 8u * g, 1u);
-      ptx::mbar_init(qe0 + 8u * g, 1u + 4u * kEpiGroups);
+      ptx::mbar_init(qe0 + 8u * g, 1u + 4u * kEpiGroups);  // MMA commit + every epilogue warp
     }
     ptx::mbar_init(drain_bar, 1u);
     ptx::fence_barrier_init();
@@ -152,77 +152,78 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
 
   if (warp == 0) {
     // ============================ producer ==============================
-    int seg = -1, ci = 0, q_issued = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    Ring st{0u, 0u, static_cast<uint32_t>(S)};
+    Ring qr{0u, 0u, 2u};
+    int issued = 0, q_issued = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const Unit U = load_unit(p, u, num_rb, n_tiles);
-      ++seg;
-      if (!warp_wait_bounded(qe0 + 8u * (seg & 1), ((seg >> 1) & 1) ^ 1, abort_flag, &g_prefill_watchdog,
-                             kSiteQEmpty))
+      if (!(ok = warp_wait_bounded(qe0 + 8u * qr.idx, qr.phase ^ 1u, abort_flag, &g_prefill_watchdog,
+                                   kSiteQEmpty)))
         break;
       if (lane == 0) {
-        const uint32_t qf = qf0 + 8u * (seg & 1);
+        const uint32_t qf = qf0 + 8u * qr.idx;
         ptx::mbar_arrive_expect_tx(qf, N * (kHeadDim + 4));
-        ptx::tma_load_2d(ptx::smem_u32(q_s + (seg & 1) * N * kHeadDim), &tm_q, qf, 0, U.m0 * HEADS);
-        ptx::tma_load_1d(ptx::smem_u32(w_s + (seg & 1) * N), &tm_w, qf, U.m0 * HEADS);
+        ptx::tma_load_2d(ptx::smem_u32(q_s + qr.idx * N * kHeadDim), &tm_q, qf, 0, U.m0 * HEADS);
+        ptx::tma_load_1d(ptx::smem_u32(w_s + qr.idx * N), &tm_w, qf, U.m0 * HEADS);
       }
+      qr.next();
       ++q_issued;
-      bool ok = true;
-      for (int k = 0; k < U.n_j; ++k) {
-        const int j = U.sidx + k * p.split;
-        if (!is_compute(U, j)) continue;
-        const int s = ci % S;
-        if (!(ok = warp_wait_bounded(empty0 + 8u * s, ((ci / S) & 1) ^ 1, abort_flag, &g_prefill_watchdog,
+      for (int c = 0, j = U.j0; c < U.n_comp; ++c, j += p.split) {
+        if (!(ok = warp_wait_bounded(empty0 + 8u * st.idx, st.phase ^ 1u, abort_flag, &g_prefill_watchdog,
                                      kSiteStageEmpty)))
           break;
         if (lane == 0) {
-          const uint32_t full = full0 + 8u * s;
+          const uint32_t full = full0 + 8u * st.idx;
           ptx::mbar_arrive_expect_tx(full, kKTileBytes + kTileTokens * 4);
-          ptx::tma_load_2d(ptx::smem_u32(k_s + s * kKTileBytes), &tm_k, full, 0, j * kTileTokens);
-          ptx::tma_load_1d(ptx::smem_u32(sc_s + s * kTileTokens), &tm_s, full, j * kTileTokens);
+          ptx::tma_load_2d(ptx::smem_u32(k_s + st.idx * kKTileBytes), &tm_k, full, 0, j * kTileTokens);
+          ptx::tma_load_1d(ptx::smem_u32(sc_s + st.idx * kTileTokens), &tm_s, full, j * kTileTokens);
         }
-        ++ci;
+        st.next();
+        ++issued;
       }
-      if (!ok) break;
     }
     if (*abort_flag && lane == 0) {
-      for (int c = max(0, ci - S); c < ci; ++c) wait_drain(full0 + 8u * (c % S), (c / S) & 1, &g_prefill_watchdog);
+      for (int c = max(0, issued - S); c < issued; ++c)
+        wait_drain(full0 + 8u * (c % S), (c / S) & 1, &g_prefill_watchdog);
       for (int sg = max(0, q_issued - 2); sg < q_issued; ++sg)
         wait_drain(qf0 + 8u * (sg & 1), (sg >> 1) & 1, &g_prefill_watchdog);
     }
   } else if (warp == 1) {
     // ============================== MMA =================================
     const uint32_t idesc = ptx::idesc_e4m3_f32(kTileTokens, N);
-    int seg = -1, ci = 0;
+    const uint64_t a_desc0 = ptx::smem_desc_sw128(ptx::smem_u32(k_s));
+    const uint64_t b_desc0 = ptx::smem_desc_sw128(ptx::smem_u32(q_s));
+    const uint64_t q_step = static_cast<uint64_t>((N * kHeadDim) >> 4);
+    Ring st{0u, 0u, static_cast<uint32_t>(S)};
+    Ring ac{0u, 0u, static_cast<uint32_t>(AB)};
+    Ring qr{0u, 0u, 2u};
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const Unit U = load_unit(p, u, num_rb, n_tiles);
-      ++seg;
-      if (lane == 0) ok = wait_bounded(qf0 + 8u * (seg & 1), (seg >> 1) & 1, abort_flag, &g_prefill_watchdog,
-                                       kSiteQFull);
-      if (lane == 0 && ok) {
-        const uint64_t b_desc = ptx::smem_desc_sw128(ptx::smem_u32(q_s + (seg & 1) * N * kHeadDim));
-        for (int k = 0; k < U.n_j; ++k) {
-          const int j = U.sidx + k * p.split;
-          if (!is_compute(U, j)) continue;
-          const int s = ci % S;
-          const int g = ci % AB;
-          if (!(ok = wait_bounded(full0 + 8u * s, (ci / S) & 1, abort_flag, &g_prefill_watchdog, kSiteStageFull)))
+      if (lane == 0) {
+        ok = wait_bounded(qf0 + 8u * qr.idx, qr.phase, abort_flag, &g_prefill_watchdog, kSiteQFull);
+        const uint64_t b_desc = b_desc0 + qr.idx * q_step;
+        for (int c = 0; c < U.n_comp && ok; ++c) {
+          if (!(ok = wait_bounded(full0 + 8u * st.idx, st.phase, abort_flag, &g_prefill_watchdog, kSiteStageFull)))
             break;
-          if (!(ok = wait_bounded(acce0 + 8u * g, ((ci / AB) & 1) ^ 1, abort_flag, &g_prefill_watchdog,
+          if (!(ok = wait_bounded(acce0 + 8u * ac.idx, ac.phase ^ 1u, abort_flag, &g_prefill_watchdog,
                                   kSiteAccEmpty)))
             break;
           ptx::tc_fence_after();
-          const uint64_t a_desc = ptx::smem_desc_sw128(ptx::smem_u32(k_s + s * kKTileBytes));
-          const uint32_t d_tmem = tmem + g * acc_cols;
+          const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(st.idx) * (kKTileBytes >> 4);
+          const uint32_t d_tmem = tmem + ac.idx * acc_cols;
 #pragma unroll
           for (int kk = 0; kk < kHeadDim / 32; ++kk)
             ptx::mma_f8f6f4(d_tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, kk > 0 ? 1u : 0u);
-          ptx::mma_commit(empty0 + 8u * s);
-          ptx::mma_commit(accf0 + 8u * g);
-          ++ci;
+          ptx::mma_commit(empty0 + 8u * st.idx);
+          ptx::mma_commit(accf0 + 8u * ac.idx);
+          st.next();
+          ac.next();
         }
-        ptx::mma_commit(qe0 + 8u * (seg & 1));
+        if (ok) ptx::mma_commit(qe0 + 8u * qr.idx);
       }
+      qr.next();
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     }
     if (lane == 0 && *abort_flag) {
@@ -231,69 +232,67 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
     }
   } else {
     // =========================== epilogue ===============================
-    // Computed tile ci goes to accumulator buffer ci % AB, served by the
-    // kEpiGroups / AB warpgroups of that buffer, which split the block's
-    // rows; pure -inf tiles are dealt round-robin to the warpgroups.
-    const int ew = warp - kEpiWarp0;   // 0 .. 4*kEpiGroups-1
+    // Computed tile number ci (counted over the CTA) goes to accumulator
+    // ci % AB and to warpgroup ci % 2; -inf tiles alternate between the
+    // warpgroups by their own count.
+    const int ew = warp - kEpiWarp0;      // 0 .. 4*kEpiGroups-1
     const int grp = ew >> 2;
     const int et = (ew & 3) * 32 + lane;  // 0..127 within the warpgroup
-    const int quad = warp & 3;         // TMEM lane quadrant
-    const int row = quad * 32 + lane;  // token within the tile
-    const int parts = kEpiGroups / AB;
-    const int my_buf = grp / parts;
-    const int part = grp % parts;
-    const int rows_per_part = (BM + parts - 1) / parts;
-    const int r_begin = part * rows_per_part;
-    const int nrows = max(0, min(BM, r_begin + rows_per_part) - r_begin);
+    const int quad = warp & 3;            // TMEM lane quadrant
+    const int row = quad * 32 + lane;     // token within the tile
     const float ninf = __int_as_float(0xff800000);
-    int seg = -1, ci = 0, fi = 0;
+    Ring st{0u, 0u, static_cast<uint32_t>(S)};
+    Ring ac{0u, 0u, static_cast<uint32_t>(AB)};
+    Ring qr{0u, 0u, 2u};
+    int ci = 0, fi = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const Unit U = load_unit(p, u, num_rb, n_tiles);
-      ++seg;
-      if (!(ok = warp_wait_bounded(qf0 + 8u * (seg & 1), (seg >> 1) & 1, abort_flag, &g_prefill_watchdog,
-                                   kSiteQFull)))
+      if (!(ok = warp_wait_bounded(qf0 + 8u * qr.idx, qr.phase, abort_flag, &g_prefill_watchdog, kSiteQFull)))
         break;
+      const float* w = w_s + qr.idx * N;
       for (int k = 0; k < U.n_j; ++k) {
         const int j = U.sidx + k * p.split;
         const int col0 = j * kTileTokens;
-        if (is_compute(U, j)) {
-          const int c = ci++;
-          if (c % AB != my_buf) continue;
-          const int s = c % S;
-          if (!(ok = warp_wait_bounded(full0 + 8u * s, (c / S) & 1, abort_flag, &g_prefill_watchdog,
-                                       kSiteStageFull)))
-            break;
-          const float scale = sc_s[s * kTileTokens + row];
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(empty0 + 8u * s);
-          if (!(ok = warp_wait_bounded(accf0 + 8u * my_buf, (c / AB) & 1, abort_flag, &g_prefill_watchdog,
-                                       kSiteAccFull)))
-            break;
-          ptx::tc_fence_after();
-          const uint32_t taddr = tmem + my_buf * acc_cols + (static_cast<uint32_t>(quad * 32) << 16) +
-                                 static_cast<uint32_t>(r_begin * HEADS);
-          const int n = col0 + row;
-          const uint32_t acce = acce0 + 8u * my_buf;
-          reduce_rows<HEADS, 4>(
-              taddr, w_s + (seg & 1) * N + r_begin * HEADS, nrows,
-              [&]() {
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(acce);
-              },
-              [&](int kr, float v) {
-                const int rr = r_begin + kr;
-                const int lo = __shfl_sync(0xffffffffu, U.row_lo, rr);
-                const int hi = __shfl_sync(0xffffffffu, U.row_hi, rr);
-                const int m = U.m0 + rr;
-                if (m < p.rows && n < p.cols)
-                  __stcs(p.out + static_cast<int64_t>(m) * p.out_stride + n, (n >= lo && n < hi) ? v * scale : ninf);
-              });
+        if (j >= U.t_lo && j < U.t_hi) {
+          const bool mine = (ci & 1) == grp;
+          ++ci;
+          if (mine) {
+            if (!(ok = warp_wait_bounded(full0 + 8u * st.idx, st.phase, abort_flag, &g_prefill_watchdog,
+                                         kSiteStageFull)))
+              break;
+            const float scale = sc_s[st.idx * kTileTokens + row];
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(empty0 + 8u * st.idx);
+            if (!(ok = warp_wait_bounded(accf0 + 8u * ac.idx, ac.phase, abort_flag, &g_prefill_watchdog,
+                                         kSiteAccFull)))
+              break;
+            ptx::tc_fence_after();
+            const uint32_t taddr = tmem + ac.idx * acc_cols + (static_cast<uint32_t>(quad * 32) << 16);
+            const int n = col0 + row;
+            const uint32_t acce = acce0 + 8u * ac.idx;
+            reduce_rows<HEADS, 8>(
+                taddr, w, BM,
+                [&]() {
+                  ptx::tc_fence_before();
+                  __syncwarp();
+                  if (lane == 0) ptx::mbar_arrive(acce);
+                },
+                [&](int r, float v) {
+                  const int lo = __shfl_sync(0xffffffffu, U.row_lo, r);
+                  const int hi = __shfl_sync(0xffffffffu, U.row_hi, r);
+                  const int m = U.m0 + r;
+                  if (m < p.rows && n < p.cols)
+                    __stcs(p.out + static_cast<int64_t>(m) * p.out_stride + n, (n >= lo && n < hi) ? v * scale : ninf);
+                });
+          }
+          st.next();
+          ac.next();
         } else {
           // a tile no row of the block reaches: -inf for all the block's rows
-          const int f = fi++;
-          if (f % kEpiGroups != grp) continue;
+          const bool mine = (fi & 1) == grp;
+          ++fi;
+          if (!mine) continue;
           const int ncols = min(kTileTokens, p.cols - col0);
           if (p.vec_ok && ncols == kTileTokens) {
             const float4 f4 = make_float4(ninf, ninf, ninf, ninf);
@@ -312,7 +311,8 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
       }
       if (!ok) break;
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(qe0 + 8u * (seg & 1));
+      if (lane == 0) ptx::mbar_arrive(qe0 + 8u * qr.idx);
+      qr.next();
     }
   }
 

@@ -14,26 +14,30 @@
 //    on the device from context_lens (a prefix sum in shared memory), so no
 //    host synchronisation is needed and every CTA gets the same number of
 //    tiles (+-1).
-//  * Producer warp: one TMA per cache block (3-D view [block][row][128 B],
-//    128-byte swizzle) and one bulk copy of the block's scales into a ring of
-//    `stages` shared-memory slots; block-table entries are prefetched 32
-//    blocks ahead.  For block size 1 (co-packed 132-byte tokens, only 4-byte
-//    aligned) four producer warps gather each token with 4-byte cp.async in
-//    the same swizzled layout instead.
+//  * Producer warp: per tile, one 3-D TMA per cache block for the K rows
+//    (view [block][row][128 B], 128-byte swizzle) and one 2-D TMA per block
+//    for its scales, into a ring of `stages` shared-memory slots; block-table
+//    entries are prefetched 32 blocks ahead.  For block size 1 (co-packed
+//    132-byte tokens, only 4-byte aligned) two producer warps gather each
+//    token with 4-byte cp.async into the same swizzled layout instead.
 //  * MMA warp: the K tile is the A operand (M = 128 tokens) and the request's
 //    whole Q block [next_n*heads, 128] is the B operand, so N = next_n*heads:
 //    one K tile feeds every speculative row in one tcgen05.mma chain (the fold
 //    of next_n into the MMA asked for in aiter issue 5477, The ask).  Four
-//    K=32 e4m3 MMAs accumulate in f32 in tensor memory.  Q and the weights of
-//    the current and the next request are double-buffered.
-//  * Four epilogue warpgroups.  Tensor memory holds 4 accumulators (2 when
-//    next_n*heads > 128); tiles go round-robin to them, so up to four tiles
-//    are in the epilogue at once, and the warpgroups serving one buffer split
-//    its rows.  Thread = token: 32-column tcgen05.ld loads, double-buffered,
-//    then ReLU, multiply by the weights, sum the heads, multiply once by the
+//    K=32 e4m3 MMAs accumulate in f32 in tensor memory, which holds 2..16
+//    accumulators (as many as 512 columns allow).  Q and the weights of the
+//    current and the next request are double-buffered.
+//  * Two epilogue warpgroups take alternate tiles.  Thread = token (TMEM
+//    lane): read the token's scale and free the stage, then walk the 32-column
+//    chunks of the accumulator with double-buffered tcgen05.ld (the weights
+//    for a chunk are loaded from shared memory while its data is in flight),
+//    ReLU, multiply by the weights, sum the heads, multiply once by the
 //    token's kv_scale (the hoist of aiter PR 5047, Technical Details: scale
 //    >= 0 and ReLU is positive-homogeneous) and store if inside the causal
 //    window.  A warp stores 32 consecutive floats per row: coalesced 128 B.
+//  * Control loops keep ring indices and phases as counters (no division per
+//    tile): the single-thread control loops, not the copies, set the pace of
+//    a 16 KB tile when they are not kept short.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -85,9 +89,9 @@ __device__ __forceinline__ int32_t load_table(const PagedParams& p, int b, int64
   return __ldg(p.block_tables + static_cast<int64_t>(b) * p.bt_stride + idx);
 }
 
-__device__ __forceinline__ int64_t clamp_block(int32_t v, int64_t num_blocks) {
-  int64_t x = v < 0 ? 0 : v;
-  return x >= num_blocks ? num_blocks - 1 : x;
+__device__ __forceinline__ int32_t clamp_block(int32_t v, int64_t num_blocks) {
+  const int32_t hi = static_cast<int32_t>(num_blocks - 1);
+  return v < 0 ? 0 : (v > hi ? hi : v);
 }
 
 }  // namespace
@@ -95,7 +99,7 @@ __device__ __forceinline__ int64_t clamp_block(int32_t v, int64_t num_blocks) {
 template <int HEADS, bool GATHER>
 __global__ void __launch_bounds__(paged_threads(GATHER), 1)
     paged_logits_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
-                        const PagedParams p) {
+                        const __grid_constant__ CUtensorMap tm_sc, const PagedParams p) {
   constexpr int kProdWarps = paged_producer_warps(GATHER);
   constexpr int kMmaWarp = kProdWarps;
   constexpr int kEpiWarp0 = kMmaWarp + 1;
@@ -106,6 +110,8 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
   const int N = p.n_cols;
   const int S = p.stages;
   const int B = p.batch;
+  const int AB = p.acc_bufs;
+  const uint32_t acc_cols = kTmemCols / AB;
   const PagedSmem L = paged_smem_layout(N, S, B);
   uint8_t* q_s = smem + L.q;
   uint8_t* k_s = smem + L.k;
@@ -118,14 +124,11 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
 
   const uint32_t full0 = ptx::smem_u32(bars);
   const uint32_t empty0 = full0 + 8u * S;
-  const uint32_t accf0 = empty0 + 8u * S;  // [4]
-  const uint32_t acce0 = accf0 + 32u;      // [4]
-  const uint32_t qf0 = acce0 + 32u;        // [2]
-  const uint32_t qe0 = qf0 + 16u;          // [2]
+  const uint32_t accf0 = empty0 + 8u * S;           // [kMaxAccBufs]
+  const uint32_t acce0 = accf0 + 8u * kMaxAccBufs;  // [kMaxAccBufs]
+  const uint32_t qf0 = acce0 + 8u * kMaxAccBufs;    // [2]
+  const uint32_t qe0 = qf0 + 16u;                   // [2]
   const uint32_t drain_bar = qe0 + 16u;
-  const int AB = p.acc_bufs;                        // accumulator buffers (2 or 4)
-  const uint32_t acc_cols = kTmemCols / AB;         // columns per buffer
-  const uint32_t epi_per_buf = 4u * kEpiGroups / AB;  // epilogue warps serving one buffer
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -140,11 +143,11 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
     misc[1] = 0u;
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(full0 + 8u * s, GATHER ? 32u * kProdWarps : 1u);
-      ptx::mbar_init(empty0 + 8u * s, 1u + epi_per_buf);  // MMA commit + the warps that read the tile's scales
+      ptx::mbar_init(empty0 + 8u * s, 1u + 4u);  // MMA commit + the 4 warps that read the tile's scales
     }
-    for (int g = 0; g < 4; ++g) {
+    for (int g = 0; g < AB; ++g) {
       ptx::mbar_init(accf0 + 8u * g, 1u);
-      ptx::mbar_init(acce0 + 8u * g, epi_per_buf);
+      ptx::mbar_init(acce0 + 8u * g, 4u);
     }
     for (int g = 0; g < 2; ++g) {
       ptx::mbar_init(qf0 + 8u * g, 1u);
@@ -155,7 +158,10 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
   }
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tm_q);
-    if (!GATHER) ptx::prefetch_tmap(&tm_kv);
+    if (!GATHER) {
+      ptx::prefetch_tmap(&tm_kv);
+      ptx::prefetch_tmap(&tm_sc);
+    }
   }
   if (warp == kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(misc), kTmemCols);
@@ -190,55 +196,57 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
 
   if (warp < kProdWarps) {
     // =========================== producer ===============================
-    int seg = -1, q_issued = 0;
-    int issued = 0;
+    Ring st{0u, 0u, static_cast<uint32_t>(S)};  // K ring
+    Ring qr{0u, 0u, 2u};                          // Q/weight double buffer
+    int issued = 0, q_issued = 0;
     int64_t ctx_eff = 0;
     if constexpr (!GATHER) {
-      const int blk = p.block_size;             // 16, 32, 64 or 128
-      const int P = kTileTokens / blk;          // cache blocks per tile
-      const uint32_t blk_bytes = blk * (kHeadDim + 4);
-      int64_t chunk = 0, need_blocks = 0;
+      const int blk = p.block_size;     // 16, 32, 64 or 128
+      const int P = kTileTokens / blk;  // cache blocks per tile
+      const uint32_t blk_bytes = static_cast<uint32_t>(blk) * (kHeadDim + 4);
+      const uint32_t blk_k_bytes = static_cast<uint32_t>(blk) * kHeadDim;
+      int chunk = 0, need_blocks = 0;
       int32_t tbl_cur = 0, tbl_nxt = 0;
       for (int it = 0; it < n_items; ++it) {
-        const bool new_seg = (it == 0) || (cur.t == 0);
-        if (new_seg) {
-          ++seg;
-          if (!warp_wait_bounded(qe0 + 8u * (seg & 1), ((seg >> 1) & 1) ^ 1, abort_flag, &g_paged_watchdog,
-                                 kSiteQEmpty))
+        if (it == 0 || cur.t == 0) {
+          if (!warp_wait_bounded(qe0 + 8u * qr.idx, qr.phase ^ 1u, abort_flag, &g_paged_watchdog, kSiteQEmpty))
             break;
           if (lane == 0) {
-            const uint32_t qf = qf0 + 8u * (seg & 1);
+            const uint32_t qf = qf0 + 8u * qr.idx;
             ptx::mbar_arrive_expect_tx(qf, N * (kHeadDim + 4));
-            ptx::tma_load_2d(ptx::smem_u32(q_s + (seg & 1) * N * kHeadDim), &tm_q, qf, 0, cur.b * N);
-            ptx::bulk_g2s(ptx::smem_u32(w_s + (seg & 1) * N), p.weights + static_cast<int64_t>(cur.b) * N, N * 4,
-                          qf);
+            ptx::tma_load_2d(ptx::smem_u32(q_s + qr.idx * N * kHeadDim), &tm_q, qf, 0, cur.b * N);
+            ptx::bulk_g2s(ptx::smem_u32(w_s + qr.idx * N), p.weights + static_cast<int64_t>(cur.b) * N, N * 4, qf);
           }
+          qr.next();
           ++q_issued;
           ctx_eff = clamp_ctx(__ldg(p.context_lens + cur.b), p);
-          need_blocks = (ctx_eff + blk - 1) / blk;
-          chunk = (static_cast<int64_t>(cur.t) * P) & ~31ll;
+          need_blocks = static_cast<int>((ctx_eff + blk - 1) / blk);
+          chunk = (cur.t * P) & ~31;
           tbl_cur = load_table(p, cur.b, chunk + lane, need_blocks);
           tbl_nxt = load_table(p, cur.b, chunk + 32 + lane, need_blocks);
         }
-        const int s = it % S;
-        if (!warp_wait_bounded(empty0 + 8u * s, ((it / S) & 1) ^ 1, abort_flag, &g_paged_watchdog,
-                               kSiteStageEmpty))
+        if (!warp_wait_bounded(empty0 + 8u * st.idx, st.phase ^ 1u, abort_flag, &g_paged_watchdog, kSiteStageEmpty))
           break;
-        const int64_t first_tok = static_cast<int64_t>(cur.t) * kTileTokens;
-        const int64_t first_blk = static_cast<int64_t>(cur.t) * P;
-        const int valid = static_cast<int>(ctx_eff - first_tok < kTileTokens ? ctx_eff - first_tok : kTileTokens);
+        const int first_blk = cur.t * P;
+        const int valid = min(kTileTokens, static_cast<int>(ctx_eff - static_cast<int64_t>(cur.t) * kTileTokens));
         const int nblk = (valid + blk - 1) / blk;
-        const uint32_t full = full0 + 8u * s;
+        const uint32_t full = full0 + 8u * st.idx;
         if (lane == 0) ptx::mbar_arrive_expect_tx(full, nblk * blk_bytes);
         __syncwarp();
-        const int32_t id = __shfl_sync(0xffffffffu, tbl_cur, static_cast<int>(first_blk - chunk + lane) & 31);
+        const int32_t id = __shfl_sync(0xffffffffu, tbl_cur, (first_blk - chunk + lane) & 31);
         if (lane < nblk) {
-          const int64_t page = clamp_block(id, p.num_blocks);
-          ptx::tma_load_3d(ptx::smem_u32(k_s + s * kKTileBytes + lane * blk * kHeadDim), &tm_kv, full, 0, 0,
-                           static_cast<int32_t>(page));
-          ptx::bulk_g2s(ptx::smem_u32(sc_s + s * kTileTokens + lane * blk),
-                        p.kv_cache + page * blk_bytes + static_cast<int64_t>(blk) * kHeadDim, blk * 4, full);
+          const int32_t page = clamp_block(id, p.num_blocks);
+          ptx::tma_load_3d(ptx::smem_u32(k_s + st.idx * kKTileBytes + lane * blk_k_bytes), &tm_kv, full, 0, 0, page);
+          // A tensor TMA needs a 128-byte-aligned destination: block sizes
+          // >= 32 give one per block; block size 16 (64-byte scale runs)
+          // uses the plain bulk copy, which needs only 16 bytes.
+          if (blk >= 32)
+            ptx::tma_load_2d(ptx::smem_u32(sc_s + st.idx * kTileTokens + lane * blk), &tm_sc, full, 0, page);
+          else
+            ptx::bulk_g2s(ptx::smem_u32(sc_s + st.idx * kTileTokens + lane * blk),
+                          p.kv_cache + static_cast<int64_t>(page) * blk_bytes + blk_k_bytes, blk * 4, full);
         }
+        st.next();
         issued = it + 1;
         if (first_blk + P >= chunk + 32) {  // next tile starts a new 32-block chunk
           chunk += 32;
@@ -250,60 +258,58 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
       if (*abort_flag && lane == 0) {  // let issued copies land before the CTA exits
         for (int it = max(0, issued - S); it < issued; ++it)
           wait_drain(full0 + 8u * (it % S), (it / S) & 1, &g_paged_watchdog);
-        for (int sg = max(0, q_issued - 2); sg < q_issued; ++sg) wait_drain(qf0 + 8u * (sg & 1), (sg >> 1) & 1, &g_paged_watchdog);
+        for (int sg = max(0, q_issued - 2); sg < q_issued; ++sg)
+          wait_drain(qf0 + 8u * (sg & 1), (sg >> 1) & 1, &g_paged_watchdog);
       }
     } else {
       // Block size 1: token p of request b is the 132-byte cache row
       // block_tables[b][p].  Producer warp w gathers tokens [64w, 64w+64) of
       // a tile, one token per instruction: lane l copies bytes [4l, 4l+4)
       // into the 128-byte-swizzled row; lane l also copies the scales of
-      // tokens 64w+l and 64w+32+l.
-      constexpr int kLag = 4;  // tiles in flight per thread before arriving
-      const int pw = warp;     // 0..1
+      // tokens 64w+l and 64w+32+l.  Copies are tracked per thread with
+      // cp.async groups; a tile is published kLag tiles after it was issued.
+      constexpr int kLag = 4;
+      const int pw = warp;  // 0..1
       int32_t slot_a = 0, slot_b = 0, nxt_a = 0, nxt_b = 0;
       int pending = 0;
+      Ring pub{0u, 0u, static_cast<uint32_t>(S)};  // next stage to publish
       for (int it = 0; it < n_items; ++it) {
-        const bool new_seg = (it == 0) || (cur.t == 0);
-        if (new_seg) {
-          ++seg;
-          if (seg >= 2 && pending > 0) {
+        if (it == 0 || cur.t == 0) {
+          if (q_issued >= 2 && pending > 0) {
             // The Q buffer is freed only once the consumers finish request
-            // seg-2, whose last tiles may still be among the deferred
+            // q_issued-2, whose last tiles may still be among the deferred
             // arrivals: publish every tile in flight before waiting on it.
             ptx::cp_async_wait<0>();
             ptx::fence_proxy_async_smem();
-            for (int done = issued - pending; done < issued; ++done) ptx::mbar_arrive(full0 + 8u * (done % S));
-            pending = 0;
+            for (; pending > 0; --pending) {
+              ptx::mbar_arrive(full0 + 8u * pub.idx);
+              pub.next();
+            }
           }
-          if (!warp_wait_bounded(qe0 + 8u * (seg & 1), ((seg >> 1) & 1) ^ 1, abort_flag, &g_paged_watchdog,
-                                 kSiteQEmpty))
+          if (!warp_wait_bounded(qe0 + 8u * qr.idx, qr.phase ^ 1u, abort_flag, &g_paged_watchdog, kSiteQEmpty))
             break;
           if (pw == 0 && lane == 0) {
-            const uint32_t qf = qf0 + 8u * (seg & 1);
+            const uint32_t qf = qf0 + 8u * qr.idx;
             ptx::mbar_arrive_expect_tx(qf, N * (kHeadDim + 4));
-            ptx::tma_load_2d(ptx::smem_u32(q_s + (seg & 1) * N * kHeadDim), &tm_q, qf, 0, cur.b * N);
-            ptx::bulk_g2s(ptx::smem_u32(w_s + (seg & 1) * N), p.weights + static_cast<int64_t>(cur.b) * N, N * 4,
-                          qf);
+            ptx::tma_load_2d(ptx::smem_u32(q_s + qr.idx * N * kHeadDim), &tm_q, qf, 0, cur.b * N);
+            ptx::bulk_g2s(ptx::smem_u32(w_s + qr.idx * N), p.weights + static_cast<int64_t>(cur.b) * N, N * 4, qf);
           }
+          qr.next();
           ++q_issued;
           ctx_eff = clamp_ctx(__ldg(p.context_lens + cur.b), p);
           const int64_t t0 = static_cast<int64_t>(cur.t) * kTileTokens + pw * 64 + lane;
           slot_a = load_table(p, cur.b, t0, ctx_eff);
           slot_b = load_table(p, cur.b, t0 + 32, ctx_eff);
         }
-        // prefetch the next tile's slots (same request only)
-        if (cur.t + 1 < cur.tiles_b) {
+        if (cur.t + 1 < cur.tiles_b) {  // prefetch the next tile's slots (same request only)
           const int64_t t1 = static_cast<int64_t>(cur.t + 1) * kTileTokens + pw * 64 + lane;
           nxt_a = load_table(p, cur.b, t1, ctx_eff);
           nxt_b = load_table(p, cur.b, t1 + 32, ctx_eff);
         }
-        const int s = it % S;
-        if (!warp_wait_bounded(empty0 + 8u * s, ((it / S) & 1) ^ 1, abort_flag, &g_paged_watchdog,
-                               kSiteStageEmpty))
+        if (!warp_wait_bounded(empty0 + 8u * st.idx, st.phase ^ 1u, abort_flag, &g_paged_watchdog, kSiteStageEmpty))
           break;
-        const int64_t first_tok = static_cast<int64_t>(cur.t) * kTileTokens;
-        const int valid = static_cast<int>(ctx_eff - first_tok < kTileTokens ? ctx_eff - first_tok : kTileTokens);
-        const uint32_t tile_s = ptx::smem_u32(k_s + s * kKTileBytes);
+        const int valid = min(kTileTokens, static_cast<int>(ctx_eff - static_cast<int64_t>(cur.t) * kTileTokens));
+        const uint32_t tile_s = ptx::smem_u32(k_s + st.idx * kKTileBytes);
         const uint32_t chunk_in_row = static_cast<uint32_t>(lane >> 2);
         const uint32_t byte_in_chunk = static_cast<uint32_t>(lane & 3) * 4u;
 #pragma unroll 4
@@ -321,17 +327,19 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
           const int tok = pw * 64 + half * 32 + lane;
           if (tok < valid) {
             const int64_t row = clamp_block(half ? slot_b : slot_a, p.num_blocks);
-            ptx::cp_async_4(ptx::smem_u32(sc_s + s * kTileTokens + tok), p.kv_cache + row * (kHeadDim + 4) + kHeadDim);
+            ptx::cp_async_4(ptx::smem_u32(sc_s + st.idx * kTileTokens + tok),
+                            p.kv_cache + row * (kHeadDim + 4) + kHeadDim);
           }
         }
         ptx::cp_async_commit();
         ++pending;
+        st.next();
         issued = it + 1;
         if (pending > kLag) {  // the tile issued kLag tiles ago has landed
           ptx::cp_async_wait<kLag>();
           ptx::fence_proxy_async_smem();
-          const int done = it - kLag;
-          ptx::mbar_arrive(full0 + 8u * (done % S));
+          ptx::mbar_arrive(full0 + 8u * pub.idx);
+          pub.next();
           --pending;
         }
         slot_a = nxt_a;
@@ -340,38 +348,46 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
       }
       ptx::cp_async_wait<0>();
       ptx::fence_proxy_async_smem();
-      for (int done = issued - pending; done < issued; ++done) ptx::mbar_arrive(full0 + 8u * (done % S));
+      for (; pending > 0; --pending) {
+        ptx::mbar_arrive(full0 + 8u * pub.idx);
+        pub.next();
+      }
       if (*abort_flag && pw == 0 && lane == 0)
-        for (int sg = max(0, q_issued - 2); sg < q_issued; ++sg) wait_drain(qf0 + 8u * (sg & 1), (sg >> 1) & 1, &g_paged_watchdog);
+        for (int sg = max(0, q_issued - 2); sg < q_issued; ++sg)
+          wait_drain(qf0 + 8u * (sg & 1), (sg >> 1) & 1, &g_paged_watchdog);
     }
   } else if (warp == kMmaWarp) {
     // ============================= MMA ==================================
     if (lane == 0) {
       const uint32_t idesc = ptx::idesc_e4m3_f32(kTileTokens, N);
-      int seg = -1;
-      bool ok = true;
-      for (int it = 0; it < n_items && ok; ++it) {
+      const uint64_t a_desc0 = ptx::smem_desc_sw128(ptx::smem_u32(k_s));
+      const uint64_t b_desc0 = ptx::smem_desc_sw128(ptx::smem_u32(q_s));
+      const uint64_t q_step = static_cast<uint64_t>((N * kHeadDim) >> 4);  // Q buffer stride, descriptor units
+      Ring st{0u, 0u, static_cast<uint32_t>(S)};
+      Ring ac{0u, 0u, static_cast<uint32_t>(AB)};
+      Ring qr{0u, 0u, 2u};
+      uint64_t b_desc = b_desc0;
+      for (int it = 0; it < n_items; ++it) {
         if (it == 0 || cur.t == 0) {
-          ++seg;
-          if (!(ok = wait_bounded(qf0 + 8u * (seg & 1), (seg >> 1) & 1, abort_flag, &g_paged_watchdog, kSiteQFull)))
-            break;
+          if (!wait_bounded(qf0 + 8u * qr.idx, qr.phase, abort_flag, &g_paged_watchdog, kSiteQFull)) break;
+          b_desc = b_desc0 + qr.idx * q_step;
         }
-        const int s = it % S;
-        const int g = it % AB;
-        if (!(ok = wait_bounded(full0 + 8u * s, (it / S) & 1, abort_flag, &g_paged_watchdog, kSiteStageFull))) break;
-        if (!(ok = wait_bounded(acce0 + 8u * g, ((it / AB) & 1) ^ 1, abort_flag, &g_paged_watchdog, kSiteAccEmpty)))
-          break;
+        if (!wait_bounded(full0 + 8u * st.idx, st.phase, abort_flag, &g_paged_watchdog, kSiteStageFull)) break;
+        if (!wait_bounded(acce0 + 8u * ac.idx, ac.phase ^ 1u, abort_flag, &g_paged_watchdog, kSiteAccEmpty)) break;
         ptx::tc_fence_after();
-        const uint64_t a_desc = ptx::smem_desc_sw128(ptx::smem_u32(k_s + s * kKTileBytes));
-        const uint64_t b_desc = ptx::smem_desc_sw128(ptx::smem_u32(q_s + (seg & 1) * N * kHeadDim));
-        const uint32_t d_tmem = tmem + g * acc_cols;
+        const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(st.idx) * (kKTileBytes >> 4);
+        const uint32_t d_tmem = tmem + ac.idx * acc_cols;
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 32; ++kk)  // K = 32 e4m3 per MMA: advance 32 bytes in the swizzled row
           ptx::mma_f8f6f4(d_tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, kk > 0 ? 1u : 0u);
-        ptx::mma_commit(empty0 + 8u * s);
-        ptx::mma_commit(accf0 + 8u * g);
-        const bool seg_end = cur.advance() || (it + 1 == n_items);
-        if (seg_end) ptx::mma_commit(qe0 + 8u * (seg & 1));
+        ptx::mma_commit(empty0 + 8u * st.idx);
+        ptx::mma_commit(accf0 + 8u * ac.idx);
+        st.next();
+        ac.next();
+        if (cur.advance() || it + 1 == n_items) {
+          ptx::mma_commit(qe0 + 8u * qr.idx);
+          qr.next();
+        }
       }
       if (*abort_flag) {
         ptx::mma_commit(drain_bar);
@@ -380,61 +396,52 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
     }
   } else {
     // =========================== epilogue ===============================
-    // kEpiGroups warpgroups.  Tile it goes to accumulator buffer it % AB and
-    // is served by the kEpiGroups / AB warpgroups of that buffer, which split
-    // its speculative rows.  Thread = token (TMEM lane): read the token's
-    // scale and free the stage, then reduce its rows out of TMEM with
-    // double-buffered loads, releasing the accumulator after the last load.
-    const int ew = warp - kEpiWarp0;      // 0 .. 4*kEpiGroups-1
-    const int grp = ew >> 2;
-    const int quad = warp & 3;            // TMEM lane quadrant this warp may access
-    const int row = quad * 32 + lane;     // token within the tile
+    const int ew = warp - kEpiWarp0;   // 0 .. 4*kEpiGroups-1
+    const int grp = ew >> 2;           // serves tiles with it % 2 == grp
+    const int quad = warp & 3;         // TMEM lane quadrant this warp may access
+    const int row = quad * 32 + lane;  // token within the tile
     const int next_n = p.next_n;
-    const int parts = kEpiGroups / AB;    // warpgroups per tile
-    const int my_buf = grp / parts;
-    const int part = grp % parts;
-    const int rows_per_part = (next_n + parts - 1) / parts;
-    const int n_begin = part * rows_per_part;
-    const int nrows = max(0, min(next_n, n_begin + rows_per_part) - n_begin);
-    int seg = -1;
+    Ring st{0u, 0u, static_cast<uint32_t>(S)};
+    Ring ac{0u, 0u, static_cast<uint32_t>(AB)};
+    Ring qr{0u, 0u, 2u};
     int32_t ctx = 0;
+    const float* w = w_s;
     for (int it = 0; it < n_items; ++it) {
       if (it == 0 || cur.t == 0) {
-        ++seg;
-        if (!warp_wait_bounded(qf0 + 8u * (seg & 1), (seg >> 1) & 1, abort_flag, &g_paged_watchdog, kSiteQFull)) break;
+        if (!warp_wait_bounded(qf0 + 8u * qr.idx, qr.phase, abort_flag, &g_paged_watchdog, kSiteQFull)) break;
+        w = w_s + qr.idx * N;
         ctx = __ldg(p.context_lens + cur.b);
       }
-      if (it % AB == my_buf) {
-        const int s = it % S;
-        if (!warp_wait_bounded(full0 + 8u * s, (it / S) & 1, abort_flag, &g_paged_watchdog, kSiteStageFull)) break;
-        const float scale = sc_s[s * kTileTokens + row];
+      if ((it & 1) == grp) {
+        if (!warp_wait_bounded(full0 + 8u * st.idx, st.phase, abort_flag, &g_paged_watchdog, kSiteStageFull)) break;
+        const float scale = sc_s[st.idx * kTileTokens + row];
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(empty0 + 8u * s);
-        if (!warp_wait_bounded(accf0 + 8u * my_buf, (it / AB) & 1, abort_flag, &g_paged_watchdog, kSiteAccFull))
-          break;
+        if (lane == 0) ptx::mbar_arrive(empty0 + 8u * st.idx);
+        if (!warp_wait_bounded(accf0 + 8u * ac.idx, ac.phase, abort_flag, &g_paged_watchdog, kSiteAccFull)) break;
         ptx::tc_fence_after();
-        const uint32_t taddr = tmem + my_buf * acc_cols + (static_cast<uint32_t>(quad * 32) << 16) +
-                               static_cast<uint32_t>(n_begin * HEADS);
+        const uint32_t taddr = tmem + ac.idx * acc_cols + (static_cast<uint32_t>(quad * 32) << 16);
         const int64_t pos = static_cast<int64_t>(cur.t) * kTileTokens + row;
-        const int64_t last = static_cast<int64_t>(ctx) - next_n + n_begin;
-        float* out_col = p.out + (static_cast<int64_t>(cur.b) * next_n + n_begin) * p.out_stride + pos;
-        const uint32_t acce = acce0 + 8u * my_buf;
-        reduce_rows<HEADS, 4>(
-            taddr, w_s + (seg & 1) * N + n_begin * HEADS, nrows,
+        const int64_t last = static_cast<int64_t>(ctx) - next_n;
+        float* out_col = p.out + static_cast<int64_t>(cur.b) * next_n * p.out_stride + pos;
+        const uint32_t acce = acce0 + 8u * ac.idx;
+        reduce_rows<HEADS, 8>(
+            taddr, w, next_n,
             [&]() {
               ptx::tc_fence_before();
               __syncwarp();
               if (lane == 0) ptx::mbar_arrive(acce);
             },
-            [&](int k, float v) {
-              if (pos <= last + k && pos < p.max_model_len)
-                __stcs(out_col + static_cast<int64_t>(k) * p.out_stride, v * scale);
+            [&](int n, float v) {
+              if (pos <= last + n && pos < p.max_model_len)
+                __stcs(out_col + static_cast<int64_t>(n) * p.out_stride, v * scale);
             });
       }
-      const bool seg_end = cur.advance() || (it + 1 == n_items);
-      if (seg_end) {
+      st.next();
+      ac.next();
+      if (cur.advance() || it + 1 == n_items) {
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(qe0 + 8u * (seg & 1));
+        if (lane == 0) ptx::mbar_arrive(qe0 + 8u * qr.idx);
+        qr.next();
       }
     }
   }
@@ -447,15 +454,15 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
   }
 }
 
-cudaError_t launch_paged(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const PagedParams& p, int heads,
-                         bool gather, int grid, int smem_bytes, cudaStream_t stream) {
-  void (*kern)(CUtensorMap, CUtensorMap, PagedParams) = nullptr;
+cudaError_t launch_paged(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const CUtensorMap& tm_sc,
+                         const PagedParams& p, int heads, bool gather, int grid, int smem_bytes, cudaStream_t stream) {
+  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, PagedParams) = nullptr;
   if (heads == 32) kern = gather ? paged_logits_kernel<32, true> : paged_logits_kernel<32, false>;
   else if (heads == 64) kern = gather ? paged_logits_kernel<64, true> : paged_logits_kernel<64, false>;
   else return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
-  kern<<<grid, paged_threads(gather), smem_bytes, stream>>>(tm_q, tm_kv, p);
+  kern<<<grid, paged_threads(gather), smem_bytes, stream>>>(tm_q, tm_kv, tm_sc, p);
   return cudaGetLastError();
 }
 
