@@ -141,6 +141,24 @@ def recorded_traffic(workload: str):
     return rec.get("dram_bytes_per_launch")
 
 
+# ------------------------------------------------------------ multi-rank
+def reduce_max(value: float, world: int, device) -> float:
+    """Max of a per-rank time over all ranks (identity on one rank).  Ranks
+    run independent replicas of the workload: no data-path collective, only
+    this timing reduction."""
+    if world <= 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_us_per_call(max_total_ms: float, steps_per_rank: int, world: int) -> float:
+    """All ranks' calls divided by the slowest rank's device time, in us/call."""
+    return max_total_ms * 1e3 / (steps_per_rank * world)
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -334,12 +352,8 @@ def run_ours(args, rank, world):
     clocks = ClockSampler.summarize(sampler.stop())
     clocks["window"] = "timed region" if t_wall >= 1.0 else "timed region + 1 s soak of the same step"
 
-    total_ms = float(sum(per_call_ms))
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    us_per_call = total_ms * 1e3 / (args.steps * world)
+    total_ms = reduce_max(float(sum(per_call_ms)), world, dev)
+    us_per_call = whole_job_us_per_call(total_ms, args.steps, world)
     mean_ms = total_ms / args.steps
     median_us = statistics.median(per_call_ms) * 1e3
 
@@ -389,12 +403,8 @@ def run_ours(args, rank, world):
             host_out.copy_(staging, non_blocking=True)
         e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_us = e2e_ms * 1e3 / (e2e_steps * world)
+    e2e_ms = reduce_max(e0.elapsed_time(e1), world, dev)
+    e2e_us = whole_job_us_per_call(e2e_ms, e2e_steps, world)
 
     status = fp8idx.device_status()
     hbm_peak = float(peaks["hbm_gbs"])
