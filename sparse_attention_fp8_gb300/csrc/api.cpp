@@ -153,21 +153,23 @@ fp8idx_status plan_paged(int32_t batch, int32_t next_n, int32_t heads, int32_t h
   if (num_sms <= 0) return fail(FP8IDX_ERR_INVALID, "num_sms must be positive");
   const bool gather = block_size == 1;
   const int n_cols = next_n * heads;
-  int stages = (o && o->stages > 0) ? o->stages : 12;
+  const int sub = paged_sub_tiles(n_cols, gather);
+  int stages = (o && o->stages > 0) ? o->stages : 12 / sub;  // stages hold `sub` 128-token tiles each
   const int min_stages = gather ? 6 : 2;
-  while (stages > min_stages && (int)paged_smem_layout(n_cols, stages, batch).total > smem_limit) --stages;
-  if (stages < min_stages || (int)paged_smem_layout(n_cols, stages, batch).total > smem_limit)
+  while (stages > min_stages && (int)paged_smem_layout(n_cols, stages, batch, sub).total > smem_limit) --stages;
+  if (stages < min_stages || (int)paged_smem_layout(n_cols, stages, batch, sub).total > smem_limit)
     return fail(FP8IDX_ERR_UNSUPPORTED, "decode: shared memory too small for %d stages", stages);
   // Upper bound on work items without reading context_lens: every request
   // full to max_model_len.  The persistent grid never exceeds the SM count.
-  const int64_t tiles_per_req = (static_cast<int64_t>(std::max(max_model_len, 0)) + kTileTokens - 1) / kTileTokens;
+  const int64_t item_tokens = static_cast<int64_t>(kTileTokens) * sub;
+  const int64_t tiles_per_req = (static_cast<int64_t>(std::max(max_model_len, 0)) + item_tokens - 1) / item_tokens;
   const int64_t items_ub = static_cast<int64_t>(batch) * tiles_per_req;
   int grid = static_cast<int>(std::min<int64_t>(num_sms, std::max<int64_t>(items_ub, 1)));
   if (o && o->num_ctas > 0) grid = std::min(o->num_ctas, num_sms);
   std::memset(plan, 0, sizeof(*plan));
   plan->grid = grid;
   plan->threads = paged_threads(gather);
-  plan->smem_bytes = (int)paged_smem_layout(n_cols, stages, batch).total;
+  plan->smem_bytes = (int)paged_smem_layout(n_cols, stages, batch, sub).total;
   plan->stages = stages;
   plan->tile_n = n_cols;
   plan->block_m = next_n;
@@ -306,7 +308,8 @@ fp8idx_status paged_impl(const fp8idx_tensor* q, const fp8idx_tensor* kv, const 
   p.block_size = (int32_t)blk;
   p.n_cols = n_cols;
   p.stages = plan.stages;
-  p.acc_bufs = paged_acc_buffers(n_cols);
+  p.sub_tiles = paged_sub_tiles(n_cols, plan.gather != 0);
+  p.acc_bufs = paged_acc_buffers(n_cols, p.sub_tiles);
   cudaError_t e = launch_paged(tm_q, tm_kv, tm_sc, p, (int)H, plan.gather != 0, plan.grid, plan.smem_bytes,
                                static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));

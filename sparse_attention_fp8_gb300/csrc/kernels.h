@@ -33,7 +33,8 @@ struct PagedParams {
   int32_t block_size;
   int32_t n_cols;    // next_n * heads = MMA N
   int32_t stages;
-  int32_t acc_bufs;  // TMEM accumulator buffers: paged_acc_buffers(n_cols)
+  int32_t acc_bufs;   // TMEM accumulator buffers: paged_acc_buffers(n_cols, sub_tiles)
+  int32_t sub_tiles;  // 128-token MMA tiles per pipeline item (1 or 2)
 };
 
 // Two epilogue warpgroups take alternate tiles; tensor memory holds 2..16
@@ -41,12 +42,21 @@ struct PagedParams {
 // n_cols), so the MMA warp can run that many tiles ahead of the epilogue.
 constexpr int kEpiGroups = 2;
 constexpr int kMaxAccBufs = 16;
-__host__ __device__ constexpr int paged_acc_buffers(int n_cols) {
-  return n_cols <= 32 ? 16 : n_cols <= 64 ? 8 : n_cols <= 128 ? 4 : 2;
+__host__ __device__ constexpr int pow2_cols(int n_cols) {
+  return n_cols <= 32 ? 32 : n_cols <= 64 ? 64 : n_cols <= 128 ? 128 : 256;
+}
+// Decode pipeline items: two 128-token tiles per item (one barrier round
+// trip for 256 tokens) when two accumulators of an item still leave room for
+// double buffering, else one.  The per-block gather path keeps one.
+__host__ __device__ constexpr int paged_sub_tiles(int n_cols, bool gather) {
+  return (!gather && n_cols <= 128) ? 2 : 1;
+}
+__host__ __device__ constexpr int paged_acc_buffers(int n_cols, int sub_tiles = 1) {
+  return 512 / (pow2_cols(n_cols) * sub_tiles) > kMaxAccBufs ? kMaxAccBufs : 512 / (pow2_cols(n_cols) * sub_tiles);
 }
 
 // Roles: producer warp(s), one MMA warp, kEpiGroups epilogue warpgroups.
-__host__ __device__ constexpr int paged_producer_warps(bool gather) { return gather ? 2 : 1; }
+__host__ __device__ constexpr int paged_producer_warps(bool gather) { return 2; }
 __host__ __device__ constexpr int paged_threads(bool gather) {
   return 32 * (paged_producer_warps(gather) + 1 + 4 * kEpiGroups);
 }
@@ -54,12 +64,12 @@ __host__ __device__ constexpr int paged_threads(bool gather) {
 struct PagedSmem {
   uint32_t q, k, scale, w, tp, bars, misc, total;
 };
-__host__ __device__ inline PagedSmem paged_smem_layout(int n_cols, int stages, int batch) {
+__host__ __device__ inline PagedSmem paged_smem_layout(int n_cols, int stages, int batch, int sub_tiles) {
   PagedSmem L;
   uint32_t off = 0;
   L.q = off;     off += 2u * n_cols * kHeadDim;          // two Q buffers (1024-aligned: n_cols % 8 == 0)
-  L.k = off;     off += (uint32_t)stages * kKTileBytes;   // K tile ring
-  L.scale = off; off += (uint32_t)stages * kTileTokens * 4;
+  L.k = off;     off += (uint32_t)(stages * sub_tiles) * kKTileBytes;   // K ring: sub_tiles tiles per stage
+  L.scale = off; off += (uint32_t)(stages * sub_tiles) * kTileTokens * 4;
   L.w = off;     off += 2u * n_cols * 4;                  // two weight rows
   L.tp = off;    off += (uint32_t)(batch + 1) * 4;        // per-request tile prefix
   off = (off + 7u) & ~7u;

@@ -111,8 +111,13 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
   const int S = p.stages;
   const int B = p.batch;
   const int AB = p.acc_bufs;
-  const uint32_t acc_cols = kTmemCols / AB;
-  const PagedSmem L = paged_smem_layout(N, S, B);
+  const int T = p.sub_tiles;                         // 128-token tiles per item
+  const int ITEM = kTileTokens * T;                  // tokens per item
+  const uint32_t acc_cols = kTmemCols / AB;          // TMEM columns per item
+  const uint32_t sub_cols = acc_cols / T;            // ... per 128-token tile
+  const uint32_t stage_k = static_cast<uint32_t>(T) * kKTileBytes;
+  const uint32_t stage_sc = static_cast<uint32_t>(T) * kTileTokens;  // scales (floats) per stage
+  const PagedSmem L = paged_smem_layout(N, S, B, T);
   uint8_t* q_s = smem + L.q;
   uint8_t* k_s = smem + L.k;
   float* sc_s = reinterpret_cast<float*>(smem + L.scale);
@@ -136,7 +141,7 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
   // ---- prologue: per-request tile counts, barriers, tensor memory --------
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
     const int64_t c = clamp_ctx(__ldg(p.context_lens + b), p);
-    tp[b + 1] = static_cast<int32_t>((c + kTileTokens - 1) / kTileTokens);
+    tp[b + 1] = static_cast<int32_t>((c + ITEM - 1) / ITEM);
   }
   if (threadIdx.x == 0) {
     tp[0] = 0;
@@ -201,53 +206,60 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
     int issued = 0, q_issued = 0;
     int64_t ctx_eff = 0;
     if constexpr (!GATHER) {
+      // Two producer warps take alternate items; both walk every item to keep
+      // the ring and the block-table prefetch in step.  Warp 0 also loads Q.
+      const int pw = warp;              // 0..1
       const int blk = p.block_size;     // 16, 32, 64 or 128
-      const int P = kTileTokens / blk;  // cache blocks per tile
+      const int P = ITEM / blk;         // cache blocks per item (divides 32)
       const uint32_t blk_bytes = static_cast<uint32_t>(blk) * (kHeadDim + 4);
       const uint32_t blk_k_bytes = static_cast<uint32_t>(blk) * kHeadDim;
       int chunk = 0, need_blocks = 0;
       int32_t tbl_cur = 0, tbl_nxt = 0;
       for (int it = 0; it < n_items; ++it) {
         if (it == 0 || cur.t == 0) {
-          if (!warp_wait_bounded(qe0 + 8u * qr.idx, qr.phase ^ 1u, abort_flag, &g_paged_watchdog, kSiteQEmpty))
-            break;
-          if (lane == 0) {
-            const uint32_t qf = qf0 + 8u * qr.idx;
-            ptx::mbar_arrive_expect_tx(qf, N * (kHeadDim + 4));
-            ptx::tma_load_2d(ptx::smem_u32(q_s + qr.idx * N * kHeadDim), &tm_q, qf, 0, cur.b * N);
-            ptx::bulk_g2s(ptx::smem_u32(w_s + qr.idx * N), p.weights + static_cast<int64_t>(cur.b) * N, N * 4, qf);
+          if (pw == 0) {
+            if (!warp_wait_bounded(qe0 + 8u * qr.idx, qr.phase ^ 1u, abort_flag, &g_paged_watchdog, kSiteQEmpty))
+              break;
+            if (lane == 0) {
+              const uint32_t qf = qf0 + 8u * qr.idx;
+              ptx::mbar_arrive_expect_tx(qf, N * (kHeadDim + 4));
+              ptx::tma_load_2d(ptx::smem_u32(q_s + qr.idx * N * kHeadDim), &tm_q, qf, 0, cur.b * N);
+              ptx::bulk_g2s(ptx::smem_u32(w_s + qr.idx * N), p.weights + static_cast<int64_t>(cur.b) * N, N * 4, qf);
+            }
+            qr.next();
+            ++q_issued;
           }
-          qr.next();
-          ++q_issued;
           ctx_eff = clamp_ctx(__ldg(p.context_lens + cur.b), p);
           need_blocks = static_cast<int>((ctx_eff + blk - 1) / blk);
           chunk = (cur.t * P) & ~31;
           tbl_cur = load_table(p, cur.b, chunk + lane, need_blocks);
           tbl_nxt = load_table(p, cur.b, chunk + 32 + lane, need_blocks);
         }
+        const int first_blk = cur.t * P;
+        const int32_t id = __shfl_sync(0xffffffffu, tbl_cur, (first_blk - chunk + lane) & 31);
+        if ((it & 1) == pw) {
         if (!warp_wait_bounded(empty0 + 8u * st.idx, st.phase ^ 1u, abort_flag, &g_paged_watchdog, kSiteStageEmpty))
           break;
-        const int first_blk = cur.t * P;
-        const int valid = min(kTileTokens, static_cast<int>(ctx_eff - static_cast<int64_t>(cur.t) * kTileTokens));
+        const int valid = min(ITEM, static_cast<int>(ctx_eff - static_cast<int64_t>(cur.t) * ITEM));
         const int nblk = (valid + blk - 1) / blk;
         const uint32_t full = full0 + 8u * st.idx;
         if (lane == 0) ptx::mbar_arrive_expect_tx(full, nblk * blk_bytes);
         __syncwarp();
-        const int32_t id = __shfl_sync(0xffffffffu, tbl_cur, (first_blk - chunk + lane) & 31);
         if (lane < nblk) {
           const int32_t page = clamp_block(id, p.num_blocks);
-          ptx::tma_load_3d(ptx::smem_u32(k_s + st.idx * kKTileBytes + lane * blk_k_bytes), &tm_kv, full, 0, 0, page);
+          ptx::tma_load_3d(ptx::smem_u32(k_s + st.idx * stage_k + lane * blk_k_bytes), &tm_kv, full, 0, 0, page);
           // A tensor TMA needs a 128-byte-aligned destination: block sizes
           // >= 32 give one per block; block size 16 (64-byte scale runs)
           // uses the plain bulk copy, which needs only 16 bytes.
           if (blk >= 32)
-            ptx::tma_load_2d(ptx::smem_u32(sc_s + st.idx * kTileTokens + lane * blk), &tm_sc, full, 0, page);
+            ptx::tma_load_2d(ptx::smem_u32(sc_s + st.idx * stage_sc + lane * blk), &tm_sc, full, 0, page);
           else
-            ptx::bulk_g2s(ptx::smem_u32(sc_s + st.idx * kTileTokens + lane * blk),
+            ptx::bulk_g2s(ptx::smem_u32(sc_s + st.idx * stage_sc + lane * blk),
                           p.kv_cache + static_cast<int64_t>(page) * blk_bytes + blk_k_bytes, blk * 4, full);
         }
-        st.next();
         issued = it + 1;
+        }
+        st.next();
         if (first_blk + P >= chunk + 32) {  // next tile starts a new 32-block chunk
           chunk += 32;
           tbl_cur = tbl_nxt;
@@ -257,7 +269,7 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
       }
       if (*abort_flag && lane == 0) {  // let issued copies land before the CTA exits
         for (int it = max(0, issued - S); it < issued; ++it)
-          wait_drain(full0 + 8u * (it % S), (it / S) & 1, &g_paged_watchdog);
+          if ((it & 1) == pw) wait_drain(full0 + 8u * (it % S), (it / S) & 1, &g_paged_watchdog);
         for (int sg = max(0, q_issued - 2); sg < q_issued; ++sg)
           wait_drain(qf0 + 8u * (sg & 1), (sg >> 1) & 1, &g_paged_watchdog);
       }
@@ -375,11 +387,13 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
         if (!wait_bounded(full0 + 8u * st.idx, st.phase, abort_flag, &g_paged_watchdog, kSiteStageFull)) break;
         if (!wait_bounded(acce0 + 8u * ac.idx, ac.phase ^ 1u, abort_flag, &g_paged_watchdog, kSiteAccEmpty)) break;
         ptx::tc_fence_after();
-        const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(st.idx) * (kKTileBytes >> 4);
-        const uint32_t d_tmem = tmem + ac.idx * acc_cols;
+        for (int k = 0; k < T; ++k) {  // one 128-token tile per sub-tile, into its own TMEM columns
+          const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(st.idx * T + k) * (kKTileBytes >> 4);
+          const uint32_t d_tmem = tmem + ac.idx * acc_cols + k * sub_cols;
 #pragma unroll
-        for (int kk = 0; kk < kHeadDim / 32; ++kk)  // K = 32 e4m3 per MMA: advance 32 bytes in the swizzled row
-          ptx::mma_f8f6f4(d_tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kHeadDim / 32; ++kk)  // K = 32 e4m3 per MMA: advance 32 bytes in the swizzled row
+            ptx::mma_f8f6f4(d_tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, kk > 0 ? 1u : 0u);
+        }
         ptx::mma_commit(empty0 + 8u * st.idx);
         ptx::mma_commit(accf0 + 8u * ac.idx);
         st.next();
@@ -414,27 +428,34 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
       }
       if ((it & 1) == grp) {
         if (!warp_wait_bounded(full0 + 8u * st.idx, st.phase, abort_flag, &g_paged_watchdog, kSiteStageFull)) break;
-        const float scale = sc_s[st.idx * kTileTokens + row];
+        const float scale0 = sc_s[st.idx * stage_sc + row];
+        const float scale1 = T > 1 ? sc_s[st.idx * stage_sc + kTileTokens + row] : 0.f;
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(empty0 + 8u * st.idx);
         if (!warp_wait_bounded(accf0 + 8u * ac.idx, ac.phase, abort_flag, &g_paged_watchdog, kSiteAccFull)) break;
         ptx::tc_fence_after();
-        const uint32_t taddr = tmem + ac.idx * acc_cols + (static_cast<uint32_t>(quad * 32) << 16);
-        const int64_t pos = static_cast<int64_t>(cur.t) * kTileTokens + row;
         const int64_t last = static_cast<int64_t>(ctx) - next_n;
-        float* out_col = p.out + static_cast<int64_t>(cur.b) * next_n * p.out_stride + pos;
         const uint32_t acce = acce0 + 8u * ac.idx;
-        reduce_rows<HEADS, 8>(
-            taddr, w, next_n,
-            [&]() {
-              ptx::tc_fence_before();
-              __syncwarp();
-              if (lane == 0) ptx::mbar_arrive(acce);
-            },
-            [&](int n, float v) {
-              if (pos <= last + n && pos < p.max_model_len)
-                __stcs(out_col + static_cast<int64_t>(n) * p.out_stride, v * scale);
-            });
+        for (int k = 0; k < T; ++k) {
+          const uint32_t taddr = tmem + ac.idx * acc_cols + k * sub_cols + (static_cast<uint32_t>(quad * 32) << 16);
+          const int64_t pos = static_cast<int64_t>(cur.t) * ITEM + k * kTileTokens + row;
+          const float scale = k ? scale1 : scale0;
+          float* out_col = p.out + static_cast<int64_t>(cur.b) * next_n * p.out_stride + pos;
+          const bool last_sub = (k + 1 == T);
+          reduce_rows<HEADS, 8>(
+              taddr, w, next_n,
+              [&]() {
+                if (last_sub) {
+                  ptx::tc_fence_before();
+                  __syncwarp();
+                  if (lane == 0) ptx::mbar_arrive(acce);
+                }
+              },
+              [&](int n, float v) {
+                if (pos <= last + n && pos < p.max_model_len)
+                  __stcs(out_col + static_cast<int64_t>(n) * p.out_stride, v * scale);
+              });
+        }
       }
       st.next();
       ac.next();

@@ -50,7 +50,7 @@ def test_planner_decode(lib):
     assert p.grid == 148 and p.tile_n == 192 and p.gather == 0
     assert p.smem_bytes <= 232448 and p.stages >= 4
     small = fp8idx.plan_paged(1, 1, 32, 128, 64, 1024, num_sms=148)
-    assert small.grid == 8  # one CTA per 128-token tile when there are fewer tiles than SMs
+    assert small.grid == 4  # one CTA per 256-token item when there are fewer items than SMs
     g = fp8idx.plan_paged(64, 4, 64, 128, 1, 32768, num_sms=148)
     assert g.gather == 1 and g.tile_n == 256 and g.stages >= 6
     o = fp8idx.plan_paged(16, 6, 32, 128, 64, 1048576, num_sms=148, options=fp8idx.Options(num_ctas=7, stages=3))
