@@ -77,17 +77,25 @@ struct Ring {
   }
 };
 
-// acc0 + acc1 += sum_{j<32} relu(x_j) * w_j for one 32-column TMEM chunk in
-// registers and its 32 weights in registers.  Two packed f32x2 accumulators.
+// One 32-column TMEM chunk in registers, with its 32 weights in registers:
+//   acc0 += sum over even pairs of max(x, 0) * w
+//   acc1 += sum over odd pairs of (x + |x|) * w   (= 2 * relu(x) * w, exact)
+// so that sum_j relu(x_j) * w_j = acc0.x + acc0.y + (acc1.x + acc1.y) / 2.
+// Half of the ReLUs run as max on the ALU pipe and half as an add with an
+// absolute-value operand on the FMA pipe, which balances the two pipes.
 __device__ __forceinline__ void relu_dot32(const uint32_t (&r)[32], const float4 (&wv)[8], float2& acc0,
                                            float2& acc1) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const float2 x01 = make_float2(fmaxf(__uint_as_float(r[4 * j + 0]), 0.f), fmaxf(__uint_as_float(r[4 * j + 1]), 0.f));
-    const float2 x23 = make_float2(fmaxf(__uint_as_float(r[4 * j + 2]), 0.f), fmaxf(__uint_as_float(r[4 * j + 3]), 0.f));
-    acc0 = __ffma2_rn(x01, make_float2(wv[j].x, wv[j].y), acc0);
-    acc1 = __ffma2_rn(x23, make_float2(wv[j].z, wv[j].w), acc1);
+    const float x0 = __uint_as_float(r[4 * j + 0]), x1 = __uint_as_float(r[4 * j + 1]);
+    const float x2 = __uint_as_float(r[4 * j + 2]), x3 = __uint_as_float(r[4 * j + 3]);
+    acc0 = __ffma2_rn(make_float2(fmaxf(x0, 0.f), fmaxf(x1, 0.f)), make_float2(wv[j].x, wv[j].y), acc0);
+    acc1 = __ffma2_rn(make_float2(x2 + fabsf(x2), x3 + fabsf(x3)), make_float2(wv[j].z, wv[j].w), acc1);
   }
+}
+
+__device__ __forceinline__ float relu_dot_total(float2 acc0, float2 acc1) {
+  return (acc0.x + acc0.y) + 0.5f * (acc1.x + acc1.y);
 }
 
 // The epilogue's TMEM-to-register reduction for one tile and one thread's
@@ -124,7 +132,7 @@ __device__ __forceinline__ void reduce_rows(uint32_t taddr, const float* w, int 
         release();
       relu_dot32(cur, wv, a0, a1);
       if ((c + 1) % kChunksPerRow == 0) {
-        emit(c / kChunksPerRow, (a0.x + a0.y) + (a1.x + a1.y));
+        emit(c / kChunksPerRow, relu_dot_total(a0, a1));
         a0 = make_float2(0.f, 0.f);
         a1 = make_float2(0.f, 0.f);
       }
