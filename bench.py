@@ -320,7 +320,7 @@ def run_ours(args, rank, world):
         # previous contents and the read writes back the dirty lines here,
         # outside the timed region, so each timed call starts from a clean L2.
         flush.zero_()
-        torch.sum(flush, dtype=torch.int64, out=flush_sink)
+        torch.sum(flush, dim=0, dtype=torch.int64, out=flush_sink)
     torch.cuda.synchronize()
     sampler = ClockSampler(dev.index)
     sampler.start()
