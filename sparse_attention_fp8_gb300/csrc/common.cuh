@@ -30,7 +30,7 @@ enum WaitSite : uint32_t {
 // has aborted or the wait ran out (then it aborts the CTA and flags `wd`).
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                              unsigned int* wd, uint32_t site) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
+  if (ptx::mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   while (true) {
 #pragma unroll 1
@@ -57,9 +57,13 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, unsign
   }
 }
 
-// One warp-collective bounded wait: lane 0 polls, the verdict is broadcast.
+// One warp-collective bounded wait.  Fast path: every lane tests the phase
+// and the warp votes (a completed phase cannot be overtaken before this
+// warp's own later arrivals, so the lanes agree).  Slow path: lane 0 polls,
+// the verdict is broadcast.
 __device__ __forceinline__ bool warp_wait_bounded(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                                   unsigned int* wd, uint32_t site) {
+  if (__all_sync(0xffffffffu, ptx::mbar_test_wait(bar, parity))) return true;
   int ok = 0;
   if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, abort_flag, wd, site) ? 1 : 0;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
