@@ -103,34 +103,34 @@ __device__ __forceinline__ float relu_dot_total(float2 acc0, float2 acc1) {
 }
 
 // The epilogue's TMEM-to-register reduction for one tile and one thread's
-// token: output row k (k < nrows) is sum_h relu(acc[k*HEADS + h]) * w[k*HEADS + h]
-// over TMEM columns starting at `taddr`.  The 32-column loads are
+// token: output row k (k < NCH * 32 / HEADS) is
+//   sum_h relu(acc[k*HEADS + h]) * w[k*HEADS + h]
+// over the NCH 32-column chunks starting at TMEM address `taddr`.  The chunk
+// count is a template parameter so the loop is straight-line code.  Loads are
 // double-buffered (chunk c+1 is in flight while chunk c is reduced) and each
 // chunk's 32 weights are read from shared memory (broadcast) before waiting
 // on its data; once the last load has landed `release()` hands the
-// accumulator back to the MMA warp, and `emit(k, sum)` receives each finished
-// row.  At most MAX_CHUNKS chunks.
-template <int HEADS, int MAX_CHUNKS, class Release, class Emit>
-__device__ __forceinline__ void reduce_rows(uint32_t taddr, const float* w, int nrows, Release release, Emit emit) {
+// accumulator back to the MMA warp, and `emit(k, sum)` receives each row.
+template <int HEADS, int NCH, class Release, class Emit>
+__device__ __forceinline__ void reduce_rows(uint32_t taddr, const float* w, Release release, Emit emit) {
   constexpr int kChunksPerRow = HEADS / 32;
-  const int nchunks = nrows * kChunksPerRow;
-  uint32_t ra[32], rb[32];
-  float4 wv[8];
-  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
-  if (nchunks > 0)
-    ptx::tmem_ld_32x32b_x32(taddr, ra);
-  else
+  static_assert(NCH >= 0 && NCH % kChunksPerRow == 0, "whole rows");
+  if constexpr (NCH == 0) {
     release();
+  } else {
+    uint32_t ra[32], rb[32];
+    float4 wv[8];
+    float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+    ptx::tmem_ld_32x32b_x32(taddr, ra);
 #pragma unroll
-  for (int c = 0; c < MAX_CHUNKS; ++c) {
-    if (c < nchunks) {
+    for (int c = 0; c < NCH; ++c) {
       uint32_t(&cur)[32] = (c & 1) ? rb : ra;
       uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
       const float4* w4 = reinterpret_cast<const float4*>(w + c * 32);
 #pragma unroll
       for (int j = 0; j < 8; ++j) wv[j] = w4[j];
       ptx::tmem_wait_ld_regs(cur);
-      if (c + 1 < nchunks)
+      if (c + 1 < NCH)
         ptx::tmem_ld_32x32b_x32(taddr + (c + 1) * 32, nxt);
       else
         release();
@@ -141,6 +141,29 @@ __device__ __forceinline__ void reduce_rows(uint32_t taddr, const float* w, int 
         a1 = make_float2(0.f, 0.f);
       }
     }
+  }
+}
+
+template <int N>
+struct IntC {
+  static constexpr int value = N;
+};
+
+// Calls f(IntC<n>{}) for the runtime chunk count n, 1 <= n <= MAX (n a
+// multiple of STEP); the per-count code is instantiated once per kernel.
+template <int STEP, int MAX, class F>
+__device__ __forceinline__ void with_chunk_count(int n, F f) {
+  static_assert(MAX <= 8, "at most 8 chunks (256 columns)");
+  switch (n) {
+    case 1: if constexpr (STEP == 1 && MAX >= 1) f(IntC<1>{}); break;
+    case 2: if constexpr (MAX >= 2) f(IntC<2>{}); break;
+    case 3: if constexpr (STEP == 1 && MAX >= 3) f(IntC<3>{}); break;
+    case 4: if constexpr (MAX >= 4) f(IntC<4>{}); break;
+    case 5: if constexpr (STEP == 1 && MAX >= 5) f(IntC<5>{}); break;
+    case 6: if constexpr (MAX >= 6) f(IntC<6>{}); break;
+    case 7: if constexpr (STEP == 1 && MAX >= 7) f(IntC<7>{}); break;
+    case 8: if constexpr (MAX >= 8) f(IntC<8>{}); break;
+    default: break;
   }
 }
 

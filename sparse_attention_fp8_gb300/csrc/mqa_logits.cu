@@ -241,79 +241,84 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
     const int quad = warp & 3;            // TMEM lane quadrant
     const int row = quad * 32 + lane;     // token within the tile
     const float ninf = __int_as_float(0xff800000);
-    Ring st{0u, 0u, static_cast<uint32_t>(S)};
-    Ring ac{0u, 0u, static_cast<uint32_t>(AB)};
-    Ring qr{0u, 0u, 2u};
-    int ci = 0, fi = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const Unit U = load_unit(p, u, num_rb, n_tiles);
-      if (!(ok = warp_wait_bounded(qf0 + 8u * qr.idx, qr.phase, abort_flag, &g_prefill_watchdog, kSiteQFull)))
-        break;
-      const float* w = w_s + qr.idx * N;
-      for (int k = 0; k < U.n_j; ++k) {
-        const int j = U.sidx + k * p.split;
-        const int col0 = j * kTileTokens;
-        if (j >= U.t_lo && j < U.t_hi) {
-          const bool mine = (ci & 1) == grp;
-          ++ci;
-          if (mine) {
-            if (!(ok = warp_wait_bounded(full0 + 8u * st.idx, st.phase, abort_flag, &g_prefill_watchdog,
-                                         kSiteStageFull)))
-              break;
-            const float scale = sc_s[st.idx * kTileTokens + row];
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(empty0 + 8u * st.idx);
-            if (!(ok = warp_wait_bounded(accf0 + 8u * ac.idx, ac.phase, abort_flag, &g_prefill_watchdog,
-                                         kSiteAccFull)))
-              break;
-            ptx::tc_fence_after();
-            const uint32_t taddr = tmem + ac.idx * acc_cols + (static_cast<uint32_t>(quad * 32) << 16);
-            const int n = col0 + row;
-            const uint32_t acce = acce0 + 8u * ac.idx;
-            reduce_rows<HEADS, 8>(
-                taddr, w, BM,
-                [&]() {
-                  ptx::tc_fence_before();
-                  __syncwarp();
-                  if (lane == 0) ptx::mbar_arrive(acce);
-                },
-                [&](int r, float v) {
-                  const int lo = __shfl_sync(0xffffffffu, U.row_lo, r);
-                  const int hi = __shfl_sync(0xffffffffu, U.row_hi, r);
-                  const int m = U.m0 + r;
-                  if (m < p.rows && n < p.cols)
-                    __stcs(p.out + static_cast<int64_t>(m) * p.out_stride + n, (n >= lo && n < hi) ? v * scale : ninf);
-                });
-          }
-          st.next();
-          ac.next();
-        } else {
-          // a tile no row of the block reaches: -inf for all the block's rows
-          const bool mine = (fi & 1) == grp;
-          ++fi;
-          if (!mine) continue;
-          const int ncols = min(kTileTokens, p.cols - col0);
-          if (p.vec_ok && ncols == kTileTokens) {
-            const float4 f4 = make_float4(ninf, ninf, ninf, ninf);
-            for (int e = et; e < BM * 32; e += 128) {
-              const int m = U.m0 + (e >> 5);
-              if (m < p.rows)
-                __stcs(reinterpret_cast<float4*>(p.out + static_cast<int64_t>(m) * p.out_stride + col0) + (e & 31), f4);
+    // The loop is instantiated per chunk count (block_m * heads / 32).
+    const auto run = [&](auto nchunks) {
+      constexpr int NCH = decltype(nchunks)::value;
+      Ring st{0u, 0u, static_cast<uint32_t>(S)};
+      Ring ac{0u, 0u, static_cast<uint32_t>(AB)};
+      Ring qr{0u, 0u, 2u};
+      int ci = 0, fi = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const Unit U = load_unit(p, u, num_rb, n_tiles);
+        if (!(ok = warp_wait_bounded(qf0 + 8u * qr.idx, qr.phase, abort_flag, &g_prefill_watchdog, kSiteQFull)))
+          break;
+        const float* w = w_s + qr.idx * N;
+        for (int k = 0; k < U.n_j; ++k) {
+          const int j = U.sidx + k * p.split;
+          const int col0 = j * kTileTokens;
+          if (j >= U.t_lo && j < U.t_hi) {
+            const bool mine = (ci & 1) == grp;
+            ++ci;
+            if (mine) {
+              if (!(ok = warp_wait_bounded(full0 + 8u * st.idx, st.phase, abort_flag, &g_prefill_watchdog,
+                                           kSiteStageFull)))
+                break;
+              const float scale = sc_s[st.idx * kTileTokens + row];
+              __syncwarp();
+              if (lane == 0) ptx::mbar_arrive(empty0 + 8u * st.idx);
+              if (!(ok = warp_wait_bounded(accf0 + 8u * ac.idx, ac.phase, abort_flag, &g_prefill_watchdog,
+                                           kSiteAccFull)))
+                break;
+              ptx::tc_fence_after();
+              const uint32_t taddr = tmem + ac.idx * acc_cols + (static_cast<uint32_t>(quad * 32) << 16);
+              const int n = col0 + row;
+              const uint32_t acce = acce0 + 8u * ac.idx;
+              reduce_rows<HEADS, NCH>(
+                  taddr, w,
+                  [&]() {
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(acce);
+                  },
+                  [&](int r, float v) {
+                    const int lo = __shfl_sync(0xffffffffu, U.row_lo, r);
+                    const int hi = __shfl_sync(0xffffffffu, U.row_hi, r);
+                    const int m = U.m0 + r;
+                    if (m < p.rows && n < p.cols)
+                      __stcs(p.out + static_cast<int64_t>(m) * p.out_stride + n, (n >= lo && n < hi) ? v * scale : ninf);
+                  });
             }
+            st.next();
+            ac.next();
           } else {
-            for (int rr = 0; rr < BM; ++rr) {
-              const int m = U.m0 + rr;
-              if (m < p.rows && row < ncols) __stcs(p.out + static_cast<int64_t>(m) * p.out_stride + col0 + row, ninf);
+            // a tile no row of the block reaches: -inf for all the block's rows
+            const bool mine = (fi & 1) == grp;
+            ++fi;
+            if (!mine) continue;
+            const int ncols = min(kTileTokens, p.cols - col0);
+            if (p.vec_ok && ncols == kTileTokens) {
+              const float4 f4 = make_float4(ninf, ninf, ninf, ninf);
+              for (int e = et; e < BM * 32; e += 128) {
+                const int m = U.m0 + (e >> 5);
+                if (m < p.rows)
+                  __stcs(reinterpret_cast<float4*>(p.out + static_cast<int64_t>(m) * p.out_stride + col0) + (e & 31), f4);
+              }
+            } else {
+              for (int rr = 0; rr < BM; ++rr) {
+                const int m = U.m0 + rr;
+                if (m < p.rows && row < ncols) __stcs(p.out + static_cast<int64_t>(m) * p.out_stride + col0 + row, ninf);
+              }
             }
           }
         }
+        if (!ok) break;
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(qe0 + 8u * qr.idx);
+        qr.next();
       }
-      if (!ok) break;
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(qe0 + 8u * qr.idx);
-      qr.next();
-    }
+    };
+    with_chunk_count<HEADS / 32, 8>(BM * (HEADS / 32), run);
   }
 
   ptx::tc_fence_before();

@@ -148,11 +148,12 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
     misc[1] = 0u;
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(full0 + 8u * s, GATHER ? 32u * kProdWarps : 1u);
-      ptx::mbar_init(empty0 + 8u * s, 1u + 4u);  // MMA commit + the 4 warps that read the tile's scales
+      // MMA commit + the epilogue warps that read the stage's scales
+      ptx::mbar_init(empty0 + 8u * s, 1u + 4u * (T > 1 ? kEpiGroups : 1));
     }
     for (int g = 0; g < AB; ++g) {
       ptx::mbar_init(accf0 + 8u * g, 1u);
-      ptx::mbar_init(acce0 + 8u * g, 4u);
+      ptx::mbar_init(acce0 + 8u * g, 4u * (T > 1 ? kEpiGroups : 1));  // the epilogue warps that read it
     }
     for (int g = 0; g < 2; ++g) {
       ptx::mbar_init(qf0 + 8u * g, 1u);
@@ -410,61 +411,71 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
     }
   } else {
     // =========================== epilogue ===============================
+    // With two 128-token tiles per item both warpgroups work on every item,
+    // group g on tile g, so an accumulator goes back to the MMA warp after
+    // half the time.  With one tile per item the groups take alternate items
+    // (all next_n rows each), which keeps the per-tile barrier traffic of a
+    // wide accumulator at one round per group and tile.  The loop is
+    // instantiated per chunk count (next_n * heads / 32).
     const int ew = warp - kEpiWarp0;   // 0 .. 4*kEpiGroups-1
-    const int grp = ew >> 2;           // serves tiles with it % 2 == grp
+    const int grp = ew >> 2;
     const int quad = warp & 3;         // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;  // token within the tile
     const int next_n = p.next_n;
-    Ring st{0u, 0u, static_cast<uint32_t>(S)};
-    Ring ac{0u, 0u, static_cast<uint32_t>(AB)};
-    Ring qr{0u, 0u, 2u};
-    int32_t ctx = 0;
-    const float* w = w_s;
-    for (int it = 0; it < n_items; ++it) {
-      if (it == 0 || cur.t == 0) {
-        if (!warp_wait_bounded(qf0 + 8u * qr.idx, qr.phase, abort_flag, &g_paged_watchdog, kSiteQFull)) break;
-        w = w_s + qr.idx * N;
-        ctx = __ldg(p.context_lens + cur.b);
-      }
-      if ((it & 1) == grp) {
-        if (!warp_wait_bounded(full0 + 8u * st.idx, st.phase, abort_flag, &g_paged_watchdog, kSiteStageFull)) break;
-        const float scale0 = sc_s[st.idx * stage_sc + row];
-        const float scale1 = T > 1 ? sc_s[st.idx * stage_sc + kTileTokens + row] : 0.f;
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(empty0 + 8u * st.idx);
-        if (!warp_wait_bounded(accf0 + 8u * ac.idx, ac.phase, abort_flag, &g_paged_watchdog, kSiteAccFull)) break;
-        ptx::tc_fence_after();
-        const int64_t last = static_cast<int64_t>(ctx) - next_n;
-        const uint32_t acce = acce0 + 8u * ac.idx;
-        for (int k = 0; k < T; ++k) {
-          const uint32_t taddr = tmem + ac.idx * acc_cols + k * sub_cols + (static_cast<uint32_t>(quad * 32) << 16);
-          const int64_t pos = static_cast<int64_t>(cur.t) * ITEM + k * kTileTokens + row;
-          const float scale = k ? scale1 : scale0;
+    const auto run = [&](auto nchunks, auto shared) {
+      constexpr int NCH = decltype(nchunks)::value;
+      constexpr bool kShared = decltype(shared)::value != 0;
+      const int k_tile = kShared ? grp : 0;
+      const uint32_t col_off = static_cast<uint32_t>(k_tile) * sub_cols + (static_cast<uint32_t>(quad * 32) << 16);
+      Ring st{0u, 0u, static_cast<uint32_t>(S)};
+      Ring ac{0u, 0u, static_cast<uint32_t>(AB)};
+      Ring qr{0u, 0u, 2u};
+      int32_t ctx = 0;
+      const float* w = w_s;
+      for (int it = 0; it < n_items; ++it) {
+        if (it == 0 || cur.t == 0) {
+          if (!warp_wait_bounded(qf0 + 8u * qr.idx, qr.phase, abort_flag, &g_paged_watchdog, kSiteQFull)) break;
+          w = w_s + qr.idx * N;
+          ctx = __ldg(p.context_lens + cur.b);
+        }
+        if (kShared || (it & 1) == grp) {
+          if (!warp_wait_bounded(full0 + 8u * st.idx, st.phase, abort_flag, &g_paged_watchdog, kSiteStageFull))
+            break;
+          const float scale = sc_s[st.idx * stage_sc + k_tile * kTileTokens + row];
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(empty0 + 8u * st.idx);
+          if (!warp_wait_bounded(accf0 + 8u * ac.idx, ac.phase, abort_flag, &g_paged_watchdog, kSiteAccFull)) break;
+          ptx::tc_fence_after();
+          const int64_t pos = static_cast<int64_t>(cur.t) * ITEM + k_tile * kTileTokens + row;
+          const int64_t room = static_cast<int64_t>(ctx) - next_n - pos;  // row n is written iff n + room >= 0
+          const bool in_model = pos < p.max_model_len;
           float* out_col = p.out + static_cast<int64_t>(cur.b) * next_n * p.out_stride + pos;
-          const bool last_sub = (k + 1 == T);
-          reduce_rows<HEADS, 8>(
-              taddr, w, next_n,
+          const uint32_t acce = acce0 + 8u * ac.idx;
+          reduce_rows<HEADS, NCH>(
+              tmem + ac.idx * acc_cols + col_off, w,
               [&]() {
-                if (last_sub) {
-                  ptx::tc_fence_before();
-                  __syncwarp();
-                  if (lane == 0) ptx::mbar_arrive(acce);
-                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(acce);
               },
               [&](int n, float v) {
-                if (pos <= last + n && pos < p.max_model_len)
-                  __stcs(out_col + static_cast<int64_t>(n) * p.out_stride, v * scale);
+                if (n + room >= 0 && in_model) __stcs(out_col + static_cast<int64_t>(n) * p.out_stride, v * scale);
               });
         }
+        st.next();
+        ac.next();
+        if (cur.advance() || it + 1 == n_items) {
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(qe0 + 8u * qr.idx);
+          qr.next();
+        }
       }
-      st.next();
-      ac.next();
-      if (cur.advance() || it + 1 == n_items) {
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(qe0 + 8u * qr.idx);
-        qr.next();
-      }
-    }
+    };
+    const int nch = next_n * (HEADS / 32);
+    if (T > 1)
+      with_chunk_count<HEADS / 32, 4>(nch, [&](auto nc) { run(nc, IntC<1>{}); });
+    else
+      with_chunk_count<HEADS / 32, 8>(nch, [&](auto nc) { run(nc, IntC<0>{}); });
   }
 
   ptx::tc_fence_before();
