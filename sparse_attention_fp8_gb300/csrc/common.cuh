@@ -81,25 +81,42 @@ struct Ring {
   }
 };
 
-// One 32-column TMEM chunk in registers, with its 32 weights in registers:
-//   acc0 += sum over even pairs of max(x, 0) * w
-//   acc1 += sum over odd pairs of (x + |x|) * w   (= 2 * relu(x) * w, exact)
-// so that sum_j relu(x_j) * w_j = acc0.x + acc0.y + (acc1.x + acc1.y) / 2.
-// Half of the ReLUs run as max on the ALU pipe and half as an add with an
-// absolute-value operand on the FMA pipe, which balances the two pipes.
+// One 32-column TMEM chunk in registers, with its 32 weights in registers,
+// reduced into two float2 accumulators.  x + |x| = 2 * relu(x) exactly, and
+// doubling commutes with rounding, so every form below yields the same bits
+// once relu_dot_total applies its factor of 1/2.
+//  * PACKED: every ReLU as a packed x + |x| (one f32x2 add per pair), then a
+//    packed FMA with the weights: acc0/acc1 hold 2 * sum relu(x) * w.
+//  * otherwise: half of the ReLUs as max(x, 0) on the ALU pipe (acc0 holds
+//    sum relu(x) * w) and half as x + |x| on the FMA pipe (acc1 holds twice
+//    its sum), which balances the two pipes.
+// Which one is faster depends on the head count (measured: packed for 32
+// heads, mixed for 64).
+template <bool PACKED>
 __device__ __forceinline__ void relu_dot32(const uint32_t (&r)[32], const float4 (&wv)[8], float2& acc0,
                                            float2& acc1) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const float x0 = __uint_as_float(r[4 * j + 0]), x1 = __uint_as_float(r[4 * j + 1]);
     const float x2 = __uint_as_float(r[4 * j + 2]), x3 = __uint_as_float(r[4 * j + 3]);
-    acc0 = __ffma2_rn(make_float2(fmaxf(x0, 0.f), fmaxf(x1, 0.f)), make_float2(wv[j].x, wv[j].y), acc0);
-    acc1 = __ffma2_rn(make_float2(x2 + fabsf(x2), x3 + fabsf(x3)), make_float2(wv[j].z, wv[j].w), acc1);
+    if constexpr (PACKED) {
+      const float2 r01 = __fadd2_rn(make_float2(x0, x1), make_float2(fabsf(x0), fabsf(x1)));
+      const float2 r23 = __fadd2_rn(make_float2(x2, x3), make_float2(fabsf(x2), fabsf(x3)));
+      acc0 = __ffma2_rn(r01, make_float2(wv[j].x, wv[j].y), acc0);
+      acc1 = __ffma2_rn(r23, make_float2(wv[j].z, wv[j].w), acc1);
+    } else {
+      acc0 = __ffma2_rn(make_float2(fmaxf(x0, 0.f), fmaxf(x1, 0.f)), make_float2(wv[j].x, wv[j].y), acc0);
+      acc1 = __ffma2_rn(make_float2(x2 + fabsf(x2), x3 + fabsf(x3)), make_float2(wv[j].z, wv[j].w), acc1);
+    }
   }
 }
 
+template <bool PACKED>
 __device__ __forceinline__ float relu_dot_total(float2 acc0, float2 acc1) {
-  return (acc0.x + acc0.y) + 0.5f * (acc1.x + acc1.y);
+  if constexpr (PACKED)
+    return 0.5f * ((acc0.x + acc0.y) + (acc1.x + acc1.y));
+  else
+    return (acc0.x + acc0.y) + 0.5f * (acc1.x + acc1.y);
 }
 
 // The epilogue's TMEM-to-register reduction for one tile and one thread's
@@ -114,6 +131,7 @@ __device__ __forceinline__ float relu_dot_total(float2 acc0, float2 acc1) {
 template <int HEADS, int NCH, class Release, class Emit>
 __device__ __forceinline__ void reduce_rows(uint32_t taddr, const float* w, Release release, Emit emit) {
   constexpr int kChunksPerRow = HEADS / 32;
+  constexpr bool kPacked = HEADS == 32;
   static_assert(NCH >= 0 && NCH % kChunksPerRow == 0, "whole rows");
   if constexpr (NCH == 0) {
     release();
@@ -134,9 +152,9 @@ __device__ __forceinline__ void reduce_rows(uint32_t taddr, const float* w, Rele
         ptx::tmem_ld_32x32b_x32(taddr + (c + 1) * 32, nxt);
       else
         release();
-      relu_dot32(cur, wv, a0, a1);
+      relu_dot32<kPacked>(cur, wv, a0, a1);
       if ((c + 1) % kChunksPerRow == 0) {
-        emit(c / kChunksPerRow, relu_dot_total(a0, a1));
+        emit(c / kChunksPerRow, relu_dot_total<kPacked>(a0, a1));
         a0 = make_float2(0.f, 0.f);
         a1 = make_float2(0.f, 0.f);
       }
