@@ -119,44 +119,64 @@ __device__ __forceinline__ float relu_dot_total(float2 acc0, float2 acc1) {
     return (acc0.x + acc0.y) + 0.5f * (acc1.x + acc1.y);
 }
 
+// First chunk of round k when NB chunk buffers rotate: one chunk per round
+// with 2 buffers, rounds of 2 and 1 chunks alternating with 3, two with 4.
+template <int NB>
+__host__ __device__ constexpr int round_start(int k) {
+  return NB == 2 ? k : NB == 3 ? (3 * k + 1) / 2 : 2 * k;
+}
+
 // The epilogue's TMEM-to-register reduction for one tile and one thread's
 // token: output row k (k < NCH * 32 / HEADS) is
 //   sum_h relu(acc[k*HEADS + h]) * w[k*HEADS + h]
 // over the NCH 32-column chunks starting at TMEM address `taddr`.  The chunk
-// count is a template parameter so the loop is straight-line code.  Loads are
-// double-buffered (chunk c+1 is in flight while chunk c is reduced) and each
-// chunk's 32 weights are read from shared memory (broadcast) before waiting
-// on its data; once the last load has landed `release()` hands the
-// accumulator back to the MMA warp, and `emit(k, sum)` receives each row.
+// count is a template parameter so the loop is straight-line code.  Chunks
+// rotate through NB register buffers (chunk c in buffer c % NB).  Because
+// tcgen05.wait::ld waits for every outstanding load, the work is cut into
+// rounds: wait for the round's chunks, issue the next round's loads into the
+// free buffers, then reduce the round's chunks (weights read from shared
+// memory, a broadcast) while those loads are in flight.  Once the last load
+// has landed `release()` hands the accumulator back to the MMA warp;
+// `emit(k, sum)` receives each row.  NB (measured): 4 for six or more chunks
+// of 32 heads, else 3 (2 for a single chunk).
 template <int HEADS, int NCH, class Release, class Emit>
 __device__ __forceinline__ void reduce_rows(uint32_t taddr, const float* w, Release release, Emit emit) {
   constexpr int kChunksPerRow = HEADS / 32;
   constexpr bool kPacked = HEADS == 32;
+  constexpr int NB = (HEADS == 32 && NCH >= 6) ? 4 : NCH >= 2 ? 3 : 2;
   static_assert(NCH >= 0 && NCH % kChunksPerRow == 0, "whole rows");
   if constexpr (NCH == 0) {
     release();
   } else {
-    uint32_t ra[32], rb[32];
-    float4 wv[8];
+    uint32_t r[NB][32];
     float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
-    ptx::tmem_ld_32x32b_x32(taddr, ra);
 #pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-      uint32_t(&cur)[32] = (c & 1) ? rb : ra;
-      uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
-      const float4* w4 = reinterpret_cast<const float4*>(w + c * 32);
+    for (int c = 0; c < round_start<NB>(1) && c < NCH; ++c) ptx::tmem_ld_32x32b_x32(taddr + c * 32, r[c % NB]);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) wv[j] = w4[j];
-      ptx::tmem_wait_ld_regs(cur);
-      if (c + 1 < NCH)
-        ptx::tmem_ld_32x32b_x32(taddr + (c + 1) * 32, nxt);
-      else
+    for (int k = 0; round_start<NB>(k) < NCH; ++k) {
+      const int s0 = round_start<NB>(k);
+      const int e0 = round_start<NB>(k + 1) < NCH ? round_start<NB>(k + 1) : NCH;
+      const int e1 = round_start<NB>(k + 2) < NCH ? round_start<NB>(k + 2) : NCH;
+      ptx::tmem_wait_ld_regs(r[s0 % NB]);
+      if (e0 - s0 > 1) ptx::reg_fence(r[(s0 + 1) % NB]);
+      if (e0 < NCH) {
+#pragma unroll
+        for (int c = e0; c < e1; ++c) ptx::tmem_ld_32x32b_x32(taddr + c * 32, r[c % NB]);
+      } else {
         release();
-      relu_dot32<kPacked>(cur, wv, a0, a1);
-      if ((c + 1) % kChunksPerRow == 0) {
-        emit(c / kChunksPerRow, relu_dot_total<kPacked>(a0, a1));
-        a0 = make_float2(0.f, 0.f);
-        a1 = make_float2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int c = s0; c < e0; ++c) {
+        float4 wv[8];
+        const float4* w4 = reinterpret_cast<const float4*>(w + c * 32);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) wv[j] = w4[j];
+        relu_dot32<kPacked>(r[c % NB], wv, a0, a1);
+        if ((c + 1) % kChunksPerRow == 0) {
+          emit(c / kChunksPerRow, relu_dot_total<kPacked>(a0, a1));
+          a0 = make_float2(0.f, 0.f);
+          a1 = make_float2(0.f, 0.f);
+        }
       }
     }
   }

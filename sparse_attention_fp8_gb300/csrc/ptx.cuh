@@ -195,6 +195,19 @@ __device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32]) {
       : "memory");
 }
 
+// Orders later uses of `r` after the preceding volatile asm (a wait): an
+// empty statement that claims to rewrite the registers.
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
 // Shared-memory matrix descriptor (tcgen05 format) for a K-major operand in
 // the 128-byte swizzle layout: rows of 128 bytes, 8-row atoms of 1024 bytes
 // stacked along M/N (stride-dimension offset 1024).  The leading-dimension
