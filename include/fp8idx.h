@@ -159,7 +159,7 @@ fp8idx_status fp8_paged_mqa_logits_ex(const fp8idx_tensor* q_fp8,
  *  q_fp8        [M, heads, head_dim] U8 (e4m3), contiguous, 16-byte aligned.
  *  k_fp8        [N, head_dim] U8 (e4m3), contiguous, 16-byte aligned.
  *  kv_scale     [N] F32, contiguous, 16-byte aligned, values >= 0.
- *  weights      [M, heads] F32, contiguous.
+ *  weights      [M, heads] F32, contiguous, 16-byte aligned (loaded by TMA).
  *  cu_seqlen_ks, cu_seqlen_ke  [M] I32, contiguous.
  *  out          [M, >= N] F32, stride[1] == 1, stride[0] >= N.
  * Supported (fp8idx_prefill_is_supported): head_dim 128; heads 32 or 64;

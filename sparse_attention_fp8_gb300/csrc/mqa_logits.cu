@@ -6,7 +6,8 @@
 //               for n in [ks[m], ke[m]) (clamped to [0, N)), -inf elsewhere,
 // with every element written (the fused -inf fill of that PR).
 //
-// Design: persistent, one CTA per SM, warp-specialised like the decode kernel.
+// Design: persistent, one CTA per SM, warp-specialised like the decode kernel
+// (producer warp, MMA warp, two epilogue warpgroups).
 //  * A work unit is (row block, column split): block_m query rows whose Q
 //    block [block_m*heads, 128] is the MMA B operand (N = block_m*heads, 256
 //    at 32 heads), and the column tiles j = split_idx, split_idx + split, ...
@@ -17,12 +18,13 @@
 //  * Per unit every role derives the union of the block's windows from
 //    ks/ke; tiles meeting it are computed (TMA of K and its scales, four K=32
 //    e4m3 tcgen05.mma into one of the TMEM accumulators), the others are
-//    written with -inf directly.  Q and the weights are double-buffered
-//    across units.
-//  * Two epilogue warpgroups take alternate computed tiles and share the -inf
-//    tiles.  A thread owns one token: it walks the accumulator's 32-column
-//    chunks with double-buffered TMEM loads, applies ReLU * weight, sums the
-//    heads, scales by the token's kv_scale and stores the value or -inf.
+//    written with -inf directly.  Q and the weights (both by TMA) are
+//    double-buffered across units.
+//  * The two epilogue warpgroups take alternate computed tiles and share the
+//    -inf tiles.  A thread owns one token: it reduces the accumulator's
+//    32-column chunks (common.cuh reduce_rows, instantiated per chunk count
+//    block_m*heads/32), scales by the token's kv_scale and stores the value
+//    or -inf per element of the rows' windows.
 #include <cuda.h>
 #include <cuda_runtime.h>
 

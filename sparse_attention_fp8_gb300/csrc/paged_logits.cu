@@ -8,36 +8,39 @@
 //                          * kv_scale_b[p]       for p <= ctx_b - next_n + n,
 // with K_b[p] and its scale read from the paged cache through block_tables.
 //
-// Design (one persistent CTA per SM, warp-specialised):
-//  * Work items are (request b, 128-token tile t) for t < ceil(ctx_b / 128);
-//    each CTA takes one contiguous range of the flattened item list, found
-//    on the device from context_lens (a prefix sum in shared memory), so no
-//    host synchronisation is needed and every CTA gets the same number of
-//    tiles (+-1).
-//  * Producer warp: per tile, one 3-D TMA per cache block for the K rows
-//    (view [block][row][128 B], 128-byte swizzle) and one 2-D TMA per block
-//    for its scales, into a ring of `stages` shared-memory slots; block-table
-//    entries are prefetched 32 blocks ahead.  For block size 1 (co-packed
-//    132-byte tokens, only 4-byte aligned) two producer warps gather each
-//    token with 4-byte cp.async into the same swizzled layout instead.
-//  * MMA warp: the K tile is the A operand (M = 128 tokens) and the request's
-//    whole Q block [next_n*heads, 128] is the B operand, so N = next_n*heads:
-//    one K tile feeds every speculative row in one tcgen05.mma chain (the fold
-//    of next_n into the MMA asked for in aiter issue 5477, The ask).  Four
-//    K=32 e4m3 MMAs accumulate in f32 in tensor memory, which holds 2..16
-//    accumulators (as many as 512 columns allow).  Q and the weights of the
-//    current and the next request are double-buffered.
-//  * Two epilogue warpgroups take alternate tiles.  Thread = token (TMEM
-//    lane): read the token's scale and free the stage, then walk the 32-column
-//    chunks of the accumulator with double-buffered tcgen05.ld (the weights
-//    for a chunk are loaded from shared memory while its data is in flight),
-//    ReLU, multiply by the weights, sum the heads, multiply once by the
-//    token's kv_scale (the hoist of aiter PR 5047, Technical Details: scale
-//    >= 0 and ReLU is positive-homogeneous) and store if inside the causal
-//    window.  A warp stores 32 consecutive floats per row: coalesced 128 B.
+// Design (one persistent CTA per SM, warp-specialised, 11 warps):
+//  * Work items are (request b, T consecutive 128-token tiles): T = 2 when
+//    next_n*heads <= 128 (one barrier round trip per 256 tokens), else 1.
+//    Each CTA takes one contiguous range of the flattened item list, found on
+//    the device from context_lens (a prefix sum in shared memory), so no host
+//    synchronisation is needed and every CTA gets the same number of items
+//    (+-1).
+//  * Producer warps 0-1 take alternate items: per item one 3-D TMA per cache
+//    block for the K rows (view [block][row][128 B], 128-byte swizzle) and one
+//    2-D TMA (or, for 16-token blocks, a bulk copy) per block for its scales,
+//    into a ring of shared-memory stages; block-table entries are prefetched
+//    32 blocks ahead.  For block size 1 (co-packed 132-byte tokens, only
+//    4-byte aligned) each producer warp gathers 64 tokens of a tile with
+//    4-byte cp.async into the same swizzled layout instead.  Warp 0 also
+//    loads each request's Q block and weights into one of two buffers.
+//  * MMA warp 2: the K tile is the A operand (M = 128 tokens) and the
+//    request's whole Q block [next_n*heads, 128] is the B operand, so
+//    N = next_n*heads: one K tile feeds every speculative row in one
+//    tcgen05.mma chain (the fold of next_n into the MMA asked for in aiter
+//    issue 5477, The ask).  Four K=32 e4m3 MMAs accumulate in f32 in tensor
+//    memory, which holds 2..16 accumulators (as many as 512 columns allow).
+//  * Epilogue warpgroups (warps 3-10): with two tiles per item group g reads
+//    tile g of every item; with one, the groups take alternate items.  Thread
+//    = token (TMEM lane): read the token's scale and free the stage, then
+//    reduce the accumulator's 32-column chunks (common.cuh reduce_rows: loads
+//    rotate through register buffers, ReLU as packed x+|x|, packed FMA with
+//    the weights, head sum in the thread), multiply once by the token's
+//    kv_scale (the hoist of aiter PR 5047, Technical Details: scale >= 0 and
+//    ReLU is positive-homogeneous) and store if inside the causal window.  A
+//    warp stores 32 consecutive floats per row: coalesced 128 B.  The loop is
+//    instantiated per chunk count (next_n*heads/32).
 //  * Control loops keep ring indices and phases as counters (no division per
-//    tile): the single-thread control loops, not the copies, set the pace of
-//    a 16 KB tile when they are not kept short.
+//    tile); every wait is bounded (common.cuh).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
