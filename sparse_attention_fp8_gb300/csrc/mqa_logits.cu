@@ -251,8 +251,19 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
       Ring qr{0u, 0u, 2u};
       int ci = 0, fi = 0;
       bool ok = true;
+      constexpr int kRows = NCH / (HEADS / 32);  // block_m
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const Unit U = load_unit(p, u, num_rb, n_tiles);
+        // Every row's clamped window in registers for the whole unit (the
+        // emit below indexes them with compile-time row numbers).
+        int lo_r[kRows], hi_r[kRows];
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+          lo_r[r] = __shfl_sync(0xffffffffu, U.row_lo, r);
+          hi_r[r] = __shfl_sync(0xffffffffu, U.row_hi, r);
+        }
+        const int rows_valid = p.rows - U.m0;  // rows r >= rows_valid lie past M
+        float* const out_block = p.out + static_cast<int64_t>(U.m0) * p.out_stride;
         if (!(ok = warp_wait_bounded(qf0 + 8u * qr.idx, qr.phase, abort_flag, &g_prefill_watchdog, kSiteQFull)))
           break;
         const float* w = w_s + qr.idx * N;
@@ -275,6 +286,8 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
               ptx::tc_fence_after();
               const uint32_t taddr = tmem + ac.idx * acc_cols + (static_cast<uint32_t>(quad * 32) << 16);
               const int n = col0 + row;
+              const bool col_ok = n < p.cols;
+              float* const out_col = out_block + n;
               const uint32_t acce = acce0 + 8u * ac.idx;
               reduce_rows<HEADS, NCH>(
                   taddr, w,
@@ -284,11 +297,9 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
                     if (lane == 0) ptx::mbar_arrive(acce);
                   },
                   [&](int r, float v) {
-                    const int lo = __shfl_sync(0xffffffffu, U.row_lo, r);
-                    const int hi = __shfl_sync(0xffffffffu, U.row_hi, r);
-                    const int m = U.m0 + r;
-                    if (m < p.rows && n < p.cols)
-                      __stcs(p.out + static_cast<int64_t>(m) * p.out_stride + n, (n >= lo && n < hi) ? v * scale : ninf);
+                    if (r < rows_valid && col_ok)
+                      __stcs(out_col + static_cast<int64_t>(r) * p.out_stride,
+                             (n >= lo_r[r] && n < hi_r[r]) ? v * scale : ninf);
                   });
             }
             st.next();
