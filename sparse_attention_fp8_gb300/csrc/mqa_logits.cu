@@ -235,11 +235,10 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
   } else {
     // =========================== epilogue ===============================
     // Computed tile number ci (counted over the CTA) goes to accumulator
-    // ci % AB and to warpgroup ci % 2; -inf tiles alternate between the
-    // warpgroups by their own count.
+    // ci % AB and to warpgroup ci % 2; a unit's -inf tiles are shared by all
+    // epilogue warps after its computed tiles.
     const int ew = warp - kEpiWarp0;      // 0 .. 4*kEpiGroups-1
     const int grp = ew >> 2;
-    const int et = (ew & 3) * 32 + lane;  // 0..127 within the warpgroup
     const int quad = warp & 3;            // TMEM lane quadrant
     const int row = quad * 32 + lane;     // token within the tile
     const float ninf = __int_as_float(0xff800000);
@@ -249,7 +248,7 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
       Ring st{0u, 0u, static_cast<uint32_t>(S)};
       Ring ac{0u, 0u, static_cast<uint32_t>(AB)};
       Ring qr{0u, 0u, 2u};
-      int ci = 0, fi = 0;
+      int ci = 0;
       bool ok = true;
       constexpr int kRows = NCH / (HEADS / 32);  // block_m
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -267,61 +266,66 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
         if (!(ok = warp_wait_bounded(qf0 + 8u * qr.idx, qr.phase, abort_flag, &g_prefill_watchdog, kSiteQFull)))
           break;
         const float* w = w_s + qr.idx * N;
-        for (int k = 0; k < U.n_j; ++k) {
-          const int j = U.sidx + k * p.split;
-          const int col0 = j * kTileTokens;
-          if (j >= U.t_lo && j < U.t_hi) {
-            const bool mine = (ci & 1) == grp;
-            ++ci;
-            if (mine) {
-              if (!(ok = warp_wait_bounded(full0 + 8u * st.idx, st.phase, abort_flag, &g_prefill_watchdog,
-                                           kSiteStageFull)))
-                break;
-              const float scale = sc_s[st.idx * kTileTokens + row];
-              __syncwarp();
-              if (lane == 0) ptx::mbar_arrive(empty0 + 8u * st.idx);
-              if (!(ok = warp_wait_bounded(accf0 + 8u * ac.idx, ac.phase, abort_flag, &g_prefill_watchdog,
-                                           kSiteAccFull)))
-                break;
-              ptx::tc_fence_after();
-              const uint32_t taddr = tmem + ac.idx * acc_cols + (static_cast<uint32_t>(quad * 32) << 16);
-              const int n = col0 + row;
-              const bool col_ok = n < p.cols;
-              float* const out_col = out_block + n;
-              const uint32_t acce = acce0 + 8u * ac.idx;
-              reduce_rows<HEADS, NCH>(
-                  taddr, w,
-                  [&]() {
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(acce);
-                  },
-                  [&](int r, float v) {
-                    if (r < rows_valid && col_ok)
-                      __stcs(out_col + static_cast<int64_t>(r) * p.out_stride,
-                             (n >= lo_r[r] && n < hi_r[r]) ? v * scale : ninf);
-                  });
-            }
-            st.next();
-            ac.next();
-          } else {
-            // a tile no row of the block reaches: -inf for all the block's rows
-            const bool mine = (fi & 1) == grp;
-            ++fi;
-            if (!mine) continue;
-            const int ncols = min(kTileTokens, p.cols - col0);
-            if (p.vec_ok && ncols == kTileTokens) {
-              const float4 f4 = make_float4(ninf, ninf, ninf, ninf);
-              for (int e = et; e < BM * 32; e += 128) {
-                const int m = U.m0 + (e >> 5);
-                if (m < p.rows)
-                  __stcs(reinterpret_cast<float4*>(p.out + static_cast<int64_t>(m) * p.out_stride + col0) + (e & 31), f4);
-              }
+        // Computed tiles j0, j0 + split, ...: alternate between the groups.
+        for (int c = 0; c < U.n_comp; ++c) {
+          const int col0 = (U.j0 + c * p.split) * kTileTokens;
+          const bool mine = (ci & 1) == grp;
+          ++ci;
+          if (mine) {
+            if (!(ok = warp_wait_bounded(full0 + 8u * st.idx, st.phase, abort_flag, &g_prefill_watchdog,
+                                         kSiteStageFull)))
+              break;
+            const float scale = sc_s[st.idx * kTileTokens + row];
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(empty0 + 8u * st.idx);
+            if (!(ok = warp_wait_bounded(accf0 + 8u * ac.idx, ac.phase, abort_flag, &g_prefill_watchdog,
+                                         kSiteAccFull)))
+              break;
+            ptx::tc_fence_after();
+            const uint32_t taddr = tmem + ac.idx * acc_cols + (static_cast<uint32_t>(quad * 32) << 16);
+            const int n = col0 + row;
+            const bool col_ok = n < p.cols;
+            float* const out_col = out_block + n;
+            const uint32_t acce = acce0 + 8u * ac.idx;
+            reduce_rows<HEADS, NCH>(
+                taddr, w,
+                [&]() {
+                  ptx::tc_fence_before();
+                  __syncwarp();
+                  if (lane == 0) ptx::mbar_arrive(acce);
+                },
+                [&](int r, float v) {
+                  if (r < rows_valid && col_ok)
+                    __stcs(out_col + static_cast<int64_t>(r) * p.out_stride,
+                           (n >= lo_r[r] && n < hi_r[r]) ? v * scale : ninf);
+                });
+          }
+          st.next();
+          ac.next();
+        }
+        if (!ok) break;
+        // The unit's other column tiles (k < k_lo or k >= k_lo + n_comp) meet
+        // no row's window: -inf, spread over all epilogue threads, a float4
+        // per thread and step (scalar stores at a ragged right edge or when
+        // the rows are not 16-byte aligned).
+        {
+          const int k_lo = (U.j0 - U.sidx) / p.split;
+          const int total = (U.n_j - U.n_comp) * kRows * 32;
+          const float4 f4 = make_float4(ninf, ninf, ninf, ninf);
+          for (int e = ew * 32 + lane; e < total; e += 32 * 4 * kEpiGroups) {
+            const int f = e / (kRows * 32);
+            const int rem = e - f * (kRows * 32);
+            const int r = rem >> 5;
+            const int k = f < k_lo ? f : f + U.n_comp;
+            const int c4 = (U.sidx + k * p.split) * kTileTokens + (rem & 31) * 4;
+            if (r >= rows_valid) continue;
+            float* const dst = out_block + static_cast<int64_t>(r) * p.out_stride + c4;
+            if (p.vec_ok && c4 + 4 <= p.cols) {
+              __stcs(reinterpret_cast<float4*>(dst), f4);
             } else {
-              for (int rr = 0; rr < BM; ++rr) {
-                const int m = U.m0 + rr;
-                if (m < p.rows && row < ncols) __stcs(p.out + static_cast<int64_t>(m) * p.out_stride + col0 + row, ninf);
-              }
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                if (c4 + i < p.cols) __stcs(dst + i, ninf);
             }
           }
         }
