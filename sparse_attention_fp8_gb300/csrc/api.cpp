@@ -385,7 +385,23 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const fp8idx_tensor* k, const
   p.reverse = plan.reverse_rows;
   p.vec_ok = (aligned16(out->data) && (p.out_stride % 4) == 0) ? 1 : 0;
   p.acc_bufs = paged_acc_buffers(plan.tile_n);
-  cudaError_t e = launch_prefill(tm_q, tm_k, tm_s, tm_w, p, (int)H, plan.grid, plan.smem_bytes,
+  // -inf tiles as TMA stores need 16-byte aligned rows (the tensor map's
+  // stride rule); otherwise the epilogue warps write them.  A TMA store
+  // writes whole 16-byte units, so the map is N rounded down to a multiple
+  // of 4 columns wide and the kernel writes the rest of the row directly.
+  CUtensorMap tm_out;
+  std::memset(&tm_out, 0, sizeof(tm_out));
+  p.tma_fill = 0;
+  p.fill_cols = (int32_t)(N & ~3ll);
+  if (p.vec_ok && p.fill_cols > 0) {
+    const uint64_t dims[2] = {(uint64_t)p.fill_cols, (uint64_t)M};
+    const uint64_t strides[1] = {(uint64_t)p.out_stride * 4u};
+    const uint32_t box[2] = {(uint32_t)kTileTokens, (uint32_t)plan.block_m};
+    TRY(encode(&tm_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, out->data, dims, strides, box,
+               CU_TENSOR_MAP_SWIZZLE_NONE, "out"));
+    p.tma_fill = 1;
+  }
+  cudaError_t e = launch_prefill(tm_q, tm_k, tm_s, tm_w, tm_out, p, (int)H, plan.grid, plan.smem_bytes,
                                  static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
   return ok();

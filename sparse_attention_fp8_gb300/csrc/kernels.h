@@ -94,19 +94,25 @@ struct PrefillParams {
   int32_t reverse;  // 1: row blocks dealt from the last one
   int32_t vec_ok;   // out rows are 16-byte aligned: float4 -inf fill
   int32_t acc_bufs; // TMEM accumulator buffers: paged_acc_buffers(n_cols)
+  int32_t tma_fill; // 1: -inf tiles are TMA stores of a constant shared tile (needs vec_ok)
+  int32_t fill_cols; // columns covered by the -inf tensor map: N rounded down to a multiple of 4
 };
 
 // Roles: producer warp, MMA warp, kEpiGroups epilogue warpgroups.
 __host__ __device__ constexpr int prefill_threads() { return 32 * (1 + 1 + 4 * kEpiGroups); }
 
 struct PrefillSmem {
-  uint32_t q, k, scale, w, bars, misc, total;
+  uint32_t q, k, ninf, scale, w, bars, misc, total;
 };
+// The -inf tile (block_m rows x 128 floats, the source of the TMA -inf
+// stores) is at most 8 x 512 B: block_m * heads <= 256 with heads >= 32.
+constexpr int kNinfTileBytes = 8 * kTileTokens * 4;
 __host__ __device__ inline PrefillSmem prefill_smem_layout(int n_cols, int stages) {
   PrefillSmem L;
   uint32_t off = 0;
   L.q = off;     off += 2u * n_cols * kHeadDim;            // two Q blocks
   L.k = off;     off += (uint32_t)stages * kKTileBytes;
+  L.ninf = off;  off += kNinfTileBytes;                     // 1024-aligned (follows whole K tiles)
   L.scale = off; off += (uint32_t)stages * kTileTokens * 4;
   L.w = off;     off += 2u * n_cols * 4;                    // two weight blocks
   off = (off + 7u) & ~7u;
@@ -122,8 +128,8 @@ __host__ __device__ inline PrefillSmem prefill_smem_layout(int n_cols, int stage
 cudaError_t launch_paged(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const CUtensorMap& tm_sc,
                          const PagedParams& p, int heads, bool gather, int grid, int smem_bytes, cudaStream_t stream);
 cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_s,
-                           const CUtensorMap& tm_w, const PrefillParams& p, int heads, int grid, int smem_bytes,
-                           cudaStream_t stream);
+                           const CUtensorMap& tm_w, const CUtensorMap& tm_out, const PrefillParams& p, int heads,
+                           int grid, int smem_bytes, cudaStream_t stream);
 
 // Watchdog words of the two translation units (synchronous read, optional clear).
 cudaError_t read_paged_watchdog(unsigned int* value, bool clear);

@@ -18,10 +18,15 @@
 //  * Per unit every role derives the union of the block's windows from
 //    ks/ke; tiles meeting it are computed (TMA of K and its scales, four K=32
 //    e4m3 tcgen05.mma into one of the TMEM accumulators), the others are
-//    written with -inf directly.  Q and the weights (both by TMA) are
-//    double-buffered across units.
-//  * The two epilogue warpgroups take alternate computed tiles and share the
-//    -inf tiles.  A thread owns one token: it reduces the accumulator's
+//    written with -inf.  Q and the weights (both by TMA) are double-buffered
+//    across units.
+//  * The -inf tiles are TMA stores of a constant -inf tile in shared memory,
+//    issued by the producer warp between its K loads (spread evenly over the
+//    unit), so the fill runs alongside the MMA and the epilogue.  When the
+//    output rows are not 16-byte aligned (no tensor map) the epilogue warps
+//    write them after the unit's computed tiles instead.
+//  * The two epilogue warpgroups take alternate computed tiles.  A thread
+//    owns one token: it reduces the accumulator's
 //    32-column chunks (common.cuh reduce_rows, instantiated per chunk count
 //    block_m*heads/32), scales by the token's kv_scale and stores the value
 //    or -inf per element of the rows' windows.
@@ -89,7 +94,7 @@ template <int HEADS>
 __global__ void __launch_bounds__(prefill_threads(), 1)
     mqa_logits_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_w,
-                      const PrefillParams p) {
+                      const __grid_constant__ CUtensorMap tm_out, const PrefillParams p) {
   constexpr int kEpiWarp0 = 2;
   constexpr uint32_t kTmemCols = 512;
   extern __shared__ uint8_t smem_raw[];
@@ -102,6 +107,7 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
   const PrefillSmem L = prefill_smem_layout(N, S);
   uint8_t* q_s = smem + L.q;
   uint8_t* k_s = smem + L.k;
+  float4* ninf_s = reinterpret_cast<float4*>(smem + L.ninf);
   float* sc_s = reinterpret_cast<float*>(smem + L.scale);
   float* w_s = reinterpret_cast<float*>(smem + L.w);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
@@ -142,6 +148,13 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
     ptx::prefetch_tmap(&tm_k);
     ptx::prefetch_tmap(&tm_s);
     ptx::prefetch_tmap(&tm_w);
+    if (p.tma_fill) ptx::prefetch_tmap(&tm_out);
+  }
+  if (p.tma_fill) {  // the constant -inf tile read by the TMA stores
+    for (int i = threadIdx.x; i < kNinfTileBytes / 16; i += blockDim.x)
+      ninf_s[i] = make_float4(__int_as_float(0xff800000), __int_as_float(0xff800000), __int_as_float(0xff800000),
+                              __int_as_float(0xff800000));
+    ptx::fence_proxy_async_smem();
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(misc), kTmemCols);
@@ -171,6 +184,35 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
       }
       qr.next();
       ++q_issued;
+      // With tma_fill the unit's -inf tiles (all but the computed ones) are
+      // TMA stores of the constant tile, spread evenly over the unit's K
+      // loads so that they follow the pace of the MMA and never queue up far
+      // ahead of the next K tile.
+      const int n_inf = p.tma_fill ? U.n_j - U.n_comp : 0;
+      const int k_lo = (U.j0 - U.sidx) / p.split;
+      // The tensor map covers the first fill_cols = N rounded down to whole
+      // 16-byte units (a TMA store writes whole 16-byte units, so a narrower
+      // map would spill past column N); the lanes write the last tile's
+      // remaining N - fill_cols (< 4) columns directly.
+      int f_done = 0;
+      const auto fill_to = [&](int f_end) {
+        if (f_end <= f_done) return;
+        for (int f = f_done; f < f_end; ++f) {
+          const int k = f < k_lo ? f : f + U.n_comp;
+          const int col0 = (U.sidx + k * p.split) * kTileTokens;
+          if (lane == 0) ptx::tma_store_2d(&tm_out, ptx::smem_u32(ninf_s), col0, U.m0);
+          const int tail = p.cols - p.fill_cols;
+          if (tail > 0 && col0 + kTileTokens > p.fill_cols && lane < BM * tail) {
+            const int r = lane / tail;
+            if (U.m0 + r < p.rows)
+              p.out[static_cast<int64_t>(U.m0 + r) * p.out_stride + p.fill_cols + (lane - r * tail)] =
+                  __int_as_float(0xff800000);
+          }
+        }
+        if (lane == 0) ptx::bulk_commit_group();
+        f_done = f_end;
+      };
+      if (U.n_comp == 0) fill_to(n_inf);
       for (int c = 0, j = U.j0; c < U.n_comp; ++c, j += p.split) {
         if (!(ok = warp_wait_bounded(empty0 + 8u * st.idx, st.phase ^ 1u, abort_flag, &g_prefill_watchdog,
                                      kSiteStageEmpty)))
@@ -181,10 +223,14 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
           ptx::tma_load_2d(ptx::smem_u32(k_s + st.idx * kKTileBytes), &tm_k, full, 0, j * kTileTokens);
           ptx::tma_load_1d(ptx::smem_u32(sc_s + st.idx * kTileTokens), &tm_s, full, j * kTileTokens);
         }
+        fill_to(static_cast<int>(static_cast<int64_t>(c + 1) * n_inf / U.n_comp));
         st.next();
         ++issued;
       }
     }
+    // The -inf stores read the constant tile until they complete: wait for
+    // them before the CTA (and its shared memory) goes away.
+    if (lane == 0) ptx::bulk_wait_all();
     if (*abort_flag && lane == 0) {
       for (int c = max(0, issued - S); c < issued; ++c)
         wait_drain(full0 + 8u * (c % S), (c / S) & 1, &g_prefill_watchdog);
@@ -305,10 +351,10 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
         }
         if (!ok) break;
         // The unit's other column tiles (k < k_lo or k >= k_lo + n_comp) meet
-        // no row's window: -inf, spread over all epilogue threads, a float4
-        // per thread and step (scalar stores at a ragged right edge or when
-        // the rows are not 16-byte aligned).
-        {
+        // no row's window.  Without tma_fill (out rows not 16-byte aligned)
+        // they are written here with -inf, spread over all epilogue threads
+        // (float4 stores when possible, scalar at a ragged right edge).
+        if (!p.tma_fill) {
           const int k_lo = (U.j0 - U.sidx) / p.split;
           const int total = (U.n_j - U.n_comp) * kRows * 32;
           const float4 f4 = make_float4(ninf, ninf, ninf, ninf);
@@ -347,15 +393,15 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
 }
 
 cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_s,
-                           const CUtensorMap& tm_w, const PrefillParams& p, int heads, int grid, int smem_bytes,
-                           cudaStream_t stream) {
-  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, PrefillParams) = nullptr;
+                           const CUtensorMap& tm_w, const CUtensorMap& tm_out, const PrefillParams& p, int heads,
+                           int grid, int smem_bytes, cudaStream_t stream) {
+  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, PrefillParams) = nullptr;
   if (heads == 32) kern = mqa_logits_kernel<32>;
   else if (heads == 64) kern = mqa_logits_kernel<64>;
   else return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
-  kern<<<grid, prefill_threads(), smem_bytes, stream>>>(tm_q, tm_k, tm_s, tm_w, p);
+  kern<<<grid, prefill_threads(), smem_bytes, stream>>>(tm_q, tm_k, tm_s, tm_w, tm_out, p);
   return cudaGetLastError();
 }
 

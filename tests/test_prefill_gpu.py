@@ -96,6 +96,23 @@ def test_prefill_config3_full_size(fp8idx, oracle_impl):
     assert np.all(err <= 1e-3 * rowmax_min + 1e-5), f"sampled max err {err.max()}"
 
 
+@pytest.mark.parametrize("cols,pitch", [(701, 704), (701, 705), (130, 132), (64, 256)],
+                         ids=["aligned-pitch", "odd-pitch", "tail2", "wide-pitch"])
+def test_prefill_strided_out(fp8idx, oracle_impl, cols, pitch):
+    """out is a column slice of a wider NaN buffer: the -inf fill (TMA stores
+    clipped at column N when the pitch is a multiple of 4 floats, thread
+    stores otherwise) must write [0, N) of every row and nothing past it."""
+    case = workloads.prefill_case(37, cols, 32, mode="multi_req", seed=cols + pitch)
+    d = to_device(case)
+    buf = torch.full((case.rows, pitch), float("nan"), dtype=torch.float32, device="cuda")
+    out = buf[:, :cols]
+    fp8idx.fp8_mqa_logits(d["q"], d["k"], d["kv_scale"], d["weights"], d["ks"], d["ke"], out)
+    torch.cuda.synchronize()
+    host = buf.cpu().numpy()
+    assert np.isnan(host[:, cols:]).all(), "columns past N were written"
+    assert_rows_close(host[:, :cols], oracle_prefill(oracle_impl, case), what=f"N={cols} pitch={pitch}")
+
+
 def test_prefill_graph_capture_replay(fp8idx, oracle_impl):
     case = workloads.prefill_case(40, 600, 32, mode="multi_req", seed=41)
     d = to_device(case)
