@@ -98,8 +98,8 @@ struct PrefillParams {
   int32_t fill_cols; // columns covered by the -inf tensor map: N rounded down to a multiple of 4
 };
 
-// Roles: producer warp, MMA warp, kEpiGroups epilogue warpgroups.
-__host__ __device__ constexpr int prefill_threads() { return 32 * (1 + 1 + 4 * kEpiGroups); }
+// Roles: producer warp, MMA warp, kEpiGroups epilogue warpgroups, -inf filler warp.
+__host__ __device__ constexpr int prefill_threads() { return 32 * (1 + 1 + 4 * kEpiGroups + 1); }
 
 struct PrefillSmem {
   uint32_t q, k, ninf, scale, w, bars, misc, total;

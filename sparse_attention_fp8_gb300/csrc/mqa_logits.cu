@@ -7,7 +7,7 @@
 // with every element written (the fused -inf fill of that PR).
 //
 // Design: persistent, one CTA per SM, warp-specialised like the decode kernel
-// (producer warp, MMA warp, two epilogue warpgroups).
+// (producer warp, MMA warp, two epilogue warpgroups, -inf filler warp).
 //  * A work unit is (row block, column split): block_m query rows whose Q
 //    block [block_m*heads, 128] is the MMA B operand (N = block_m*heads, 256
 //    at 32 heads), and the column tiles j = split_idx, split_idx + split, ...
@@ -20,11 +20,10 @@
 //    e4m3 tcgen05.mma into one of the TMEM accumulators), the others are
 //    written with -inf.  Q and the weights (both by TMA) are double-buffered
 //    across units.
-//  * The -inf tiles are TMA stores of a constant -inf tile in shared memory,
-//    issued by the producer warp between its K loads (spread evenly over the
-//    unit), so the fill runs alongside the MMA and the epilogue.  When the
-//    output rows are not 16-byte aligned (no tensor map) the epilogue warps
-//    write them after the unit's computed tiles instead.
+//  * A filler warp writes the -inf tiles: TMA stores of a constant -inf tile
+//    in shared memory (plain streaming stores when the output rows are not
+//    16-byte aligned).  It waits on nothing, so the fill runs alongside the
+//    MMA and the epilogue, and the producer warp only issues loads.
 //  * The two epilogue warpgroups take alternate computed tiles.  A thread
 //    owns one token: it reduces the accumulator's
 //    32-column chunks (common.cuh reduce_rows, instantiated per chunk count
@@ -96,6 +95,7 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
                       const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_w,
                       const __grid_constant__ CUtensorMap tm_out, const PrefillParams p) {
   constexpr int kEpiWarp0 = 2;
+  constexpr int kFillWarp = kEpiWarp0 + 4 * kEpiGroups;
   constexpr uint32_t kTmemCols = 512;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_up_1024(smem_raw);
@@ -184,35 +184,6 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
       }
       qr.next();
       ++q_issued;
-      // With tma_fill the unit's -inf tiles (all but the computed ones) are
-      // TMA stores of the constant tile, spread evenly over the unit's K
-      // loads so that they follow the pace of the MMA and never queue up far
-      // ahead of the next K tile.
-      const int n_inf = p.tma_fill ? U.n_j - U.n_comp : 0;
-      const int k_lo = (U.j0 - U.sidx) / p.split;
-      // The tensor map covers the first fill_cols = N rounded down to whole
-      // 16-byte units (a TMA store writes whole 16-byte units, so a narrower
-      // map would spill past column N); the lanes write the last tile's
-      // remaining N - fill_cols (< 4) columns directly.
-      int f_done = 0;
-      const auto fill_to = [&](int f_end) {
-        if (f_end <= f_done) return;
-        for (int f = f_done; f < f_end; ++f) {
-          const int k = f < k_lo ? f : f + U.n_comp;
-          const int col0 = (U.sidx + k * p.split) * kTileTokens;
-          if (lane == 0) ptx::tma_store_2d(&tm_out, ptx::smem_u32(ninf_s), col0, U.m0);
-          const int tail = p.cols - p.fill_cols;
-          if (tail > 0 && col0 + kTileTokens > p.fill_cols && lane < BM * tail) {
-            const int r = lane / tail;
-            if (U.m0 + r < p.rows)
-              p.out[static_cast<int64_t>(U.m0 + r) * p.out_stride + p.fill_cols + (lane - r * tail)] =
-                  __int_as_float(0xff800000);
-          }
-        }
-        if (lane == 0) ptx::bulk_commit_group();
-        f_done = f_end;
-      };
-      if (U.n_comp == 0) fill_to(n_inf);
       for (int c = 0, j = U.j0; c < U.n_comp; ++c, j += p.split) {
         if (!(ok = warp_wait_bounded(empty0 + 8u * st.idx, st.phase ^ 1u, abort_flag, &g_prefill_watchdog,
                                      kSiteStageEmpty)))
@@ -223,14 +194,10 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
           ptx::tma_load_2d(ptx::smem_u32(k_s + st.idx * kKTileBytes), &tm_k, full, 0, j * kTileTokens);
           ptx::tma_load_1d(ptx::smem_u32(sc_s + st.idx * kTileTokens), &tm_s, full, j * kTileTokens);
         }
-        fill_to(static_cast<int>(static_cast<int64_t>(c + 1) * n_inf / U.n_comp));
         st.next();
         ++issued;
       }
     }
-    // The -inf stores read the constant tile until they complete: wait for
-    // them before the CTA (and its shared memory) goes away.
-    if (lane == 0) ptx::bulk_wait_all();
     if (*abort_flag && lane == 0) {
       for (int c = max(0, issued - S); c < issued; ++c)
         wait_drain(full0 + 8u * (c % S), (c / S) & 1, &g_prefill_watchdog);
@@ -278,11 +245,10 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
       ptx::mma_commit(drain_bar);
       wait_drain(drain_bar, 0, &g_prefill_watchdog);
     }
-  } else {
+  } else if (warp < kFillWarp) {
     // =========================== epilogue ===============================
     // Computed tile number ci (counted over the CTA) goes to accumulator
-    // ci % AB and to warpgroup ci % 2; a unit's -inf tiles are shared by all
-    // epilogue warps after its computed tiles.
+    // ci % AB and to warpgroup ci % 2.
     const int ew = warp - kEpiWarp0;      // 0 .. 4*kEpiGroups-1
     const int grp = ew >> 2;
     const int quad = warp & 3;            // TMEM lane quadrant
@@ -350,21 +316,43 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
           ac.next();
         }
         if (!ok) break;
-        // The unit's other column tiles (k < k_lo or k >= k_lo + n_comp) meet
-        // no row's window.  Without tma_fill (out rows not 16-byte aligned)
-        // they are written here with -inf, spread over all epilogue threads
-        // (float4 stores when possible, scalar at a ragged right edge).
-        if (!p.tma_fill) {
-          const int k_lo = (U.j0 - U.sidx) / p.split;
-          const int total = (U.n_j - U.n_comp) * kRows * 32;
-          const float4 f4 = make_float4(ninf, ninf, ninf, ninf);
-          for (int e = ew * 32 + lane; e < total; e += 32 * 4 * kEpiGroups) {
-            const int f = e / (kRows * 32);
-            const int rem = e - f * (kRows * 32);
-            const int r = rem >> 5;
-            const int k = f < k_lo ? f : f + U.n_comp;
-            const int c4 = (U.sidx + k * p.split) * kTileTokens + (rem & 31) * 4;
-            if (r >= rows_valid) continue;
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(qe0 + 8u * qr.idx);
+        qr.next();
+      }
+    };
+    with_chunk_count<HEADS / 32, 8>(BM * (HEADS / 32), run);
+  } else {
+    // ============================ -inf filler ===========================
+    // Every unit's column tiles that meet no row's window (k < k_lo or
+    // k >= k_lo + n_comp) get -inf.  The filler shares no data with the
+    // other roles (disjoint output elements) and waits on nothing, so it
+    // runs ahead freely.  With tma_fill lane 0 issues one TMA store of the
+    // constant -inf tile per column tile (the tensor map covers N rounded
+    // down to whole 16-byte units, since a TMA store writes whole 16-byte
+    // units; the lanes write the last tile's remaining columns directly);
+    // otherwise the lanes write streaming stores (float4 where aligned).
+    const float ninf = __int_as_float(0xff800000);
+    const float4 f4 = make_float4(ninf, ninf, ninf, ninf);
+    const int tail = p.cols - p.fill_cols;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      const Unit U = load_unit(p, u, num_rb, n_tiles);
+      const int k_lo = (U.j0 - U.sidx) / p.split;
+      const int n_inf = U.n_j - U.n_comp;
+      const int rv = min(BM, p.rows - U.m0);
+      float* const out_block = p.out + static_cast<int64_t>(U.m0) * p.out_stride;
+      for (int f = 0; f < n_inf; ++f) {
+        const int k = f < k_lo ? f : f + U.n_comp;
+        const int col0 = (U.sidx + k * p.split) * kTileTokens;
+        if (p.tma_fill) {
+          if (lane == 0) ptx::tma_store_2d(&tm_out, ptx::smem_u32(ninf_s), col0, U.m0);
+          if (tail > 0 && col0 + kTileTokens > p.fill_cols && lane < rv * tail) {
+            const int r = lane / tail;
+            out_block[static_cast<int64_t>(r) * p.out_stride + p.fill_cols + (lane - r * tail)] = ninf;
+          }
+        } else {
+          const int c4 = col0 + lane * 4;
+          for (int r = 0; r < rv; ++r) {
             float* const dst = out_block + static_cast<int64_t>(r) * p.out_stride + c4;
             if (p.vec_ok && c4 + 4 <= p.cols) {
               __stcs(reinterpret_cast<float4*>(dst), f4);
@@ -375,13 +363,12 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
             }
           }
         }
-        if (!ok) break;
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(qe0 + 8u * qr.idx);
-        qr.next();
       }
-    };
-    with_chunk_count<HEADS / 32, 8>(BM * (HEADS / 32), run);
+      if (p.tma_fill && lane == 0) ptx::bulk_commit_group();
+    }
+    // The TMA stores read the constant tile until they complete: wait for
+    // them before the CTA (and its shared memory) goes away.
+    if (p.tma_fill && lane == 0) ptx::bulk_wait_all();
   }
 
   ptx::tc_fence_before();
