@@ -77,6 +77,9 @@ typedef struct {
   int32_t split_n;      /* prefill: column-tile splits per row block          */
   int32_t reverse_rows; /* prefill: -1 planner, 0 natural, 1 longest-first    */
   int32_t block_m;      /* prefill: query rows per CTA (block_m*heads <= 256) */
+  int32_t clean_logits; /* prefill: 0 or 1 write -inf outside each row's     */
+                        /* window (the default); -1 leaves those elements    */
+                        /* untouched (the pages' clean_logits=False)         */
 } fp8idx_options;
 
 /* The launch the planner chose (filled by the fp8idx_plan_* queries). */
@@ -152,7 +155,9 @@ fp8idx_status fp8_paged_mqa_logits_ex(const fp8idx_tensor* q_fp8,
  * e4m3 buffer with a separate [N] f32 scale; row m is defined for n in
  * [cu_seqlen_ks[m], cu_seqlen_ke[m]) and is -inf elsewhere.  Every element of
  * out is written (the "clean_logits" semantics, same PR, Technical Details:
- * the -inf fill is fused into the kernel).  Windows are clamped to [0, N);
+ * the -inf fill is fused into the kernel); with opts->clean_logits = -1 only
+ * the windows are written (clean_logits=False, same PR, Test Plan: both
+ * settings are graded).  Windows are clamped to [0, N);
  * ke <= ks, or ke <= 0, gives an all -inf row (same PR, Test Plan: empty and
  * past_end windows are legal input).
  *
@@ -162,8 +167,9 @@ fp8idx_status fp8_paged_mqa_logits_ex(const fp8idx_tensor* q_fp8,
  *  weights      [M, heads] F32, contiguous, 16-byte aligned (loaded by TMA).
  *  cu_seqlen_ks, cu_seqlen_ke  [M] I32, contiguous.
  *  out          [M, >= N] F32, stride[1] == 1, stride[0] >= N.
- * Supported (fp8idx_prefill_is_supported): head_dim 128; heads 32 or 64;
- * M, N >= 0 with M*heads and N below 2^31.
+ * Supported (fp8idx_prefill_is_supported): head_dim 128; heads 32, 64 or
+ * 128 (the pages' prefill sweep, same PR, Test Plan); M, N >= 0 with
+ * M*heads and N below 2^31.
  */
 fp8idx_status fp8_mqa_logits(const fp8idx_tensor* q_fp8,
                              const fp8idx_tensor* k_fp8,
@@ -181,6 +187,44 @@ fp8idx_status fp8_mqa_logits_ex(const fp8idx_tensor* q_fp8,
                                 const fp8idx_tensor* cu_seqlen_ke,
                                 const fp8idx_tensor* out,
                                 const fp8idx_options* opts, void* stream);
+
+/*
+ * Top-k consumers of the logits: the positions of each row's k largest
+ * logits inside the row's window.  The step after the logits on the pages is
+ * a per-row top-k selection with index_topk 2048 or 512 (aiter PR 5047,
+ * section "GLM-5.2-MXFP4 E2E": stale finite logits outside the window would
+ * corrupt it, hence the -inf contract; aiter issue 5477, section Measurement:
+ * index_topk 512).  The pages do not define the selection further; this
+ * library's definition: indices[r, j] for j < min(k, L_r) is the position
+ * (column of the logits row) of the j-th entry of row r's window sorted by
+ * logit descending, ties by position ascending (so the result is unique;
+ * -0.0 == +0.0); indices[r, j] = -1 for j >= L_r, the window length.
+ *
+ *  logits   [rows, width] F32, stride[1] == 1, stride[0] >= width.  Only the
+ *           windows are read, so values outside them do not matter.
+ *  indices  [rows, k] I32 output, stride[1] == 1, stride[0] >= k.
+ *  k        1 .. 2048.
+ * No NaN inside a window (precondition).  One CTA per row; no scratch
+ * memory.  Returns FP8IDX_OK, FP8IDX_ERR_INVALID, FP8IDX_ERR_UNSUPPORTED
+ * (k out of range) or FP8IDX_ERR_CUDA.
+ *
+ * fp8_paged_topk: decode windows.  rows = batch*next_n; row r = b*next_n+n
+ * has window [0, min(context_lens[b] - next_n + n + 1, max_model_len)) -- the
+ * columns fp8_paged_mqa_logits writes.  context_lens [batch] I32 contiguous;
+ * max_model_len <= width.
+ */
+fp8idx_status fp8_paged_topk(const fp8idx_tensor* logits,
+                             const fp8idx_tensor* context_lens,
+                             int32_t next_n, int32_t max_model_len, int32_t k,
+                             const fp8idx_tensor* indices, void* stream);
+
+/* fp8_mqa_topk: prefill windows.  Row m has window
+ * [max(cu_seqlen_ks[m], 0), min(cu_seqlen_ke[m], width)) -- the columns
+ * fp8_mqa_logits computes.  cu_seqlen_ks/ke [rows] I32 contiguous. */
+fp8idx_status fp8_mqa_topk(const fp8idx_tensor* logits,
+                           const fp8idx_tensor* cu_seqlen_ks,
+                           const fp8idx_tensor* cu_seqlen_ke, int32_t k,
+                           const fp8idx_tensor* indices, void* stream);
 
 /* Support gates, after the pages' is_supported(num_heads, head_dim,
  * kv_block_size) (aiter PR 5047, Technical Details) and is_supported(

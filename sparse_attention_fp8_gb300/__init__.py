@@ -12,7 +12,10 @@ Entry points (same names as the C ABI):
   fp8_paged_mqa_logits(q_fp8, kv_cache, weights, context_lens, block_tables,
                        max_model_len, out, stream=None, options=None)
   fp8_mqa_logits(q_fp8, k_fp8, kv_scale, weights, cu_seqlen_ks, cu_seqlen_ke,
-                 out, stream=None, options=None)
+                 out, stream=None, options=None, clean_logits=True)
+  fp8_paged_topk(logits, context_lens, next_n, max_model_len, k, indices,
+                 stream=None)
+  fp8_mqa_topk(logits, cu_seqlen_ks, cu_seqlen_ke, k, indices, stream=None)
 """
 from ._native import (  # noqa: F401
     FP8IDX_ERR_CUDA,
@@ -25,7 +28,9 @@ from ._native import (  # noqa: F401
     Plan,
     device_status,
     fp8_mqa_logits,
+    fp8_mqa_topk,
     fp8_paged_mqa_logits,
+    fp8_paged_topk,
     library,
     library_path,
     paged_is_supported,

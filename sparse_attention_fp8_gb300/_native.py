@@ -32,7 +32,7 @@ class _Tensor(ctypes.Structure):
 
 class _Options(ctypes.Structure):
     _fields_ = [("num_ctas", ctypes.c_int32), ("stages", ctypes.c_int32), ("split_n", ctypes.c_int32),
-                ("reverse_rows", ctypes.c_int32), ("block_m", ctypes.c_int32)]
+                ("reverse_rows", ctypes.c_int32), ("block_m", ctypes.c_int32), ("clean_logits", ctypes.c_int32)]
 
 
 class _Plan(ctypes.Structure):
@@ -42,15 +42,18 @@ class _Plan(ctypes.Structure):
 
 @dataclasses.dataclass
 class Options:
-    """Tunables; 0 (or -1 for reverse_rows) = host heuristic."""
+    """Tunables; 0 (or -1 for reverse_rows) = host heuristic.  clean_logits:
+    0/1 = write -inf outside the prefill windows, -1 = leave them untouched."""
     num_ctas: int = 0
     stages: int = 0
     split_n: int = 0
     reverse_rows: int = -1
     block_m: int = 0
+    clean_logits: int = 0
 
     def _c(self):
-        return _Options(self.num_ctas, self.stages, self.split_n, self.reverse_rows, self.block_m)
+        return _Options(self.num_ctas, self.stages, self.split_n, self.reverse_rows, self.block_m,
+                        self.clean_logits)
 
 
 @dataclasses.dataclass
@@ -92,7 +95,10 @@ def library():
             lib.fp8_paged_mqa_logits_ex.argtypes = [T, T, T, T, T, ctypes.c_int32, T, P(_Options), V]
             lib.fp8_mqa_logits.argtypes = [T, T, T, T, T, T, T, V]
             lib.fp8_mqa_logits_ex.argtypes = [T, T, T, T, T, T, T, P(_Options), V]
-            for f in ("fp8_paged_mqa_logits", "fp8_paged_mqa_logits_ex", "fp8_mqa_logits", "fp8_mqa_logits_ex"):
+            lib.fp8_paged_topk.argtypes = [T, T, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, T, V]
+            lib.fp8_mqa_topk.argtypes = [T, T, T, ctypes.c_int32, T, V]
+            for f in ("fp8_paged_mqa_logits", "fp8_paged_mqa_logits_ex", "fp8_mqa_logits", "fp8_mqa_logits_ex",
+                      "fp8_paged_topk", "fp8_mqa_topk"):
                 getattr(lib, f).restype = ctypes.c_int
             lib.fp8idx_paged_is_supported.argtypes = [ctypes.c_int32] * 4
             lib.fp8idx_paged_is_supported.restype = ctypes.c_int
@@ -171,8 +177,11 @@ def fp8_paged_mqa_logits(q_fp8, kv_cache, weights, context_lens, block_tables, m
 
 
 def fp8_mqa_logits(q_fp8, k_fp8, kv_scale, weights, cu_seqlen_ks, cu_seqlen_ke, out, stream=None,
-                   options: Options | None = None):
-    """Prefill logits into ``out`` (every element written, -inf outside windows)."""
+                   options: Options | None = None, clean_logits: bool = True):
+    """Prefill logits into ``out``: every element written, -inf outside the
+    windows (clean_logits=False: only the windows are written)."""
+    if not clean_logits:
+        options = dataclasses.replace(options or Options(), clean_logits=-1)
     lib = library()
     args = [_desc(q_fp8), _desc(k_fp8), _desc(kv_scale), _desc(weights), _desc(cu_seqlen_ks),
             _desc(cu_seqlen_ke)]
@@ -186,6 +195,25 @@ def fp8_mqa_logits(q_fp8, k_fp8, kv_scale, weights, cu_seqlen_ks, cu_seqlen_ke, 
         st = lib.fp8_mqa_logits_ex(*refs, ctypes.byref(o), ctypes.byref(oc), s)
     _check(st)
     return out
+
+
+def fp8_paged_topk(logits, context_lens, next_n, max_model_len, k, indices, stream=None):
+    """Decode top-k: indices [rows, k] of each row's k largest logits in its
+    causal window (value descending, position ascending; -1 past the window)."""
+    lib = library()
+    lg, cl, ix = _desc(logits), _desc(context_lens), _desc(indices)
+    _check(lib.fp8_paged_topk(ctypes.byref(lg), ctypes.byref(cl), int(next_n), int(max_model_len), int(k),
+                              ctypes.byref(ix), _stream(stream, logits)))
+    return indices
+
+
+def fp8_mqa_topk(logits, cu_seqlen_ks, cu_seqlen_ke, k, indices, stream=None):
+    """Prefill top-k over the windows [ks, ke) (same order and padding)."""
+    lib = library()
+    lg, a, b, ix = _desc(logits), _desc(cu_seqlen_ks), _desc(cu_seqlen_ke), _desc(indices)
+    _check(lib.fp8_mqa_topk(ctypes.byref(lg), ctypes.byref(a), ctypes.byref(b), int(k), ctypes.byref(ix),
+                            _stream(stream, logits)))
+    return indices
 
 
 def paged_is_supported(heads, head_dim, block_size, next_n) -> bool:

@@ -141,7 +141,9 @@ bool paged_supported(int heads, int head_dim, int block_size, int next_n) {
   return block_size == 1 || block_size == 16 || block_size == 32 || block_size == 64 || block_size == 128;
 }
 
-bool prefill_supported(int heads, int head_dim) { return head_dim == kHeadDim && (heads == 32 || heads == 64); }
+bool prefill_supported(int heads, int head_dim) {
+  return head_dim == kHeadDim && (heads == 32 || heads == 64 || heads == 128);
+}
 
 fp8idx_status plan_paged(int32_t batch, int32_t next_n, int32_t heads, int32_t head_dim, int32_t block_size,
                          int32_t max_model_len, int32_t num_sms, int32_t smem_limit, const fp8idx_options* o,
@@ -384,6 +386,7 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const fp8idx_tensor* k, const
   p.split = plan.split_n;
   p.reverse = plan.reverse_rows;
   p.vec_ok = (aligned16(out->data) && (p.out_stride % 4) == 0) ? 1 : 0;
+  p.clean = (opts && opts->clean_logits < 0) ? 0 : 1;
   p.acc_bufs = paged_acc_buffers(plan.tile_n);
   // -inf tiles as TMA stores need 16-byte aligned rows (the tensor map's
   // stride rule); otherwise the epilogue warps write them.  A TMA store
@@ -393,7 +396,7 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const fp8idx_tensor* k, const
   std::memset(&tm_out, 0, sizeof(tm_out));
   p.tma_fill = 0;
   p.fill_cols = (int32_t)(N & ~3ll);
-  if (p.vec_ok && p.fill_cols > 0) {
+  if (p.clean && p.vec_ok && p.fill_cols > 0) {
     const uint64_t dims[2] = {(uint64_t)p.fill_cols, (uint64_t)M};
     const uint64_t strides[1] = {(uint64_t)p.out_stride * 4u};
     const uint32_t box[2] = {(uint32_t)kTileTokens, (uint32_t)plan.block_m};
@@ -404,6 +407,63 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const fp8idx_tensor* k, const
   cudaError_t e = launch_prefill(tm_q, tm_k, tm_s, tm_w, tm_out, p, (int)H, plan.grid, plan.smem_bytes,
                                  static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+// ------------------------------------------------------------------ top-k
+// mode 0: prefill windows from ks/ke over the row width; mode 1: decode
+// windows from context_lens/next_n within max_model_len columns.
+fp8idx_status topk_impl(int mode, const fp8idx_tensor* logits, const fp8idx_tensor* ks, const fp8idx_tensor* ke,
+                        const fp8idx_tensor* cl, int32_t next_n, int32_t max_model_len, int32_t k,
+                        const fp8idx_tensor* indices, void* stream) {
+  g_last_error.clear();
+  TRY(check_tensor(logits, "logits", FP8IDX_F32, 2));
+  TRY(check_tensor(indices, "indices", FP8IDX_I32, 2));
+  const int64_t R = logits->shape[0], W = logits->shape[1];
+  if (k < 1 || k > kTopkMaxK) return fail(FP8IDX_ERR_UNSUPPORTED, "top-k: k=%d not in [1, %d]", k, kTopkMaxK);
+  if (W > 1 && logits->stride[1] != 1) return fail(FP8IDX_ERR_INVALID, "logits must have unit inner stride");
+  if (R > 1 && logits->stride[0] < W) return fail(FP8IDX_ERR_INVALID, "logits rows overlap");
+  if (indices->shape[0] != R || indices->shape[1] != k || (k > 1 && indices->stride[1] != 1) ||
+      (R > 1 && indices->stride[0] < k))
+    return fail(FP8IDX_ERR_INVALID, "indices must be [rows, k] with unit inner stride");
+  if (W >= (1ll << 31) || R >= (1ll << 31)) return fail(FP8IDX_ERR_UNSUPPORTED, "top-k: logits too large");
+  TopkParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.mode = mode;
+  p.k = k;
+  p.rows = (int32_t)R;
+  if (mode == 0) {
+    TRY(check_tensor(ks, "cu_seqlen_ks", FP8IDX_I32, 1));
+    TRY(check_tensor(ke, "cu_seqlen_ke", FP8IDX_I32, 1));
+    if (ks->shape[0] != R || ke->shape[0] != R || !contiguous(ks) || !contiguous(ke))
+      return fail(FP8IDX_ERR_INVALID, "cu_seqlen_ks/ke must be contiguous [rows]");
+    p.ks = static_cast<const int32_t*>(ks->data);
+    p.ke = static_cast<const int32_t*>(ke->data);
+    p.cols = (int32_t)W;
+    p.next_n = 1;
+  } else {
+    TRY(check_tensor(cl, "context_lens", FP8IDX_I32, 1));
+    if (next_n < 1) return fail(FP8IDX_ERR_INVALID, "next_n must be positive");
+    if (!contiguous(cl) || cl->shape[0] * next_n != R)
+      return fail(FP8IDX_ERR_INVALID, "context_lens must be contiguous [rows / next_n]");
+    if (max_model_len < 0 || max_model_len > W)
+      return fail(FP8IDX_ERR_INVALID, "max_model_len must be in [0, logits width]");
+    p.context_lens = static_cast<const int32_t*>(cl->data);
+    p.cols = max_model_len;
+    p.next_n = next_n;
+  }
+  if (R == 0) return ok();
+  p.logits = static_cast<const float*>(logits->data);
+  p.stride = R > 1 ? logits->stride[0] : W;
+  p.out = static_cast<int32_t*>(indices->data);
+  p.out_stride = R > 1 ? indices->stride[0] : k;
+  DeviceInfo dev;
+  TRY(device_info(&dev));
+  int cap = kTopkMaxCap;
+  while (cap > 1024 && (int)topk_smem_layout(cap).total > dev.smem_optin) cap >>= 1;
+  p.cap = cap;
+  cudaError_t e = launch_topk(p, (int)topk_smem_layout(cap).total, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "top-k launch: %s", cudaGetErrorString(e));
   return ok();
 }
 
@@ -436,6 +496,16 @@ fp8idx_status fp8_mqa_logits_ex(const fp8idx_tensor* q_fp8, const fp8idx_tensor*
                                 const fp8idx_tensor* cu_seqlen_ks, const fp8idx_tensor* cu_seqlen_ke,
                                 const fp8idx_tensor* out, const fp8idx_options* opts, void* stream) {
   return prefill_impl(q_fp8, k_fp8, kv_scale, weights, cu_seqlen_ks, cu_seqlen_ke, out, opts, stream);
+}
+
+fp8idx_status fp8_paged_topk(const fp8idx_tensor* logits, const fp8idx_tensor* context_lens, int32_t next_n,
+                             int32_t max_model_len, int32_t k, const fp8idx_tensor* indices, void* stream) {
+  return topk_impl(1, logits, nullptr, nullptr, context_lens, next_n, max_model_len, k, indices, stream);
+}
+
+fp8idx_status fp8_mqa_topk(const fp8idx_tensor* logits, const fp8idx_tensor* cu_seqlen_ks,
+                           const fp8idx_tensor* cu_seqlen_ke, int32_t k, const fp8idx_tensor* indices, void* stream) {
+  return topk_impl(0, logits, cu_seqlen_ks, cu_seqlen_ke, nullptr, 1, 0, k, indices, stream);
 }
 
 int fp8idx_paged_is_supported(int32_t heads, int32_t head_dim, int32_t block_size, int32_t next_n) {
@@ -484,6 +554,6 @@ fp8idx_status fp8idx_device_status(int32_t clear) {
   return FP8IDX_OK;
 }
 
-int32_t fp8idx_version(void) { return 100; }
+int32_t fp8idx_version(void) { return 101; }
 
 }  // extern "C"

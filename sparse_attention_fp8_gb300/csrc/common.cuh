@@ -193,14 +193,14 @@ template <int STEP, int MAX, class F>
 __device__ __forceinline__ void with_chunk_count(int n, F f) {
   static_assert(MAX <= 8, "at most 8 chunks (256 columns)");
   switch (n) {
-    case 1: if constexpr (STEP == 1 && MAX >= 1) f(IntC<1>{}); break;
-    case 2: if constexpr (MAX >= 2) f(IntC<2>{}); break;
-    case 3: if constexpr (STEP == 1 && MAX >= 3) f(IntC<3>{}); break;
-    case 4: if constexpr (MAX >= 4) f(IntC<4>{}); break;
-    case 5: if constexpr (STEP == 1 && MAX >= 5) f(IntC<5>{}); break;
-    case 6: if constexpr (MAX >= 6) f(IntC<6>{}); break;
-    case 7: if constexpr (STEP == 1 && MAX >= 7) f(IntC<7>{}); break;
-    case 8: if constexpr (MAX >= 8) f(IntC<8>{}); break;
+    case 1: if constexpr (1 % STEP == 0 && MAX >= 1) f(IntC<1>{}); break;
+    case 2: if constexpr (2 % STEP == 0 && MAX >= 2) f(IntC<2>{}); break;
+    case 3: if constexpr (3 % STEP == 0 && MAX >= 3) f(IntC<3>{}); break;
+    case 4: if constexpr (4 % STEP == 0 && MAX >= 4) f(IntC<4>{}); break;
+    case 5: if constexpr (5 % STEP == 0 && MAX >= 5) f(IntC<5>{}); break;
+    case 6: if constexpr (6 % STEP == 0 && MAX >= 6) f(IntC<6>{}); break;
+    case 7: if constexpr (7 % STEP == 0 && MAX >= 7) f(IntC<7>{}); break;
+    case 8: if constexpr (8 % STEP == 0 && MAX >= 8) f(IntC<8>{}); break;
     default: break;
   }
 }

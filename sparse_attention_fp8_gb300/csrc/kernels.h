@@ -96,6 +96,7 @@ struct PrefillParams {
   int32_t acc_bufs; // TMEM accumulator buffers: paged_acc_buffers(n_cols)
   int32_t tma_fill; // 1: -inf tiles are TMA stores of a constant shared tile (needs vec_ok)
   int32_t fill_cols; // columns covered by the -inf tensor map: N rounded down to a multiple of 4
+  int32_t clean;     // 1: -inf outside the windows; 0: only the windows are written
 };
 
 // Roles: producer warp, MMA warp, kEpiGroups epilogue warpgroups, -inf filler warp.
@@ -122,6 +123,42 @@ __host__ __device__ inline PrefillSmem prefill_smem_layout(int n_cols, int stage
   return L;
 }
 
+// ----------------------------------------------------------------- top-k
+struct TopkParams {
+  const float* logits;
+  int64_t stride;               // elements between logits rows
+  const int32_t* ks;            // mode 0: row windows [max(ks,0), min(ke,cols))
+  const int32_t* ke;
+  const int32_t* context_lens;  // mode 1: row b*next_n+n has window [0, ctx_b - next_n + n + 1) within cols
+  int32_t* out;
+  int64_t out_stride;
+  int32_t rows;
+  int32_t k;
+  int32_t cols;    // row width the windows are clamped to (N, or max_model_len)
+  int32_t next_n;
+  int32_t mode;    // 0 prefill windows, 1 decode windows
+  int32_t cap;     // candidates held in shared memory
+};
+constexpr int kTopkThreads = 512;
+constexpr int kTopkBins = 4096;  // 12-bit radix levels (the last level has 8 bits)
+constexpr int kTopkMaxK = 2048;
+constexpr int kTopkMaxCap = 16384;
+struct TopkLayout {
+  uint32_t hist, cand_key, cand_pos, sel, scan, misc, total;
+};
+__host__ __device__ inline TopkLayout topk_smem_layout(int cap) {
+  TopkLayout L;
+  uint32_t off = 0;
+  L.sel = off;      off += 8u * kTopkMaxK;
+  L.hist = off;     off += 4u * kTopkBins;
+  L.cand_key = off; off += 4u * (uint32_t)cap;
+  L.cand_pos = off; off += 4u * (uint32_t)cap;
+  L.scan = off;     off += 4u * 32u;
+  L.misc = off;     off += 4u * 8u;
+  L.total = off;
+  return L;
+}
+
 // ------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error.  The tensor maps are encoded
 // by the caller; `heads` selects the template instance.
@@ -130,6 +167,8 @@ cudaError_t launch_paged(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, cons
 cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_s,
                            const CUtensorMap& tm_w, const CUtensorMap& tm_out, const PrefillParams& p, int heads,
                            int grid, int smem_bytes, cudaStream_t stream);
+
+cudaError_t launch_topk(const TopkParams& p, int smem_bytes, cudaStream_t stream);
 
 // Watchdog words of the two translation units (synchronous read, optional clear).
 cudaError_t read_paged_watchdog(unsigned int* value, bool clear);

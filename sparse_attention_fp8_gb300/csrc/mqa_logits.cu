@@ -307,9 +307,9 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
                   if (lane == 0) ptx::mbar_arrive(acce);
                 },
                 [&](int r, float v) {
-                  if (r < rows_valid && col_ok)
-                    __stcs(out_col + static_cast<int64_t>(r) * p.out_stride,
-                           (n >= lo_r[r] && n < hi_r[r]) ? v * scale : ninf);
+                  const bool inside = n >= lo_r[r] && n < hi_r[r];
+                  if (r < rows_valid && col_ok && (inside || p.clean))
+                    __stcs(out_col + static_cast<int64_t>(r) * p.out_stride, inside ? v * scale : ninf);
                 });
           }
           st.next();
@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
     const float ninf = __int_as_float(0xff800000);
     const float4 f4 = make_float4(ninf, ninf, ninf, ninf);
     const int tail = p.cols - p.fill_cols;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    for (int u = blockIdx.x; u < n_units && p.clean; u += gridDim.x) {
       const Unit U = load_unit(p, u, num_rb, n_tiles);
       const int k_lo = (U.j0 - U.sidx) / p.split;
       const int n_inf = U.n_j - U.n_comp;
@@ -385,6 +385,7 @@ cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, con
   void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, PrefillParams) = nullptr;
   if (heads == 32) kern = mqa_logits_kernel<32>;
   else if (heads == 64) kern = mqa_logits_kernel<64>;
+  else if (heads == 128) kern = mqa_logits_kernel<128>;
   else return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;

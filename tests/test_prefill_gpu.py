@@ -25,10 +25,11 @@ def fp8idx():
     return m
 
 
-def run_prefill(fp8idx, case, options=None):
+def run_prefill(fp8idx, case, options=None, clean_logits=True):
     d = to_device(case)
     out = torch.full((case.rows, case.cols), float("nan"), dtype=torch.float32, device="cuda")
-    fp8idx.fp8_mqa_logits(d["q"], d["k"], d["kv_scale"], d["weights"], d["ks"], d["ke"], out, options=options)
+    fp8idx.fp8_mqa_logits(d["q"], d["k"], d["kv_scale"], d["weights"], d["ks"], d["ke"], out, options=options,
+                          clean_logits=clean_logits)
     torch.cuda.synchronize()
     return out.cpu().numpy()
 
@@ -40,13 +41,25 @@ def oracle_prefill(o, case, rows=None):
 MODES = ["causal", "multi_req", "misaligned", "empty", "past_end", "cp"]
 
 
-@pytest.mark.parametrize("heads", [32, 64])
+@pytest.mark.parametrize("heads", [32, 64, 128])
 @pytest.mark.parametrize("mode", MODES)
 def test_prefill_window_modes(fp8idx, oracle_impl, mode, heads):
     # M not a multiple of the row block, N not a multiple of the 128-token tile
     case = workloads.prefill_case(45, 700, heads, mode=mode, seed=100 + MODES.index(mode))
     gpu = run_prefill(fp8idx, case)
     assert_rows_close(gpu, oracle_prefill(oracle_impl, case), what=f"{mode}/h{heads}")
+
+
+@pytest.mark.parametrize("heads", [32, 128])
+@pytest.mark.parametrize("mode", MODES)
+def test_prefill_no_clean_logits(fp8idx, oracle_impl, mode, heads):
+    """clean_logits=False: exactly the windows are written (the NaN poison
+    must survive everywhere else, including past_end windows that start
+    beyond N, which the pages report as the out-of-bounds case)."""
+    case = workloads.prefill_case(45, 701, heads, mode=mode, seed=200 + MODES.index(mode))
+    gpu = run_prefill(fp8idx, case, clean_logits=False)
+    ref = oracle_prefill(oracle_impl, case)
+    assert_rows_close(gpu, ref, written=np.isfinite(ref), what=f"no-clean {mode}/h{heads}")
 
 
 @pytest.mark.parametrize("shape", [(1, 1), (3, 128), (8, 129), (17, 256), (64, 1000), (200, 520)])

@@ -12,4 +12,5 @@ from .synth import (  # noqa: F401
     e4m3_codes,
     make_config,
     prefill_case,
+    prefill_windows,
 )
