@@ -6,7 +6,8 @@ default workload is the MTP-verify decode batch (batch 16, next_n 6, 32 heads,
 131072-token contexts, max_model_len 1048576, KV block size 64) -- the shape
 the indexer pages quote their decode figure on.  Other workloads:
 --workload {decode_b1, decode_ragged, decode_mtp_verify, decode_mtp_verify_n1,
-prefill_4x1024, decode_blk1}.
+prefill_4x1024, decode_blk1}, and the top-k consumer of the logits (k = 2048)
+on two of those shapes: --workload {topk_decode_mtp_verify, topk_prefill_4x1024}.
 
 Prints ONE JSON line (rank 0):
   value      = us per call (all ranks' calls / max-over-ranks device time),
@@ -58,6 +59,13 @@ WORKLOADS = {
     "prefill_4x1024": (3, None),
     "decode_blk1": (4, None),
 }
+# top-k consumer workloads: (config index, k); the logits are the library's
+# own output for that configuration, produced before the timed region
+TOPK_WORKLOADS = {
+    "topk_decode_mtp_verify": (2, 2048),
+    "topk_prefill_4x1024": (3, 2048),
+}
+TOPK_METRIC = "top-k of the indexer logits us/call; essential GB/s and % of HBM roofline (1 GB300)"
 DEFAULT_WORKLOAD = "decode_mtp_verify"
 L2_FLUSH_BYTES = 512 << 20
 L2_BYTES = 126 << 20  # GB300 L2 (nvidia-smi reports about 126 MiB)
@@ -482,9 +490,202 @@ def run_ours(args, rank, world):
     return line
 
 
+# ---------------------------------------------------------- top-k arm
+def topk_windows(idx, case):
+    from oracle import topk as T  # window arithmetic only (no selection)
+    if workloads.CONFIGS[idx]["kind"] == "decode":
+        return T.decode_windows(case.context_lens, case.next_n, case.max_model_len)
+    return T.prefill_windows(case.ks, case.ke, case.cols)
+
+
+def topk_cpu_baseline(logits_host_rows, rows, lo, hi, k, n_rows_total, budget_s=10.0):
+    """The numpy top-k oracle on a bounded sample of rows, scaled to all rows."""
+    from oracle import topk as T
+    done, t_total = 0, 0.0
+    while done < len(rows) and t_total < budget_s:
+        r = rows[done]
+        t0 = time.perf_counter()
+        T.topk_rows(logits_host_rows[done:done + 1], lo[r:r + 1], hi[r:r + 1], k)
+        t_total += time.perf_counter() - t0
+        done += 1
+    return {"value": t_total / done * n_rows_total * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {n_rows_total} rows ({t_total:.1f} s), scaled to all rows"}
+
+
+def run_topk(args, rank, world):
+    import torch
+    import sparse_attention_fp8_gb300 as fp8idx
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    idx, k = TOPK_WORKLOADS[args.workload]
+    case = workloads.make_config(idx)
+    kind = workloads.CONFIGS[idx]["kind"]
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.Stream(device=dev)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    # the logits this top-k consumes: the library's own output for the configuration
+    if kind == "decode":
+        d = {key: up(getattr(case, key)) for key in ("q", "kv_cache", "weights", "context_lens", "block_tables")}
+        rows = case.batch * case.next_n
+        logits = torch.full((rows, case.max_model_len), float("-inf"), device=dev)
+        fp8idx.fp8_paged_mqa_logits(d["q"], d["kv_cache"], d["weights"], d["context_lens"], d["block_tables"],
+                                    case.max_model_len, logits)
+        win = {"context_lens": d["context_lens"]}
+        del d
+
+        def call(s=stream):
+            fp8idx.fp8_paged_topk(logits, win["context_lens"], case.next_n, case.max_model_len, k, indices, stream=s)
+    else:
+        d = {key: up(getattr(case, key)) for key in ("q", "k", "kv_scale", "weights", "ks", "ke")}
+        rows = case.rows
+        logits = torch.empty((rows, case.cols), device=dev)
+        fp8idx.fp8_mqa_logits(d["q"], d["k"], d["kv_scale"], d["weights"], d["ks"], d["ke"], logits)
+        win = {"ks": d["ks"], "ke": d["ke"]}
+        del d
+
+        def call(s=stream):
+            fp8idx.fp8_mqa_topk(logits, win["ks"], win["ke"], k, indices, stream=s)
+    indices = torch.empty((rows, k), dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+    lo, hi = topk_windows(idx, case)
+    window_elems = int(np.maximum(hi - lo, 0).sum())
+    nbytes = {"logits": window_elems * 4, "indices": rows * k * 4, "windows": int(sum(t.numel() * 4 for t in win.values())),
+              "total": window_elems * 4 + rows * k * 4 + int(sum(t.numel() * 4 for t in win.values()))}
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
+    with torch.cuda.stream(stream):
+        call()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        call()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            graph.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    # L2 flushed before every call (written, then read back), outside the events
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.zero_()
+            torch.sum(flush, dim=0, dtype=torch.int64, out=flush_sink)
+            starts[i].record(stream)
+            graph.replay()
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    per_call_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    if time.time() - t0 < 1.0:  # soak so the clock sampler sees the load
+        with torch.cuda.stream(stream):
+            t1 = time.time()
+            while time.time() - t1 < 1.0:
+                for _ in range(50):
+                    graph.replay()
+                torch.cuda.synchronize()
+    clocks = ClockSampler.summarize(sampler.stop())
+    clocks["window"] = "timed region + 1 s soak of the same step"
+    total_ms = reduce_max(float(sum(per_call_ms)), world, dev)
+    us_per_call = whole_job_us_per_call(total_ms, args.steps, world)
+    mean_ms = total_ms / args.steps
+    median_us = statistics.median(per_call_ms) * 1e3
+
+    # end to end: the windows' logits from pinned host memory, indices back
+    if kind == "decode":
+        width = int(hi.max()) if rows else 0
+    else:
+        width = case.cols
+    host_logits = torch.empty((rows, width), dtype=torch.float32).pin_memory()
+    host_logits.copy_(logits[:, :width].cpu())
+    host_idx = torch.empty((rows, k), dtype=torch.int32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            logits[:, :width].copy_(host_logits, non_blocking=True)
+            call()
+            host_idx.copy_(indices, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_us = whole_job_us_per_call(reduce_max(e0.elapsed_time(e1), world, dev), e2e_steps, world)
+
+    hbm_peak = float(peaks["hbm_gbs"])
+    achieved_gbs = nbytes["total"] / (mean_ms * 1e-3) / 1e9
+    line = {
+        "metric": TOPK_METRIC, "value": round(us_per_call, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(mean_ms, 6), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 -> i32", "data": "synthetic (logits of the library's kernel)",
+        "config": {"workload": args.workload, "desc": f"top-{k} per row of: {case.name}",
+                   "l2": "flushed before every call (512 MB written, then read back)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "median_us": round(median_us, 3),
+        "essential_bytes": nbytes,
+        "essential_gbs": round(achieved_gbs, 1),
+        "roofline_fraction": round(achieved_gbs / hbm_peak, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved_gbs / hbm_peak, 4), "traffic": recorded_traffic(args.workload),
+                     "peak_source": f"{peak_src} hbm_gbs"},
+        "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": rows * width * 4,
+                "d2h_bytes_per_step": rows * k * 4,
+                "note": "per-step logits windows H2D from pinned memory, call, indices D2H"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rng = np.random.default_rng(0)
+        sample = np.sort(rng.choice(rows, size=min(rows, 64), replace=False))
+        line["cpu_baseline"] = topk_cpu_baseline(logits[torch.from_numpy(sample).to(dev)].cpu().numpy(), sample,
+                                                 lo, hi, k, rows)
+    return line
+
+
 # ---------------------------------------------------------- reference arm
+def run_reference_topk(args):
+    """Reference arm of a top-k workload: the numpy oracle on a bounded
+    sample of rows of the same shape and windows (normal random logits)."""
+    from oracle import topk as T
+    idx, k = TOPK_WORKLOADS[args.workload]
+    case = workloads.make_config(idx)
+    lo, hi = topk_windows(idx, case)
+    rows = lo.size
+    rng = np.random.default_rng(1)
+    vals = []
+    for _ in range(args.warmup + args.steps):
+        r = np.sort(rng.choice(rows, size=min(rows, 8), replace=False))
+        width = int(hi[r].max())
+        sample = rng.normal(size=(r.size, width)).astype(np.float32)
+        t0 = time.perf_counter()
+        T.topk_rows(sample, lo[r], hi[r], k)
+        vals.append((time.perf_counter() - t0) / r.size * rows * 1e6)
+    v = float(np.mean(vals[args.warmup:]))
+    return {
+        "impl": "reference", "metric": TOPK_METRIC, "value": round(v, 1), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v / 1e3, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 -> i32", "data": "synthetic",
+        "config": {"workload": args.workload, "desc": f"top-{k} per row of: {case.name}"},
+        "cpu_baseline": {"value": round(v, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "8 random rows per step, scaled to all rows"},
+        "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference(args):
     import oracle
+    if args.workload in TOPK_WORKLOADS:
+        return run_reference_topk(args)
     idx, case = make_case(args.workload)
     kind = workloads.CONFIGS[idx]["kind"]
     _, _, units = case_bytes_flops(idx, case)
@@ -518,7 +719,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(TOPK_WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
@@ -532,7 +733,7 @@ def main(argv=None):
         import torch
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         torch.distributed.init_process_group("nccl")
-    line = run_ours(args, rank, world)
+    line = run_topk(args, rank, world) if args.workload in TOPK_WORKLOADS else run_ours(args, rank, world)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

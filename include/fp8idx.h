@@ -195,10 +195,11 @@ fp8idx_status fp8_mqa_logits_ex(const fp8idx_tensor* q_fp8,
  * section "GLM-5.2-MXFP4 E2E": stale finite logits outside the window would
  * corrupt it, hence the -inf contract; aiter issue 5477, section Measurement:
  * index_topk 512).  The pages do not define the selection further; this
- * library's definition: indices[r, j] for j < min(k, L_r) is the position
- * (column of the logits row) of the j-th entry of row r's window sorted by
- * logit descending, ties by position ascending (so the result is unique;
- * -0.0 == +0.0); indices[r, j] = -1 for j >= L_r, the window length.
+ * library's definition: row r selects the min(k, L_r) positions (columns of
+ * the logits row) of its window with the largest logits, equal logits taken
+ * from the lowest positions first (so the set is unique; -0.0 == +0.0);
+ * indices[r, 0 .. min(k, L_r)) lists them in ascending position order and
+ * indices[r, j] = -1 for j >= L_r, the window length.
  *
  *  logits   [rows, width] F32, stride[1] == 1, stride[0] >= width.  Only the
  *           windows are read, so values outside them do not matter.

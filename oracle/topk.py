@@ -6,9 +6,10 @@ The selection that follows the logits on the pages is a per-row top-k
 (index_topk 2048 or 512: aiter PR 5047 "GLM-5.2-MXFP4 E2E"; aiter issue 5477,
 Measurement).  The pages say no more about it; the definition followed here
 (the library's): the k positions of a row's window with the largest logits,
-ordered by logit descending and position ascending (which makes the result
-unique; -0.0 equals +0.0), padded with -1 past the window length.  Plain
-numpy: a lexicographic sort of each window.
+equal logits taken from the lowest positions first (which makes the set
+unique; -0.0 equals +0.0), listed in ascending position order and padded
+with -1 past the window length.  Plain numpy: a lexicographic sort of each
+window, then a sort of the chosen positions.
 """
 from __future__ import annotations
 
@@ -35,8 +36,8 @@ def prefill_windows(ks, ke, width: int):
 
 
 def topk_rows(logits: np.ndarray, lo, hi, k: int) -> np.ndarray:
-    """int32 [rows, k]: per row the window positions sorted by (logit desc,
-    position asc), the first k of them, -1 past the window."""
+    """int32 [rows, k]: per row the first k window positions in (logit desc,
+    position asc) order, listed by position, -1 past the window."""
     logits = np.asarray(logits)
     out = np.full((logits.shape[0], k), -1, dtype=np.int32)
     for r in range(logits.shape[0]):
@@ -46,6 +47,6 @@ def topk_rows(logits: np.ndarray, lo, hi, k: int) -> np.ndarray:
         pos = np.arange(a, b)
         vals = logits[r, a:b].astype(np.float64)  # numeric comparison: -0.0 == +0.0
         order = np.lexsort((pos, -vals))  # last key is primary: value descending, then position
-        sel = pos[order[:k]]
+        sel = np.sort(pos[order[:k]])
         out[r, :sel.size] = sel
     return out

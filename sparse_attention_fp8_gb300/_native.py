@@ -199,7 +199,8 @@ def fp8_mqa_logits(q_fp8, k_fp8, kv_scale, weights, cu_seqlen_ks, cu_seqlen_ke, 
 
 def fp8_paged_topk(logits, context_lens, next_n, max_model_len, k, indices, stream=None):
     """Decode top-k: indices [rows, k] of each row's k largest logits in its
-    causal window (value descending, position ascending; -1 past the window)."""
+    causal window (equal logits: lowest positions), listed by position, -1
+    past the window."""
     lib = library()
     lg, cl, ix = _desc(logits), _desc(context_lens), _desc(indices)
     _check(lib.fp8_paged_topk(ctypes.byref(lg), ctypes.byref(cl), int(next_n), int(max_model_len), int(k),
@@ -208,7 +209,7 @@ def fp8_paged_topk(logits, context_lens, next_n, max_model_len, k, indices, stre
 
 
 def fp8_mqa_topk(logits, cu_seqlen_ks, cu_seqlen_ke, k, indices, stream=None):
-    """Prefill top-k over the windows [ks, ke) (same order and padding)."""
+    """Prefill top-k over the windows [ks, ke) (same rule, order and padding)."""
     lib = library()
     lg, a, b, ix = _desc(logits), _desc(cu_seqlen_ks), _desc(cu_seqlen_ke), _desc(indices)
     _check(lib.fp8_mqa_topk(ctypes.byref(lg), ctypes.byref(a), ctypes.byref(b), int(k), ctypes.byref(ix),

@@ -457,6 +457,7 @@ fp8idx_status topk_impl(int mode, const fp8idx_tensor* logits, const fp8idx_tens
   p.stride = R > 1 ? logits->stride[0] : W;
   p.out = static_cast<int32_t*>(indices->data);
   p.out_stride = R > 1 ? indices->stride[0] : k;
+  p.vec_ok = (aligned16(logits->data) && (p.stride % 4) == 0) ? 1 : 0;
   DeviceInfo dev;
   TRY(device_info(&dev));
   int cap = kTopkMaxCap;

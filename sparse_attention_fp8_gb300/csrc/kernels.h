@@ -138,18 +138,18 @@ struct TopkParams {
   int32_t next_n;
   int32_t mode;    // 0 prefill windows, 1 decode windows
   int32_t cap;     // candidates held in shared memory
+  int32_t vec_ok;  // every row starts 16-byte aligned: float4 loads inside the windows
 };
 constexpr int kTopkThreads = 512;
 constexpr int kTopkBins = 4096;  // 12-bit radix levels (the last level has 8 bits)
 constexpr int kTopkMaxK = 2048;
-constexpr int kTopkMaxCap = 16384;
+constexpr int kTopkMaxCap = 8192;  // 80 KB of shared memory per CTA: two CTAs per SM
 struct TopkLayout {
-  uint32_t hist, cand_key, cand_pos, sel, scan, misc, total;
+  uint32_t hist, cand_key, cand_pos, scan, misc, total;
 };
 __host__ __device__ inline TopkLayout topk_smem_layout(int cap) {
   TopkLayout L;
   uint32_t off = 0;
-  L.sel = off;      off += 8u * kTopkMaxK;
   L.hist = off;     off += 4u * kTopkBins;
   L.cand_key = off; off += 4u * (uint32_t)cap;
   L.cand_pos = off; off += 4u * (uint32_t)cap;

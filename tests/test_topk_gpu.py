@@ -89,6 +89,22 @@ def test_mqa_topk_special_values(fp8idx):
         assert np.array_equal(gpu_mqa_topk(fp8idx, logits, ks, ke, k), want), f"k={k}"
 
 
+@pytest.mark.parametrize("shift,pad", [(1, 1), (2, 6), (0, 3)], ids=["unaligned-base", "shift2", "odd-stride"])
+def test_mqa_topk_unaligned_rows(fp8idx, shift, pad):
+    """Rows that do not start on 16 bytes (scalar loads) and windows with
+    partial 4-value groups at both ends."""
+    rng = np.random.default_rng(shift * 7 + pad)
+    m, n = 21, 9000
+    ks, ke = workloads.prefill_windows("past_end", m, n, rng, 4)
+    buf = torch.from_numpy(rng.normal(size=(m, n + pad)).astype(np.float32)).cuda()
+    lg = buf[:, shift:shift + n]
+    want = T.topk_rows(lg.cpu().numpy(), *T.prefill_windows(ks, ke, n), 1000)
+    out = torch.full((m, 1000), -7, dtype=torch.int32, device="cuda")
+    fp8idx.fp8_mqa_topk(lg, torch.from_numpy(ks).cuda(), torch.from_numpy(ke).cuda(), 1000, out)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), want)
+
+
 def test_paged_topk_ragged(fp8idx):
     rng = np.random.default_rng(11)
     batch, next_n, mml = 9, 3, 70000

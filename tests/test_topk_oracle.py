@@ -2,8 +2,9 @@
 library routines and invariants -- not against itself.
 
 The definition (the library's reading of the pages' top-k step): per row,
-the window positions sorted by logit descending then position ascending, the
-first k, -1 past the window length; -0.0 equals +0.0.
+the k window positions with the largest logits (equal logits: lowest
+positions first), listed by position, -1 past the window length; -0.0 equals
++0.0.
 """
 import inspect
 import textwrap
@@ -22,18 +23,21 @@ def pin_hand_cases(topk):
     row = _rows([3, 1, 4, 1, 5, 9, 2, 6])
     full = (np.array([0]), np.array([8]))
     # 9@5 > 6@7 > 5@4 > 4@2 > 3@0 > 2@6 > 1@1 = 1@3 (tie: lower position first)
-    assert topk(row, *full, 3).tolist() == [[5, 7, 4]]
-    assert topk(row, *full, 8).tolist() == [[5, 7, 4, 2, 0, 6, 1, 3]]
+    assert topk(row, *full, 3).tolist() == [[4, 5, 7]]
+    assert topk(row, *full, 7).tolist() == [[0, 1, 2, 4, 5, 6, 7]]  # of the two 1s, position 1
+    assert topk(row, *full, 8).tolist() == [[0, 1, 2, 3, 4, 5, 6, 7]]
     # window [2, 6): 4@2, 1@3, 5@4, 9@5
-    assert topk(row, np.array([2]), np.array([6]), 3).tolist() == [[5, 4, 2]]
+    assert topk(row, np.array([2]), np.array([6]), 3).tolist() == [[2, 4, 5]]
     # window shorter than k: padded with -1
-    assert topk(row, np.array([6]), np.array([8]), 4).tolist() == [[7, 6, -1, -1]]
+    assert topk(row, np.array([6]), np.array([8]), 4).tolist() == [[6, 7, -1, -1]]
     # empty window
     assert topk(row, np.array([5]), np.array([5]), 2).tolist() == [[-1, -1]]
+    # equal values: the lowest positions
+    assert topk(_rows([1.0, 5.0, 5.0, 5.0]), np.array([0]), np.array([4]), 2).tolist() == [[1, 2]]
     # -0.0 equals +0.0 (position order decides), -inf is the smallest value
-    assert topk(_rows([-0.0, 0.0, -1.0]), np.array([0]), np.array([3]), 2).tolist() == [[0, 1]]
-    assert topk(_rows([0.0, -0.0, -1.0]), np.array([0]), np.array([3]), 2).tolist() == [[0, 1]]
-    assert topk(_rows([-np.inf, 1.0, -np.inf]), np.array([0]), np.array([3]), 3).tolist() == [[1, 0, 2]]
+    assert topk(_rows([-1.0, -0.0, 0.0, -0.0]), np.array([0]), np.array([4]), 2).tolist() == [[1, 2]]
+    assert topk(_rows([-1.0, 0.0, -0.0, 0.0]), np.array([0]), np.array([4]), 2).tolist() == [[1, 2]]
+    assert topk(_rows([-np.inf, 1.0, -np.inf, -np.inf]), np.array([0]), np.array([4]), 2).tolist() == [[0, 1]]
 
 
 def pin_windows(decode_windows, prefill_windows):
@@ -76,8 +80,10 @@ def pin_partition(topk):
 
 
 def pin_invariants(topk):
-    """Order, uniqueness, window membership, padding; doubling every value
-    (exact) changes nothing."""
+    """Position order, uniqueness, window membership, padding; nothing left
+    out is larger than anything kept, and at the boundary value the kept
+    positions are the lowest ones; doubling every value (exact) changes
+    nothing."""
     rng = np.random.default_rng(2)
     logits = np.round(rng.normal(size=(25, 700)) * 4).astype(np.float32)
     lo = rng.integers(0, 300, 25)
@@ -91,13 +97,15 @@ def pin_invariants(topk):
         assert (got[r, min(k, n):] == -1).all()
         assert len(set(sel.tolist())) == sel.size
         assert ((sel >= lo[r]) & (sel < hi[r])).all()
-        v = logits[r, sel]
-        assert (np.diff(v) <= 0).all()
-        tie = np.diff(v) == 0
-        assert (np.diff(sel)[tie] > 0).all()
-        if n > k:  # nothing left out is larger than the last one kept
+        assert (np.diff(sel) > 0).all()
+        if n > k:
             rest = np.setdiff1d(np.arange(lo[r], hi[r]), sel)
-            assert logits[r, rest].max() <= v[-1]
+            low = logits[r, sel].min()
+            assert logits[r, rest].max() <= low
+            kept_at_low = sel[logits[r, sel] == low]
+            left_at_low = rest[logits[r, rest] == low]
+            if left_at_low.size:
+                assert kept_at_low.max() < left_at_low.min()
     assert np.array_equal(topk(logits * 2, lo, hi, k), got)
 
 
@@ -116,6 +124,7 @@ def test_topk_oracle_pins():
 # Plausible mistakes planted in copies of the oracle; each must fail a pin.
 MUTANTS = {
     "ascending": ("np.lexsort((pos, -vals))", "np.lexsort((pos, vals))"),
+    "unsorted_output": ("sel = np.sort(pos[order[:k]])", "sel = pos[order[:k]]"),
     "ties_descending": ("np.lexsort((pos, -vals))", "np.lexsort((-pos, -vals))"),
     "raw_bit_order": ("logits[r, a:b].astype(np.float64)", "logits[r, a:b].astype(np.float64).view(np.int64)"),
     "pad_zero": ("np.full((logits.shape[0], k), -1, dtype=np.int32)", "np.zeros((logits.shape[0], k), dtype=np.int32)"),
