@@ -6,7 +6,8 @@ default workload is the MTP-verify decode batch (batch 16, next_n 6, 32 heads,
 131072-token contexts, max_model_len 1048576, KV block size 64) -- the shape
 the indexer pages quote their decode figure on.  Other workloads:
 --workload {decode_b1, decode_ragged, decode_mtp_verify, decode_mtp_verify_n1,
-prefill_4x1024, decode_blk1}, and the top-k consumer of the logits (k = 2048)
+prefill_4x1024, decode_blk1, prefill_paged_4x1024 (the prefill shape with K read
+from a paged cache, block 64)}, and the top-k consumer of the logits (k = 2048)
 on two of those shapes: --workload {topk_decode_mtp_verify, topk_prefill_4x1024}.
 
 Prints ONE JSON line (rank 0):
@@ -58,7 +59,9 @@ WORKLOADS = {
     "decode_mtp_verify_n1": (2, 1),
     "prefill_4x1024": (3, None),
     "decode_blk1": (4, None),
+    "prefill_paged_4x1024": (3, None),  # config 3 with K in a paged cache (block 64), gathered in the kernel
 }
+PAGED_PREFILL = {"prefill_paged_4x1024"}
 # top-k consumer workloads: (config index, k); the logits are the library's
 # own output for that configuration, produced before the timed region
 TOPK_WORKLOADS = {
@@ -236,7 +239,23 @@ class ClockSampler:
 # ------------------------------------------------------------------- helpers
 def make_case(workload):
     idx, next_n = WORKLOADS[workload]
+    if workload in PAGED_PREFILL:
+        c = workloads.CONFIGS[idx]
+        lens = [c["n"] // c["requests"]] * c["requests"]
+        rows = [c["m"] // c["requests"]] * c["requests"]
+        return idx, workloads.paged_prefill_case(lens, rows, c["heads"], block_size=64, seed=1000 + idx,
+                                                 name=c["desc"] + ", K paged (block 64)")
     return idx, workloads.make_config(idx, next_n=next_n)
+
+
+def contiguous_view(case):
+    """The gathered-K prefill case the CPU oracle reads (oracle gather)."""
+    import oracle
+    if not isinstance(case, workloads.PagedPrefillCase):
+        return case
+    k, s = oracle.gather_paged_k(case.kv_cache, case.block_tables, case.cu_seq_lens, case.block_size)
+    return workloads.PrefillCase(q=case.q, k=k, kv_scale=s, weights=case.weights, ks=case.ks, ke=case.ke,
+                                 name=case.name)
 
 
 def case_bytes_flops(idx, case):
@@ -316,6 +335,15 @@ def run_ours(args, rank, world):
                                         case.max_model_len, out, stream=s)
         step_inputs = ("q", "weights", "context_lens", "block_tables")
         result_cols = int(min(case.max_model_len, max(int(case.context_lens.max()), 1)))
+    elif args.workload in PAGED_PREFILL:
+        d = {k: up(getattr(case, k)) for k in ("q", "kv_cache", "block_tables", "cu_seq_lens", "weights", "ks", "ke")}
+        out = torch.empty((case.rows, case.cols), device=dev)
+
+        def call(s=stream):
+            fp8idx.fp8_mqa_logits_paged(d["q"], d["kv_cache"], d["block_tables"], d["cu_seq_lens"], d["weights"],
+                                        d["ks"], d["ke"], out, stream=s)
+        step_inputs = ("q", "weights", "ks", "ke", "cu_seq_lens", "block_tables")
+        result_cols = case.cols
     else:
         d = {k: up(getattr(case, k)) for k in ("q", "k", "kv_scale", "weights", "ks", "ke")}
         out = torch.empty((case.rows, case.cols), device=dev)
@@ -480,13 +508,14 @@ def run_ours(args, rank, world):
                    "frac": round(tflops / fp8_peak, 4), "peak_source": f"{peak_src} bf16_tflops x2 (fp8:bf16)"},
         "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "per-step inputs H2D from pinned memory, call, written logits D2H; "
-                        + ("the paged K cache stays resident" if kind == "decode" else "")},
+                        + ("the paged K cache stays resident" if kind == "decode" or args.workload in PAGED_PREFILL
+                           else "")},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "device_status": "ok" if status == 0 else f"watchdog {status}",
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(case, kind, units)
+        line["cpu_baseline"] = cpu_baseline(contiguous_view(case), kind, units)
     return line
 
 
@@ -687,6 +716,7 @@ def run_reference(args):
     if args.workload in TOPK_WORKLOADS:
         return run_reference_topk(args)
     idx, case = make_case(args.workload)
+    case = contiguous_view(case)
     kind = workloads.CONFIGS[idx]["kind"]
     _, _, units = case_bytes_flops(idx, case)
     o = oracle.Oracle()

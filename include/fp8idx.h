@@ -189,6 +189,38 @@ fp8idx_status fp8_mqa_logits_ex(const fp8idx_tensor* q_fp8,
                                 const fp8idx_options* opts, void* stream);
 
 /*
+ * Prefill with the K gather fused in: fp8_mqa_logits_paged.
+ * On the pages the prefill caller first gathers each request's K (and its
+ * scale) out of the paged cache into the contiguous [N, 128] buffer that
+ * fp8_mqa_logits reads (aiter PR 5046, section Motivation: "the caller has
+ * already gathered K out of the paged cache").  This entry point reads K
+ * through the block tables instead: column n, with cu_seq_lens[r] <= n <
+ * cu_seq_lens[r+1], is token n - cu_seq_lens[r] of request r, i.e. slot
+ * (t % block_size) of physical block block_tables[r][t / block_size] of the
+ * split-page cache described under fp8_paged_mqa_logits.  The result equals
+ * fp8_mqa_logits on the gathered buffer.
+ *
+ *  q_fp8, weights, cu_seqlen_ks, cu_seqlen_ke, out  as for fp8_mqa_logits;
+ *               N = out->shape[1] is the gathered length.
+ *  kv_cache     [num_blocks, block_size*(head_dim+4)] U8, contiguous,
+ *               16-byte aligned; block_size in {16, 32, 64, 128}.
+ *  block_tables [requests, max_blocks] I32, rows contiguous.
+ *  cu_seq_lens  [requests + 1] I32 (device), contiguous: 0 = cu[0] <= cu[1]
+ *               <= ... <= cu[requests] = N, and each request's length at
+ *               most max_blocks*block_size (preconditions; requests <= 4096).
+ * opts may be NULL (heuristic); clean_logits as for fp8_mqa_logits_ex.
+ */
+fp8idx_status fp8_mqa_logits_paged(const fp8idx_tensor* q_fp8,
+                                   const fp8idx_tensor* kv_cache,
+                                   const fp8idx_tensor* block_tables,
+                                   const fp8idx_tensor* cu_seq_lens,
+                                   const fp8idx_tensor* weights,
+                                   const fp8idx_tensor* cu_seqlen_ks,
+                                   const fp8idx_tensor* cu_seqlen_ke,
+                                   const fp8idx_tensor* out,
+                                   const fp8idx_options* opts, void* stream);
+
+/*
  * Top-k consumers of the logits: the positions of each row's k largest
  * logits inside the row's window.  The step after the logits on the pages is
  * a per-row top-k selection with index_topk 2048 or 512 (aiter PR 5047,

@@ -187,3 +187,25 @@ class Oracle:
                                       vals.ctypes.data)
         del keep
         return vals
+
+
+def gather_paged_k(kv_cache, block_tables, cu_seq_lens, block_size: int, dim: int = 128):
+    """The caller's gather the prefill page describes (aiter PR 5046,
+    Motivation: K gathered out of the paged cache into a contiguous [N, 128]
+    buffer with a separate [N] f32 scale): request r's tokens t < its length
+    cu[r+1] - cu[r] come from slot t % block_size of block
+    block_tables[r][t // block_size]; a block holds block_size rows of `dim`
+    e4m3 bytes followed by block_size f32 scales.  Plain numpy indexing."""
+    kv = np.asarray(kv_cache, dtype=np.uint8)
+    cu = np.asarray(cu_seq_lens, dtype=np.int64)
+    n = int(cu[-1])
+    k = np.zeros((n, dim), np.uint8)
+    s = np.zeros((n,), np.float32)
+    for r in range(cu.size - 1):
+        for t in range(int(cu[r + 1] - cu[r])):
+            blk = int(block_tables[r][t // block_size])
+            slot = t % block_size
+            page = kv[blk]
+            k[cu[r] + t] = page[slot * dim:(slot + 1) * dim]
+            s[cu[r] + t] = page[block_size * dim + 4 * slot: block_size * dim + 4 * slot + 4].view(np.float32)[0]
+    return k, s

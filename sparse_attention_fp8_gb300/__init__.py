@@ -13,6 +13,9 @@ Entry points (same names as the C ABI):
                        max_model_len, out, stream=None, options=None)
   fp8_mqa_logits(q_fp8, k_fp8, kv_scale, weights, cu_seqlen_ks, cu_seqlen_ke,
                  out, stream=None, options=None, clean_logits=True)
+  fp8_mqa_logits_paged(q_fp8, kv_cache, block_tables, cu_seq_lens, weights,
+                       cu_seqlen_ks, cu_seqlen_ke, out, stream=None,
+                       options=None, clean_logits=True)
   fp8_paged_topk(logits, context_lens, next_n, max_model_len, k, indices,
                  stream=None)
   fp8_mqa_topk(logits, cu_seqlen_ks, cu_seqlen_ke, k, indices, stream=None)
@@ -28,6 +31,7 @@ from ._native import (  # noqa: F401
     Plan,
     device_status,
     fp8_mqa_logits,
+    fp8_mqa_logits_paged,
     fp8_mqa_topk,
     fp8_paged_mqa_logits,
     fp8_paged_topk,

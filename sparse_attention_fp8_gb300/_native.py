@@ -95,10 +95,11 @@ def library():
             lib.fp8_paged_mqa_logits_ex.argtypes = [T, T, T, T, T, ctypes.c_int32, T, P(_Options), V]
             lib.fp8_mqa_logits.argtypes = [T, T, T, T, T, T, T, V]
             lib.fp8_mqa_logits_ex.argtypes = [T, T, T, T, T, T, T, P(_Options), V]
+            lib.fp8_mqa_logits_paged.argtypes = [T, T, T, T, T, T, T, T, P(_Options), V]
             lib.fp8_paged_topk.argtypes = [T, T, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, T, V]
             lib.fp8_mqa_topk.argtypes = [T, T, T, ctypes.c_int32, T, V]
             for f in ("fp8_paged_mqa_logits", "fp8_paged_mqa_logits_ex", "fp8_mqa_logits", "fp8_mqa_logits_ex",
-                      "fp8_paged_topk", "fp8_mqa_topk"):
+                      "fp8_mqa_logits_paged", "fp8_paged_topk", "fp8_mqa_topk"):
                 getattr(lib, f).restype = ctypes.c_int
             lib.fp8idx_paged_is_supported.argtypes = [ctypes.c_int32] * 4
             lib.fp8idx_paged_is_supported.restype = ctypes.c_int
@@ -193,6 +194,23 @@ def fp8_mqa_logits(q_fp8, k_fp8, kv_scale, weights, cu_seqlen_ks, cu_seqlen_ke, 
     else:
         oc = options._c()
         st = lib.fp8_mqa_logits_ex(*refs, ctypes.byref(o), ctypes.byref(oc), s)
+    _check(st)
+    return out
+
+
+def fp8_mqa_logits_paged(q_fp8, kv_cache, block_tables, cu_seq_lens, weights, cu_seqlen_ks, cu_seqlen_ke, out,
+                         stream=None, options: Options | None = None, clean_logits: bool = True):
+    """Prefill logits with K read from the paged cache: column n of request r
+    (cu_seq_lens[r] <= n < cu_seq_lens[r+1]) is its token n - cu_seq_lens[r]."""
+    if not clean_logits:
+        options = dataclasses.replace(options or Options(), clean_logits=-1)
+    lib = library()
+    args = [_desc(q_fp8), _desc(kv_cache), _desc(block_tables), _desc(cu_seq_lens), _desc(weights),
+            _desc(cu_seqlen_ks), _desc(cu_seqlen_ke)]
+    o = _desc(out)
+    oc = options._c() if options is not None else None
+    st = lib.fp8_mqa_logits_paged(*[ctypes.byref(a) for a in args], ctypes.byref(o),
+                                  ctypes.byref(oc) if oc is not None else None, _stream(stream, q_fp8))
     _check(st)
     return out
 

@@ -183,7 +183,7 @@ fp8idx_status plan_paged(int32_t batch, int32_t next_n, int32_t heads, int32_t h
 }
 
 fp8idx_status plan_prefill(int64_t rows, int64_t cols, int32_t heads, int32_t head_dim, int32_t num_sms,
-                           int32_t smem_limit, const fp8idx_options* o, fp8idx_plan* plan) {
+                           int32_t smem_limit, const fp8idx_options* o, fp8idx_plan* plan, int cu_entries = 0) {
   if (!prefill_supported(heads, head_dim))
     return fail(FP8IDX_ERR_UNSUPPORTED, "prefill: heads=%d head_dim=%d not supported", heads, head_dim);
   if (rows < 0 || cols < 0 || rows * heads >= (1ll << 31) || cols >= (1ll << 31))
@@ -194,8 +194,8 @@ fp8idx_status plan_prefill(int64_t rows, int64_t cols, int32_t heads, int32_t he
     return fail(FP8IDX_ERR_UNSUPPORTED, "prefill: block_m %d too large for %d heads", block_m, heads);
   const int n_cols = block_m * heads;
   int stages = (o && o->stages > 0) ? o->stages : 12;
-  while (stages > 2 && (int)prefill_smem_layout(n_cols, stages).total > smem_limit) --stages;
-  if ((int)prefill_smem_layout(n_cols, stages).total > smem_limit)
+  while (stages > 2 && (int)prefill_smem_layout(n_cols, stages, cu_entries).total > smem_limit) --stages;
+  if ((int)prefill_smem_layout(n_cols, stages, cu_entries).total > smem_limit)
     return fail(FP8IDX_ERR_UNSUPPORTED, "prefill: shared memory too small");
   const int64_t num_rb = (rows + block_m - 1) / block_m;
   const int64_t n_tiles = (cols + kTileTokens - 1) / kTileTokens;
@@ -217,7 +217,7 @@ fp8idx_status plan_prefill(int64_t rows, int64_t cols, int32_t heads, int32_t he
   std::memset(plan, 0, sizeof(*plan));
   plan->grid = grid;
   plan->threads = prefill_threads();
-  plan->smem_bytes = (int)prefill_smem_layout(n_cols, stages).total;
+  plan->smem_bytes = (int)prefill_smem_layout(n_cols, stages, cu_entries).total;
   plan->stages = stages;
   plan->tile_n = n_cols;
   plan->block_m = block_m;
@@ -319,21 +319,53 @@ fp8idx_status paged_impl(const fp8idx_tensor* q, const fp8idx_tensor* kv, const 
 }
 
 // ---------------------------------------------------------------- prefill
-fp8idx_status prefill_impl(const fp8idx_tensor* q, const fp8idx_tensor* k, const fp8idx_tensor* s,
-                           const fp8idx_tensor* w, const fp8idx_tensor* ks, const fp8idx_tensor* ke,
-                           const fp8idx_tensor* out, const fp8idx_options* opts, void* stream) {
+// The K source of a prefill call: contiguous (k, s) or paged (kv, bt, cu).
+struct PrefillK {
+  const fp8idx_tensor* k = nullptr;
+  const fp8idx_tensor* s = nullptr;
+  const fp8idx_tensor* kv = nullptr;
+  const fp8idx_tensor* bt = nullptr;
+  const fp8idx_tensor* cu = nullptr;
+};
+
+fp8idx_status prefill_impl(const fp8idx_tensor* q, const PrefillK& src, const fp8idx_tensor* w,
+                           const fp8idx_tensor* ks, const fp8idx_tensor* ke, const fp8idx_tensor* out,
+                           const fp8idx_options* opts, void* stream) {
   g_last_error.clear();
+  const bool paged = src.kv != nullptr;
   TRY(check_tensor(q, "q_fp8", FP8IDX_U8, 3));
-  TRY(check_tensor(k, "k_fp8", FP8IDX_U8, 2));
-  TRY(check_tensor(s, "kv_scale", FP8IDX_F32, 1));
   TRY(check_tensor(w, "weights", FP8IDX_F32, 2));
   TRY(check_tensor(ks, "cu_seqlen_ks", FP8IDX_I32, 1));
   TRY(check_tensor(ke, "cu_seqlen_ke", FP8IDX_I32, 1));
   TRY(check_tensor(out, "out", FP8IDX_F32, 2));
-  const int64_t M = q->shape[0], H = q->shape[1], D = q->shape[2], N = k->shape[0];
-  if (!contiguous(q) || !contiguous(k) || !contiguous(s) || !contiguous(w) || !contiguous(ks) || !contiguous(ke))
+  const int64_t M = q->shape[0], H = q->shape[1], D = q->shape[2];
+  int64_t N = 0, blk = 0, R = 0;
+  if (!paged) {
+    TRY(check_tensor(src.k, "k_fp8", FP8IDX_U8, 2));
+    TRY(check_tensor(src.s, "kv_scale", FP8IDX_F32, 1));
+    N = src.k->shape[0];
+    if (!contiguous(src.k) || !contiguous(src.s)) return fail(FP8IDX_ERR_INVALID, "prefill inputs must be contiguous");
+    if (src.k->shape[1] != D || src.s->shape[0] != N)
+      return fail(FP8IDX_ERR_INVALID, "k_fp8 must be [N, head_dim], kv_scale [N]");
+  } else {
+    TRY(check_tensor(src.kv, "kv_cache", FP8IDX_U8, 2));
+    TRY(check_tensor(src.bt, "block_tables", FP8IDX_I32, 2));
+    TRY(check_tensor(src.cu, "cu_seq_lens", FP8IDX_I32, 1));
+    N = out->shape[1];
+    R = src.bt->shape[0];
+    if (!contiguous(src.kv) || !contiguous(src.cu)) return fail(FP8IDX_ERR_INVALID, "kv_cache and cu_seq_lens must be contiguous");
+    if (src.bt->shape[1] > 1 && src.bt->stride[1] != 1) return fail(FP8IDX_ERR_INVALID, "block_tables rows must be contiguous");
+    if (src.cu->shape[0] != R + 1) return fail(FP8IDX_ERR_INVALID, "cu_seq_lens must be [requests + 1]");
+    if (src.kv->shape[1] % (D + 4) != 0) return fail(FP8IDX_ERR_INVALID, "kv_cache rows must be block_size*(head_dim+4) bytes");
+    blk = src.kv->shape[1] / (D + 4);
+    if (blk != 16 && blk != 32 && blk != 64 && blk != 128)
+      return fail(FP8IDX_ERR_UNSUPPORTED, "paged prefill: block_size %lld not in {16, 32, 64, 128}", (long long)blk);
+    if (R < 1 || R > kMaxBatch) return fail(FP8IDX_ERR_UNSUPPORTED, "paged prefill: %lld requests (1..%d)", (long long)R, kMaxBatch);
+    if (src.bt->shape[1] < 1 || src.kv->shape[0] < 1) return fail(FP8IDX_ERR_INVALID, "empty block table or cache");
+    if (!aligned16(src.kv->data)) return fail(FP8IDX_ERR_INVALID, "kv_cache must be 16-byte aligned");
+  }
+  if (!contiguous(q) || !contiguous(w) || !contiguous(ks) || !contiguous(ke))
     return fail(FP8IDX_ERR_INVALID, "prefill inputs must be contiguous");
-  if (k->shape[1] != D || s->shape[0] != N) return fail(FP8IDX_ERR_INVALID, "k_fp8 must be [N, head_dim], kv_scale [N]");
   if (w->shape[0] != M || w->shape[1] != H) return fail(FP8IDX_ERR_INVALID, "weights must be [M, heads]");
   if (ks->shape[0] != M || ke->shape[0] != M) return fail(FP8IDX_ERR_INVALID, "cu_seqlen_ks/ke must be [M]");
   if (out->shape[0] != M || out->shape[1] != N || (N > 1 && out->stride[1] != 1) || (M > 1 && out->stride[0] < N))
@@ -341,12 +373,12 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const fp8idx_tensor* k, const
   if (!prefill_supported((int)H, (int)D))
     return fail(FP8IDX_ERR_UNSUPPORTED, "prefill: heads=%lld head_dim=%lld not supported", (long long)H, (long long)D);
   if (M == 0 || N == 0) return ok();
-  if (!aligned16(q->data) || !aligned16(k->data) || !aligned16(s->data) || !aligned16(w->data))
+  if (!aligned16(q->data) || !aligned16(w->data) || (!paged && (!aligned16(src.k->data) || !aligned16(src.s->data))))
     return fail(FP8IDX_ERR_INVALID, "q_fp8, k_fp8, kv_scale and weights must be 16-byte aligned");
   DeviceInfo dev;
   TRY(device_info(&dev));
   fp8idx_plan plan;
-  TRY(plan_prefill(M, N, (int)H, (int)D, dev.sms, dev.smem_optin, opts, &plan));
+  TRY(plan_prefill(M, N, (int)H, (int)D, dev.sms, dev.smem_optin, opts, &plan, paged ? (int)R + 1 : 0));
   CUtensorMap tm_q, tm_k, tm_s;
   {
     const uint64_t dims[2] = {(uint64_t)D, (uint64_t)(M * H)};
@@ -354,17 +386,22 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const fp8idx_tensor* k, const
     const uint32_t box[2] = {(uint32_t)D, (uint32_t)plan.tile_n};
     TRY(encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q->data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "q"));
   }
-  {
-    const uint64_t dims[2] = {(uint64_t)D, (uint64_t)N};
-    const uint64_t strides[1] = {(uint64_t)D};
-    const uint32_t box[2] = {(uint32_t)D, (uint32_t)kTileTokens};
-    TRY(encode(&tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, k->data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "k"));
-  }
-  {
-    const uint64_t dims[1] = {(uint64_t)N};
-    const uint32_t box[1] = {(uint32_t)kTileTokens};
-    TRY(encode(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, s->data, dims, nullptr, box, CU_TENSOR_MAP_SWIZZLE_NONE,
-               "kv_scale"));
+  std::memset(&tm_k, 0, sizeof(tm_k));
+  std::memset(&tm_s, 0, sizeof(tm_s));
+  if (!paged) {
+    {
+      const uint64_t dims[2] = {(uint64_t)D, (uint64_t)N};
+      const uint64_t strides[1] = {(uint64_t)D};
+      const uint32_t box[2] = {(uint32_t)D, (uint32_t)kTileTokens};
+      TRY(encode(&tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, src.k->data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                 "k"));
+    }
+    {
+      const uint64_t dims[1] = {(uint64_t)N};
+      const uint32_t box[1] = {(uint32_t)kTileTokens};
+      TRY(encode(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, src.s->data, dims, nullptr, box,
+                 CU_TENSOR_MAP_SWIZZLE_NONE, "kv_scale"));
+    }
   }
   CUtensorMap tm_w;
   {
@@ -374,6 +411,17 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const fp8idx_tensor* k, const
                "weights"));
   }
   PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (paged) {
+    p.kv_cache = static_cast<const uint8_t*>(src.kv->data);
+    p.block_tables = static_cast<const int32_t*>(src.bt->data);
+    p.cu_seq_lens = static_cast<const int32_t*>(src.cu->data);
+    p.bt_stride = R > 1 ? src.bt->stride[0] : src.bt->shape[1];
+    p.num_blocks = src.kv->shape[0];
+    p.max_blocks = (int32_t)src.bt->shape[1];
+    p.block_size = (int32_t)blk;
+    p.n_req = (int32_t)R;
+  }
   p.ks = static_cast<const int32_t*>(ks->data);
   p.ke = static_cast<const int32_t*>(ke->data);
   p.out = static_cast<float*>(out->data);
@@ -404,7 +452,7 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const fp8idx_tensor* k, const
                CU_TENSOR_MAP_SWIZZLE_NONE, "out"));
     p.tma_fill = 1;
   }
-  cudaError_t e = launch_prefill(tm_q, tm_k, tm_s, tm_w, tm_out, p, (int)H, plan.grid, plan.smem_bytes,
+  cudaError_t e = launch_prefill(tm_q, tm_k, tm_s, tm_w, tm_out, p, (int)H, paged, plan.grid, plan.smem_bytes,
                                  static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
   return ok();
@@ -489,14 +537,32 @@ fp8idx_status fp8_paged_mqa_logits_ex(const fp8idx_tensor* q_fp8, const fp8idx_t
 fp8idx_status fp8_mqa_logits(const fp8idx_tensor* q_fp8, const fp8idx_tensor* k_fp8, const fp8idx_tensor* kv_scale,
                              const fp8idx_tensor* weights, const fp8idx_tensor* cu_seqlen_ks,
                              const fp8idx_tensor* cu_seqlen_ke, const fp8idx_tensor* out, void* stream) {
-  return prefill_impl(q_fp8, k_fp8, kv_scale, weights, cu_seqlen_ks, cu_seqlen_ke, out, nullptr, stream);
+  PrefillK src;
+  src.k = k_fp8;
+  src.s = kv_scale;
+  return prefill_impl(q_fp8, src, weights, cu_seqlen_ks, cu_seqlen_ke, out, nullptr, stream);
 }
 
 fp8idx_status fp8_mqa_logits_ex(const fp8idx_tensor* q_fp8, const fp8idx_tensor* k_fp8,
                                 const fp8idx_tensor* kv_scale, const fp8idx_tensor* weights,
                                 const fp8idx_tensor* cu_seqlen_ks, const fp8idx_tensor* cu_seqlen_ke,
                                 const fp8idx_tensor* out, const fp8idx_options* opts, void* stream) {
-  return prefill_impl(q_fp8, k_fp8, kv_scale, weights, cu_seqlen_ks, cu_seqlen_ke, out, opts, stream);
+  PrefillK src;
+  src.k = k_fp8;
+  src.s = kv_scale;
+  return prefill_impl(q_fp8, src, weights, cu_seqlen_ks, cu_seqlen_ke, out, opts, stream);
+}
+
+fp8idx_status fp8_mqa_logits_paged(const fp8idx_tensor* q_fp8, const fp8idx_tensor* kv_cache,
+                                   const fp8idx_tensor* block_tables, const fp8idx_tensor* cu_seq_lens,
+                                   const fp8idx_tensor* weights, const fp8idx_tensor* cu_seqlen_ks,
+                                   const fp8idx_tensor* cu_seqlen_ke, const fp8idx_tensor* out,
+                                   const fp8idx_options* opts, void* stream) {
+  PrefillK src;
+  src.kv = kv_cache;
+  src.bt = block_tables;
+  src.cu = cu_seq_lens;
+  return prefill_impl(q_fp8, src, weights, cu_seqlen_ks, cu_seqlen_ke, out, opts, stream);
 }
 
 fp8idx_status fp8_paged_topk(const fp8idx_tensor* logits, const fp8idx_tensor* context_lens, int32_t next_n,

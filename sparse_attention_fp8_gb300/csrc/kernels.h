@@ -97,18 +97,31 @@ struct PrefillParams {
   int32_t tma_fill; // 1: -inf tiles are TMA stores of a constant shared tile (needs vec_ok)
   int32_t fill_cols; // columns covered by the -inf tensor map: N rounded down to a multiple of 4
   int32_t clean;     // 1: -inf outside the windows; 0: only the windows are written
+  // paged K (the gather fused into the producer): column n of request r
+  // (cu_seq_lens[r] <= n < cu_seq_lens[r+1]) is token n - cu_seq_lens[r] of
+  // that request, read through its block-table row from the split-page cache
+  const uint8_t* kv_cache;
+  const int32_t* block_tables;
+  const int32_t* cu_seq_lens;  // [n_req + 1]
+  int64_t bt_stride;
+  int64_t num_blocks;
+  int32_t max_blocks;
+  int32_t block_size;          // 16, 32, 64 or 128
+  int32_t n_req;
 };
 
 // Roles: producer warp, MMA warp, kEpiGroups epilogue warpgroups, -inf filler warp.
 __host__ __device__ constexpr int prefill_threads() { return 32 * (1 + 1 + 4 * kEpiGroups + 1); }
 
 struct PrefillSmem {
-  uint32_t q, k, ninf, scale, w, bars, misc, total;
+  uint32_t q, k, ninf, scale, w, cu, bars, misc, total;
 };
 // The -inf tile (block_m rows x 128 floats, the source of the TMA -inf
 // stores) is at most 8 x 512 B: block_m * heads <= 256 with heads >= 32.
 constexpr int kNinfTileBytes = 8 * kTileTokens * 4;
-__host__ __device__ inline PrefillSmem prefill_smem_layout(int n_cols, int stages) {
+// cu_entries: request offsets kept in shared memory by the paged variant (0
+// for contiguous K).
+__host__ __device__ inline PrefillSmem prefill_smem_layout(int n_cols, int stages, int cu_entries = 0) {
   PrefillSmem L;
   uint32_t off = 0;
   L.q = off;     off += 2u * n_cols * kHeadDim;            // two Q blocks
@@ -116,6 +129,7 @@ __host__ __device__ inline PrefillSmem prefill_smem_layout(int n_cols, int stage
   L.ninf = off;  off += kNinfTileBytes;                     // 1024-aligned (follows whole K tiles)
   L.scale = off; off += (uint32_t)stages * kTileTokens * 4;
   L.w = off;     off += 2u * n_cols * 4;                    // two weight blocks
+  L.cu = off;    off += 4u * (uint32_t)cu_entries;
   off = (off + 7u) & ~7u;
   L.bars = off;  off += 8u * (2u * stages + 2u * kMaxAccBufs + 5u);  // full/empty per stage, accf/acce, qf/qe x2, drain
   L.misc = off;  off += 32u;
@@ -166,7 +180,7 @@ cudaError_t launch_paged(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, cons
                          const PagedParams& p, int heads, bool gather, int grid, int smem_bytes, cudaStream_t stream);
 cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_s,
                            const CUtensorMap& tm_w, const CUtensorMap& tm_out, const PrefillParams& p, int heads,
-                           int grid, int smem_bytes, cudaStream_t stream);
+                           bool paged, int grid, int smem_bytes, cudaStream_t stream);
 
 cudaError_t launch_topk(const TopkParams& p, int smem_bytes, cudaStream_t stream);
 

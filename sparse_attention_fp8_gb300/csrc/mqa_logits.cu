@@ -89,7 +89,7 @@ __device__ __forceinline__ Unit load_unit(const PrefillParams& p, int u, int num
 
 }  // namespace
 
-template <int HEADS>
+template <int HEADS, bool PAGED>
 __global__ void __launch_bounds__(prefill_threads(), 1)
     mqa_logits_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_w,
@@ -104,12 +104,13 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
   const int BM = p.block_m;
   const int AB = p.acc_bufs;
   const uint32_t acc_cols = kTmemCols / AB;
-  const PrefillSmem L = prefill_smem_layout(N, S);
+  const PrefillSmem L = prefill_smem_layout(N, S, PAGED ? p.n_req + 1 : 0);
   uint8_t* q_s = smem + L.q;
   uint8_t* k_s = smem + L.k;
   float4* ninf_s = reinterpret_cast<float4*>(smem + L.ninf);
   float* sc_s = reinterpret_cast<float*>(smem + L.scale);
   float* w_s = reinterpret_cast<float*>(smem + L.w);
+  int32_t* cu_s = reinterpret_cast<int32_t*>(smem + L.cu);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile uint32_t* abort_flag = misc + 1;
@@ -131,7 +132,7 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
   if (threadIdx.x == 0) {
     misc[1] = 0u;
     for (int s = 0; s < S; ++s) {
-      ptx::mbar_init(full0 + 8u * s, 1u);
+      ptx::mbar_init(full0 + 8u * s, PAGED ? 32u : 1u);  // paged: every producer lane publishes its copies
       ptx::mbar_init(empty0 + 8u * s, 1u + 4u);  // MMA commit + the 4 warps that read the tile's scales
     }
     for (int g = 0; g < AB; ++g) {
@@ -145,8 +146,10 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
     ptx::mbar_init(drain_bar, 1u);
     ptx::fence_barrier_init();
     ptx::prefetch_tmap(&tm_q);
-    ptx::prefetch_tmap(&tm_k);
-    ptx::prefetch_tmap(&tm_s);
+    if (!PAGED) {
+      ptx::prefetch_tmap(&tm_k);
+      ptx::prefetch_tmap(&tm_s);
+    }
     ptx::prefetch_tmap(&tm_w);
     if (p.tma_fill) ptx::prefetch_tmap(&tm_out);
   }
@@ -156,6 +159,8 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
                               __int_as_float(0xff800000));
     ptx::fence_proxy_async_smem();
   }
+  if (PAGED)
+    for (int i = threadIdx.x; i <= p.n_req; i += blockDim.x) cu_s[i] = __ldg(p.cu_seq_lens + i);
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(misc), kTmemCols);
     ptx::tmem_relinquish();
@@ -171,8 +176,24 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
     Ring qr{0u, 0u, 2u};
     int issued = 0, q_issued = 0;
     bool ok = true;
+    // Paged K: a tile's copies are tracked by cp.async groups per lane and
+    // published (wait, proxy fence, arrive) kLag tiles after they were issued.
+    constexpr int kLag = 4;
+    int pending = 0;
+    Ring pub{0u, 0u, static_cast<uint32_t>(S)};
+    const auto publish_all = [&]() {
+      ptx::cp_async_wait<0>();
+      ptx::fence_proxy_async_smem();
+      for (; pending > 0; --pending) {
+        ptx::mbar_arrive(full0 + 8u * pub.idx);
+        pub.next();
+      }
+    };
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const Unit U = load_unit(p, u, num_rb, n_tiles);
+      // The Q buffer frees once the consumers finish unit q_issued - 2, whose
+      // last tiles may still be unpublished: publish them before waiting.
+      if (PAGED && q_issued >= 2 && pending > 0) publish_all();
       if (!(ok = warp_wait_bounded(qe0 + 8u * qr.idx, qr.phase ^ 1u, abort_flag, &g_prefill_watchdog,
                                    kSiteQEmpty)))
         break;
@@ -188,19 +209,83 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
         if (!(ok = warp_wait_bounded(empty0 + 8u * st.idx, st.phase ^ 1u, abort_flag, &g_prefill_watchdog,
                                      kSiteStageEmpty)))
           break;
-        if (lane == 0) {
-          const uint32_t full = full0 + 8u * st.idx;
-          ptx::mbar_arrive_expect_tx(full, kKTileBytes + kTileTokens * 4);
-          ptx::tma_load_2d(ptx::smem_u32(k_s + st.idx * kKTileBytes), &tm_k, full, 0, j * kTileTokens);
-          ptx::tma_load_1d(ptx::smem_u32(sc_s + st.idx * kTileTokens), &tm_s, full, j * kTileTokens);
+        if constexpr (!PAGED) {
+          if (lane == 0) {
+            const uint32_t full = full0 + 8u * st.idx;
+            ptx::mbar_arrive_expect_tx(full, kKTileBytes + kTileTokens * 4);
+            ptx::tma_load_2d(ptx::smem_u32(k_s + st.idx * kKTileBytes), &tm_k, full, 0, j * kTileTokens);
+            ptx::tma_load_1d(ptx::smem_u32(sc_s + st.idx * kTileTokens), &tm_s, full, j * kTileTokens);
+          }
+        } else {
+          // Gather: per step 4 tokens, 8 lanes per token, a 16-byte chunk
+          // per lane into the 128-byte-swizzled row (chunk ^ (row & 7)); the
+          // token's first lane also copies its scale.
+          const int64_t n0 = static_cast<int64_t>(j) * kTileTokens;
+          int rq = 0;  // request of the tile's first column: largest r with cu[r] <= n0
+          {
+            int lo_r = 0, hi_r = p.n_req;
+            while (hi_r - lo_r > 1) {
+              const int mid = (lo_r + hi_r) >> 1;
+              if (cu_s[mid] <= n0) lo_r = mid; else hi_r = mid;
+            }
+            rq = lo_r;
+          }
+          const uint32_t tile_s = ptx::smem_u32(k_s + st.idx * kKTileBytes);
+          const uint32_t chunk = static_cast<uint32_t>(lane & 7);
+          const int lg = 31 - __clz(p.block_size);  // block sizes are powers of two
+          const int64_t page_bytes = static_cast<int64_t>(p.block_size) * (kHeadDim + 4);
+          // All 32 block-table reads of the lane's tokens first (independent
+          // loads in flight together), then the copies.
+          int32_t blk_id[kTileTokens / 4];
+          int32_t slot_of[kTileTokens / 4];
+#pragma unroll
+          for (int step = 0; step < kTileTokens / 4; ++step) {
+            const int i = 4 * step + (lane >> 3);
+            const int64_t n = n0 + i;
+            blk_id[step] = -1;
+            slot_of[step] = 0;
+            if (n < p.cols) {
+              while (rq + 1 < p.n_req && cu_s[rq + 1] <= n) ++rq;
+              const int32_t t = static_cast<int32_t>(n - cu_s[rq]);
+              int32_t bi = t >> lg;
+              if (bi > p.max_blocks - 1) bi = p.max_blocks - 1;
+              slot_of[step] = t - (bi << lg);
+              blk_id[step] = __ldg(p.block_tables + static_cast<int64_t>(rq) * p.bt_stride + bi);
+            }
+          }
+#pragma unroll
+          for (int step = 0; step < kTileTokens / 4; ++step) {
+            const int i = 4 * step + (lane >> 3);
+            if (n0 + i < p.cols) {
+              int64_t b = blk_id[step];
+              b = b < 0 ? 0 : (b >= p.num_blocks ? p.num_blocks - 1 : b);
+              const uint8_t* page = p.kv_cache + b * page_bytes;
+              ptx::cp_async_16(tile_s + i * kHeadDim + (((chunk ^ static_cast<uint32_t>(i & 7)) << 4)),
+                               page + static_cast<int64_t>(slot_of[step]) * kHeadDim + chunk * 16);
+              if (chunk == 0)
+                ptx::cp_async_4(ptx::smem_u32(sc_s + st.idx * kTileTokens + i),
+                                page + static_cast<int64_t>(p.block_size) * kHeadDim + slot_of[step] * 4);
+            }
+          }
+          ptx::cp_async_commit();
+          ++pending;
+          if (pending > kLag) {  // the tile issued kLag tiles ago has landed
+            ptx::cp_async_wait<kLag>();
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(full0 + 8u * pub.idx);
+            pub.next();
+            --pending;
+          }
         }
         st.next();
         ++issued;
       }
     }
+    if constexpr (PAGED) publish_all();  // also lets every copy land before the CTA exits
     if (*abort_flag && lane == 0) {
-      for (int c = max(0, issued - S); c < issued; ++c)
-        wait_drain(full0 + 8u * (c % S), (c / S) & 1, &g_prefill_watchdog);
+      if (!PAGED)
+        for (int c = max(0, issued - S); c < issued; ++c)
+          wait_drain(full0 + 8u * (c % S), (c / S) & 1, &g_prefill_watchdog);
       for (int sg = max(0, q_issued - 2); sg < q_issued; ++sg)
         wait_drain(qf0 + 8u * (sg & 1), (sg >> 1) & 1, &g_prefill_watchdog);
     }
@@ -381,11 +466,11 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
 
 cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_s,
                            const CUtensorMap& tm_w, const CUtensorMap& tm_out, const PrefillParams& p, int heads,
-                           int grid, int smem_bytes, cudaStream_t stream) {
+                           bool paged, int grid, int smem_bytes, cudaStream_t stream) {
   void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, PrefillParams) = nullptr;
-  if (heads == 32) kern = mqa_logits_kernel<32>;
-  else if (heads == 64) kern = mqa_logits_kernel<64>;
-  else if (heads == 128) kern = mqa_logits_kernel<128>;
+  if (heads == 32) kern = paged ? mqa_logits_kernel<32, true> : mqa_logits_kernel<32, false>;
+  else if (heads == 64) kern = paged ? mqa_logits_kernel<64, true> : mqa_logits_kernel<64, false>;
+  else if (heads == 128) kern = paged ? mqa_logits_kernel<128, true> : mqa_logits_kernel<128, false>;
   else return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;

@@ -1,0 +1,90 @@
+"""GPU parity of fp8_mqa_logits_paged (prefill with the K gather from the
+paged cache fused into the kernel) against the CPU oracle (the oracle's own
+gather, then the prefill oracle), and bit-identity with fp8_mqa_logits on the
+gathered K: only the K source differs between the two paths."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from parity import assert_rows_close, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fp8idx():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sparse_attention_fp8_gb300 as m
+    m.library()
+    return m
+
+
+def run_paged(fp8idx, case, clean_logits=True, options=None):
+    d = to_device(case)
+    out = torch.full((case.rows, case.cols), float("nan"), device="cuda")
+    fp8idx.fp8_mqa_logits_paged(d["q"], d["kv_cache"], d["block_tables"], d["cu_seq_lens"], d["weights"], d["ks"],
+                                d["ke"], out, clean_logits=clean_logits, options=options)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def gathered(case):
+    return oracle.gather_paged_k(case.kv_cache, case.block_tables, case.cu_seq_lens, case.block_size)
+
+
+@pytest.mark.parametrize("blk", [16, 32, 64, 128])
+@pytest.mark.parametrize("heads", [32, 64])
+def test_paged_prefill_block_sizes(fp8idx, oracle_impl, blk, heads):
+    case = workloads.paged_prefill_case([700, 0, 333, 1030, 5], [64, 0, 333, 100, 5], heads, block_size=blk,
+                                        seed=blk + heads, poison=True, extra_blocks=7)
+    k, s = gathered(case)
+    ref = oracle_impl.mqa_logits(case.q, k, s, case.weights, case.ks, case.ke)
+    gpu = run_paged(fp8idx, case)
+    assert_rows_close(gpu, ref, what=f"blk{blk}/h{heads}")
+    # the same K through the contiguous entry point: identical bits
+    d = to_device(case)
+    out = torch.full((case.rows, case.cols), float("nan"), device="cuda")
+    fp8idx.fp8_mqa_logits(d["q"], torch.from_numpy(k).cuda(), torch.from_numpy(s).cuda(), d["weights"], d["ks"],
+                          d["ke"], out)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), gpu, equal_nan=True)
+
+
+def test_paged_prefill_many_small_requests(fp8idx, oracle_impl):
+    """Tiles that span several requests (lengths well below the 128-token tile)."""
+    rng = np.random.default_rng(3)
+    lens = rng.integers(0, 90, 40)
+    rows = np.minimum(lens, rng.integers(0, 6, 40))
+    case = workloads.paged_prefill_case(lens, rows, 32, block_size=16, seed=8, poison=True, extra_blocks=2)
+    k, s = gathered(case)
+    assert_rows_close(run_paged(fp8idx, case), oracle_impl.mqa_logits(case.q, k, s, case.weights, case.ks, case.ke),
+                      what="small requests")
+
+
+def test_paged_prefill_no_clean_and_overrides(fp8idx, oracle_impl):
+    case = workloads.paged_prefill_case([900, 257], [70, 40], 32, block_size=64, seed=11, poison=True)
+    k, s = gathered(case)
+    ref = oracle_impl.mqa_logits(case.q, k, s, case.weights, case.ks, case.ke)
+    assert_rows_close(run_paged(fp8idx, case, clean_logits=False), ref, written=np.isfinite(ref), what="no-clean")
+    for opts in (dict(split_n=1), dict(stages=2), dict(block_m=3, split_n=3)):
+        gpu = run_paged(fp8idx, case, options=fp8idx.Options(**opts))
+        assert_rows_close(gpu, ref, what=str(opts))
+
+
+def test_paged_prefill_errors(fp8idx):
+    case = workloads.paged_prefill_case([10], [2], 32, block_size=16, seed=1)
+    d = to_device(case)
+    out = torch.empty((case.rows, case.cols), device="cuda")
+    with pytest.raises(fp8idx.Fp8IdxError) as e:  # cu_seq_lens must have requests + 1 entries
+        fp8idx.fp8_mqa_logits_paged(d["q"], d["kv_cache"], d["block_tables"], d["cu_seq_lens"][:1], d["weights"],
+                                    d["ks"], d["ke"], out)
+    assert e.value.status == fp8idx.FP8IDX_ERR_INVALID
+    blk1 = workloads.paged_prefill_case([10], [2], 32, block_size=1, seed=1)
+    d1 = to_device(blk1)
+    with pytest.raises(fp8idx.Fp8IdxError) as e:
+        fp8idx.fp8_mqa_logits_paged(d1["q"], d1["kv_cache"], d1["block_tables"], d1["cu_seq_lens"], d1["weights"],
+                                    d1["ks"], d1["ke"], torch.empty((blk1.rows, blk1.cols), device="cuda"))
+    assert e.value.status == fp8idx.FP8IDX_ERR_UNSUPPORTED

@@ -7,10 +7,12 @@ contains none of the logits arithmetic.
 from .synth import (  # noqa: F401
     CONFIGS,
     DecodeCase,
+    PagedPrefillCase,
     PrefillCase,
     decode_case,
     e4m3_codes,
     make_config,
+    paged_prefill_case,
     prefill_case,
     prefill_windows,
 )

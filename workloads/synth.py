@@ -287,3 +287,54 @@ def make_config(idx: int, next_n: int | None = None):
             c["next_n"] = next_n
         return decode_case(seed=seed, name=desc, **c)
     return prefill_case(seed=seed, name=desc, **c)
+
+
+@dataclasses.dataclass
+class PagedPrefillCase:
+    q: np.ndarray             # [M, H, D] u8
+    kv_cache: np.ndarray      # [num_blocks, block_size*(D+4)] u8
+    block_tables: np.ndarray  # [R, max_blocks] i32
+    cu_seq_lens: np.ndarray   # [R + 1] i32
+    weights: np.ndarray       # [M, H] f32
+    ks: np.ndarray            # [M] i32
+    ke: np.ndarray            # [M] i32
+    block_size: int
+    name: str = ""
+
+    @property
+    def rows(self):
+        return self.q.shape[0]
+
+    @property
+    def cols(self):
+        return int(self.cu_seq_lens[-1])
+
+    @property
+    def heads(self):
+        return self.q.shape[1]
+
+
+def paged_prefill_case(seq_lens, rows_per_req, heads, block_size=64, dim=128, seed=0, poison=False,
+                       extra_blocks=0, name=""):
+    """Requests with K lengths seq_lens in a permuted paged cache (as in
+    decode_case); request r contributes rows_per_req[r] query rows, the last
+    positions of the request (causal chunk): row i of request r has window
+    [cu[r], cu[r] + len_r - rows_r + i + 1) in the gathered columns."""
+    seq = np.asarray(seq_lens, dtype=np.int64)
+    rows = np.asarray(rows_per_req, dtype=np.int64)
+    mml = max(int(seq.max()) if seq.size else 1, 1)
+    base = decode_case(seq.size, 1, heads, dim=dim, max_model_len=mml, block_size=block_size,
+                       context_lens=seq, seed=seed, poison=poison, extra_blocks=extra_blocks)
+    rng = np.random.default_rng(seed + 7)
+    cu = np.concatenate([[0], np.cumsum(seq)]).astype(np.int32)
+    ks, ke = [], []
+    for r in range(seq.size):
+        for i in range(int(rows[r])):
+            ks.append(cu[r])
+            ke.append(cu[r] + seq[r] - rows[r] + i + 1)
+    m = len(ks)
+    q = _q_codes(rng, (m, heads, dim))
+    w = _weights(rng, m, heads)
+    return PagedPrefillCase(q=q, kv_cache=base.kv_cache, block_tables=base.block_tables, cu_seq_lens=cu,
+                            weights=w, ks=np.asarray(ks, np.int32), ke=np.asarray(ke, np.int32),
+                            block_size=block_size, name=name)
