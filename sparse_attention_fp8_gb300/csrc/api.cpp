@@ -142,7 +142,7 @@ bool paged_supported(int heads, int head_dim, int block_size, int next_n) {
 }
 
 bool prefill_supported(int heads, int head_dim) {
-  return head_dim == kHeadDim && (heads == 32 || heads == 64 || heads == 128);
+  return (head_dim == kHeadDim || head_dim == 64) && (heads == 32 || heads == 64 || heads == 128);
 }
 
 fp8idx_status plan_paged(int32_t batch, int32_t next_n, int32_t heads, int32_t head_dim, int32_t block_size,
@@ -194,8 +194,8 @@ fp8idx_status plan_prefill(int64_t rows, int64_t cols, int32_t heads, int32_t he
     return fail(FP8IDX_ERR_UNSUPPORTED, "prefill: block_m %d too large for %d heads", block_m, heads);
   const int n_cols = block_m * heads;
   int stages = (o && o->stages > 0) ? o->stages : 12;
-  while (stages > 2 && (int)prefill_smem_layout(n_cols, stages, cu_entries).total > smem_limit) --stages;
-  if ((int)prefill_smem_layout(n_cols, stages, cu_entries).total > smem_limit)
+  while (stages > 2 && (int)prefill_smem_layout(n_cols, stages, cu_entries, head_dim).total > smem_limit) --stages;
+  if ((int)prefill_smem_layout(n_cols, stages, cu_entries, head_dim).total > smem_limit)
     return fail(FP8IDX_ERR_UNSUPPORTED, "prefill: shared memory too small");
   const int64_t num_rb = (rows + block_m - 1) / block_m;
   const int64_t n_tiles = (cols + kTileTokens - 1) / kTileTokens;
@@ -217,7 +217,7 @@ fp8idx_status plan_prefill(int64_t rows, int64_t cols, int32_t heads, int32_t he
   std::memset(plan, 0, sizeof(*plan));
   plan->grid = grid;
   plan->threads = prefill_threads();
-  plan->smem_bytes = (int)prefill_smem_layout(n_cols, stages, cu_entries).total;
+  plan->smem_bytes = (int)prefill_smem_layout(n_cols, stages, cu_entries, head_dim).total;
   plan->stages = stages;
   plan->tile_n = n_cols;
   plan->block_m = block_m;
@@ -356,6 +356,7 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const PrefillK& src, const fp
     if (!contiguous(src.kv) || !contiguous(src.cu)) return fail(FP8IDX_ERR_INVALID, "kv_cache and cu_seq_lens must be contiguous");
     if (src.bt->shape[1] > 1 && src.bt->stride[1] != 1) return fail(FP8IDX_ERR_INVALID, "block_tables rows must be contiguous");
     if (src.cu->shape[0] != R + 1) return fail(FP8IDX_ERR_INVALID, "cu_seq_lens must be [requests + 1]");
+    if (D != kHeadDim) return fail(FP8IDX_ERR_UNSUPPORTED, "paged prefill: head_dim %lld (only 128)", (long long)D);
     if (src.kv->shape[1] % (D + 4) != 0) return fail(FP8IDX_ERR_INVALID, "kv_cache rows must be block_size*(head_dim+4) bytes");
     blk = src.kv->shape[1] / (D + 4);
     if (blk != 16 && blk != 32 && blk != 64 && blk != 128)
@@ -384,7 +385,8 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const PrefillK& src, const fp
     const uint64_t dims[2] = {(uint64_t)D, (uint64_t)(M * H)};
     const uint64_t strides[1] = {(uint64_t)D};
     const uint32_t box[2] = {(uint32_t)D, (uint32_t)plan.tile_n};
-    TRY(encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q->data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "q"));
+    TRY(encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q->data, dims, strides, box,
+               D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, "q"));
   }
   std::memset(&tm_k, 0, sizeof(tm_k));
   std::memset(&tm_s, 0, sizeof(tm_s));
@@ -393,8 +395,8 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const PrefillK& src, const fp
       const uint64_t dims[2] = {(uint64_t)D, (uint64_t)N};
       const uint64_t strides[1] = {(uint64_t)D};
       const uint32_t box[2] = {(uint32_t)D, (uint32_t)kTileTokens};
-      TRY(encode(&tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, src.k->data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
-                 "k"));
+      TRY(encode(&tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, src.k->data, dims, strides, box,
+                 D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, "k"));
     }
     {
       const uint64_t dims[1] = {(uint64_t)N};
@@ -452,7 +454,7 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const PrefillK& src, const fp
                CU_TENSOR_MAP_SWIZZLE_NONE, "out"));
     p.tma_fill = 1;
   }
-  cudaError_t e = launch_prefill(tm_q, tm_k, tm_s, tm_w, tm_out, p, (int)H, paged, plan.grid, plan.smem_bytes,
+  cudaError_t e = launch_prefill(tm_q, tm_k, tm_s, tm_w, tm_out, p, (int)H, (int)D, paged, plan.grid, plan.smem_bytes,
                                  static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
   return ok();

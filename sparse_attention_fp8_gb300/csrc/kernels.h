@@ -121,11 +121,13 @@ struct PrefillSmem {
 constexpr int kNinfTileBytes = 8 * kTileTokens * 4;
 // cu_entries: request offsets kept in shared memory by the paged variant (0
 // for contiguous K).
-__host__ __device__ inline PrefillSmem prefill_smem_layout(int n_cols, int stages, int cu_entries = 0) {
+// head_dim: bytes per Q/K row (128, or 64 with the 64-byte swizzle).
+__host__ __device__ inline PrefillSmem prefill_smem_layout(int n_cols, int stages, int cu_entries = 0,
+                                                           int head_dim = kHeadDim) {
   PrefillSmem L;
   uint32_t off = 0;
-  L.q = off;     off += 2u * n_cols * kHeadDim;            // two Q blocks
-  L.k = off;     off += (uint32_t)stages * kKTileBytes;
+  L.q = off;     off += 2u * n_cols * head_dim;            // two Q blocks
+  L.k = off;     off += (uint32_t)stages * kTileTokens * head_dim;
   L.ninf = off;  off += kNinfTileBytes;                     // 1024-aligned (follows whole K tiles)
   L.scale = off; off += (uint32_t)stages * kTileTokens * 4;
   L.w = off;     off += 2u * n_cols * 4;                    // two weight blocks
@@ -180,7 +182,7 @@ cudaError_t launch_paged(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, cons
                          const PagedParams& p, int heads, bool gather, int grid, int smem_bytes, cudaStream_t stream);
 cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_s,
                            const CUtensorMap& tm_w, const CUtensorMap& tm_out, const PrefillParams& p, int heads,
-                           bool paged, int grid, int smem_bytes, cudaStream_t stream);
+                           int head_dim, bool paged, int grid, int smem_bytes, cudaStream_t stream);
 
 cudaError_t launch_topk(const TopkParams& p, int smem_bytes, cudaStream_t stream);
 

@@ -89,7 +89,7 @@ __device__ __forceinline__ Unit load_unit(const PrefillParams& p, int u, int num
 
 }  // namespace
 
-template <int HEADS, bool PAGED>
+template <int HEADS, bool PAGED, int DIM>
 __global__ void __launch_bounds__(prefill_threads(), 1)
     mqa_logits_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_w,
@@ -104,7 +104,10 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
   const int BM = p.block_m;
   const int AB = p.acc_bufs;
   const uint32_t acc_cols = kTmemCols / AB;
-  const PrefillSmem L = prefill_smem_layout(N, S, PAGED ? p.n_req + 1 : 0);
+  static_assert(DIM == 128 || (DIM == 64 && !PAGED), "head_dim 128, or 64 with contiguous K");
+  constexpr int kRow = DIM;                        // bytes per Q/K row
+  constexpr int kTileB = kTileTokens * DIM;        // bytes per K tile
+  const PrefillSmem L = prefill_smem_layout(N, S, PAGED ? p.n_req + 1 : 0, DIM);
   uint8_t* q_s = smem + L.q;
   uint8_t* k_s = smem + L.k;
   float4* ninf_s = reinterpret_cast<float4*>(smem + L.ninf);
@@ -199,8 +202,8 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
         break;
       if (lane == 0) {
         const uint32_t qf = qf0 + 8u * qr.idx;
-        ptx::mbar_arrive_expect_tx(qf, N * (kHeadDim + 4));
-        ptx::tma_load_2d(ptx::smem_u32(q_s + qr.idx * N * kHeadDim), &tm_q, qf, 0, U.m0 * HEADS);
+        ptx::mbar_arrive_expect_tx(qf, N * (kRow + 4));
+        ptx::tma_load_2d(ptx::smem_u32(q_s + qr.idx * N * kRow), &tm_q, qf, 0, U.m0 * HEADS);
         ptx::tma_load_1d(ptx::smem_u32(w_s + qr.idx * N), &tm_w, qf, U.m0 * HEADS);
       }
       qr.next();
@@ -212,8 +215,8 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
         if constexpr (!PAGED) {
           if (lane == 0) {
             const uint32_t full = full0 + 8u * st.idx;
-            ptx::mbar_arrive_expect_tx(full, kKTileBytes + kTileTokens * 4);
-            ptx::tma_load_2d(ptx::smem_u32(k_s + st.idx * kKTileBytes), &tm_k, full, 0, j * kTileTokens);
+            ptx::mbar_arrive_expect_tx(full, kTileB + kTileTokens * 4);
+            ptx::tma_load_2d(ptx::smem_u32(k_s + st.idx * kTileB), &tm_k, full, 0, j * kTileTokens);
             ptx::tma_load_1d(ptx::smem_u32(sc_s + st.idx * kTileTokens), &tm_s, full, j * kTileTokens);
           }
         } else {
@@ -230,7 +233,7 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
             }
             rq = lo_r;
           }
-          const uint32_t tile_s = ptx::smem_u32(k_s + st.idx * kKTileBytes);
+          const uint32_t tile_s = ptx::smem_u32(k_s + st.idx * kTileB);
           const uint32_t chunk = static_cast<uint32_t>(lane & 7);
           const int lg = 31 - __clz(p.block_size);  // block sizes are powers of two
           const int64_t page_bytes = static_cast<int64_t>(p.block_size) * (kHeadDim + 4);
@@ -292,9 +295,10 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
   } else if (warp == 1) {
     // ============================== MMA =================================
     const uint32_t idesc = ptx::idesc_e4m3_f32(kTileTokens, N);
-    const uint64_t a_desc0 = ptx::smem_desc_sw128(ptx::smem_u32(k_s));
-    const uint64_t b_desc0 = ptx::smem_desc_sw128(ptx::smem_u32(q_s));
-    const uint64_t q_step = static_cast<uint64_t>((N * kHeadDim) >> 4);
+    // 128-byte rows in the 128-byte swizzle, 64-byte rows in the 64-byte one
+    const uint64_t a_desc0 = DIM == 128 ? ptx::smem_desc_sw128(ptx::smem_u32(k_s)) : ptx::smem_desc_sw64(ptx::smem_u32(k_s));
+    const uint64_t b_desc0 = DIM == 128 ? ptx::smem_desc_sw128(ptx::smem_u32(q_s)) : ptx::smem_desc_sw64(ptx::smem_u32(q_s));
+    const uint64_t q_step = static_cast<uint64_t>((N * kRow) >> 4);
     Ring st{0u, 0u, static_cast<uint32_t>(S)};
     Ring ac{0u, 0u, static_cast<uint32_t>(AB)};
     Ring qr{0u, 0u, 2u};
@@ -311,10 +315,10 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
                                   kSiteAccEmpty)))
             break;
           ptx::tc_fence_after();
-          const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(st.idx) * (kKTileBytes >> 4);
+          const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(st.idx) * (kTileB >> 4);
           const uint32_t d_tmem = tmem + ac.idx * acc_cols;
 #pragma unroll
-          for (int kk = 0; kk < kHeadDim / 32; ++kk)
+          for (int kk = 0; kk < DIM / 32; ++kk)  // K = 32 e4m3 per MMA: 32 bytes into the swizzled row
             ptx::mma_f8f6f4(d_tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, kk > 0 ? 1u : 0u);
           ptx::mma_commit(empty0 + 8u * st.idx);
           ptx::mma_commit(accf0 + 8u * ac.idx);
@@ -466,12 +470,18 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
 
 cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_s,
                            const CUtensorMap& tm_w, const CUtensorMap& tm_out, const PrefillParams& p, int heads,
-                           bool paged, int grid, int smem_bytes, cudaStream_t stream) {
+                           int head_dim, bool paged, int grid, int smem_bytes, cudaStream_t stream) {
   void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, PrefillParams) = nullptr;
-  if (heads == 32) kern = paged ? mqa_logits_kernel<32, true> : mqa_logits_kernel<32, false>;
-  else if (heads == 64) kern = paged ? mqa_logits_kernel<64, true> : mqa_logits_kernel<64, false>;
-  else if (heads == 128) kern = paged ? mqa_logits_kernel<128, true> : mqa_logits_kernel<128, false>;
-  else return cudaErrorInvalidValue;
+  if (head_dim == 128) {
+    if (heads == 32) kern = paged ? mqa_logits_kernel<32, true, 128> : mqa_logits_kernel<32, false, 128>;
+    else if (heads == 64) kern = paged ? mqa_logits_kernel<64, true, 128> : mqa_logits_kernel<64, false, 128>;
+    else if (heads == 128) kern = paged ? mqa_logits_kernel<128, true, 128> : mqa_logits_kernel<128, false, 128>;
+  } else if (head_dim == 64 && !paged) {
+    if (heads == 32) kern = mqa_logits_kernel<32, false, 64>;
+    else if (heads == 64) kern = mqa_logits_kernel<64, false, 64>;
+    else if (heads == 128) kern = mqa_logits_kernel<128, false, 64>;
+  }
+  if (kern == nullptr) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
   kern<<<grid, prefill_threads(), smem_bytes, stream>>>(tm_q, tm_k, tm_s, tm_w, tm_out, p);

@@ -241,6 +241,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
+// The same for the 64-byte swizzle layout (rows of 64 bytes, 8-row atoms of
+// 512 bytes: stride-dimension offset 512; layout code 4 at [61,64)).
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1u) << 16;
+  d |= static_cast<uint64_t>(512u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(4u) << 61;
+  return d;
+}
+
 // Instruction descriptor, kind::f8f6f4: D f32 (bits 4-5 = 1), A and B e4m3
 // (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N>>3 at bit 17,
 // M>>4 at bit 24.

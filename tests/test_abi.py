@@ -43,7 +43,9 @@ def test_support_gates(lib):
     assert not fp8idx.paged_is_supported(32, 128, 8, 1)    # block size 8
     assert fp8idx.prefill_is_supported(32, 128) and fp8idx.prefill_is_supported(64, 128)
     assert fp8idx.prefill_is_supported(128, 128)
+    assert fp8idx.prefill_is_supported(32, 64) and fp8idx.prefill_is_supported(128, 64)
     assert not fp8idx.prefill_is_supported(256, 128)
+    assert not fp8idx.prefill_is_supported(32, 96)
 
 
 def test_planner_decode(lib):

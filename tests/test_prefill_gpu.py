@@ -50,6 +50,24 @@ def test_prefill_window_modes(fp8idx, oracle_impl, mode, heads):
     assert_rows_close(gpu, oracle_prefill(oracle_impl, case), what=f"{mode}/h{heads}")
 
 
+@pytest.mark.parametrize("heads", [32, 64, 128])
+@pytest.mark.parametrize("mode", MODES)
+def test_prefill_head_dim_64(fp8idx, oracle_impl, mode, heads):
+    """head_dim 64 (64-byte rows in the 64-byte swizzle, two K=32 MMAs per
+    tile), the other head size of the pages' prefill sweep."""
+    case = workloads.prefill_case(45, 700, heads, dim=64, mode=mode, seed=300 + MODES.index(mode))
+    assert_rows_close(run_prefill(fp8idx, case), oracle_prefill(oracle_impl, case), what=f"d64 {mode}/h{heads}")
+
+
+@pytest.mark.parametrize("opts", [dict(split_n=1), dict(block_m=3), dict(stages=2)], ids=["split1", "bm3", "st2"])
+def test_prefill_head_dim_64_overrides_and_no_clean(fp8idx, oracle_impl, opts):
+    case = workloads.prefill_case(70, 1300, 32, dim=64, mode="multi_req", seed=31)
+    ref = oracle_prefill(oracle_impl, case)
+    assert_rows_close(run_prefill(fp8idx, case, options=fp8idx.Options(**opts)), ref, what=f"d64 {opts}")
+    gpu = run_prefill(fp8idx, case, options=fp8idx.Options(**opts), clean_logits=False)
+    assert_rows_close(gpu, ref, written=np.isfinite(ref), what=f"d64 no-clean {opts}")
+
+
 @pytest.mark.parametrize("heads", [32, 128])
 @pytest.mark.parametrize("mode", MODES)
 def test_prefill_no_clean_logits(fp8idx, oracle_impl, mode, heads):
@@ -106,6 +124,33 @@ def test_prefill_config3_full_size(fp8idx, oracle_impl):
     cols = lo + (rng.random(rows.size) * (hi - lo)).astype(np.int64)
     ref = oracle_impl.mqa_logits_at(case.q, case.k, case.kv_scale, case.weights, case.ks, case.ke, rows, cols)
     err = np.abs(gpu[rows, cols].astype(np.float64) - ref)
+    assert np.all(err <= 1e-3 * rowmax_min + 1e-5), f"sampled max err {err.max()}"
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("m,n", [(2048, 65536), (1024, 131072)], ids=["2048x65536", "1024x131072"])
+def test_prefill_real_chunk_shapes(fp8idx, oracle_impl, m, n):
+    """The pages' other real chunk shapes (one causal request per chunk):
+    exact -inf mask of every row, full oracle rows at both ends, sampled
+    in-window elements."""
+    case = workloads.prefill_case(m, n, 32, mode="causal", seed=m + n)
+    gpu = run_prefill(fp8idx, case)
+    cols = np.arange(n)[None, :]
+    for r0 in range(0, m, 128):
+        lo = np.maximum(case.ks[r0:r0 + 128].astype(np.int64), 0)[:, None]
+        hi = np.minimum(case.ke[r0:r0 + 128].astype(np.int64), n)[:, None]
+        inside = (cols >= lo) & (cols < hi)
+        assert np.array_equal(np.isneginf(gpu[r0:r0 + 128]), ~inside), f"rows {r0}..: -inf mask"
+    rowmax_min = np.inf
+    for r in (0, m - 1):
+        ref = oracle_prefill(oracle_impl, case, rows=(r, r + 1))
+        assert_rows_close(gpu[r:r + 1], ref, what=f"row {r}")
+        rowmax_min = min(rowmax_min, np.abs(ref[np.isfinite(ref)]).max())
+    rng = np.random.default_rng(2)
+    rows = rng.integers(0, m, 2048)
+    cols_s = case.ks[rows] + (rng.random(rows.size) * (case.ke[rows] - case.ks[rows])).astype(np.int64)
+    ref = oracle_impl.mqa_logits_at(case.q, case.k, case.kv_scale, case.weights, case.ks, case.ke, rows, cols_s)
+    err = np.abs(gpu[rows, cols_s].astype(np.float64) - ref)
     assert np.all(err <= 1e-3 * rowmax_min + 1e-5), f"sampled max err {err.max()}"
 
 

@@ -270,6 +270,11 @@ CONFIGS = {
             desc="decode MTP-verify B16 next_n6 H32 ctx131072 mml1048576 blk64"),
     3: dict(kind="prefill", m=4096, n=32768, heads=32, mode="config3",
             requests=4, desc="prefill M4096 N32768 H32 4x1024 causal rows"),
+    # the prefill page's other real chunk shapes (one causal request per chunk)
+    5: dict(kind="prefill", m=2048, n=65536, heads=32, mode="causal", requests=1,
+            desc="prefill M2048 N65536 H32 one causal request"),
+    6: dict(kind="prefill", m=1024, n=131072, heads=32, mode="causal", requests=1,
+            desc="prefill M1024 N131072 H32 one causal request"),
     4: dict(kind="decode", batch=64, next_n=4, heads=64, max_model_len=32768,
             block_size=1, var_ratio=0.3,
             desc="decode B64 next_n4 H64 mml32768 ragged(0.3) blk1"),
