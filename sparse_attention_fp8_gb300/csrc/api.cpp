@@ -379,7 +379,13 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const PrefillK& src, const fp
   DeviceInfo dev;
   TRY(device_info(&dev));
   fp8idx_plan plan;
-  TRY(plan_prefill(M, N, (int)H, (int)D, dev.sms, dev.smem_optin, opts, &plan, paged ? (int)R + 1 : 0));
+  fp8idx_options popts;
+  if (paged) {  // paged K: one unit per row block (the -inf fill works on its whole row range)
+    popts = opts ? *opts : fp8idx_options{};
+    popts.split_n = 1;
+  }
+  TRY(plan_prefill(M, N, (int)H, (int)D, dev.sms, dev.smem_optin, paged ? &popts : opts, &plan,
+                   paged ? 2 * ((int)R + 1) : 0));
   CUtensorMap tm_q, tm_k, tm_s;
   {
     const uint64_t dims[2] = {(uint64_t)D, (uint64_t)(M * H)};
@@ -390,7 +396,21 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const PrefillK& src, const fp
   }
   std::memset(&tm_k, 0, sizeof(tm_k));
   std::memset(&tm_s, 0, sizeof(tm_s));
-  if (!paged) {
+  if (paged) {
+    // K rows of the cache: [block][row][128 B]; scales: [block][blk f32] after the block's K rows
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)blk, (uint64_t)src.kv->shape[0]};
+    const uint64_t strides[2] = {(uint64_t)D, (uint64_t)src.kv->shape[1]};
+    const uint32_t box[3] = {(uint32_t)D, (uint32_t)blk, 1u};
+    TRY(encode(&tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, src.kv->data, dims, strides, box,
+               CU_TENSOR_MAP_SWIZZLE_128B, "kv_cache"));
+    if (blk >= 32) {
+      const uint64_t sdims[2] = {(uint64_t)blk, (uint64_t)src.kv->shape[0]};
+      const uint64_t sstrides[1] = {(uint64_t)src.kv->shape[1]};
+      const uint32_t sbox[2] = {(uint32_t)blk, 1u};
+      TRY(encode(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, static_cast<const uint8_t*>(src.kv->data) + blk * D,
+                 sdims, sstrides, sbox, CU_TENSOR_MAP_SWIZZLE_NONE, "kv_cache scales"));
+    }
+  } else {
     {
       const uint64_t dims[2] = {(uint64_t)D, (uint64_t)N};
       const uint64_t strides[1] = {(uint64_t)D};

@@ -51,11 +51,27 @@ struct Unit {
   int n_comp;  // computed tiles of this unit (j0, j0 + split, ...)
   int row_lo;  // this lane's row window (lanes < block_m), clamped; empty: 0,0
   int row_hi;
+  int g_lo;    // paged K: output columns [g_lo, g_hi) covered by the computed tiles
+  int g_hi;
 };
+
+// Paged K runs in a padded column space where every request starts on a
+// tile boundary: request r owns padded tiles [tp[r], tp[r+1]), tile
+// tp[r] + t holding its tokens [128t, 128t + 128), i.e. whole cache blocks.
+// Largest r < n with a[r] <= v (a non-decreasing, a[0] <= v).
+__device__ __forceinline__ int upper_index(const int32_t* a, int n, int64_t v) {
+  int lo = 0, hi = n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (a[mid] <= v) lo = mid; else hi = mid;
+  }
+  return lo;
+}
 
 // Warp-collective: unit u's geometry and window union.  Every lane gets the
 // union; lane r < block_m also gets row r's window.
-__device__ __forceinline__ Unit load_unit(const PrefillParams& p, int u, int num_rb, int n_tiles) {
+__device__ __forceinline__ Unit load_unit(const PrefillParams& p, int u, int num_rb, int n_tiles,
+                                          const int32_t* cu = nullptr, const int32_t* tp = nullptr) {
   Unit U;
   const int lane = threadIdx.x & 31;
   const int rb_index = u / p.split;
@@ -82,6 +98,15 @@ __device__ __forceinline__ Unit load_unit(const PrefillParams& p, int u, int num
   }
   U.t_lo = hi > lo ? lo / kTileTokens : 0;
   U.t_hi = hi > lo ? (hi + kTileTokens - 1) / kTileTokens : 0;
+  U.g_lo = U.g_hi = 0;
+  if (cu != nullptr && hi > lo) {  // paged: padded tiles of the first and last union columns
+    const int ra = upper_index(cu, p.n_req, lo), rb2 = upper_index(cu, p.n_req, hi - 1);
+    const int ta = (lo - cu[ra]) / kTileTokens, tb = (hi - 1 - cu[rb2]) / kTileTokens;
+    U.t_lo = tp[ra] + ta;
+    U.t_hi = tp[rb2] + tb + 1;
+    U.g_lo = cu[ra] + ta * kTileTokens;
+    U.g_hi = min(cu[rb2] + (tb + 1) * kTileTokens, cu[rb2 + 1]);
+  }
   U.j0 = (U.t_lo <= U.sidx) ? U.sidx : U.sidx + ((U.t_lo - U.sidx + p.split - 1) / p.split) * p.split;
   U.n_comp = (U.t_hi > U.j0) ? (U.t_hi - U.j0 + p.split - 1) / p.split : 0;
   return U;
@@ -107,13 +132,14 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
   static_assert(DIM == 128 || (DIM == 64 && !PAGED), "head_dim 128, or 64 with contiguous K");
   constexpr int kRow = DIM;                        // bytes per Q/K row
   constexpr int kTileB = kTileTokens * DIM;        // bytes per K tile
-  const PrefillSmem L = prefill_smem_layout(N, S, PAGED ? p.n_req + 1 : 0, DIM);
+  const PrefillSmem L = prefill_smem_layout(N, S, PAGED ? 2 * (p.n_req + 1) : 0, DIM);
   uint8_t* q_s = smem + L.q;
   uint8_t* k_s = smem + L.k;
   float4* ninf_s = reinterpret_cast<float4*>(smem + L.ninf);
   float* sc_s = reinterpret_cast<float*>(smem + L.scale);
   float* w_s = reinterpret_cast<float*>(smem + L.w);
-  int32_t* cu_s = reinterpret_cast<int32_t*>(smem + L.cu);
+  int32_t* cu_s = reinterpret_cast<int32_t*>(smem + L.cu);  // paged: [n_req + 1] request offsets
+  int32_t* tp_s = cu_s + (PAGED ? p.n_req + 1 : 0);          // paged: [n_req + 1] padded tile prefix
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile uint32_t* abort_flag = misc + 1;
@@ -129,13 +155,12 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int num_rb = (p.rows + BM - 1) / BM;
-  const int n_tiles = (p.cols + kTileTokens - 1) / kTileTokens;
   const int n_units = num_rb * p.split;
 
   if (threadIdx.x == 0) {
     misc[1] = 0u;
     for (int s = 0; s < S; ++s) {
-      ptx::mbar_init(full0 + 8u * s, PAGED ? 32u : 1u);  // paged: every producer lane publishes its copies
+      ptx::mbar_init(full0 + 8u * s, 1u);
       ptx::mbar_init(empty0 + 8u * s, 1u + 4u);  // MMA commit + the 4 warps that read the tile's scales
     }
     for (int g = 0; g < AB; ++g) {
@@ -162,8 +187,25 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
                               __int_as_float(0xff800000));
     ptx::fence_proxy_async_smem();
   }
-  if (PAGED)
+  if (PAGED) {
     for (int i = threadIdx.x; i <= p.n_req; i += blockDim.x) cu_s[i] = __ldg(p.cu_seq_lens + i);
+    __syncthreads();
+    if (warp == 0) {  // padded tiles per request, inclusive scan
+      if (lane == 0) tp_s[0] = 0;
+      int running = 0;
+      for (int base = 0; base < p.n_req; base += 32) {
+        const int r = base + lane;
+        int v = r < p.n_req ? (max(cu_s[r + 1] - cu_s[r], 0) + kTileTokens - 1) / kTileTokens : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += t;
+        }
+        if (r < p.n_req) tp_s[r + 1] = running + v;
+        running += __shfl_sync(0xffffffffu, v, 31);
+      }
+    }
+  }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(misc), kTmemCols);
     ptx::tmem_relinquish();
@@ -172,6 +214,9 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = misc[0];
+  const int n_tiles = PAGED ? tp_s[p.n_req] : (p.cols + kTileTokens - 1) / kTileTokens;
+  const int32_t* const ucu = PAGED ? cu_s : nullptr;  // load_unit's paged mapping
+  const int32_t* const utp = PAGED ? tp_s : nullptr;
 
   if (warp == 0) {
     // ============================ producer ==============================
@@ -179,24 +224,8 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
     Ring qr{0u, 0u, 2u};
     int issued = 0, q_issued = 0;
     bool ok = true;
-    // Paged K: a tile's copies are tracked by cp.async groups per lane and
-    // published (wait, proxy fence, arrive) kLag tiles after they were issued.
-    constexpr int kLag = 4;
-    int pending = 0;
-    Ring pub{0u, 0u, static_cast<uint32_t>(S)};
-    const auto publish_all = [&]() {
-      ptx::cp_async_wait<0>();
-      ptx::fence_proxy_async_smem();
-      for (; pending > 0; --pending) {
-        ptx::mbar_arrive(full0 + 8u * pub.idx);
-        pub.next();
-      }
-    };
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const Unit U = load_unit(p, u, num_rb, n_tiles);
-      // The Q buffer frees once the consumers finish unit q_issued - 2, whose
-      // last tiles may still be unpublished: publish them before waiting.
-      if (PAGED && q_issued >= 2 && pending > 0) publish_all();
+      const Unit U = load_unit(p, u, num_rb, n_tiles, ucu, utp);
       if (!(ok = warp_wait_bounded(qe0 + 8u * qr.idx, qr.phase ^ 1u, abort_flag, &g_prefill_watchdog,
                                    kSiteQEmpty)))
         break;
@@ -220,75 +249,40 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
             ptx::tma_load_1d(ptx::smem_u32(sc_s + st.idx * kTileTokens), &tm_s, full, j * kTileTokens);
           }
         } else {
-          // Gather: per step 4 tokens, 8 lanes per token, a 16-byte chunk
-          // per lane into the 128-byte-swizzled row (chunk ^ (row & 7)); the
-          // token's first lane also copies its scale.
-          const int64_t n0 = static_cast<int64_t>(j) * kTileTokens;
-          int rq = 0;  // request of the tile's first column: largest r with cu[r] <= n0
-          {
-            int lo_r = 0, hi_r = p.n_req;
-            while (hi_r - lo_r > 1) {
-              const int mid = (lo_r + hi_r) >> 1;
-              if (cu_s[mid] <= n0) lo_r = mid; else hi_r = mid;
-            }
-            rq = lo_r;
-          }
-          const uint32_t tile_s = ptx::smem_u32(k_s + st.idx * kTileB);
-          const uint32_t chunk = static_cast<uint32_t>(lane & 7);
-          const int lg = 31 - __clz(p.block_size);  // block sizes are powers of two
-          const int64_t page_bytes = static_cast<int64_t>(p.block_size) * (kHeadDim + 4);
-          // All 32 block-table reads of the lane's tokens first (independent
-          // loads in flight together), then the copies.
-          int32_t blk_id[kTileTokens / 4];
-          int32_t slot_of[kTileTokens / 4];
-#pragma unroll
-          for (int step = 0; step < kTileTokens / 4; ++step) {
-            const int i = 4 * step + (lane >> 3);
-            const int64_t n = n0 + i;
-            blk_id[step] = -1;
-            slot_of[step] = 0;
-            if (n < p.cols) {
-              while (rq + 1 < p.n_req && cu_s[rq + 1] <= n) ++rq;
-              const int32_t t = static_cast<int32_t>(n - cu_s[rq]);
-              int32_t bi = t >> lg;
-              if (bi > p.max_blocks - 1) bi = p.max_blocks - 1;
-              slot_of[step] = t - (bi << lg);
-              blk_id[step] = __ldg(p.block_tables + static_cast<int64_t>(rq) * p.bt_stride + bi);
-            }
-          }
-#pragma unroll
-          for (int step = 0; step < kTileTokens / 4; ++step) {
-            const int i = 4 * step + (lane >> 3);
-            if (n0 + i < p.cols) {
-              int64_t b = blk_id[step];
-              b = b < 0 ? 0 : (b >= p.num_blocks ? p.num_blocks - 1 : b);
-              const uint8_t* page = p.kv_cache + b * page_bytes;
-              ptx::cp_async_16(tile_s + i * kHeadDim + (((chunk ^ static_cast<uint32_t>(i & 7)) << 4)),
-                               page + static_cast<int64_t>(slot_of[step]) * kHeadDim + chunk * 16);
-              if (chunk == 0)
-                ptx::cp_async_4(ptx::smem_u32(sc_s + st.idx * kTileTokens + i),
-                                page + static_cast<int64_t>(p.block_size) * kHeadDim + slot_of[step] * 4);
-            }
-          }
-          ptx::cp_async_commit();
-          ++pending;
-          if (pending > kLag) {  // the tile issued kLag tiles ago has landed
-            ptx::cp_async_wait<kLag>();
-            ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(full0 + 8u * pub.idx);
-            pub.next();
-            --pending;
+          // Padded tile j: request r's tokens [128t, 128t + 128), whole cache
+          // blocks: one 3-D TMA per block for its K rows and one copy of its
+          // scales (2-D TMA, or a bulk copy for 16-token blocks whose 64-byte
+          // scale runs are not 128-byte aligned in the stage).
+          const int r = upper_index(tp_s, p.n_req, j);
+          const int t = j - tp_s[r];
+          const int len = cu_s[r + 1] - cu_s[r];
+          const int valid = min(kTileTokens, len - t * kTileTokens);
+          const int blk = p.block_size;
+          const int nblk = (valid + blk - 1) / blk;
+          const int fb = t * kTileTokens / blk;
+          const uint32_t full = full0 + 8u * st.idx;
+          if (lane == 0) ptx::mbar_arrive_expect_tx(full, nblk * blk * (DIM + 4));
+          __syncwarp();
+          if (lane < nblk) {
+            int64_t b_id = __ldg(p.block_tables + static_cast<int64_t>(r) * p.bt_stride + min(fb + lane, p.max_blocks - 1));
+            b_id = b_id < 0 ? 0 : (b_id >= p.num_blocks ? p.num_blocks - 1 : b_id);
+            ptx::tma_load_3d(ptx::smem_u32(k_s + st.idx * kTileB + lane * blk * DIM), &tm_k, full, 0, 0,
+                             static_cast<int32_t>(b_id));
+            if (blk >= 32)
+              ptx::tma_load_2d(ptx::smem_u32(sc_s + st.idx * kTileTokens + lane * blk), &tm_s, full, 0,
+                               static_cast<int32_t>(b_id));
+            else
+              ptx::bulk_g2s(ptx::smem_u32(sc_s + st.idx * kTileTokens + lane * blk),
+                            p.kv_cache + b_id * blk * (DIM + 4) + blk * DIM, blk * 4, full);
           }
         }
         st.next();
         ++issued;
       }
     }
-    if constexpr (PAGED) publish_all();  // also lets every copy land before the CTA exits
     if (*abort_flag && lane == 0) {
-      if (!PAGED)
-        for (int c = max(0, issued - S); c < issued; ++c)
-          wait_drain(full0 + 8u * (c % S), (c / S) & 1, &g_prefill_watchdog);
+      for (int c = max(0, issued - S); c < issued; ++c)
+        wait_drain(full0 + 8u * (c % S), (c / S) & 1, &g_prefill_watchdog);
       for (int sg = max(0, q_issued - 2); sg < q_issued; ++sg)
         wait_drain(qf0 + 8u * (sg & 1), (sg >> 1) & 1, &g_prefill_watchdog);
     }
@@ -304,7 +298,7 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
     Ring qr{0u, 0u, 2u};
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const Unit U = load_unit(p, u, num_rb, n_tiles);
+      const Unit U = load_unit(p, u, num_rb, n_tiles, ucu, utp);
       if (lane == 0) {
         ok = wait_bounded(qf0 + 8u * qr.idx, qr.phase, abort_flag, &g_prefill_watchdog, kSiteQFull);
         const uint64_t b_desc = b_desc0 + qr.idx * q_step;
@@ -353,7 +347,7 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
       bool ok = true;
       constexpr int kRows = NCH / (HEADS / 32);  // block_m
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const Unit U = load_unit(p, u, num_rb, n_tiles);
+        const Unit U = load_unit(p, u, num_rb, n_tiles, ucu, utp);
         // Every row's clamped window in registers for the whole unit (the
         // emit below indexes them with compile-time row numbers).
         int lo_r[kRows], hi_r[kRows];
@@ -384,8 +378,15 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
               break;
             ptx::tc_fence_after();
             const uint32_t taddr = tmem + ac.idx * acc_cols + (static_cast<uint32_t>(quad * 32) << 16);
-            const int n = col0 + row;
-            const bool col_ok = n < p.cols;
+            int n = col0 + row;
+            bool col_ok = n < p.cols;
+            if constexpr (PAGED) {  // padded tile -> the request's output columns; padding is not written
+              const int j = U.j0 + c;
+              const int r = upper_index(tp_s, p.n_req, j);
+              const int local = (j - tp_s[r]) * kTileTokens + row;
+              n = cu_s[r] + local;
+              col_ok = local < cu_s[r + 1] - cu_s[r];
+            }
             float* const out_col = out_block + n;
             const uint32_t acce = acce0 + 8u * ac.idx;
             reduce_rows<HEADS, NCH>(
@@ -424,8 +425,35 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
     const float ninf = __int_as_float(0xff800000);
     const float4 f4 = make_float4(ninf, ninf, ninf, ninf);
     const int tail = p.cols - p.fill_cols;
-    for (int u = blockIdx.x; u < n_units && p.clean; u += gridDim.x) {
-      const Unit U = load_unit(p, u, num_rb, n_tiles);
+    for (int u = blockIdx.x; PAGED && u < n_units && p.clean; u += gridDim.x) {
+      // paged: -inf on [0, g_lo) and [g_hi, N), the columns outside the
+      // computed tiles, per 128-column output tile: a TMA store when the
+      // whole tile is outside, lane stores for the outside part otherwise
+      const Unit U = load_unit(p, u, num_rb, n_tiles, ucu, utp);
+      const int rv = min(BM, p.rows - U.m0);
+      float* const out_block = p.out + static_cast<int64_t>(U.m0) * p.out_stride;
+      const int n_out_tiles = (p.cols + kTileTokens - 1) / kTileTokens;
+      for (int k = 0; k < n_out_tiles; ++k) {
+        const int c0 = k * kTileTokens, c1 = min(c0 + kTileTokens, p.cols);
+        const bool outside = c1 <= U.g_lo || c0 >= U.g_hi;
+        if (outside && p.tma_fill) {
+          if (lane == 0) ptx::tma_store_2d(&tm_out, ptx::smem_u32(ninf_s), c0, U.m0);
+          if (tail > 0 && c0 + kTileTokens > p.fill_cols && lane < rv * tail) {
+            const int r = lane / tail;
+            out_block[static_cast<int64_t>(r) * p.out_stride + p.fill_cols + (lane - r * tail)] = ninf;
+          }
+        } else if (c0 < U.g_lo || c1 > U.g_hi) {
+          for (int e = lane; e < rv * kTileTokens; e += 32) {
+            const int r = e / kTileTokens, col = c0 + (e - r * kTileTokens);
+            if (col < c1 && (col < U.g_lo || col >= U.g_hi))
+              __stcs(out_block + static_cast<int64_t>(r) * p.out_stride + col, ninf);
+          }
+        }
+      }
+      if (p.tma_fill && lane == 0) ptx::bulk_commit_group();
+    }
+    for (int u = blockIdx.x; !PAGED && u < n_units && p.clean; u += gridDim.x) {
+      const Unit U = load_unit(p, u, num_rb, n_tiles, ucu, utp);
       const int k_lo = (U.j0 - U.sidx) / p.split;
       const int n_inf = U.n_j - U.n_comp;
       const int rv = min(BM, p.rows - U.m0);
