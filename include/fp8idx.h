@@ -72,7 +72,9 @@ typedef struct {
  * after the pages' "zero means use the host heuristic" (aiter PR 5047,
  * Technical Details; aiter PR 5046, Technical Details). */
 typedef struct {
-  int32_t num_ctas;     /* decode: persistent CTAs (<= SMs)                  */
+  int32_t num_ctas;     /* decode: persistent CTAs (<= SMs); top-k: CTAs per  */
+                        /* row, 1 .. 8 (more than one: a thread-block      */
+                        /* cluster per row)                                */
   int32_t stages;       /* K-tile pipeline depth in shared memory             */
   int32_t split_n;      /* prefill: column-tile splits per row block          */
   int32_t reverse_rows; /* prefill: -1 planner, 0 natural, 1 longest-first    */
@@ -237,9 +239,11 @@ fp8idx_status fp8_mqa_logits_paged(const fp8idx_tensor* q_fp8,
  *           windows are read, so values outside them do not matter.
  *  indices  [rows, k] I32 output, stride[1] == 1, stride[0] >= k.
  *  k        1 .. 2048.
- * No NaN inside a window (precondition).  One CTA per row; no scratch
- * memory.  Returns FP8IDX_OK, FP8IDX_ERR_INVALID, FP8IDX_ERR_UNSUPPORTED
- * (k out of range) or FP8IDX_ERR_CUDA.
+ * No NaN inside a window (precondition).  One CTA per row, or, when the
+ * rows number at most a quarter of the SMs and the width allows at least
+ * 8192 values per CTA, a thread-block cluster of up to 8 CTAs per row
+ * sharing its window; no scratch memory.  Returns FP8IDX_OK, FP8IDX_ERR_INVALID,
+ * FP8IDX_ERR_UNSUPPORTED (k or num_ctas out of range) or FP8IDX_ERR_CUDA.
  *
  * fp8_paged_topk: decode windows.  rows = batch*next_n; row r = b*next_n+n
  * has window [0, min(context_lens[b] - next_n + n + 1, max_model_len)) -- the
@@ -258,6 +262,20 @@ fp8idx_status fp8_mqa_topk(const fp8idx_tensor* logits,
                            const fp8idx_tensor* cu_seqlen_ks,
                            const fp8idx_tensor* cu_seqlen_ke, int32_t k,
                            const fp8idx_tensor* indices, void* stream);
+
+/* As above, with tunables (NULL = heuristic): opts->num_ctas fixes the CTAs
+ * per row (0 = heuristic, 1 .. 8); the other fields are ignored.  The result
+ * does not depend on it. */
+fp8idx_status fp8_paged_topk_ex(const fp8idx_tensor* logits,
+                                const fp8idx_tensor* context_lens,
+                                int32_t next_n, int32_t max_model_len,
+                                int32_t k, const fp8idx_tensor* indices,
+                                const fp8idx_options* opts, void* stream);
+fp8idx_status fp8_mqa_topk_ex(const fp8idx_tensor* logits,
+                              const fp8idx_tensor* cu_seqlen_ks,
+                              const fp8idx_tensor* cu_seqlen_ke, int32_t k,
+                              const fp8idx_tensor* indices,
+                              const fp8idx_options* opts, void* stream);
 
 /* Support gates, after the pages' is_supported(num_heads, head_dim,
  * kv_block_size) (aiter PR 5047, Technical Details) and is_supported(

@@ -98,8 +98,11 @@ def library():
             lib.fp8_mqa_logits_paged.argtypes = [T, T, T, T, T, T, T, T, P(_Options), V]
             lib.fp8_paged_topk.argtypes = [T, T, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, T, V]
             lib.fp8_mqa_topk.argtypes = [T, T, T, ctypes.c_int32, T, V]
+            lib.fp8_paged_topk_ex.argtypes = [T, T, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, T, P(_Options), V]
+            lib.fp8_mqa_topk_ex.argtypes = [T, T, T, ctypes.c_int32, T, P(_Options), V]
             for f in ("fp8_paged_mqa_logits", "fp8_paged_mqa_logits_ex", "fp8_mqa_logits", "fp8_mqa_logits_ex",
-                      "fp8_mqa_logits_paged", "fp8_paged_topk", "fp8_mqa_topk"):
+                      "fp8_mqa_logits_paged", "fp8_paged_topk", "fp8_mqa_topk", "fp8_paged_topk_ex",
+                      "fp8_mqa_topk_ex"):
                 getattr(lib, f).restype = ctypes.c_int
             lib.fp8idx_paged_is_supported.argtypes = [ctypes.c_int32] * 4
             lib.fp8idx_paged_is_supported.restype = ctypes.c_int
@@ -215,23 +218,26 @@ def fp8_mqa_logits_paged(q_fp8, kv_cache, block_tables, cu_seq_lens, weights, cu
     return out
 
 
-def fp8_paged_topk(logits, context_lens, next_n, max_model_len, k, indices, stream=None):
+def fp8_paged_topk(logits, context_lens, next_n, max_model_len, k, indices, stream=None, ctas_per_row: int = 0):
     """Decode top-k: indices [rows, k] of each row's k largest logits in its
     causal window (equal logits: lowest positions), listed by position, -1
-    past the window."""
+    past the window.  ctas_per_row: 0 = heuristic, 1..8 = fixed (the result
+    does not depend on it)."""
     lib = library()
     lg, cl, ix = _desc(logits), _desc(context_lens), _desc(indices)
-    _check(lib.fp8_paged_topk(ctypes.byref(lg), ctypes.byref(cl), int(next_n), int(max_model_len), int(k),
-                              ctypes.byref(ix), _stream(stream, logits)))
+    oc = Options(num_ctas=int(ctas_per_row))._c()
+    _check(lib.fp8_paged_topk_ex(ctypes.byref(lg), ctypes.byref(cl), int(next_n), int(max_model_len), int(k),
+                                 ctypes.byref(ix), ctypes.byref(oc), _stream(stream, logits)))
     return indices
 
 
-def fp8_mqa_topk(logits, cu_seqlen_ks, cu_seqlen_ke, k, indices, stream=None):
+def fp8_mqa_topk(logits, cu_seqlen_ks, cu_seqlen_ke, k, indices, stream=None, ctas_per_row: int = 0):
     """Prefill top-k over the windows [ks, ke) (same rule, order and padding)."""
     lib = library()
     lg, a, b, ix = _desc(logits), _desc(cu_seqlen_ks), _desc(cu_seqlen_ke), _desc(indices)
-    _check(lib.fp8_mqa_topk(ctypes.byref(lg), ctypes.byref(a), ctypes.byref(b), int(k), ctypes.byref(ix),
-                            _stream(stream, logits)))
+    oc = Options(num_ctas=int(ctas_per_row))._c()
+    _check(lib.fp8_mqa_topk_ex(ctypes.byref(lg), ctypes.byref(a), ctypes.byref(b), int(k), ctypes.byref(ix),
+                               ctypes.byref(oc), _stream(stream, logits)))
     return indices
 
 

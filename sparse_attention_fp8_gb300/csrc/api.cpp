@@ -485,7 +485,7 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const PrefillK& src, const fp
 // windows from context_lens/next_n within max_model_len columns.
 fp8idx_status topk_impl(int mode, const fp8idx_tensor* logits, const fp8idx_tensor* ks, const fp8idx_tensor* ke,
                         const fp8idx_tensor* cl, int32_t next_n, int32_t max_model_len, int32_t k,
-                        const fp8idx_tensor* indices, void* stream) {
+                        const fp8idx_tensor* indices, const fp8idx_options* opts, void* stream) {
   g_last_error.clear();
   TRY(check_tensor(logits, "logits", FP8IDX_F32, 2));
   TRY(check_tensor(indices, "indices", FP8IDX_I32, 2));
@@ -496,7 +496,11 @@ fp8idx_status topk_impl(int mode, const fp8idx_tensor* logits, const fp8idx_tens
   if (indices->shape[0] != R || indices->shape[1] != k || (k > 1 && indices->stride[1] != 1) ||
       (R > 1 && indices->stride[0] < k))
     return fail(FP8IDX_ERR_INVALID, "indices must be [rows, k] with unit inner stride");
-  if (W >= (1ll << 31) || R >= (1ll << 31)) return fail(FP8IDX_ERR_UNSUPPORTED, "top-k: logits too large");
+  if (W >= (1ll << 31) || R * kTopkMaxCluster >= (1ll << 31))
+    return fail(FP8IDX_ERR_UNSUPPORTED, "top-k: logits too large");
+  const int32_t ctas_req = opts ? opts->num_ctas : 0;
+  if (ctas_req < 0 || ctas_req > kTopkMaxCluster)
+    return fail(FP8IDX_ERR_UNSUPPORTED, "top-k: num_ctas=%d not in [0, %d]", ctas_req, kTopkMaxCluster);
   TopkParams p;
   std::memset(&p, 0, sizeof(p));
   p.mode = mode;
@@ -530,10 +534,21 @@ fp8idx_status topk_impl(int mode, const fp8idx_tensor* logits, const fp8idx_tens
   p.vec_ok = (aligned16(logits->data) && (p.stride % 4) == 0) ? 1 : 0;
   DeviceInfo dev;
   TRY(device_info(&dev));
+  // CTAs per row: a cluster per row only when the rows leave most SMs idle
+  // (at most a quarter of the SM count) and the longest possible window
+  // gives each CTA at least kTopkMinSlice values; with more rows the
+  // cluster's barriers cost more than the extra SMs return (measured).
+  int ctas = 1;
+  if (p.cols >= 2 * kTopkMinSlice && 4 * R <= dev.sms) {
+    const int64_t by_rows = dev.sms / R, by_len = p.cols / kTopkMinSlice;
+    ctas = (int)std::min<int64_t>(kTopkMaxCluster, std::min(by_rows, by_len));
+    if (ctas < 2) ctas = 1;
+  }
+  if (ctas_req > 0) ctas = ctas_req;
   int cap = kTopkMaxCap;
   while (cap > 1024 && (int)topk_smem_layout(cap).total > dev.smem_optin) cap >>= 1;
   p.cap = cap;
-  cudaError_t e = launch_topk(p, (int)topk_smem_layout(cap).total, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_topk(p, ctas, (int)topk_smem_layout(cap).total, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "top-k launch: %s", cudaGetErrorString(e));
   return ok();
 }
@@ -589,12 +604,22 @@ fp8idx_status fp8_mqa_logits_paged(const fp8idx_tensor* q_fp8, const fp8idx_tens
 
 fp8idx_status fp8_paged_topk(const fp8idx_tensor* logits, const fp8idx_tensor* context_lens, int32_t next_n,
                              int32_t max_model_len, int32_t k, const fp8idx_tensor* indices, void* stream) {
-  return topk_impl(1, logits, nullptr, nullptr, context_lens, next_n, max_model_len, k, indices, stream);
+  return topk_impl(1, logits, nullptr, nullptr, context_lens, next_n, max_model_len, k, indices, nullptr, stream);
 }
 
 fp8idx_status fp8_mqa_topk(const fp8idx_tensor* logits, const fp8idx_tensor* cu_seqlen_ks,
                            const fp8idx_tensor* cu_seqlen_ke, int32_t k, const fp8idx_tensor* indices, void* stream) {
-  return topk_impl(0, logits, cu_seqlen_ks, cu_seqlen_ke, nullptr, 1, 0, k, indices, stream);
+  return topk_impl(0, logits, cu_seqlen_ks, cu_seqlen_ke, nullptr, 1, 0, k, indices, nullptr, stream);
+}
+fp8idx_status fp8_paged_topk_ex(const fp8idx_tensor* logits, const fp8idx_tensor* context_lens, int32_t next_n,
+                                int32_t max_model_len, int32_t k, const fp8idx_tensor* indices,
+                                const fp8idx_options* opts, void* stream) {
+  return topk_impl(1, logits, nullptr, nullptr, context_lens, next_n, max_model_len, k, indices, opts, stream);
+}
+fp8idx_status fp8_mqa_topk_ex(const fp8idx_tensor* logits, const fp8idx_tensor* cu_seqlen_ks,
+                              const fp8idx_tensor* cu_seqlen_ke, int32_t k, const fp8idx_tensor* indices,
+                              const fp8idx_options* opts, void* stream) {
+  return topk_impl(0, logits, cu_seqlen_ks, cu_seqlen_ke, nullptr, 1, 0, k, indices, opts, stream);
 }
 
 int fp8idx_paged_is_supported(int32_t heads, int32_t head_dim, int32_t block_size, int32_t next_n) {
@@ -636,10 +661,13 @@ const char* fp8idx_last_error(void) { return g_last_error.c_str(); }
 
 fp8idx_status fp8idx_device_status(int32_t clear) {
   g_last_error.clear();
-  unsigned int a = 0, b = 0;
-  if (read_paged_watchdog(&a, clear != 0) != cudaSuccess || read_prefill_watchdog(&b, clear != 0) != cudaSuccess)
+  unsigned int a = 0, b = 0, c = 0;
+  if (read_paged_watchdog(&a, clear != 0) != cudaSuccess || read_prefill_watchdog(&b, clear != 0) != cudaSuccess ||
+      read_topk_watchdog(&c, clear != 0) != cudaSuccess)
     return fail(FP8IDX_ERR_CUDA, "reading the device watchdog failed");
-  if (a | b) return fail(FP8IDX_ERR_TIMEOUT, "device wait timed out (decode sites 0x%x, prefill sites 0x%x)", a, b);
+  if (a | b | c)
+    return fail(FP8IDX_ERR_TIMEOUT, "device wait timed out (decode sites 0x%x, prefill sites 0x%x, top-k sites 0x%x)",
+                a, b, c);
   return FP8IDX_OK;
 }
 

@@ -159,18 +159,30 @@ struct TopkParams {
 constexpr int kTopkThreads = 512;
 constexpr int kTopkBins = 4096;  // 12-bit radix levels (the last level has 8 bits)
 constexpr int kTopkMaxK = 2048;
-constexpr int kTopkMaxCap = 8192;  // 80 KB of shared memory per CTA: two CTAs per SM
+constexpr int kTopkMaxCap = 8192;  // 97 KB of shared memory per CTA: two CTAs per SM
+constexpr int kTopkMaxCluster = 8;      // CTAs per row at most (portable cluster size)
+constexpr int kTopkMinSlice = 8192;     // window values per CTA below which a row keeps one CTA
+// Shared memory of one top-k CTA: the copy buffer for a short window, which
+// also holds the histogram and (in a cluster) the cluster's summed
+// histogram once the window is in the candidate arrays; the candidates; scan
+// slots; flags; the copy's mbarrier.
 struct TopkLayout {
-  uint32_t hist, cand_key, cand_pos, scan, misc, total;
+  uint32_t ring, hist, hsum, cand_key, cand_pos, scan, misc, bar, total;
 };
 __host__ __device__ inline TopkLayout topk_smem_layout(int cap) {
   TopkLayout L;
-  uint32_t off = 0;
-  L.hist = off;     off += 4u * kTopkBins;
+  // (the histogram area also stages a compaction of up to cap words)
+  constexpr uint32_t kHists = 8u * kTopkBins, kWindow = (4u * (kTopkMaxCap + 4) + 15u) & ~15u;
+  constexpr uint32_t kRing = kHists > kWindow ? kHists : kWindow;
+  L.ring = 0;
+  L.hist = 0;
+  L.hsum = 4u * kTopkBins;
+  uint32_t off = kRing;
   L.cand_key = off; off += 4u * (uint32_t)cap;
   L.cand_pos = off; off += 4u * (uint32_t)cap;
   L.scan = off;     off += 4u * 32u;
   L.misc = off;     off += 4u * 8u;
+  L.bar = off;      off += 8u;
   L.total = off;
   return L;
 }
@@ -184,10 +196,12 @@ cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, con
                            const CUtensorMap& tm_w, const CUtensorMap& tm_out, const PrefillParams& p, int heads,
                            int head_dim, bool paged, int grid, int smem_bytes, cudaStream_t stream);
 
-cudaError_t launch_topk(const TopkParams& p, int smem_bytes, cudaStream_t stream);
+// ctas: CTAs per row (1: one CTA per row; 2..kTopkMaxCluster: one cluster per row)
+cudaError_t launch_topk(const TopkParams& p, int ctas, int smem_bytes, cudaStream_t stream);
 
 // Watchdog words of the two translation units (synchronous read, optional clear).
 cudaError_t read_paged_watchdog(unsigned int* value, bool clear);
 cudaError_t read_prefill_watchdog(unsigned int* value, bool clear);
+cudaError_t read_topk_watchdog(unsigned int* value, bool clear);
 
 }  // namespace fp8idx

@@ -13,36 +13,52 @@
 // Design: one CTA (512 threads) per row, two CTAs per SM.
 //  * Keys: the f32 bit pattern mapped to an unsigned integer with the same
 //    order (negative values bit-inverted, positive ones with the sign bit set).
-//  * The window is read as aligned float4 groups (scalar loads for the
-//    partial groups at its ends), several groups in flight per thread.
 //  * Radix select of the k-th largest key T: three levels of histograms
-//    (12, 12, 8 bits of the key; plain shared atomics).  A window of at most
-//    `cap` values is copied into shared memory once and selected there.  A
-//    longer one is sampled with a stride S (at most cap samples); the
-//    sample's (2k/S + 32)-th largest key is a lower threshold, and one
-//    ordered pass over the window keeps the values above it (about 2k + 32S
-//    of them) in shared memory for the exact select.  If that count falls
-//    outside [k, cap] (adversarial or heavily tied rows), the levels and the
-//    selection re-read the window instead.
+//    (12, 12, 8 bits of the key; plain shared atomics).
+//  * A window of at most `cap` values is brought into shared memory by one
+//    bulk copy and selected there.  A longer one is sampled with a stride S
+//    (at most cap samples); the sample's (2k/S + 32)-th largest key is a
+//    lower threshold, and the values above it (about 2k + 32S of them) are
+//    compacted into shared memory, in position order, for the exact select:
+//    every warp counts the candidates of its own segment of the window, one
+//    barrier turns the counts into offsets, and every warp re-reads its
+//    segment (from L2) and writes its candidates -- no block barrier per
+//    chunk.  If the kept count falls outside [k, cap] (adversarial or
+//    heavily tied rows), the levels and the selection re-read the window
+//    from global memory instead.
 //  * Selection: an ordered pass keeps every key above the k-th key T and the
 //    first (k - #above) keys equal to T in position order (block-wide
 //    prefix sums), so ties resolve to the lowest positions, and writes the
 //    kept positions straight to the output in position order.
+// Rows too few to fill the GPU (fewer than two per SM) with long windows
+// are each split over a thread-block cluster of C CTAs instead: every step
+// above runs per slice of the window, each CTA adding its histogram counts
+// into every cluster member's sum histogram (remote shared-memory
+// reductions) before each bin search, the candidate counts agreed
+// cluster-wide, and each CTA's output offsets taken from the counts of the
+// lower-ranked slices.
 // The kernel uses no global scratch memory and no atomics outside shared
-// memory.
+// memory.  The wait on the bulk copy is bounded: a wait that runs out sets a
+// watchdog bit (read by the host) and the row finishes on whatever data it
+// has, so no CTA leaves a cluster barrier unmatched.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
+#include "common.cuh"
 #include "kernels.h"
 
 namespace fp8idx {
+
+static __device__ unsigned int g_topk_watchdog;
 
 namespace {
 
 constexpr int kT = kTopkThreads;
 constexpr int kWarps = kT / 32;
-constexpr int kPer = 8;  // elements per thread per chunk of an ordered pass
+constexpr int kPer = 8;     // elements per thread per chunk of an ordered pass
+constexpr int kTopkPrefetch = 32768;  // bytes per bulk L2 prefetch
 
 __device__ __forceinline__ uint32_t order_key(float x) {
   const uint32_t u = __float_as_uint(x + 0.0f);  // -0.0 + 0.0 = +0.0: both zeros share one key
@@ -50,11 +66,14 @@ __device__ __forceinline__ uint32_t order_key(float x) {
 }
 
 struct TopkShared {
-  uint32_t* hist;      // [kTopkBins]
+  uint32_t* hist;      // [kTopkBins] this CTA's counts
+  uint32_t* hsum;      // [kTopkBins] the cluster's counts (== hist with one CTA per row)
+  float* ring;         // a short window's values as copied (overlaps hist, hsum)
   uint32_t* cand_key;  // [cap]
   int32_t* cand_pos;   // [cap]
-  uint32_t* scan;      // [kWarps] warp totals + scratch
-  uint32_t* misc;      // [8]
+  uint32_t* scan;      // [2 * kWarps] warp totals
+  uint32_t* misc;      // [8]: 0,1 bin search result; 4,5 cluster exchange; 7 abort flag
+  uint32_t bar;        // the copy's mbarrier (shared address)
 };
 
 // Exclusive prefix sum over the block of one value per thread (in thread
@@ -92,43 +111,62 @@ __device__ __forceinline__ void hist_add(uint32_t* hist, bool active, uint32_t b
 }
 
 // Finds the bin b of the `need`-th largest key: above = #keys in bins > b,
-// above < need <= above + hist[b].  nbins is 4096 or 256.  Result in
-// misc[0] (bin), misc[1] (above).
-__device__ __forceinline__ void find_bin(const uint32_t* hist, int nbins, uint32_t need, uint32_t* warp_tot,
-                                         uint32_t* misc) {
-  const int per = (nbins + kT - 1) / kT;  // bins per thread, counted from the top
-  const int b_hi = nbins - 1 - static_cast<int>(threadIdx.x) * per;
+// above < need <= above + hist[b].  NBINS is 4096 (8 bins per thread, read
+// as two 16-byte vectors: consecutive threads, consecutive addresses) or
+// 256 (one bin per thread).  Result in misc[0] (bin), misc[1] (above).
+template <int NBINS>
+__device__ __forceinline__ void find_bin(const uint32_t* hist, uint32_t need, uint32_t* warp_tot, uint32_t* misc) {
+  constexpr int kPerT = NBINS >= kT ? NBINS / kT : 1;
+  static_assert(kPerT == 8 || kPerT == 1, "bins per thread");
+  const int t = threadIdx.x;
+  uint32_t h[kPerT];  // h[j]: bin b_hi - j, counted from the top
+  const int b_hi = NBINS - 1 - t * kPerT;
+  if constexpr (kPerT == 8) {
+    const uint4* v = reinterpret_cast<const uint4*>(hist + (NBINS - 8 * (t + 1)));
+    const uint4 lo4 = v[0], hi4 = v[1];
+    h[0] = hi4.w, h[1] = hi4.z, h[2] = hi4.y, h[3] = hi4.x;
+    h[4] = lo4.w, h[5] = lo4.z, h[6] = lo4.y, h[7] = lo4.x;
+  } else {
+    h[0] = b_hi >= 0 ? hist[b_hi] : 0u;
+  }
   uint32_t s = 0;
-  for (int j = 0; j < per; ++j)
-    if (b_hi - j >= 0) s += hist[b_hi - j];
+#pragma unroll
+  for (int j = 0; j < kPerT; ++j) s += h[j];
   uint32_t total;
   uint32_t above = block_scan(s, warp_tot, &total);  // keys in bins above this thread's
-  for (int j = 0; j < per; ++j) {
-    const int b = b_hi - j;
-    if (b < 0) break;
-    const uint32_t h = hist[b];
-    if (above < need && above + h >= need) {
-      misc[0] = static_cast<uint32_t>(b);
+#pragma unroll
+  for (int j = 0; j < kPerT; ++j) {
+    if (above < need && above + h[j] >= need) {
+      misc[0] = static_cast<uint32_t>(b_hi - j);
       misc[1] = above;
     }
-    above += h;
+    above += h[j];
   }
   __syncthreads();
 }
 
 }  // namespace
 
-__global__ void __launch_bounds__(kTopkThreads, 2) topk_rows_kernel(const TopkParams p) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
+// One row's selection by C CTAs: one CTA, or (kCluster) the C CTAs of a
+// thread-block cluster, CTA c taking the c-th of C equal slices of the
+// window.
+template <bool kCluster>
+__device__ __forceinline__ void topk_row(const TopkParams& p, uint8_t* smem_raw) {
+  namespace cg = cooperative_groups;
   const TopkLayout Lo = topk_smem_layout(p.cap);
   TopkShared sh;
   sh.hist = reinterpret_cast<uint32_t*>(smem_raw + Lo.hist);
+  sh.hsum = kCluster ? reinterpret_cast<uint32_t*>(smem_raw + Lo.hsum) : sh.hist;
+  sh.ring = reinterpret_cast<float*>(smem_raw + Lo.ring);
   sh.cand_key = reinterpret_cast<uint32_t*>(smem_raw + Lo.cand_key);
   sh.cand_pos = reinterpret_cast<int32_t*>(smem_raw + Lo.cand_pos);
   sh.scan = reinterpret_cast<uint32_t*>(smem_raw + Lo.scan);
   sh.misc = reinterpret_cast<uint32_t*>(smem_raw + Lo.misc);
+  sh.bar = ptx::smem_u32(smem_raw + Lo.bar);
 
-  const int64_t r = blockIdx.x;
+  const int C = kCluster ? static_cast<int>(cg::this_cluster().num_blocks()) : 1;
+  const int crank = kCluster ? static_cast<int>(cg::this_cluster().block_rank()) : 0;
+  const int64_t r = blockIdx.x / C;
   // The row's window [lo, hi).
   int64_t lo = 0, hi = 0;
   if (p.mode == 0) {
@@ -150,22 +188,89 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_rows_kernel(const TopkPa
 
   // Windows of at most k values: all of their positions.
   if (L <= k) {
-    for (int j = tid; j < k; j += kT) out_row[j] = j < L ? static_cast<int32_t>(lo + j) : -1;
+    if (crank == 0)
+      for (int j = tid; j < k; j += kT) out_row[j] = j < L ? static_cast<int32_t>(lo + j) : -1;
     return;
   }
-
-  // The window is read in groups of 4 positions: one float4 load for a
-  // group inside the window when the rows are 16-byte aligned, scalar loads
-  // for the (at most two) partial groups at its ends -- nothing outside
-  // [lo, hi) is read.
+  // This CTA's slice [slo, shi) of the window.
+  const int64_t slo = lo + L * crank / C, shi = lo + L * (crank + 1) / C;
+  const int64_t Ls = shi - slo;
   const float* row_base = p.logits + r * p.stride;
   const bool vec = p.vec_ok != 0;
-  const int64_t gstart = vec ? (lo & ~static_cast<int64_t>(3)) : lo;
-  const int64_t ngroups = (hi - gstart + 3) / 4;
+
+  volatile uint32_t* abort_flag = sh.misc + 7;
+  if (tid == 0) {
+    *abort_flag = 0u;
+    ptx::mbar_init(sh.bar, 1);
+    ptx::fence_barrier_init();
+  }
+  __syncthreads();
+
+  // Cluster steps.  sync_all: every CTA's shared writes so far are done and
+  // visible.  exchange2(a, b): this CTA's two values in; per value the sum
+  // over lower ranks, the sum over all and the maximum out.
+  const auto sync_all = [&]() {
+    if constexpr (kCluster) cg::this_cluster().sync();
+    else __syncthreads();
+  };
+  struct Sums {
+    uint32_t before, all, max;
+  };
+  const auto exchange2 = [&](uint32_t a, uint32_t b, Sums& sa, Sums& sb) {
+    if constexpr (!kCluster) {
+      sa = Sums{0u, a, a};
+      sb = Sums{0u, b, b};
+    } else {
+      if (tid == 0) sh.misc[4] = a, sh.misc[5] = b;
+      sync_all();
+      sa = Sums{0u, 0u, 0u};
+      sb = Sums{0u, 0u, 0u};
+      for (int c = 0; c < C; ++c) {
+        const uint32_t* m = cg::this_cluster().map_shared_rank(sh.misc, c);
+        const uint32_t x = m[4], y = m[5];
+        sa.before += c < crank ? x : 0u;
+        sb.before += c < crank ? y : 0u;
+        sa.all += x;
+        sb.all += y;
+        sa.max = x > sa.max ? x : sa.max;
+        sb.max = y > sb.max ? y : sb.max;
+      }
+      sync_all();  // before the slots are reused
+    }
+  };
+  // After a local histogram pass (its counts complete in sh.hist): every
+  // nonzero count added into each cluster member's hsum, then the cluster
+  // barrier that makes the sums complete.
+  const auto combine = [&](int nbins) {
+    if constexpr (kCluster) {
+      for (int i = tid; i < nbins; i += kT) {
+        const uint32_t v = sh.hist[i];
+        if (v)
+          for (int c = 0; c < C; ++c) atomicAdd(cg::this_cluster().map_shared_rank(sh.hsum, c) + i, v);
+      }
+      sync_all();
+    }
+  };
+  // Zeroes this CTA's counts (and sums) for a level of `nbins` bins; in a
+  // cluster, no member adds into this CTA's sums before they are zeroed.
+  const auto zero_level = [&](int nbins) {
+    for (int i = tid; i < nbins; i += kT) {
+      sh.hist[i] = 0u;
+      if constexpr (kCluster) sh.hsum[i] = 0u;
+    }
+    sync_all();
+  };
+
+  // ---- global-memory window passes (the fallback): groups of 4 positions,
+  // one float4 load for a group inside the slice when the rows are 16-byte
+  // aligned, scalar loads for the partial groups at its ends -- nothing
+  // outside [slo, shi) is read.
+  const int64_t gstart = vec ? (slo & ~static_cast<int64_t>(3)) : slo;
+  const int64_t ngroups = (shi - gstart + 3) / 4;
   const auto load_group = [&](int64_t gi, uint32_t (&key)[4]) -> uint32_t {  // returns the valid-lane mask
     const int64_t g = gstart + 4 * gi;
     if (gi >= ngroups) return 0u;
-    if (vec && g >= lo && g + 4 <= hi) {
+    if (vec && g >= slo && g + 4 <= shi) {
       const float4 f = __ldg(reinterpret_cast<const float4*>(row_base + g));
       key[0] = order_key(f.x);
       key[1] = order_key(f.y);
@@ -176,14 +281,13 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_rows_kernel(const TopkPa
     uint32_t m = 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const bool in = g + e >= lo && g + e < hi;
+      const bool in = g + e >= slo && g + e < shi;
       key[e] = in ? order_key(__ldg(row_base + g + e)) : 0u;
       m |= in ? (1u << e) : 0u;
     }
     return m;
   };
   constexpr int kU = 4;  // groups in flight per thread in the histogram passes
-  // Histogram over the window of `bin(key)` for keys with `sel(key)`.
   const auto window_hist = [&](auto sel, auto bin) {
     for (int64_t q0 = 0; q0 < ngroups; q0 += static_cast<int64_t>(kT) * kU) {
       uint32_t key[kU][4], m[kU];
@@ -195,26 +299,8 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_rows_kernel(const TopkPa
         for (int e = 0; e < 4; ++e) hist_add(sh.hist, ((m[u] >> e) & 1u) && sel(key[u][e]), bin(key[u][e]));
     }
   };
-  // Ordered pass over the window with vector loads: `f(keys, pos0, valid)`
-  // gets this thread's kPer consecutive positions of each chunk (chunks in
-  // position order, threads in position order within a chunk).
-  const auto window_ordered = [&](auto f) {
-    for (int64_t q0 = 0; q0 < ngroups; q0 += static_cast<int64_t>(kT) * (kPer / 4)) {
-      uint32_t keys[kPer], valid = 0;
-      const int64_t pos0 = gstart + 4 * (q0 + static_cast<int64_t>(tid) * (kPer / 4));
-#pragma unroll
-      for (int h = 0; h < kPer / 4; ++h) {
-        uint32_t k4[4];
-        const uint32_t m = load_group(q0 + static_cast<int64_t>(tid) * (kPer / 4) + h, k4);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) keys[4 * h + e] = k4[e];
-        valid |= m << (4 * h);
-      }
-      f(keys, pos0, valid);
-    }
-  };
 
-  // ---- sources: the window in global memory, or candidates in shared memory
+  // ---- sources: the slice in global memory, or candidates in shared memory
   const auto smem_hist = [&](int64_t n_c, auto sel, auto bin) {
     for (int64_t i0 = 0; i0 < n_c; i0 += kT) {
       const int64_t i = i0 + tid;
@@ -226,25 +312,24 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_rows_kernel(const TopkPa
   // kT*kPer elements, warp w takes the chunk's w-th run of 32*kPer, step j
   // of the run one element per lane (consecutive lanes, consecutive
   // elements: coalesced in global memory, conflict-free in shared memory).
-  // `keep(key)` returns 0 (drop) or the predicate bits; `place` gets the
-  // element's key, position and its rank among the kept elements before it
-  // in position order.  Counts per chunk go through one 16-entry scan of
-  // warp totals (double-buffered, one barrier per chunk).
+  // `place` gets the element's key, position and its rank among the
+  // elements of each predicate before it in position order.  Counts per
+  // chunk go through one 16-entry scan of warp totals (double-buffered, one
+  // barrier per chunk).
   const auto smem_get = [&](int64_t e, uint32_t& key, int32_t& pos) {
     key = sh.cand_key[e];
     pos = sh.cand_pos[e];
   };
   const auto global_get = [&](int64_t e, uint32_t& key, int32_t& pos) {
-    key = order_key(__ldg(row_base + lo + e));
-    pos = static_cast<int32_t>(lo + e);
+    key = order_key(__ldg(row_base + slo + e));
+    pos = static_cast<int32_t>(slo + e);
   };
   // Two independent counts per element (packed 16:16 per chunk: a chunk has
-  // kT*kPer < 2^16 elements): a = #(pred A) before it, b = #(pred B) before
-  // it.  Returns the total of pred A.
-  const auto ordered2 = [&](int64_t n, auto get, auto pred_a, auto pred_b, auto place) {
+  // kT*kPer < 2^16 elements), starting from done_a / done_b.
+  const auto ordered2 = [&](int64_t n, auto get, auto pred_a, auto pred_b, auto place, uint32_t done_a,
+                            uint32_t done_b) {
     const int lane = tid & 31, warp = tid >> 5;
     const uint32_t lt = (1u << lane) - 1u;
-    uint32_t done_a = 0, done_b = 0;
     int parity = 0;
     for (int64_t c0 = 0; c0 < n; c0 += static_cast<int64_t>(kT) * kPer) {
       const int64_t wbase = c0 + static_cast<int64_t>(warp) * 32 * kPer;
@@ -287,31 +372,36 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_rows_kernel(const TopkPa
       parity ^= 1;
     }
     __syncthreads();
-    return done_a;
   };
 
-  // ---- the `need`-th largest key T of a source and #keys > T, three radix
-  // levels (12, 12 and 8 bits of the key)
-  const auto radix_select = [&](auto hist_pass, uint32_t need, uint32_t* T_out, uint32_t* above_out) {
-    for (int i = tid; i < kTopkBins; i += kT) sh.hist[i] = 0u;
-    __syncthreads();
+  // ---- the `need`-th largest key T of the cluster's source and #keys > T,
+  // three radix levels (12, 12 and 8 bits of the key)
+  // (levels = 2: T is the lower edge of the 24-bit bin holding that key)
+  const auto radix_select = [&](auto hist_pass, uint32_t need, uint32_t* T_out, uint32_t* above_out,
+                                int levels = 3) {
+    zero_level(kTopkBins);
     hist_pass([](uint32_t) { return true; }, [](uint32_t key) { return key >> 20; });
     __syncthreads();
-    find_bin(sh.hist, kTopkBins, need, sh.scan, sh.misc);
+    combine(kTopkBins);
+    find_bin<kTopkBins>(sh.hsum, need, sh.scan, sh.misc);
     const uint32_t b0 = sh.misc[0], a0 = sh.misc[1];
-    __syncthreads();
-    for (int i = tid; i < kTopkBins; i += kT) sh.hist[i] = 0u;
-    __syncthreads();
+    zero_level(kTopkBins);
     hist_pass([&](uint32_t key) { return (key >> 20) == b0; }, [](uint32_t key) { return (key >> 8) & 0xFFFu; });
     __syncthreads();
-    find_bin(sh.hist, kTopkBins, need - a0, sh.scan, sh.misc);
+    combine(kTopkBins);
+    find_bin<kTopkBins>(sh.hsum, need - a0, sh.scan, sh.misc);
     const uint32_t pre24 = (b0 << 12) | sh.misc[0], a1 = a0 + sh.misc[1];
-    __syncthreads();
-    for (int i = tid; i < 256; i += kT) sh.hist[i] = 0u;
-    __syncthreads();
+    if (levels == 2) {
+      *T_out = pre24 << 8;
+      *above_out = a1;
+      __syncthreads();
+      return;
+    }
+    zero_level(256);
     hist_pass([&](uint32_t key) { return (key >> 8) == pre24; }, [](uint32_t key) { return key & 0xFFu; });
     __syncthreads();
-    find_bin(sh.hist, 256, need - a1, sh.scan, sh.misc);
+    combine(256);
+    find_bin<256>(sh.hsum, need - a1, sh.scan, sh.misc);
     *T_out = (pre24 << 8) | sh.misc[0];
     *above_out = a1 + sh.misc[1];
     __syncthreads();
@@ -321,93 +411,329 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_rows_kernel(const TopkPa
   // (k - above) keys == T, written to the output as they come
   const auto select = [&](int64_t n, auto get, uint32_t T, uint32_t above) {
     const uint32_t need_eq = static_cast<uint32_t>(k) - above;
+    uint32_t gt0 = 0, eq0 = 0;  // keys > T and == T in the slices of lower-ranked CTAs
+    if constexpr (kCluster) {
+      uint32_t n_gt = 0, n_eq = 0;
+      for (int64_t i = tid; i < n; i += kT) {
+        uint32_t key;
+        int32_t pos;
+        get(i, key, pos);
+        n_gt += key > T ? 1u : 0u;
+        n_eq += key == T ? 1u : 0u;
+      }
+      uint32_t t_gt, t_eq;
+      block_scan(n_gt, sh.scan, &t_gt);
+      block_scan(n_eq, sh.scan, &t_eq);
+      Sums s_gt, s_eq;
+      exchange2(t_gt, t_eq, s_gt, s_eq);
+      gt0 = s_gt.before;
+      eq0 = s_eq.before;
+    }
     ordered2(
         n, get, [&](uint32_t key) { return key > T; }, [&](uint32_t key) { return key == T; },
         [&](uint32_t, int32_t pos, bool gt, bool eq, uint32_t n_gt, uint32_t n_eq) {
-          if (gt) out_row[n_gt + (n_eq < need_eq ? n_eq : need_eq)] = pos;
-          else if (eq && n_eq < need_eq) out_row[n_gt + n_eq] = pos;
-        });
+          const bool w = gt || (eq && n_eq < need_eq);
+          const uint32_t idx = n_gt + (n_eq < need_eq ? n_eq : need_eq);  // == n_gt + n_eq for a kept tie
+          if (w) out_row[idx] = pos;
+        },
+        gt0, eq0);
   };
 
   uint32_t T = 0, above = 0;
-  if (L <= p.cap) {
-    // Short windows: the whole window into shared memory (positions in
-    // order), then everything runs there.
-    for (int64_t i0 = 0; i0 < L; i0 += static_cast<int64_t>(kT) * 4) {
+  if ((L + C - 1) / C + 4 <= p.cap) {
+    // Short windows: each slice into its CTA's shared memory (keys and
+    // positions in position order), then everything runs there.  Aligned
+    // rows: one bulk copy of [slo rounded down to 4, shi rounded down to 4)
+    // into the ring, the last (at most 3) values by plain loads.
+    const int64_t b0 = slo & ~static_cast<int64_t>(3), a1 = shi & ~static_cast<int64_t>(3);
+    const bool staged = vec && a1 > b0;
+    if (staged) {
+      if (tid == 0) {
+        ptx::fence_proxy_async_smem();
+        const uint32_t bytes = static_cast<uint32_t>((a1 - b0) * 4);
+        ptx::mbar_arrive_expect_tx(sh.bar, bytes);
+        ptx::bulk_g2s(ptx::smem_u32(sh.ring), row_base + b0, bytes, sh.bar);
+      }
+      // bounded: a wait that runs out flags the watchdog; in-flight bytes
+      // land before the ring is reused
+      wait_bounded(sh.bar, 0u, abort_flag, &g_topk_watchdog, kSiteStageFull);
+      if (*abort_flag && tid == 0) wait_drain(sh.bar, 0u, &g_topk_watchdog);
+    }
+    for (int64_t i0 = 0; i0 < Ls; i0 += static_cast<int64_t>(kT) * 4) {
       float v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int64_t i = i0 + u * kT + tid;
-        v[u] = i < L ? __ldg(row_base + lo + i) : 0.f;
+        const int64_t i = i0 + u * kT + tid, pos = slo + i;
+        v[u] = i >= Ls ? 0.f : (staged && pos < a1) ? sh.ring[pos - b0] : __ldg(row_base + pos);
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int64_t i = i0 + u * kT + tid;
-        if (i < L) {
+        if (i < Ls) {
           sh.cand_key[i] = order_key(v[u]);
-          sh.cand_pos[i] = static_cast<int32_t>(lo + i);
+          sh.cand_pos[i] = static_cast<int32_t>(slo + i);
         }
       }
     }
     __syncthreads();
-    radix_select([&](auto sel, auto bin) { smem_hist(L, sel, bin); }, static_cast<uint32_t>(k), &T, &above);
-    select(L, smem_get, T, above);
+    radix_select([&](auto sel, auto bin) { smem_hist(Ls, sel, bin); }, static_cast<uint32_t>(k), &T, &above);
+    select(Ls, smem_get, T, above);
     return;
   }
 
-  // Long windows.  A stride sample of at most cap values estimates a lower
-  // threshold t_low: the (2k/S + 32)-th largest sample key, S the stride, so
-  // about 2k + 32S window values lie above it (many standard deviations
-  // from both k and cap for the strides used).  One ordered pass keeps the
-  // values >= t_low in shared memory; if fewer than k or more than cap pass,
-  // the exact radix select runs over the window instead.
+  // Long windows.  First the slice's aligned part is prefetched into L2 in
+  // bulk (one thread, no registers held): DRAM streams it while the sample
+  // is ranked, and the passes below read it from L2.
+  if (vec && tid == 0) {
+    const int64_t b0 = (slo + 3) & ~static_cast<int64_t>(3), a1 = shi & ~static_cast<int64_t>(3);
+    for (int64_t c0 = b0; c0 < a1; c0 += kTopkPrefetch / 4) {
+      const int64_t n = a1 - c0 < kTopkPrefetch / 4 ? a1 - c0 : kTopkPrefetch / 4;
+      ptx::bulk_prefetch_l2(row_base + c0, static_cast<uint32_t>(n * 4));
+    }
+  }
+  // A stride sample of at most cap values (stride S over the
+  // whole window, each CTA loading the samples in its slice) estimates a
+  // lower threshold t_low: the (2k/S + 32)-th largest sample key (rounded
+  // down to its 24-bit bin), so about 2k + 32S window values lie above it
+  // (many standard deviations from both k and cap for the strides used).
+  // The values >= t_low are then compacted into shared memory; if fewer than
+  // k pass in the cluster, or more than cap in one CTA, the exact radix
+  // select runs over the window instead.
   const int64_t S = (L + p.cap - 1) / p.cap;
-  const int64_t ns = (L + S - 1) / S;
-  for (int64_t j = tid; j < ns; j += kT) sh.cand_key[j] = order_key(__ldg(row_base + lo + j * S));
+  const int64_t ns = (L + S - 1) / S;  // samples lo + jS of the whole window: <= cap
+  const int64_t j_lo = (slo - lo + S - 1) / S, j_hi = (shi - lo + S - 1) / S;  // this slice's samples
+  const int64_t ns_c = j_hi - j_lo;
+  for (int64_t j0 = 0; j0 < ns_c; j0 += static_cast<int64_t>(kT) * 8) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t j = j0 + u * kT + tid;
+      v[u] = j < ns_c ? __ldg(row_base + lo + (j_lo + j) * S) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t j = j0 + u * kT + tid;
+      if (j < ns_c) sh.cand_key[j] = order_key(v[u]);
+    }
+  }
   __syncthreads();
   {
     const int64_t want = 2 * static_cast<int64_t>(k) / S + 32;
     const uint32_t rank = static_cast<uint32_t>(want < ns ? want : ns);
-    radix_select([&](auto sel, auto bin) { smem_hist(ns, sel, bin); }, rank, &T, &above);
+    radix_select([&](auto sel, auto bin) { smem_hist(ns_c, sel, bin); }, rank, &T, &above, 2);
   }
-  const uint32_t t_low = T;
-  // candidates >= t_low in position order, from vector loads (few values
-  // pass, so the strided shared stores cost little); slots past cap are
-  // dropped, the count says whether any were
+  const uint32_t t_low = T;  // the lower edge of the 24-bit bin of the rank-th sample key
+
+  // Candidates >= t_low in position order, tested as floats against the
+  // value whose key is t_low (the key order is the float order, -0.0 ==
+  // +0.0; no NaN in a window).  Each warp owns one contiguous segment of
+  // the slice (groups of 4 positions from slo rounded down to 4; positions
+  // before slo masked) and walks it without block barriers, lane l of a
+  // step taking groups 2l and 2l+1 (8 consecutive positions).  The last (at
+  // most 3) positions of an aligned slice are appended by thread 0.  Slots
+  // past cap are dropped; the count says whether any were.
+  const float f_low = __uint_as_float((t_low & 0x80000000u) ? (t_low & 0x7FFFFFFFu) : ~t_low);
   uint32_t n_c = 0;
-  window_ordered([&](const uint32_t (&keys)[kPer], int64_t pos0, uint32_t valid) {
-    uint32_t cnt = 0;
+  {
+    const int lane = tid & 31, warp = tid >> 5;
+    // positions are below 2^31: 32-bit offsets from here on
+    const int32_t slo32 = static_cast<int32_t>(slo), shi32 = static_cast<int32_t>(shi);
+    const int32_t b0 = slo32 & ~3;
+    const int32_t a1 = vec ? (shi32 & ~3) : shi32;  // grouped part [b0, a1)
+    const int32_t G = a1 > b0 ? (a1 - b0 + 3) / 4 : 0;
+    const int32_t g_lo = static_cast<int32_t>(static_cast<int64_t>(G) * warp / kWarps);
+    const int32_t g_hi = static_cast<int32_t>(static_cast<int64_t>(G) * (warp + 1) / kWarps);
+    const int nsteps = (g_hi - g_lo + 63) / 64;  // warp-uniform
+    const uint32_t cap = static_cast<uint32_t>(p.cap);
+    // the 8 values of this lane in step st and their candidate mask
+    const auto load8 = [&](int st, float (&f)[8]) -> uint32_t {
+      uint32_t valid = 0;
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) cnt += (((valid >> j) & 1u) && keys[j] >= t_low) ? 1u : 0u;
-    uint32_t total;
-    uint32_t slot = n_c + block_scan(cnt, sh.scan, &total);
+      for (int h = 0; h < 2; ++h) {
+        const int32_t g = g_lo + st * 64 + 2 * lane + h, base = b0 + 4 * g;
+        if (g < g_hi && vec) {
+          const float4 x = __ldg(reinterpret_cast<const float4*>(row_base + base));
+          f[4 * h] = x.x, f[4 * h + 1] = x.y, f[4 * h + 2] = x.z, f[4 * h + 3] = x.w;
 #pragma unroll
-    for (int j = 0; j < kPer; ++j)
-      if (((valid >> j) & 1u) && keys[j] >= t_low) {
-        if (slot < static_cast<uint32_t>(p.cap)) {
-          sh.cand_key[slot] = keys[j];
-          sh.cand_pos[slot] = static_cast<int32_t>(pos0 + j);
+          for (int e = 0; e < 4; ++e) valid |= (base + e >= slo32) ? (1u << (4 * h + e)) : 0u;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const bool in = g < g_hi && base + e >= slo32 && base + e < a1;
+            f[4 * h + e] = in ? __ldg(row_base + base + e) : 0.f;
+            valid |= in ? (1u << (4 * h + e)) : 0u;
+          }
         }
-        ++slot;
       }
-    n_c += total;
-  });
+      return valid;
+    };
+    const auto mask8 = [&](const float (&f)[8], uint32_t valid) -> uint32_t {
+      uint32_t m = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m |= f[e] >= f_low ? (1u << e) : 0u;
+      return m & valid;
+    };
+    // One pass: each warp appends its candidates, in order, to its own
+    // share of the candidate arrays (Q = cap / kWarps entries), counting
+    // past the share if it overflows.  Two steps per iteration with one
+    // packed (16:16) warp scan; the next two steps' loads are issued before
+    // the current ones are placed.
+    const uint32_t Q = cap / kWarps;
+    // Candidates are sparse (a few per 256 values), so a lane spends work
+    // only on its set bits: each iteration every lane with a bit left places
+    // its lowest one; the warp iterates max-over-lanes times.
+    const auto place8 = [&](const float (&f)[8], uint32_t m, uint32_t s0, int st, uint32_t limit, uint32_t off) {
+      const int32_t p0 = b0 + 4 * (g_lo + st * 64 + 2 * lane);
+      while (__any_sync(0xffffffffu, m != 0u)) {
+        if (m) {
+          const int e = __ffs(m) - 1;
+          m &= m - 1u;
+          float v = f[0];
+#pragma unroll
+          for (int q = 1; q < 8; ++q) v = e == q ? f[q] : v;
+          if (s0 < limit) {
+            sh.cand_key[off + s0] = order_key(v);
+            sh.cand_pos[off + s0] = p0 + e;
+          }
+          ++s0;
+        }
+      }
+    };
+    // places steps st, st+1 (masks m0, m1) at run + their warp prefix; returns the pair's total
+    const auto place2 = [&](const float (&f0)[8], uint32_t m0, const float (&f1)[8], uint32_t m1, int st,
+                            uint32_t run, uint32_t limit, uint32_t off) -> uint32_t {
+      const uint32_t c = (static_cast<uint32_t>(__popc(m0)) << 16) | static_cast<uint32_t>(__popc(m1));
+      uint32_t x = c;  // inclusive warp scan of the packed lane counts
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      const uint32_t tot = __shfl_sync(0xffffffffu, x, 31), ex = x - c;
+      place8(f0, m0, run + (ex >> 16), st, limit, off);
+      place8(f1, m1, run + (tot >> 16) + (ex & 0xFFFFu), st + 1, limit, off);
+      return (tot >> 16) + (tot & 0xFFFFu);
+    };
+    uint32_t run = 0;
+    {
+      float fa[8], fb[8];
+      uint32_t va = load8(0, fa), vb = load8(1, fb);
+      for (int st = 0; st < nsteps; st += 2) {
+        const uint32_t ma = mask8(fa, va), mb = mask8(fb, vb);
+        float fc[8], fd[8];
+        const uint32_t vc = load8(st + 2, fc), vd = load8(st + 3, fd);  // past the segment: nothing loaded
+        run += place2(fa, ma, fb, mb, st, run, Q, static_cast<uint32_t>(warp) * Q);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) fa[e] = fc[e], fb[e] = fd[e];
+        va = vc, vb = vd;
+      }
+    }
+    if (lane == 0) sh.scan[warp] = run;
+    __syncthreads();
+    uint32_t before = 0, n_main = 0, over = 0;  // this warp's first slot, the total, any share overflowed
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const uint32_t t = sh.scan[w];
+      before += w < warp ? t : 0u;
+      n_main += t;
+      over |= t > Q ? 1u : 0u;
+    }
+    if (!over) {
+      // Compaction into position order through the idle histogram area
+      // (>= cap words): keys first, then positions; warp w copies its own
+      // share to offset `before` (coalesced, no search), a barrier, then
+      // the block copies the staged array back to the front.
+      uint32_t* const stage = sh.hist;
+#pragma unroll 1
+      for (int part = 0; part < 2; ++part) {
+        uint32_t* const arr = part == 0 ? sh.cand_key : reinterpret_cast<uint32_t*>(sh.cand_pos);
+        for (uint32_t o = lane; o < run; o += 32) stage[before + o] = arr[static_cast<uint32_t>(warp) * Q + o];
+        __syncthreads();
+        for (uint32_t i = tid; i < n_main; i += kT) arr[i] = stage[i];
+        __syncthreads();
+      }
+    } else {
+      // A share overflowed (candidates concentrated in one segment): a
+      // second pass over the segments writes every candidate at its final
+      // slot (the counts above give each warp's first slot).
+      __syncthreads();
+      uint32_t r2 = before;
+      for (int st = 0; st < nsteps; st += 2) {
+        float f0[8], f1[8];
+        const uint32_t v0 = load8(st, f0), v1 = load8(st + 1, f1);
+        r2 += place2(f0, mask8(f0, v0), f1, mask8(f1, v1), st, r2, cap, 0u);
+      }
+      __syncthreads();
+    }
+    n_c = n_main;
+    if (a1 < shi32) {  // the last (at most 3) positions of an aligned slice
+      uint32_t tail = 0;
+      for (int32_t q = a1; q < shi32; ++q) {
+        const float v = __ldg(row_base + q);
+        if (v >= f_low) {
+          if (tid == 0 && n_main + tail < cap) {
+            sh.cand_key[n_main + tail] = order_key(v);
+            sh.cand_pos[n_main + tail] = q;
+          }
+          ++tail;
+        }
+      }
+      n_c += tail;
+    }
+  }
   __syncthreads();
-  if (n_c >= static_cast<uint32_t>(k) && n_c <= static_cast<uint32_t>(p.cap)) {
+  Sums cnt, unused;
+  exchange2(n_c, 0u, cnt, unused);
+  if (cnt.all >= static_cast<uint32_t>(k) && cnt.max <= static_cast<uint32_t>(p.cap)) {
     // Every key >= the k-th largest is a candidate, in position order.
     radix_select([&](auto sel, auto bin) { smem_hist(n_c, sel, bin); }, static_cast<uint32_t>(k), &T, &above);
     select(n_c, smem_get, T, above);
   } else {
     radix_select(window_hist, static_cast<uint32_t>(k), &T, &above);
-    select(L, global_get, T, above);
+    select(Ls, global_get, T, above);
   }
 }
 
-cudaError_t launch_topk(const TopkParams& p, int smem_bytes, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+__global__ void __launch_bounds__(kTopkThreads, 2) topk_rows_kernel(const TopkParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  topk_row<false>(p, smem_raw);
+}
+
+// Launched with clusters of `ctas` CTAs along x, one cluster per row.
+__global__ void __launch_bounds__(kTopkThreads, 2) topk_rows_cluster_kernel(const TopkParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  topk_row<true>(p, smem_raw);
+}
+
+cudaError_t launch_topk(const TopkParams& p, int ctas, int smem_bytes, cudaStream_t stream) {
+  if (ctas < 1 || ctas > kTopkMaxCluster) return cudaErrorInvalidValue;
+  void (*kern)(TopkParams) = ctas > 1 ? topk_rows_cluster_kernel : topk_rows_kernel;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
-  topk_rows_kernel<<<p.rows, kTopkThreads, smem_bytes, stream>>>(p);
-  return cudaGetLastError();
+  if (ctas == 1) {
+    kern<<<p.rows, kTopkThreads, smem_bytes, stream>>>(p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.rows) * static_cast<unsigned>(ctas), 1, 1);
+  cfg.blockDim = dim3(kTopkThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(ctas);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+cudaError_t read_topk_watchdog(unsigned int* value, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_topk_watchdog, sizeof(unsigned int));
+  if (e != cudaSuccess || !clear) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_topk_watchdog, &zero, sizeof(unsigned int));
 }
 
 }  // namespace fp8idx

@@ -26,18 +26,18 @@ def fp8idx():
     return m
 
 
-def gpu_mqa_topk(fp8idx, logits, ks, ke, k):
+def gpu_mqa_topk(fp8idx, logits, ks, ke, k, ctas=0):
     lg = torch.from_numpy(np.ascontiguousarray(logits)).cuda()
     out = torch.full((logits.shape[0], k), -7, dtype=torch.int32, device="cuda")
-    fp8idx.fp8_mqa_topk(lg, torch.from_numpy(ks).cuda(), torch.from_numpy(ke).cuda(), k, out)
+    fp8idx.fp8_mqa_topk(lg, torch.from_numpy(ks).cuda(), torch.from_numpy(ke).cuda(), k, out, ctas_per_row=ctas)
     torch.cuda.synchronize()
     return out.cpu().numpy()
 
 
-def gpu_paged_topk(fp8idx, logits, context_lens, next_n, mml, k):
+def gpu_paged_topk(fp8idx, logits, context_lens, next_n, mml, k, ctas=0):
     lg = torch.from_numpy(np.ascontiguousarray(logits)).cuda()
     out = torch.full((logits.shape[0], k), -7, dtype=torch.int32, device="cuda")
-    fp8idx.fp8_paged_topk(lg, torch.from_numpy(context_lens).cuda(), next_n, mml, k, out)
+    fp8idx.fp8_paged_topk(lg, torch.from_numpy(context_lens).cuda(), next_n, mml, k, out, ctas_per_row=ctas)
     torch.cuda.synchronize()
     return out.cpu().numpy()
 
@@ -105,14 +105,35 @@ def test_mqa_topk_unaligned_rows(fp8idx, shift, pad):
     assert np.array_equal(out.cpu().numpy(), want)
 
 
-def test_paged_topk_ragged(fp8idx):
+@pytest.mark.parametrize("ctas", [0, 1, 3, 8])
+def test_paged_topk_ragged(fp8idx, ctas):
     rng = np.random.default_rng(11)
     batch, next_n, mml = 9, 3, 70000
     ctx = np.array([0, 1, 2, 3, 100, 2049, 2050, 69999, 70000], dtype=np.int32)
     logits = rng.normal(size=(batch * next_n, mml + 5)).astype(np.float32)  # wider than max_model_len
     for k in (1, 512, 2048):
         want = T.topk_rows(logits, *T.decode_windows(ctx, next_n, mml), k)
-        assert np.array_equal(gpu_paged_topk(fp8idx, logits, ctx, next_n, mml, k), want), f"k={k}"
+        assert np.array_equal(gpu_paged_topk(fp8idx, logits, ctx, next_n, mml, k, ctas), want), f"k={k}"
+
+
+@pytest.mark.parametrize("ctas", [1, 2, 3, 4, 8])
+def test_topk_ctas_per_row(fp8idx, ctas):
+    """The same rows split over 1..8 CTAs (2 or more: one thread-block
+    cluster per row): windows whose slices fit shared memory, long ones
+    (sampled threshold), heavy ties (the exact fallback), a window only a
+    few values longer than k, one shorter than k, an empty one."""
+    rng = np.random.default_rng(40 + ctas)
+    m, n = 10, 150000
+    logits = rng.normal(size=(m, n)).astype(np.float32)
+    logits[3] = rng.integers(0, 3, n).astype(np.float32)
+    logits[4, ::7] = np.round(logits[4, ::7], 1)
+    ks = np.array([0, 0, 17, 5, 0, 149990, 0, 3, 100, 0], dtype=np.int32)
+    ke = np.array([150000, 9000, 120001, 150000, 150000, 150000, 0, 70003, 2153, 40000], dtype=np.int32)
+    for k in (1, 512, 2048):
+        want = T.topk_rows(logits, *T.prefill_windows(ks, ke, n), k)
+        got = gpu_mqa_topk(fp8idx, logits, ks, ke, k, ctas)
+        bad = np.nonzero((got != want).any(axis=1))[0]
+        assert bad.size == 0, f"ctas={ctas} k={k} rows {bad.tolist()}"
 
 
 def test_topk_of_library_logits(fp8idx, oracle_impl):
@@ -143,3 +164,6 @@ def test_topk_errors(fp8idx):
     with pytest.raises(fp8idx.Fp8IdxError) as e:
         fp8idx.fp8_paged_topk(lg, ks[:3], 1, 100, 10, idx)
     assert e.value.status == fp8idx.FP8IDX_ERR_INVALID
+    with pytest.raises(fp8idx.Fp8IdxError) as e:
+        fp8idx.fp8_mqa_topk(lg, ks, ks, 10, idx, ctas_per_row=9)
+    assert e.value.status == fp8idx.FP8IDX_ERR_UNSUPPORTED
