@@ -58,7 +58,6 @@ namespace {
 constexpr int kT = kTopkThreads;
 constexpr int kWarps = kT / 32;
 constexpr int kPer = 8;     // elements per thread per chunk of an ordered pass
-constexpr int kTopkPrefetch = 32768;  // bytes per bulk L2 prefetch
 
 __device__ __forceinline__ uint32_t order_key(float x) {
   const uint32_t u = __float_as_uint(x + 0.0f);  // -0.0 + 0.0 = +0.0: both zeros share one key
@@ -481,18 +480,8 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, uint8_t* smem_raw)
     return;
   }
 
-  // Long windows.  First the slice's aligned part is prefetched into L2 in
-  // bulk (one thread, no registers held): DRAM streams it while the sample
-  // is ranked, and the passes below read it from L2.
-  if (vec && tid == 0) {
-    const int64_t b0 = (slo + 3) & ~static_cast<int64_t>(3), a1 = shi & ~static_cast<int64_t>(3);
-    for (int64_t c0 = b0; c0 < a1; c0 += kTopkPrefetch / 4) {
-      const int64_t n = a1 - c0 < kTopkPrefetch / 4 ? a1 - c0 : kTopkPrefetch / 4;
-      ptx::bulk_prefetch_l2(row_base + c0, static_cast<uint32_t>(n * 4));
-    }
-  }
-  // A stride sample of at most cap values (stride S over the
-  // whole window, each CTA loading the samples in its slice) estimates a
+  // Long windows.  A stride sample of at most cap values (stride S over
+  // the whole window, each CTA loading the samples in its slice) estimates a
   // lower threshold t_low: the (2k/S + 32)-th largest sample key (rounded
   // down to its 24-bit bin), so about 2k + 32S window values lie above it
   // (many standard deviations from both k and cap for the strides used).
@@ -503,15 +492,15 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, uint8_t* smem_raw)
   const int64_t ns = (L + S - 1) / S;  // samples lo + jS of the whole window: <= cap
   const int64_t j_lo = (slo - lo + S - 1) / S, j_hi = (shi - lo + S - 1) / S;  // this slice's samples
   const int64_t ns_c = j_hi - j_lo;
-  for (int64_t j0 = 0; j0 < ns_c; j0 += static_cast<int64_t>(kT) * 8) {
-    float v[8];
+  for (int64_t j0 = 0; j0 < ns_c; j0 += static_cast<int64_t>(kT) * 16) {  // all of a cap-8192 sample in flight
+    float v[16];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < 16; ++u) {
       const int64_t j = j0 + u * kT + tid;
       v[u] = j < ns_c ? __ldg(row_base + lo + (j_lo + j) * S) : 0.f;
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < 16; ++u) {
       const int64_t j = j0 + u * kT + tid;
       if (j < ns_c) sh.cand_key[j] = order_key(v[u]);
     }
