@@ -282,11 +282,23 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
       // block_tables[b][p].  Producer warp w gathers tokens [64w, 64w+64) of
       // a tile, one token per instruction: lane l copies bytes [4l, 4l+4)
       // into the 128-byte-swizzled row; lane l also copies the scales of
-      // tokens 64w+l and 64w+32+l.  Copies are tracked per thread with
-      // cp.async groups; a tile is published kLag tiles after it was issued.
+      // tokens 64w+l and 64w+32+l.  Each lane turns its two table entries
+      // into row addresses once (tokens past the window read row 0: in
+      // bounds, and their logits are never stored), so a token costs a
+      // shuffle of that address and one copy -- no per-token branch.
+      // Copies are tracked per thread with cp.async groups; a tile is
+      // published kLag tiles after it was issued.
       constexpr int kLag = 4;
       const int pw = warp;  // 0..1
-      int32_t slot_a = 0, slot_b = 0, nxt_a = 0, nxt_b = 0;
+      const auto row_addr = [&](int32_t slot) -> const uint8_t* {
+        return p.kv_cache + static_cast<int64_t>(clamp_block(slot, p.num_blocks)) * (kHeadDim + 4);
+      };
+      const uint8_t *src_a = p.kv_cache, *src_b = p.kv_cache, *nxt_a = p.kv_cache, *nxt_b = p.kv_cache;
+      // swizzled position of this lane's 4 bytes in a row whose (row & 7) is e
+      uint32_t swz[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        swz[e] = ((static_cast<uint32_t>(lane >> 2) ^ static_cast<uint32_t>(e)) << 4) | (static_cast<uint32_t>(lane & 3) * 4u);
       int pending = 0;
       Ring pub{0u, 0u, static_cast<uint32_t>(S)};  // next stage to publish
       for (int it = 0; it < n_items; ++it) {
@@ -314,39 +326,25 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
           ++q_issued;
           ctx_eff = clamp_ctx(__ldg(p.context_lens + cur.b), p);
           const int64_t t0 = static_cast<int64_t>(cur.t) * kTileTokens + pw * 64 + lane;
-          slot_a = load_table(p, cur.b, t0, ctx_eff);
-          slot_b = load_table(p, cur.b, t0 + 32, ctx_eff);
+          src_a = row_addr(load_table(p, cur.b, t0, ctx_eff));
+          src_b = row_addr(load_table(p, cur.b, t0 + 32, ctx_eff));
         }
-        if (cur.t + 1 < cur.tiles_b) {  // prefetch the next tile's slots (same request only)
+        if (cur.t + 1 < cur.tiles_b) {  // prefetch the next tile's rows (same request only)
           const int64_t t1 = static_cast<int64_t>(cur.t + 1) * kTileTokens + pw * 64 + lane;
-          nxt_a = load_table(p, cur.b, t1, ctx_eff);
-          nxt_b = load_table(p, cur.b, t1 + 32, ctx_eff);
+          nxt_a = row_addr(load_table(p, cur.b, t1, ctx_eff));
+          nxt_b = row_addr(load_table(p, cur.b, t1 + 32, ctx_eff));
         }
         if (!warp_wait_bounded(empty0 + 8u * st.idx, st.phase ^ 1u, abort_flag, &g_paged_watchdog, kSiteStageEmpty))
           break;
-        const int valid = min(kTileTokens, static_cast<int>(ctx_eff - static_cast<int64_t>(cur.t) * kTileTokens));
-        const uint32_t tile_s = ptx::smem_u32(k_s + st.idx * kKTileBytes);
-        const uint32_t chunk_in_row = static_cast<uint32_t>(lane >> 2);
-        const uint32_t byte_in_chunk = static_cast<uint32_t>(lane & 3) * 4u;
-#pragma unroll 4
-        for (int j = 0; j < 64; ++j) {
-          const int tok = pw * 64 + j;
-          const int32_t sid = __shfl_sync(0xffffffffu, j < 32 ? slot_a : slot_b, j & 31);
-          if (tok < valid) {
-            const int64_t row = clamp_block(sid, p.num_blocks);
-            const uint32_t dst = tile_s + tok * kHeadDim + (((chunk_in_row ^ (tok & 7)) << 4) | byte_in_chunk);
-            ptx::cp_async_4(dst, p.kv_cache + row * (kHeadDim + 4) + lane * 4);
-          }
-        }
+        const uint32_t tile_s = ptx::smem_u32(k_s + st.idx * kKTileBytes) + static_cast<uint32_t>(pw * 64 * kHeadDim);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int tok = pw * 64 + half * 32 + lane;
-          if (tok < valid) {
-            const int64_t row = clamp_block(half ? slot_b : slot_a, p.num_blocks);
-            ptx::cp_async_4(ptx::smem_u32(sc_s + st.idx * kTileTokens + tok),
-                            p.kv_cache + row * (kHeadDim + 4) + kHeadDim);
-          }
+        for (int j = 0; j < 64; ++j) {  // row (pw*64 + j) & 7 == j & 7
+          const uint8_t* row = reinterpret_cast<const uint8_t*>(
+              __shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(j < 32 ? src_a : src_b), j & 31));
+          ptx::cp_async_4(tile_s + j * kHeadDim + swz[j & 7], row + lane * 4);
         }
+        ptx::cp_async_4(ptx::smem_u32(sc_s + st.idx * kTileTokens + pw * 64 + lane), src_a + kHeadDim);
+        ptx::cp_async_4(ptx::smem_u32(sc_s + st.idx * kTileTokens + pw * 64 + 32 + lane), src_b + kHeadDim);
         ptx::cp_async_commit();
         ++pending;
         st.next();
@@ -358,8 +356,8 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
           pub.next();
           --pending;
         }
-        slot_a = nxt_a;
-        slot_b = nxt_b;
+        src_a = nxt_a;
+        src_b = nxt_b;
         cur.advance();
       }
       ptx::cp_async_wait<0>();
