@@ -379,13 +379,7 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const PrefillK& src, const fp
   DeviceInfo dev;
   TRY(device_info(&dev));
   fp8idx_plan plan;
-  fp8idx_options popts;
-  if (paged) {  // paged K: one unit per row block (the -inf fill works on its whole row range)
-    popts = opts ? *opts : fp8idx_options{};
-    popts.split_n = 1;
-  }
-  TRY(plan_prefill(M, N, (int)H, (int)D, dev.sms, dev.smem_optin, paged ? &popts : opts, &plan,
-                   paged ? 2 * ((int)R + 1) : 0));
+  TRY(plan_prefill(M, N, (int)H, (int)D, dev.sms, dev.smem_optin, opts, &plan, paged ? 2 * ((int)R + 1) : 0));
   CUtensorMap tm_q, tm_k, tm_s;
   {
     const uint64_t dims[2] = {(uint64_t)D, (uint64_t)(M * H)};

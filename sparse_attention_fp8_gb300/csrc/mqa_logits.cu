@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
             int n = col0 + row;
             bool col_ok = n < p.cols;
             if constexpr (PAGED) {  // padded tile -> the request's output columns; padding is not written
-              const int j = U.j0 + c;
+              const int j = U.j0 + c * p.split;
               const int r = upper_index(tp_s, p.n_req, j);
               const int local = (j - tp_s[r]) * kTileTokens + row;
               n = cu_s[r] + local;
@@ -433,7 +433,10 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
       const int rv = min(BM, p.rows - U.m0);
       float* const out_block = p.out + static_cast<int64_t>(U.m0) * p.out_stride;
       const int n_out_tiles = (p.cols + kTileTokens - 1) / kTileTokens;
-      for (int k = 0; k < n_out_tiles; ++k) {
+      // The union range [g_lo, g_hi) is the same for every split of a row
+      // block and is exactly covered by the computed tiles of all its
+      // splits; the splits share the rest by output tile index.
+      for (int k = U.sidx; k < n_out_tiles; k += p.split) {
         const int c0 = k * kTileTokens, c1 = min(c0 + kTileTokens, p.cols);
         const bool outside = c1 <= U.g_lo || c0 >= U.g_hi;
         if (outside && p.tma_fill) {

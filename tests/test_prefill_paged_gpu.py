@@ -53,15 +53,18 @@ def test_paged_prefill_block_sizes(fp8idx, oracle_impl, blk, heads):
     assert np.array_equal(out.cpu().numpy(), gpu, equal_nan=True)
 
 
-def test_paged_prefill_many_small_requests(fp8idx, oracle_impl):
-    """Tiles that span several requests (lengths well below the 128-token tile)."""
+@pytest.mark.parametrize("split", [0, 1, 4])
+def test_paged_prefill_many_small_requests(fp8idx, oracle_impl, split):
+    """Tiles that span several requests (lengths well below the 128-token
+    tile), with the planner's column split and forced ones."""
     rng = np.random.default_rng(3)
     lens = rng.integers(0, 90, 40)
     rows = np.minimum(lens, rng.integers(0, 6, 40))
     case = workloads.paged_prefill_case(lens, rows, 32, block_size=16, seed=8, poison=True, extra_blocks=2)
     k, s = gathered(case)
-    assert_rows_close(run_paged(fp8idx, case), oracle_impl.mqa_logits(case.q, k, s, case.weights, case.ks, case.ke),
-                      what="small requests")
+    gpu = run_paged(fp8idx, case, options=fp8idx.Options(split_n=split))
+    assert_rows_close(gpu, oracle_impl.mqa_logits(case.q, k, s, case.weights, case.ks, case.ke),
+                      what=f"small requests split {split}")
 
 
 def test_paged_prefill_no_clean_and_overrides(fp8idx, oracle_impl):
@@ -69,9 +72,30 @@ def test_paged_prefill_no_clean_and_overrides(fp8idx, oracle_impl):
     k, s = gathered(case)
     ref = oracle_impl.mqa_logits(case.q, k, s, case.weights, case.ks, case.ke)
     assert_rows_close(run_paged(fp8idx, case, clean_logits=False), ref, written=np.isfinite(ref), what="no-clean")
-    for opts in (dict(split_n=1), dict(stages=2), dict(block_m=3, split_n=3)):
+    for opts in (dict(split_n=1), dict(stages=2), dict(block_m=3, split_n=3), dict(split_n=2), dict(split_n=5),
+                 dict(split_n=13)):
         gpu = run_paged(fp8idx, case, options=fp8idx.Options(**opts))
         assert_rows_close(gpu, ref, what=str(opts))
+        gpu = run_paged(fp8idx, case, clean_logits=False, options=fp8idx.Options(**opts))
+        assert_rows_close(gpu, ref, written=np.isfinite(ref), what=f"no-clean {opts}")
+
+
+@pytest.mark.slow
+def test_paged_prefill_full_size_matches_contiguous(fp8idx):
+    """The 4 x 1024-row causal workload over 32768 gathered tokens (block 64):
+    bit-identical to the contiguous kernel on the gathered K, which the
+    prefill tests check against the oracle at this size -- so every output
+    element, the -inf fill of every split included, is covered."""
+    case = workloads.paged_prefill_case([8192] * 4, [1024] * 4, 32, block_size=64, seed=77)
+    k, s = gathered(case)
+    d = to_device(case)
+    for split in (0, 1, 3):
+        gpu = run_paged(fp8idx, case, options=fp8idx.Options(split_n=split))
+        out = torch.full((case.rows, case.cols), float("nan"), device="cuda")
+        fp8idx.fp8_mqa_logits(d["q"], torch.from_numpy(k).cuda(), torch.from_numpy(s).cuda(), d["weights"],
+                              d["ks"], d["ke"], out)
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy(), gpu, equal_nan=True), f"split {split}"
 
 
 def test_paged_prefill_errors(fp8idx):
