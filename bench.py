@@ -136,12 +136,25 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
-    """Hash of the kernel sources: a recorded ncu traffic figure is reported
-    only while the kernels it was taken on are unchanged."""
+# The source file of each workload's dominant kernel; every kernel also
+# builds from the shared headers and is planned and launched by the host.
+KERNEL_SOURCE = {"decode": "paged_logits.cu", "prefill": "mqa_logits.cu", "topk": "topk.cu"}
+SHARED_SOURCES = ("api.cpp", "common.cuh", "kernels.h", "ptx.cuh")
+
+
+def workload_kernel(workload: str) -> str:
+    if workload in TOPK_WORKLOADS:
+        return "topk"
+    return workloads.CONFIGS[WORKLOADS[workload][0]]["kind"]
+
+
+def kernel_source_hash(workload: str) -> str:
+    """Hash of the sources that build and launch the workload's dominant
+    kernel: a recorded ncu traffic figure is reported only while they are
+    unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_attention_fp8_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(SHARED_SOURCES + (KERNEL_SOURCE[workload_kernel(workload)],)):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -156,7 +169,7 @@ def recorded_traffic(workload: str):
             rec = json.load(f).get(workload)
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("kernel_hash") != kernel_source_hash():
+    if not rec or rec.get("kernel_hash") != kernel_source_hash(workload):
         return None
     return rec.get("dram_bytes_per_launch")
 
