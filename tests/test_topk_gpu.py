@@ -116,6 +116,23 @@ def test_paged_topk_ragged(fp8idx, ctas):
         assert np.array_equal(gpu_paged_topk(fp8idx, logits, ctx, next_n, mml, k, ctas), want), f"k={k}"
 
 
+def test_topk_more_rows_than_sms(fp8idx):
+    """More rows than SMs (several waves of CTAs, two per SM): short, long,
+    tied and empty windows."""
+    rng = np.random.default_rng(21)
+    m, n = 400, 24000
+    logits = rng.normal(size=(m, n)).astype(np.float32)
+    logits[::7] = np.round(logits[::7], 1)
+    ks = rng.integers(-100, n, m).astype(np.int32)
+    ke = (ks + rng.integers(-50, n, m)).astype(np.int32)
+    ks[:20], ke[:20] = 0, n
+    for k in (64, 2048):
+        want = T.topk_rows(logits, *T.prefill_windows(ks, ke, n), k)
+        got = gpu_mqa_topk(fp8idx, logits, ks, ke, k)
+        bad = np.nonzero((got != want).any(axis=1))[0]
+        assert bad.size == 0, f"k={k} rows {bad[:10].tolist()}"
+
+
 @pytest.mark.parametrize("ctas", [1, 2, 3, 4, 8])
 def test_topk_ctas_per_row(fp8idx, ctas):
     """The same rows split over 1..8 CTAs (2 or more: one thread-block
