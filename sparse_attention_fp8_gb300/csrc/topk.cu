@@ -20,18 +20,20 @@
 //    (at most cap samples); the sample's (2k/S + 32)-th largest key is a
 //    lower threshold, and the values above it (about 2k + 32S of them) are
 //    compacted into shared memory, in position order, for the exact select:
-//    every warp counts the candidates of its own segment of the window, one
-//    barrier turns the counts into offsets, and every warp re-reads its
-//    segment (from L2) and writes its candidates -- no block barrier per
-//    chunk.  If the kept count falls outside [k, cap] (adversarial or
-//    heavily tied rows), the levels and the selection re-read the window
-//    from global memory instead.
+//    in one pass every warp appends the candidates of its own segment of the
+//    window, in order, to its own share of the candidate arrays (no block
+//    barrier per chunk); a staged copy then puts the shares in position
+//    order (a share that overflows falls back to a second pass that writes
+//    every candidate at its final slot).  If the kept count falls outside
+//    [k, cap] (adversarial or heavily tied rows), the levels and the
+//    selection re-read the window from global memory instead.
 //  * Selection: an ordered pass keeps every key above the k-th key T and the
 //    first (k - #above) keys equal to T in position order (block-wide
 //    prefix sums), so ties resolve to the lowest positions, and writes the
 //    kept positions straight to the output in position order.
-// Rows too few to fill the GPU (fewer than two per SM) with long windows
-// are each split over a thread-block cluster of C CTAs instead: every step
+// Rows far too few to fill the GPU (the host's rule: at most a quarter of
+// the SM count) with long windows are each split over a thread-block cluster
+// of C CTAs instead (or as many as the caller asks for): every step
 // above runs per slice of the window, each CTA adding its histogram counts
 // into every cluster member's sum histogram (remote shared-memory
 // reductions) before each bin search, the candidate counts agreed
