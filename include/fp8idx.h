@@ -210,7 +210,9 @@ fp8idx_status fp8_mqa_logits_ex(const fp8idx_tensor* q_fp8,
  *  cu_seq_lens  [requests + 1] I32 (device), contiguous: 0 = cu[0] <= cu[1]
  *               <= ... <= cu[requests] = N, and each request's length at
  *               most max_blocks*block_size (preconditions; requests <= 4096).
- * opts may be NULL (heuristic); clean_logits as for fp8_mqa_logits_ex.
+ * opts may be NULL (heuristic); stages, split_n, reverse_rows, block_m and
+ * clean_logits as for fp8_mqa_logits_ex (split_n counts tiles of a padded
+ * column space in which every request starts on a 128-column boundary).
  */
 fp8idx_status fp8_mqa_logits_paged(const fp8idx_tensor* q_fp8,
                                    const fp8idx_tensor* kv_cache,
