@@ -60,9 +60,9 @@ WORKLOADS = {
     "decode_mtp_verify_n1": (2, 1),
     "prefill_4x1024": (3, None),
     "decode_blk1": (4, None),
-    "prefill_paged_4x1024": (3, None),
+    "prefill_paged_4x1024": (3, None),  # config 3 with K in a paged cache (block 64), gathered in the kernel
     "prefill_2048x65536": (5, None),
-    "prefill_1024x131072": (6, None),  # config 3 with K in a paged cache (block 64), gathered in the kernel
+    "prefill_1024x131072": (6, None),
 }
 PAGED_PREFILL = {"prefill_paged_4x1024"}
 # top-k consumer workloads: (config index, k); the logits are the library's

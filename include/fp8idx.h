@@ -169,9 +169,10 @@ fp8idx_status fp8_paged_mqa_logits_ex(const fp8idx_tensor* q_fp8,
  *  weights      [M, heads] F32, contiguous, 16-byte aligned (loaded by TMA).
  *  cu_seqlen_ks, cu_seqlen_ke  [M] I32, contiguous.
  *  out          [M, >= N] F32, stride[1] == 1, stride[0] >= N.
- * Supported (fp8idx_prefill_is_supported): head_dim 128; heads 32, 64 or
- * 128 (the pages' prefill sweep, same PR, Test Plan); M, N >= 0 with
- * M*heads and N below 2^31.
+ * Supported (fp8idx_prefill_is_supported): head_dim 128 or 64 (64-byte
+ * rows: Q [M, heads, 64] and K [N, 64]); heads 32, 64 or 128 (the pages'
+ * prefill sweep, same PR, Test Plan); M, N >= 0 with M*heads and N below
+ * 2^31.
  */
 fp8idx_status fp8_mqa_logits(const fp8idx_tensor* q_fp8,
                              const fp8idx_tensor* k_fp8,
@@ -286,6 +287,13 @@ fp8idx_status fp8_mqa_topk_ex(const fp8idx_tensor* logits,
 int fp8idx_paged_is_supported(int32_t heads, int32_t head_dim,
                               int32_t block_size, int32_t next_n);
 int fp8idx_prefill_is_supported(int32_t heads, int32_t head_dim);
+/* The decode gate under its short name, with the arguments of the decode
+ * page's is_supported(num_heads, head_dim, kv_block_size) plus next_n (which
+ * the fold of next_n into the MMA N dimension bounds: next_n*heads <= 256).
+ * Identical to fp8idx_paged_is_supported; prefill shapes have their own
+ * gate because the prefill kernel supports other head dims and head counts. */
+int fp8idx_is_supported(int32_t heads, int32_t head_dim,
+                        int32_t kv_block_size, int32_t next_n);
 
 /* The launch the planner would choose for a shape, for `num_sms` SMs (pass 0
  * to query the current device).  After the pages' host heuristics that pick
@@ -308,6 +316,17 @@ const char* fp8idx_last_error(void);
  * FP8IDX_ERR_TIMEOUT if one has.  This call synchronises with the device
  * (it copies the word back), so it does not belong inside a captured graph. */
 fp8idx_status fp8idx_device_status(int32_t clear);
+
+/* Test hook for the watchdog above.  Enqueues one small kernel that waits,
+ * through the same bounded wait as every pipeline stage, on a shared-memory
+ * barrier that nothing ever arrives on, and gives up after limit_us
+ * microseconds (1 .. 100000) instead of the pipelines' 2 s.  The kernel then
+ * returns normally: afterwards fp8idx_device_status() reports
+ * FP8IDX_ERR_TIMEOUT with the self-test site (bit 0x80 of the decode word)
+ * until it is cleared, and the device stays usable.  No copy, tensor-core
+ * operation or tensor memory is involved.  Returns FP8IDX_OK,
+ * FP8IDX_ERR_INVALID (limit out of range) or FP8IDX_ERR_CUDA. */
+fp8idx_status fp8idx_watchdog_selftest(int32_t limit_us, void* stream);
 
 /* Library version: major*10000 + minor*100 + patch. */
 int32_t fp8idx_version(void);

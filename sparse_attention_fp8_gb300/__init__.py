@@ -30,11 +30,13 @@ from ._native import (  # noqa: F401
     Options,
     Plan,
     device_status,
+    device_status_message,
     fp8_mqa_logits,
     fp8_mqa_logits_paged,
     fp8_mqa_topk,
     fp8_paged_mqa_logits,
     fp8_paged_topk,
+    is_supported,
     library,
     library_path,
     paged_is_supported,
@@ -42,4 +44,5 @@ from ._native import (  # noqa: F401
     plan_prefill,
     prefill_is_supported,
     version,
+    watchdog_selftest,
 )

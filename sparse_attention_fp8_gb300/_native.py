@@ -108,6 +108,8 @@ def library():
             lib.fp8idx_paged_is_supported.restype = ctypes.c_int
             lib.fp8idx_prefill_is_supported.argtypes = [ctypes.c_int32] * 2
             lib.fp8idx_prefill_is_supported.restype = ctypes.c_int
+            lib.fp8idx_is_supported.argtypes = [ctypes.c_int32] * 4
+            lib.fp8idx_is_supported.restype = ctypes.c_int
             lib.fp8idx_plan_paged.argtypes = [ctypes.c_int32] * 7 + [P(_Options), P(_Plan)]
             lib.fp8idx_plan_paged.restype = ctypes.c_int
             lib.fp8idx_plan_prefill.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
@@ -117,6 +119,8 @@ def library():
             lib.fp8idx_device_status.argtypes = [ctypes.c_int32]
             lib.fp8idx_device_status.restype = ctypes.c_int
             lib.fp8idx_version.restype = ctypes.c_int32
+            lib.fp8idx_watchdog_selftest.argtypes = [ctypes.c_int32, ctypes.c_void_p]
+            lib.fp8idx_watchdog_selftest.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -245,6 +249,11 @@ def paged_is_supported(heads, head_dim, block_size, next_n) -> bool:
     return bool(library().fp8idx_paged_is_supported(heads, head_dim, block_size, next_n))
 
 
+def is_supported(heads, head_dim, kv_block_size, next_n) -> bool:
+    """The decode gate (same as paged_is_supported)."""
+    return bool(library().fp8idx_is_supported(heads, head_dim, kv_block_size, next_n))
+
+
 def prefill_is_supported(heads, head_dim) -> bool:
     return bool(library().fp8idx_prefill_is_supported(heads, head_dim))
 
@@ -273,6 +282,20 @@ def plan_prefill(rows, cols, heads, head_dim, num_sms=0, options: Options | None
 def device_status(clear: bool = True) -> int:
     """FP8IDX_OK, or FP8IDX_ERR_TIMEOUT if an in-kernel wait ran out (synchronises)."""
     return int(library().fp8idx_device_status(1 if clear else 0))
+
+
+def device_status_message() -> str:
+    """The message of the last non-OK status (e.g. the watchdog's site bits)."""
+    msg = library().fp8idx_last_error()
+    return msg.decode() if msg else ""
+
+
+def watchdog_selftest(limit_us: int = 5000, stream=None):
+    """Enqueues the watchdog self-test: a bounded wait that nothing satisfies,
+    given up after limit_us; afterwards device_status() reports a timeout."""
+    import torch
+    s = _stream(stream, torch.empty(0, device="cuda"))
+    _check(library().fp8idx_watchdog_selftest(int(limit_us), s))
 
 
 def version() -> int:

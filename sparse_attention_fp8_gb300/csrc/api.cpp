@@ -63,6 +63,46 @@ fp8idx_status device_info(DeviceInfo* out) {
   return FP8IDX_OK;
 }
 
+// ------------------------------------------ per-kernel shared-memory limit
+struct SmemAttr {
+  const void* kernel;
+  int device;
+  int bytes;
+};
+constexpr int kMaxSmemAttrs = 256;
+SmemAttr g_smem_attr[kMaxSmemAttrs];
+int g_smem_attr_n = 0;
+std::mutex g_smem_attr_mu;
+
+}  // namespace
+
+namespace fp8idx {
+
+cudaError_t ensure_dynamic_smem(const void* kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_smem_attr_mu);
+  SmemAttr* hit = nullptr;
+  for (int i = 0; i < g_smem_attr_n; ++i)
+    if (g_smem_attr[i].kernel == kernel && g_smem_attr[i].device == dev) hit = &g_smem_attr[i];
+  if (hit != nullptr && hit->bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  if (hit != nullptr) {
+    hit->bytes = bytes;
+  } else if (g_smem_attr_n < kMaxSmemAttrs) {
+    g_smem_attr[g_smem_attr_n++] = SmemAttr{kernel, dev, bytes};
+  }
+  return cudaSuccess;
+}
+
+}  // namespace fp8idx
+
+namespace {
+
+using namespace fp8idx;
+
 // ---------------------------------------------------- tensor-map encoding
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -622,6 +662,10 @@ int fp8idx_paged_is_supported(int32_t heads, int32_t head_dim, int32_t block_siz
 
 int fp8idx_prefill_is_supported(int32_t heads, int32_t head_dim) { return prefill_supported(heads, head_dim) ? 1 : 0; }
 
+int fp8idx_is_supported(int32_t heads, int32_t head_dim, int32_t kv_block_size, int32_t next_n) {
+  return paged_supported(heads, head_dim, kv_block_size, next_n) ? 1 : 0;
+}
+
 fp8idx_status fp8idx_plan_paged(int32_t batch, int32_t next_n, int32_t heads, int32_t head_dim, int32_t block_size,
                                 int32_t max_model_len, int32_t num_sms, const fp8idx_options* opts,
                                 fp8idx_plan* plan) {
@@ -665,6 +709,16 @@ fp8idx_status fp8idx_device_status(int32_t clear) {
   return FP8IDX_OK;
 }
 
-int32_t fp8idx_version(void) { return 101; }
+fp8idx_status fp8idx_watchdog_selftest(int32_t limit_us, void* stream) {
+  g_last_error.clear();
+  if (limit_us < 1 || limit_us > 100000) return fail(FP8IDX_ERR_INVALID, "limit_us %d not in [1, 100000]", limit_us);
+  DeviceInfo dev;
+  TRY(device_info(&dev));
+  cudaError_t e = launch_watchdog_selftest(static_cast<uint64_t>(limit_us) * 1000ull, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "watchdog self-test launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+int32_t fp8idx_version(void) { return 102; }
 
 }  // extern "C"

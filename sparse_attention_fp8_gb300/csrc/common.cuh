@@ -24,12 +24,15 @@ enum WaitSite : uint32_t {
   kSiteAccEmpty = 1u << 4,
   kSiteAccFull = 1u << 5,
   kSiteDrain = 1u << 6,
+  kSiteSelfTest = 1u << 7,  // the watchdog self-test's deliberately unsatisfied wait
 };
 
 // Polls `bar` for the phase with parity `parity`.  Returns false if the CTA
-// has aborted or the wait ran out (then it aborts the CTA and flags `wd`).
+// has aborted or the wait ran out after `limit_ns` (then it aborts the CTA
+// and flags `wd`).
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                             unsigned int* wd, uint32_t site) {
+                                             unsigned int* wd, uint32_t site,
+                                             uint64_t limit_ns = kWaitTimeoutNs) {
   if (ptx::mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   while (true) {
@@ -37,7 +40,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     for (int i = 0; i < 16; ++i)
       if (ptx::mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (ptx::globaltimer_ns() - t0 > kWaitTimeoutNs) {
+    if (ptx::globaltimer_ns() - t0 > limit_ns) {
       *abort_flag = 1u;
       atomicOr(wd, site);
       return false;

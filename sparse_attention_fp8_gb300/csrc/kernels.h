@@ -187,6 +187,11 @@ __host__ __device__ inline TopkLayout topk_smem_layout(int cap) {
   return L;
 }
 
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device.  The attribute is set once per (kernel, device) and size
+// (cached on the host), not on every launch.
+cudaError_t ensure_dynamic_smem(const void* kernel, int bytes);
+
 // ------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error.  The tensor maps are encoded
 // by the caller; `heads` selects the template instance.
@@ -198,6 +203,10 @@ cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, con
 
 // ctas: CTAs per row (1: one CTA per row; 2..kTopkMaxCluster: one cluster per row)
 cudaError_t launch_topk(const TopkParams& p, int ctas, int smem_bytes, cudaStream_t stream);
+
+// Launches the watchdog self-test kernel: a bounded wait that nothing
+// satisfies, given up after limit_ns (sets the decode word's self-test bit).
+cudaError_t launch_watchdog_selftest(uint64_t limit_ns, cudaStream_t stream);
 
 // Watchdog words of the two translation units (synchronous read, optional clear).
 cudaError_t read_paged_watchdog(unsigned int* value, bool clear);

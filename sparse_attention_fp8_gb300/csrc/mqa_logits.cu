@@ -188,8 +188,25 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
     ptx::fence_proxy_async_smem();
   }
   if (PAGED) {
-    for (int i = threadIdx.x; i <= p.n_req; i += blockDim.x) cu_s[i] = __ldg(p.cu_seq_lens + i);
+    // Request offsets clamped into [0, N] and made non-decreasing (a running
+    // maximum), so offsets that break the precondition cannot move a store
+    // outside the output.
+    for (int i = threadIdx.x; i <= p.n_req; i += blockDim.x)
+      cu_s[i] = min(max(__ldg(p.cu_seq_lens + i), 0), p.cols);
     __syncthreads();
+    if (warp == 0) {
+      int carry = 0;
+      for (int base = 0; base <= p.n_req; base += 32) {
+        const int i = base + lane;
+        int v = i <= p.n_req ? cu_s[i] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) v = max(v, __shfl_up_sync(0xffffffffu, v, o));
+        v = max(v, carry);
+        if (i <= p.n_req) cu_s[i] = v;
+        carry = __shfl_sync(0xffffffffu, v, 31);
+      }
+      __syncwarp();
+    }
     if (warp == 0) {  // padded tiles per request, inclusive scan
       if (lane == 0) tp_s[0] = 0;
       int running = 0;
@@ -385,7 +402,7 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
               const int r = upper_index(tp_s, p.n_req, j);
               const int local = (j - tp_s[r]) * kTileTokens + row;
               n = cu_s[r] + local;
-              col_ok = local < cu_s[r + 1] - cu_s[r];
+              col_ok = local < cu_s[r + 1] - cu_s[r] && n < p.cols;
             }
             float* const out_col = out_block + n;
             const uint32_t acce = acce0 + 8u * ac.idx;
@@ -513,7 +530,7 @@ cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, con
     else if (heads == 128) kern = mqa_logits_kernel<128, false, 64>;
   }
   if (kern == nullptr) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem_bytes);
   if (e != cudaSuccess) return e;
   kern<<<grid, prefill_threads(), smem_bytes, stream>>>(tm_q, tm_k, tm_s, tm_w, tm_out, p);
   return cudaGetLastError();

@@ -437,7 +437,9 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
         if (it == 0 || cur.t == 0) {
           if (!warp_wait_bounded(qf0 + 8u * qr.idx, qr.phase, abort_flag, &g_paged_watchdog, kSiteQFull)) break;
           w = w_s + qr.idx * N;
-          ctx = __ldg(p.context_lens + cur.b);
+          // the producers' clamped context: positions past what they loaded
+          // are never stored, even for inputs that break the precondition
+          ctx = static_cast<int32_t>(clamp_ctx(__ldg(p.context_lens + cur.b), p));
         }
         if (kShared || (it & 1) == grp) {
           if (!warp_wait_bounded(full0 + 8u * st.idx, st.phase, abort_flag, &g_paged_watchdog, kSiteStageFull))
@@ -493,9 +495,33 @@ cudaError_t launch_paged(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, cons
   if (heads == 32) kern = gather ? paged_logits_kernel<32, true> : paged_logits_kernel<32, false>;
   else if (heads == 64) kern = gather ? paged_logits_kernel<64, true> : paged_logits_kernel<64, false>;
   else return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem_bytes);
   if (e != cudaSuccess) return e;
   kern<<<grid, paged_threads(gather), smem_bytes, stream>>>(tm_q, tm_kv, tm_sc, p);
+  return cudaGetLastError();
+}
+
+// Watchdog self-test: one warp initialises an mbarrier that nothing will
+// ever arrive on and waits for it through the same bounded wait as the
+// pipelines, with a short limit.  The wait runs out, sets the CTA's abort
+// flag and the self-test bit of this translation unit's watchdog word, and
+// the kernel returns.  No copy, MMA or tensor memory is involved.
+__global__ void __launch_bounds__(32, 1) watchdog_selftest_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0u;
+    ptx::mbar_init(ptx::smem_u32(&bar), 1u);
+    ptx::fence_barrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0)
+    (void)wait_bounded(ptx::smem_u32(&bar), 0u, &abort_flag, &g_paged_watchdog, kSiteSelfTest, limit_ns);
+  __syncwarp();
+}
+
+cudaError_t launch_watchdog_selftest(uint64_t limit_ns, cudaStream_t stream) {
+  watchdog_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
   return cudaGetLastError();
 }
 

@@ -513,7 +513,9 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, uint8_t* smem_raw)
     const uint32_t rank = static_cast<uint32_t>(want < ns ? want : ns);
     radix_select([&](auto sel, auto bin) { smem_hist(ns_c, sel, bin); }, rank, &T, &above, 2);
   }
-  const uint32_t t_low = T;  // the lower edge of the 24-bit bin of the rank-th sample key
+  // the lower edge of the 24-bit bin of the rank-th sample key, never below
+  // the key of -inf (the edge of the bin holding -inf is a NaN pattern)
+  const uint32_t t_low = T > order_key(-INFINITY) ? T : order_key(-INFINITY);
 
   // Candidates >= t_low in position order, tested as floats against the
   // value whose key is t_low (the key order is the float order, -0.0 ==
@@ -699,7 +701,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_rows_cluster_kernel(cons
 cudaError_t launch_topk(const TopkParams& p, int ctas, int smem_bytes, cudaStream_t stream) {
   if (ctas < 1 || ctas > kTopkMaxCluster) return cudaErrorInvalidValue;
   void (*kern)(TopkParams) = ctas > 1 ? topk_rows_cluster_kernel : topk_rows_kernel;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem_bytes);
   if (e != cudaSuccess) return e;
   if (ctas == 1) {
     kern<<<p.rows, kTopkThreads, smem_bytes, stream>>>(p);

@@ -22,7 +22,7 @@ def lib():
 def test_exports_every_declared_function(lib):
     names = _native.header_functions()
     expected = {"fp8_paged_mqa_logits", "fp8_paged_mqa_logits_ex", "fp8_mqa_logits", "fp8_mqa_logits_ex",
-                "fp8idx_paged_is_supported", "fp8idx_prefill_is_supported", "fp8idx_plan_paged",
+                "fp8idx_paged_is_supported", "fp8idx_prefill_is_supported", "fp8idx_is_supported", "fp8idx_plan_paged",
                 "fp8idx_plan_prefill", "fp8idx_last_error", "fp8idx_device_status", "fp8idx_version"}
     assert expected <= set(names), set(names)
     for n in names:
@@ -46,6 +46,9 @@ def test_support_gates(lib):
     assert fp8idx.prefill_is_supported(32, 64) and fp8idx.prefill_is_supported(128, 64)
     assert not fp8idx.prefill_is_supported(256, 128)
     assert not fp8idx.prefill_is_supported(32, 96)
+    # the decode gate under its short name takes the same arguments and agrees
+    for args in ((32, 128, 64, 6), (64, 128, 1, 4), (64, 128, 64, 5), (32, 64, 64, 1), (32, 128, 8, 1)):
+        assert fp8idx.is_supported(*args) == fp8idx.paged_is_supported(*args), args
 
 
 def test_planner_decode(lib):
@@ -122,3 +125,42 @@ def test_validation_rejects_before_touching_the_device(lib):
     assert st == fp8idx.FP8IDX_ERR_INVALID
     st = lib.fp8_mqa_logits(R(qp), R(k), R(_t(1, (299,))), R(wp), R(ks), R(ks), R(outp), None)
     assert st == fp8idx.FP8IDX_ERR_INVALID
+
+
+def test_misaligned_pointers_rejected(lib):
+    """Operands read by TMA or bulk copies must be 16-byte aligned: an
+    address 4 bytes off returns INVALID from the host checks, before any
+    CUDA call (fake pointers, never dereferenced)."""
+    R = ctypes.byref
+    B, n, H, D = 2, 2, 32, 128
+    good = dict(q=_t(0, (B, n, H, D)), kv=_t(0, (4, 64 * (D + 4))), w=_t(1, (B * n, H)), cl=_t(2, (B,)),
+                bt=_t(2, (B, 2)), out=_t(1, (B * n, 128)))
+    for name in ("q", "kv", "w"):
+        a = dict(good)
+        a[name] = _t(a[name].dtype, tuple(a[name].shape[:a[name].ndim]), ptr=0x1004)
+        st = lib.fp8_paged_mqa_logits(R(a["q"]), R(a["kv"]), R(a["w"]), R(a["cl"]), R(a["bt"]), 128, R(a["out"]),
+                                      None)
+        assert st == fp8idx.FP8IDX_ERR_INVALID and b"aligned" in lib.fp8idx_last_error(), name
+    M, N = 5, 300
+    good = dict(q=_t(0, (M, H, D)), k=_t(0, (N, D)), s=_t(1, (N,)), w=_t(1, (M, H)), ks=_t(2, (M,)), ke=_t(2, (M,)),
+                out=_t(1, (M, N)))
+    for name in ("q", "k", "s", "w"):
+        a = dict(good)
+        a[name] = _t(a[name].dtype, tuple(a[name].shape[:a[name].ndim]), ptr=0x1004)
+        st = lib.fp8_mqa_logits(R(a["q"]), R(a["k"]), R(a["s"]), R(a["w"]), R(a["ks"]), R(a["ke"]), R(a["out"]),
+                                None)
+        assert st == fp8idx.FP8IDX_ERR_INVALID and b"aligned" in lib.fp8idx_last_error(), name
+    # paged prefill: a misaligned cache
+    kv = _t(0, (8, 64 * (D + 4)), ptr=0x1008)
+    bt = _t(2, (1, 8))
+    cu = _t(2, (2,))
+    st = lib.fp8_mqa_logits_paged(R(good["q"]), R(kv), R(bt), R(cu), R(good["w"]), R(good["ks"]), R(good["ke"]),
+                                  R(good["out"]), None, None)
+    assert st == fp8idx.FP8IDX_ERR_INVALID and b"aligned" in lib.fp8idx_last_error()
+
+
+def test_watchdog_selftest_limit_checked_on_host(lib):
+    """The self-test's wait limit is validated before any CUDA call."""
+    for bad in (0, -5, 100001):
+        assert lib.fp8idx_watchdog_selftest(bad, None) == fp8idx.FP8IDX_ERR_INVALID
+        assert b"limit_us" in lib.fp8idx_last_error()

@@ -94,53 +94,34 @@ def test_decode_config1(fp8idx, oracle_impl):
     assert_rows_close(gpu, oracle_decode(oracle_impl, case), written=decode_window_mask(case), what="config1")
 
 
-def _full_size_sampled(fp8idx, o, case, full_rows, n_samples=4096, seed=0):
-    """Full-size run: exact window check on every row, full oracle rows for a
-    few rows, and oracle elements at random in-window positions of all rows."""
+def _full_size_dense(fp8idx, o, case, chunk_rows=16):
+    """Full-size run in the bench's launch configuration, compared with the
+    oracle element by element: every row, streamed through the oracle in
+    chunks of rows, each finite logit against its own row's oracle maximum,
+    and the written/untouched mask of every element."""
     out = run_decode(fp8idx, case)
     gpu = out.cpu().numpy()
     del out
     nrows = case.batch * case.next_n
-    for r0 in range(0, nrows, 8):
-        r1 = min(nrows, r0 + 8)
-        win = decode_window_mask(case, rows=(r0, r1))
-        untouched = np.isnan(gpu[r0:r1])
-        assert not (untouched == win).any(), f"rows {r0}..{r1}: window written incorrectly"
-        assert np.isfinite(gpu[r0:r1][win]).all()
-    rowmax_min = np.inf
-    for r in full_rows:
-        ref = oracle_decode(o, case, rows=(r, r + 1))
-        assert_rows_close(gpu[r:r + 1], ref, written=decode_window_mask(case, rows=(r, r + 1)), what=f"row {r}")
-        rowmax_min = min(rowmax_min, np.abs(ref[np.isfinite(ref)]).max())
-    rng = np.random.default_rng(seed)
-    rows = rng.integers(0, nrows, n_samples)
-    b = rows // case.next_n
-    last = case.context_lens.astype(np.int64)[b] - case.next_n + rows % case.next_n
-    keep = last >= 0
-    rows, last = rows[keep], last[keep]
-    cols = (rng.random(rows.size) * (last + 1)).astype(np.int64)
-    ref = o.paged_mqa_logits_at(case.q, case.kv_cache, case.weights, case.context_lens, case.block_tables,
-                                case.block_size, case.max_model_len, rows, cols)
-    err = np.abs(gpu[rows, cols].astype(np.float64) - ref)
-    assert np.all(err <= 1e-3 * rowmax_min + 1e-5), f"sampled max err {err.max()}"
+    for r0 in range(0, nrows, chunk_rows):
+        r1 = min(nrows, r0 + chunk_rows)
+        ref = oracle_decode(o, case, rows=(r0, r1))
+        assert_rows_close(gpu[r0:r1], ref, written=decode_window_mask(case, rows=(r0, r1)), what=f"rows {r0}..{r1}")
 
 
 @pytest.mark.slow
 def test_decode_config2_full_size(fp8idx, oracle_impl):
-    case = workloads.make_config(2)
-    _full_size_sampled(fp8idx, oracle_impl, case, full_rows=[0, 47, 95])
+    _full_size_dense(fp8idx, oracle_impl, workloads.make_config(2))
 
 
 @pytest.mark.slow
 def test_decode_config2_next_n1_full_size(fp8idx, oracle_impl):
-    case = workloads.make_config(2, next_n=1)
-    _full_size_sampled(fp8idx, oracle_impl, case, full_rows=[0, 15])
+    _full_size_dense(fp8idx, oracle_impl, workloads.make_config(2, next_n=1))
 
 
 @pytest.mark.slow
 def test_decode_config4_full_size(fp8idx, oracle_impl):
-    case = workloads.make_config(4)
-    _full_size_sampled(fp8idx, oracle_impl, case, full_rows=[0, 131, 255])
+    _full_size_dense(fp8idx, oracle_impl, workloads.make_config(4), chunk_rows=32)
 
 
 def test_decode_graph_capture_replay(fp8idx, oracle_impl):
@@ -191,4 +172,25 @@ def test_decode_empty_and_errors(fp8idx):
     with pytest.raises(fp8idx.Fp8IdxError) as e:  # 16 heads: not implemented
         fp8idx.fp8_paged_mqa_logits(q16, d["kv_cache"], w16, d["context_lens"], d["block_tables"], 128, out)
     assert e.value.status == fp8idx.FP8IDX_ERR_UNSUPPORTED
+    assert fp8idx.device_status() == fp8idx.FP8IDX_OK
+
+
+def test_decode_context_past_table_capacity(fp8idx, oracle_impl):
+    """A context longer than the block table can address (a broken
+    precondition) is clamped to the table's capacity on the device: the
+    kernel stores exactly the window of the clamped context -- what its
+    producers loaded -- and nothing past it."""
+    cap = 256
+    case = workloads.decode_case(3, 2, 32, max_model_len=cap, block_size=64, context_lens=[cap, 200, 130], seed=44,
+                                 poison=True, extra_blocks=2)
+    ref = oracle_decode(oracle_impl, case)  # the clamped contexts: [256, 200, 130]
+    d = to_device(case)
+    mml = 512
+    d["context_lens"] = torch.tensor([400, 200, 130], dtype=torch.int32, device="cuda")
+    out = torch.full((6, mml), float("nan"), device="cuda")
+    fp8idx.fp8_paged_mqa_logits(d["q"], d["kv_cache"], d["weights"], d["context_lens"], d["block_tables"], mml, out)
+    torch.cuda.synchronize()
+    gpu = out.cpu().numpy()
+    assert np.isnan(gpu[:, cap:]).all(), "positions past the table capacity were stored"
+    assert_rows_close(gpu[:, :cap], ref, written=decode_window_mask(case), what="clamped context")
     assert fp8idx.device_status() == fp8idx.FP8IDX_OK

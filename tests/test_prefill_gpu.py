@@ -99,40 +99,26 @@ def test_prefill_planner_overrides(fp8idx, oracle_impl, opts):
 
 @pytest.mark.slow
 def test_prefill_config3_full_size(fp8idx, oracle_impl):
-    """Full 4096 x 32768 run: -inf mask of every row, full oracle rows at the
-    request boundaries, and random sampled in-window elements."""
+    """Full 4096 x 32768 run compared with the oracle element by element:
+    every row (oracle streamed in chunks of 256 rows), the exact -inf mask,
+    and each finite logit against its own row's oracle maximum."""
     case = workloads.make_config(3)
     gpu = run_prefill(fp8idx, case)
-    n = np.arange(case.cols)[None, :]
     for r0 in range(0, case.rows, 256):
-        r1 = r0 + 256
-        lo = np.maximum(case.ks[r0:r1].astype(np.int64), 0)[:, None]
-        hi = np.minimum(case.ke[r0:r1].astype(np.int64), case.cols)[:, None]
-        inside = (n >= lo) & (n < hi)
-        g = gpu[r0:r1]
-        assert np.array_equal(np.isneginf(g), ~inside), f"rows {r0}..{r1}: -inf mask"
-        assert np.isfinite(g[inside]).all()
-    rowmax_min = np.inf
-    for r in (0, 1023, 1024, 2047, 4095):
-        ref = oracle_prefill(oracle_impl, case, rows=(r, r + 1))
-        assert_rows_close(gpu[r:r + 1], ref, what=f"row {r}")
-        rowmax_min = min(rowmax_min, np.abs(ref[np.isfinite(ref)]).max())
-    rng = np.random.default_rng(1)
-    rows = rng.integers(0, case.rows, 4096)
-    lo = case.ks[rows].astype(np.int64)
-    hi = case.ke[rows].astype(np.int64)
-    cols = lo + (rng.random(rows.size) * (hi - lo)).astype(np.int64)
-    ref = oracle_impl.mqa_logits_at(case.q, case.k, case.kv_scale, case.weights, case.ks, case.ke, rows, cols)
-    err = np.abs(gpu[rows, cols].astype(np.float64) - ref)
-    assert np.all(err <= 1e-3 * rowmax_min + 1e-5), f"sampled max err {err.max()}"
+        r1 = min(case.rows, r0 + 256)
+        assert_rows_close(gpu[r0:r1], oracle_prefill(oracle_impl, case, rows=(r0, r1)), what=f"rows {r0}..{r1}")
 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("m,n", [(2048, 65536), (1024, 131072)], ids=["2048x65536", "1024x131072"])
 def test_prefill_real_chunk_shapes(fp8idx, oracle_impl, m, n):
-    """The pages' other real chunk shapes (one causal request per chunk):
-    exact -inf mask of every row, full oracle rows at both ends, sampled
-    in-window elements."""
+    """The pages' other real chunk shapes (one causal request per chunk).
+    Each holds about 1.3e8 window logits, several minutes of the fp64 oracle,
+    so: the exact -inf mask of every element, full oracle rows at both ends
+    and in the middle, and 256 random in-window elements of EVERY row, each
+    judged against that row's largest sampled oracle magnitude (a lower bound
+    of the row maximum, so the bar applied is at least as strict as the
+    per-row one)."""
     case = workloads.prefill_case(m, n, 32, mode="causal", seed=m + n)
     gpu = run_prefill(fp8idx, case)
     cols = np.arange(n)[None, :]
@@ -141,17 +127,22 @@ def test_prefill_real_chunk_shapes(fp8idx, oracle_impl, m, n):
         hi = np.minimum(case.ke[r0:r0 + 128].astype(np.int64), n)[:, None]
         inside = (cols >= lo) & (cols < hi)
         assert np.array_equal(np.isneginf(gpu[r0:r0 + 128]), ~inside), f"rows {r0}..: -inf mask"
-    rowmax_min = np.inf
-    for r in (0, m - 1):
+    for r in (0, m // 2, m - 1):
         ref = oracle_prefill(oracle_impl, case, rows=(r, r + 1))
         assert_rows_close(gpu[r:r + 1], ref, what=f"row {r}")
-        rowmax_min = min(rowmax_min, np.abs(ref[np.isfinite(ref)]).max())
+    per_row = 256
     rng = np.random.default_rng(2)
-    rows = rng.integers(0, m, 2048)
-    cols_s = case.ks[rows] + (rng.random(rows.size) * (case.ke[rows] - case.ks[rows])).astype(np.int64)
+    rows = np.repeat(np.arange(m, dtype=np.int64), per_row)
+    lo = np.maximum(case.ks[rows].astype(np.int64), 0)
+    hi = np.minimum(case.ke[rows].astype(np.int64), n)
+    assert (hi > lo).all()
+    cols_s = lo + (rng.random(rows.size) * (hi - lo)).astype(np.int64)
     ref = oracle_impl.mqa_logits_at(case.q, case.k, case.kv_scale, case.weights, case.ks, case.ke, rows, cols_s)
+    rowmax = np.abs(ref).reshape(m, per_row).max(axis=1)
+    tol = 1e-3 * np.repeat(rowmax, per_row) + 1e-5
     err = np.abs(gpu[rows, cols_s].astype(np.float64) - ref)
-    assert np.all(err <= 1e-3 * rowmax_min + 1e-5), f"sampled max err {err.max()}"
+    bad = err > tol
+    assert not bad.any(), f"{int(bad.sum())} sampled logits out of tolerance, max err {err.max()}"
 
 
 @pytest.mark.parametrize("cols,pitch", [(701, 704), (701, 705), (130, 132), (64, 256)],

@@ -112,3 +112,27 @@ def test_paged_prefill_errors(fp8idx):
         fp8idx.fp8_mqa_logits_paged(d1["q"], d1["kv_cache"], d1["block_tables"], d1["cu_seq_lens"], d1["weights"],
                                     d1["ks"], d1["ke"], torch.empty((blk1.rows, blk1.cols), device="cuda"))
     assert e.value.status == fp8idx.FP8IDX_ERR_UNSUPPORTED
+
+
+def test_paged_prefill_offsets_past_n_stay_inside_out(fp8idx):
+    """cu_seq_lens that break the precondition (a last offset past N, an
+    offset that decreases) are clamped on the device into [0, N] and made
+    non-decreasing, so no store leaves the output: out is a column slice of a
+    wider NaN buffer whose guard columns must stay untouched, and every
+    element of [0, N) is written (-inf or a finite logit)."""
+    case = workloads.paged_prefill_case([300, 200, 150], [40, 30, 20], 32, block_size=16, seed=12)
+    n = case.cols  # 650
+    d = to_device(case)
+    bad = case.cu_seq_lens.copy()
+    bad[2] = bad[1] - 7          # decreasing
+    bad[3] = n + 90              # past N
+    d["cu_seq_lens"] = torch.from_numpy(bad).cuda()
+    pitch = n + 132
+    buf = torch.full((case.rows, pitch), float("nan"), device="cuda")
+    fp8idx.fp8_mqa_logits_paged(d["q"], d["kv_cache"], d["block_tables"], d["cu_seq_lens"], d["weights"], d["ks"],
+                                d["ke"], buf[:, :n])
+    torch.cuda.synchronize()
+    host = buf.cpu().numpy()
+    assert np.isnan(host[:, n:]).all(), "a store landed past column N"
+    assert not np.isnan(host[:, :n]).any(), "an element of [0, N) was left unwritten"
+    assert fp8idx.device_status() == fp8idx.FP8IDX_OK
