@@ -223,7 +223,8 @@ fp8idx_status plan_paged(int32_t batch, int32_t next_n, int32_t heads, int32_t h
 }
 
 fp8idx_status plan_prefill(int64_t rows, int64_t cols, int32_t heads, int32_t head_dim, int32_t num_sms,
-                           int32_t smem_limit, const fp8idx_options* o, fp8idx_plan* plan, int cu_entries = 0) {
+                           int32_t smem_limit, const fp8idx_options* o, fp8idx_plan* plan, int cu_entries = 0,
+                           int min_stages = 2) {
   if (!prefill_supported(heads, head_dim))
     return fail(FP8IDX_ERR_UNSUPPORTED, "prefill: heads=%d head_dim=%d not supported", heads, head_dim);
   if (rows < 0 || cols < 0 || rows * heads >= (1ll << 31) || cols >= (1ll << 31))
@@ -234,7 +235,10 @@ fp8idx_status plan_prefill(int64_t rows, int64_t cols, int32_t heads, int32_t he
     return fail(FP8IDX_ERR_UNSUPPORTED, "prefill: block_m %d too large for %d heads", block_m, heads);
   const int n_cols = block_m * heads;
   int stages = (o && o->stages > 0) ? o->stages : 12;
-  while (stages > 2 && (int)prefill_smem_layout(n_cols, stages, cu_entries, head_dim).total > smem_limit) --stages;
+  while (stages > min_stages && (int)prefill_smem_layout(n_cols, stages, cu_entries, head_dim).total > smem_limit)
+    --stages;
+  if (stages < min_stages)
+    return fail(FP8IDX_ERR_UNSUPPORTED, "prefill: %d stages (this K source needs at least %d)", stages, min_stages);
   if ((int)prefill_smem_layout(n_cols, stages, cu_entries, head_dim).total > smem_limit)
     return fail(FP8IDX_ERR_UNSUPPORTED, "prefill: shared memory too small");
   const int64_t num_rb = (rows + block_m - 1) / block_m;
@@ -396,11 +400,12 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const PrefillK& src, const fp
     if (!contiguous(src.kv) || !contiguous(src.cu)) return fail(FP8IDX_ERR_INVALID, "kv_cache and cu_seq_lens must be contiguous");
     if (src.bt->shape[1] > 1 && src.bt->stride[1] != 1) return fail(FP8IDX_ERR_INVALID, "block_tables rows must be contiguous");
     if (src.cu->shape[0] != R + 1) return fail(FP8IDX_ERR_INVALID, "cu_seq_lens must be [requests + 1]");
-    if (D != kHeadDim) return fail(FP8IDX_ERR_UNSUPPORTED, "paged prefill: head_dim %lld (only 128)", (long long)D);
+    if (D != kHeadDim && D != 64)
+      return fail(FP8IDX_ERR_UNSUPPORTED, "paged prefill: head_dim %lld (128 or 64)", (long long)D);
     if (src.kv->shape[1] % (D + 4) != 0) return fail(FP8IDX_ERR_INVALID, "kv_cache rows must be block_size*(head_dim+4) bytes");
     blk = src.kv->shape[1] / (D + 4);
-    if (blk != 16 && blk != 32 && blk != 64 && blk != 128)
-      return fail(FP8IDX_ERR_UNSUPPORTED, "paged prefill: block_size %lld not in {16, 32, 64, 128}", (long long)blk);
+    if (blk != 1 && blk != 16 && blk != 32 && blk != 64 && blk != 128)
+      return fail(FP8IDX_ERR_UNSUPPORTED, "paged prefill: block_size %lld not in {1, 16, 32, 64, 128}", (long long)blk);
     if (R < 1 || R > kMaxBatch) return fail(FP8IDX_ERR_UNSUPPORTED, "paged prefill: %lld requests (1..%d)", (long long)R, kMaxBatch);
     if (src.bt->shape[1] < 1 || src.kv->shape[0] < 1) return fail(FP8IDX_ERR_INVALID, "empty block table or cache");
     if (!aligned16(src.kv->data)) return fail(FP8IDX_ERR_INVALID, "kv_cache must be 16-byte aligned");
@@ -419,7 +424,9 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const PrefillK& src, const fp
   DeviceInfo dev;
   TRY(device_info(&dev));
   fp8idx_plan plan;
-  TRY(plan_prefill(M, N, (int)H, (int)D, dev.sms, dev.smem_optin, opts, &plan, paged ? 2 * ((int)R + 1) : 0));
+  // the block-size-1 token gather publishes tiles 4 behind: at least 6 stages
+  TRY(plan_prefill(M, N, (int)H, (int)D, dev.sms, dev.smem_optin, opts, &plan, paged ? 2 * ((int)R + 1) : 0,
+                   (paged && blk == 1) ? 6 : 2));
   CUtensorMap tm_q, tm_k, tm_s;
   {
     const uint64_t dims[2] = {(uint64_t)D, (uint64_t)(M * H)};
@@ -430,13 +437,13 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const PrefillK& src, const fp
   }
   std::memset(&tm_k, 0, sizeof(tm_k));
   std::memset(&tm_s, 0, sizeof(tm_s));
-  if (paged) {
-    // K rows of the cache: [block][row][128 B]; scales: [block][blk f32] after the block's K rows
+  if (paged && blk > 1) {  // (block size 1 is gathered per token with cp.async: no tensor maps)
+    // K rows of the cache: [block][row][D bytes]; scales: [block][blk f32] after the block's K rows
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)blk, (uint64_t)src.kv->shape[0]};
     const uint64_t strides[2] = {(uint64_t)D, (uint64_t)src.kv->shape[1]};
     const uint32_t box[3] = {(uint32_t)D, (uint32_t)blk, 1u};
     TRY(encode(&tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, src.kv->data, dims, strides, box,
-               CU_TENSOR_MAP_SWIZZLE_128B, "kv_cache"));
+               D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, "kv_cache"));
     if (blk >= 32) {
       const uint64_t sdims[2] = {(uint64_t)blk, (uint64_t)src.kv->shape[0]};
       const uint64_t sstrides[1] = {(uint64_t)src.kv->shape[1]};
@@ -444,7 +451,7 @@ fp8idx_status prefill_impl(const fp8idx_tensor* q, const PrefillK& src, const fp
       TRY(encode(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, static_cast<const uint8_t*>(src.kv->data) + blk * D,
                  sdims, sstrides, sbox, CU_TENSOR_MAP_SWIZZLE_NONE, "kv_cache scales"));
     }
-  } else {
+  } else if (!paged) {
     {
       const uint64_t dims[2] = {(uint64_t)D, (uint64_t)N};
       const uint64_t strides[1] = {(uint64_t)D};

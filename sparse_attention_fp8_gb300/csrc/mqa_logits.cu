@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
   const int BM = p.block_m;
   const int AB = p.acc_bufs;
   const uint32_t acc_cols = kTmemCols / AB;
-  static_assert(DIM == 128 || (DIM == 64 && !PAGED), "head_dim 128, or 64 with contiguous K");
+  static_assert(DIM == 128 || DIM == 64, "head_dim 128 or 64");
   constexpr int kRow = DIM;                        // bytes per Q/K row
   constexpr int kTileB = kTileTokens * DIM;        // bytes per K tile
   const PrefillSmem L = prefill_smem_layout(N, S, PAGED ? 2 * (p.n_req + 1) : 0, DIM);
@@ -160,7 +160,8 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
   if (threadIdx.x == 0) {
     misc[1] = 0u;
     for (int s = 0; s < S; ++s) {
-      ptx::mbar_init(full0 + 8u * s, 1u);
+      // TMA: one arrive with the byte count; token gather: every producer lane
+      ptx::mbar_init(full0 + 8u * s, (PAGED && p.block_size == 1) ? 32u : 1u);
       ptx::mbar_init(empty0 + 8u * s, 1u + 4u);  // MMA commit + the 4 warps that read the tile's scales
     }
     for (int g = 0; g < AB; ++g) {
@@ -241,8 +242,30 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
     Ring qr{0u, 0u, 2u};
     int issued = 0, q_issued = 0;
     bool ok = true;
+    // Block size 1 (paged K as co-packed DIM+4-byte token rows, only 4-byte
+    // aligned, so no TMA or 16-byte copy fits): the warp gathers each tile's
+    // tokens with 4-byte cp.async into the swizzled layout the MMA reads
+    // (128-byte swizzle: 16-byte chunk c of row j at chunk c ^ (j & 7);
+    // 64-byte swizzle: c ^ ((j >> 1) & 3)), and publishes a tile kLag tiles
+    // after issuing it (every lane arrives once its copies have landed).
+    constexpr int kLag = 4;
+    const bool gather = PAGED && p.block_size == 1;
+    int pending = 0;
+    Ring pub{0u, 0u, static_cast<uint32_t>(S)};
+    const auto publish_all = [&]() {
+      ptx::cp_async_wait<0>();
+      ptx::fence_proxy_async_smem();
+      for (; pending > 0; --pending) {
+        ptx::mbar_arrive(full0 + 8u * pub.idx);
+        pub.next();
+      }
+    };
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const Unit U = load_unit(p, u, num_rb, n_tiles, ucu, utp);
+      // The Q buffer is freed once the MMA has consumed the unit before the
+      // previous one, whose last tiles may still be unpublished.
+      if (gather && pending > 0 && !__all_sync(0xffffffffu, ptx::mbar_test_wait(qe0 + 8u * qr.idx, qr.phase ^ 1u)))
+        publish_all();
       if (!(ok = warp_wait_bounded(qe0 + 8u * qr.idx, qr.phase ^ 1u, abort_flag, &g_prefill_watchdog,
                                    kSiteQEmpty)))
         break;
@@ -264,6 +287,63 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
             ptx::mbar_arrive_expect_tx(full, kTileB + kTileTokens * 4);
             ptx::tma_load_2d(ptx::smem_u32(k_s + st.idx * kTileB), &tm_k, full, 0, j * kTileTokens);
             ptx::tma_load_1d(ptx::smem_u32(sc_s + st.idx * kTileTokens), &tm_s, full, j * kTileTokens);
+          }
+        } else if (gather) {
+          // Padded tile j: request r's tokens [128t, 128t + 128); token i's
+          // row is block_tables[r][i] (tokens past the request read row 0,
+          // in bounds, and are never stored).
+          const int r = upper_index(tp_s, p.n_req, j);
+          const int t = j - tp_s[r];
+          const int len = cu_s[r + 1] - cu_s[r];
+          const int32_t* bt_row = p.block_tables + static_cast<int64_t>(r) * p.bt_stride;
+          const uint8_t* src[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int tok = t * kTileTokens + 32 * q + lane;
+            int32_t slot = tok < len ? __ldg(bt_row + min(tok, p.max_blocks - 1)) : 0;
+            slot = slot < 0 ? 0 : (slot >= p.num_blocks ? static_cast<int32_t>(p.num_blocks - 1) : slot);
+            src[q] = p.kv_cache + static_cast<int64_t>(slot) * (DIM + 4);
+          }
+          const uint32_t tile_s = ptx::smem_u32(k_s + st.idx * kTileB);
+          if constexpr (DIM == 128) {
+            const uint32_t chunk = static_cast<uint32_t>(lane >> 2), inner = static_cast<uint32_t>(lane & 3) * 4u;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+#pragma unroll 8
+              for (int i = 0; i < 32; ++i) {
+                const int row = 32 * q + i;
+                const uint8_t* rp = reinterpret_cast<const uint8_t*>(
+                    __shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(src[q]), i));
+                ptx::cp_async_4(tile_s + row * DIM + (((chunk ^ static_cast<uint32_t>(row & 7)) << 4) | inner),
+                                rp + lane * 4);
+              }
+            }
+          } else {
+            // 64-byte rows: lanes 0-15 copy token `row`, lanes 16-31 token row + 1
+            const int hi = lane >> 4, l16 = lane & 15;
+            const uint32_t chunk = static_cast<uint32_t>(l16 >> 2), inner = static_cast<uint32_t>(l16 & 3) * 4u;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+#pragma unroll 8
+              for (int i = 0; i < 32; i += 2) {
+                const int row = 32 * q + i + hi;
+                const uint8_t* rp = reinterpret_cast<const uint8_t*>(
+                    __shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(src[q]), i + hi));
+                ptx::cp_async_4(tile_s + row * DIM + (((chunk ^ static_cast<uint32_t>((row >> 1) & 3)) << 4) | inner),
+                                rp + l16 * 4);
+              }
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            ptx::cp_async_4(ptx::smem_u32(sc_s + st.idx * kTileTokens + 32 * q + lane), src[q] + DIM);
+          ptx::cp_async_commit();
+          if (++pending > kLag) {  // the tile issued kLag tiles ago has landed
+            ptx::cp_async_wait<kLag>();
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(full0 + 8u * pub.idx);
+            pub.next();
+            --pending;
           }
         } else {
           // Padded tile j: request r's tokens [128t, 128t + 128), whole cache
@@ -297,8 +377,9 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
         ++issued;
       }
     }
+    if (gather) publish_all();  // (copies land before the CTA exits, abort or not)
     if (*abort_flag && lane == 0) {
-      for (int c = max(0, issued - S); c < issued; ++c)
+      for (int c = max(0, issued - S); c < issued && !gather; ++c)
         wait_drain(full0 + 8u * (c % S), (c / S) & 1, &g_prefill_watchdog);
       for (int sg = max(0, q_issued - 2); sg < q_issued; ++sg)
         wait_drain(qf0 + 8u * (sg & 1), (sg >> 1) & 1, &g_prefill_watchdog);
@@ -524,10 +605,10 @@ cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, con
     if (heads == 32) kern = paged ? mqa_logits_kernel<32, true, 128> : mqa_logits_kernel<32, false, 128>;
     else if (heads == 64) kern = paged ? mqa_logits_kernel<64, true, 128> : mqa_logits_kernel<64, false, 128>;
     else if (heads == 128) kern = paged ? mqa_logits_kernel<128, true, 128> : mqa_logits_kernel<128, false, 128>;
-  } else if (head_dim == 64 && !paged) {
-    if (heads == 32) kern = mqa_logits_kernel<32, false, 64>;
-    else if (heads == 64) kern = mqa_logits_kernel<64, false, 64>;
-    else if (heads == 128) kern = mqa_logits_kernel<128, false, 64>;
+  } else if (head_dim == 64) {
+    if (heads == 32) kern = paged ? mqa_logits_kernel<32, true, 64> : mqa_logits_kernel<32, false, 64>;
+    else if (heads == 64) kern = paged ? mqa_logits_kernel<64, true, 64> : mqa_logits_kernel<64, false, 64>;
+    else if (heads == 128) kern = paged ? mqa_logits_kernel<128, true, 64> : mqa_logits_kernel<128, false, 64>;
   }
   if (kern == nullptr) return cudaErrorInvalidValue;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem_bytes);

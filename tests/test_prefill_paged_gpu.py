@@ -32,14 +32,19 @@ def run_paged(fp8idx, case, clean_logits=True, options=None):
 
 
 def gathered(case):
-    return oracle.gather_paged_k(case.kv_cache, case.block_tables, case.cu_seq_lens, case.block_size)
+    return oracle.gather_paged_k(case.kv_cache, case.block_tables, case.cu_seq_lens, case.block_size,
+                                 dim=case.q.shape[2])
 
 
-@pytest.mark.parametrize("blk", [16, 32, 64, 128])
+@pytest.mark.parametrize("dim", [128, 64])
+@pytest.mark.parametrize("blk", [1, 16, 32, 64, 128])
 @pytest.mark.parametrize("heads", [32, 64])
-def test_paged_prefill_block_sizes(fp8idx, oracle_impl, blk, heads):
+def test_paged_prefill_block_sizes(fp8idx, oracle_impl, blk, heads, dim):
+    """Every block size (1: the co-packed cache, gathered per token) and both
+    head dims of the prefill sweep, against the oracle's own gather, and
+    bit-identical to the contiguous kernel on the gathered K."""
     case = workloads.paged_prefill_case([700, 0, 333, 1030, 5], [64, 0, 333, 100, 5], heads, block_size=blk,
-                                        seed=blk + heads, poison=True, extra_blocks=7)
+                                        dim=dim, seed=blk + heads + dim, poison=True, extra_blocks=7)
     k, s = gathered(case)
     ref = oracle_impl.mqa_logits(case.q, k, s, case.weights, case.ks, case.ke)
     gpu = run_paged(fp8idx, case)
@@ -106,11 +111,18 @@ def test_paged_prefill_errors(fp8idx):
         fp8idx.fp8_mqa_logits_paged(d["q"], d["kv_cache"], d["block_tables"], d["cu_seq_lens"][:1], d["weights"],
                                     d["ks"], d["ke"], out)
     assert e.value.status == fp8idx.FP8IDX_ERR_INVALID
+    blk8 = workloads.paged_prefill_case([10], [2], 32, block_size=8, seed=1)
+    d8 = to_device(blk8)
+    with pytest.raises(fp8idx.Fp8IdxError) as e:  # block size 8: not implemented
+        fp8idx.fp8_mqa_logits_paged(d8["q"], d8["kv_cache"], d8["block_tables"], d8["cu_seq_lens"], d8["weights"],
+                                    d8["ks"], d8["ke"], torch.empty((blk8.rows, blk8.cols), device="cuda"))
+    assert e.value.status == fp8idx.FP8IDX_ERR_UNSUPPORTED
     blk1 = workloads.paged_prefill_case([10], [2], 32, block_size=1, seed=1)
     d1 = to_device(blk1)
-    with pytest.raises(fp8idx.Fp8IdxError) as e:
+    with pytest.raises(fp8idx.Fp8IdxError) as e:  # the token gather needs at least 6 stages
         fp8idx.fp8_mqa_logits_paged(d1["q"], d1["kv_cache"], d1["block_tables"], d1["cu_seq_lens"], d1["weights"],
-                                    d1["ks"], d1["ke"], torch.empty((blk1.rows, blk1.cols), device="cuda"))
+                                    d1["ks"], d1["ke"], torch.empty((blk1.rows, blk1.cols), device="cuda"),
+                                    options=fp8idx.Options(stages=3))
     assert e.value.status == fp8idx.FP8IDX_ERR_UNSUPPORTED
 
 
@@ -136,3 +148,21 @@ def test_paged_prefill_offsets_past_n_stay_inside_out(fp8idx):
     assert np.isnan(host[:, n:]).all(), "a store landed past column N"
     assert not np.isnan(host[:, :n]).any(), "an element of [0, N) was left unwritten"
     assert fp8idx.device_status() == fp8idx.FP8IDX_OK
+
+
+@pytest.mark.parametrize("dim", [128, 64])
+def test_paged_prefill_block1_small_requests_and_overrides(fp8idx, oracle_impl, dim):
+    """Block size 1: tiles spanning many short requests, a unit count that
+    crosses the Q double buffer many times with one CTA, the minimum stage
+    count, and clean_logits off."""
+    rng = np.random.default_rng(5 + dim)
+    lens = rng.integers(0, 300, 30)
+    rows = np.minimum(lens, rng.integers(0, 9, 30))
+    case = workloads.paged_prefill_case(lens, rows, 32, block_size=1, dim=dim, seed=9, poison=True, extra_blocks=40)
+    k, s = gathered(case)
+    ref = oracle_impl.mqa_logits(case.q, k, s, case.weights, case.ks, case.ke)
+    for opts in (None, dict(num_ctas=1), dict(stages=6), dict(split_n=3, num_ctas=2)):
+        o = fp8idx.Options(**opts) if opts else None
+        assert_rows_close(run_paged(fp8idx, case, options=o), ref, what=f"blk1 d{dim} {opts}")
+    assert_rows_close(run_paged(fp8idx, case, clean_logits=False), ref, written=np.isfinite(ref),
+                      what=f"blk1 d{dim} no-clean")
