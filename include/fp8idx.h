@@ -38,6 +38,7 @@
 #ifndef FP8IDX_H_
 #define FP8IDX_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -279,6 +280,59 @@ fp8idx_status fp8_mqa_topk_ex(const fp8idx_tensor* logits,
                               const fp8idx_tensor* cu_seqlen_ke, int32_t k,
                               const fp8idx_tensor* indices,
                               const fp8idx_options* opts, void* stream);
+
+/*
+ * Fused decode logits + top-k: fp8_paged_mqa_topk.
+ * The decode logits of fp8_paged_mqa_logits followed by the selection of
+ * fp8_paged_topk on them (the index_topk step that follows the indexer on the
+ * pages: aiter PR 5047, section "GLM-5.2-MXFP4 E2E"; aiter issue 5477,
+ * section Measurement), computed without writing the logits of every row:
+ * indices[r] is exactly what fp8_paged_topk returns on the logits
+ * fp8_paged_mqa_logits writes (same window, tie rule, order and -1 padding).
+ *
+ * How: the decode kernel first runs on every 16th item (128 or 256 tokens)
+ * of each request, and each row's threshold is taken from that sample so
+ * that about 1.5k or more of the row's logits lie above it; a second pass of
+ * the decode kernel keeps, per row, only the logits above the threshold
+ * (up to fp8idx cap = min(4k + 1024, 8192) of them) and a bitmap of the
+ * positions equal to it; a per-row kernel then selects the k largest of
+ * those exactly.  A row whose candidates cannot be shown to contain its k
+ * largest (too few above the threshold, or more than the cap) is recomputed
+ * exactly instead: its request's logits are written to the workspace and
+ * the top-k kernel selects from them.  The result never depends on which
+ * path a row took.
+ *
+ *  q_fp8, kv_cache, weights, context_lens, block_tables, max_model_len
+ *               as for fp8_paged_mqa_logits (same support gate).
+ *  k            1 .. 2048.
+ *  indices      [batch*next_n, k] I32 output, stride[1] == 1.
+ *  workspace    device scratch of at least
+ *               fp8idx_paged_mqa_topk_workspace(batch, next_n,
+ *               max_model_len, k) bytes, 256-byte aligned, owned by the
+ *               caller; its contents on entry do not matter and are
+ *               overwritten.  Two calls in flight at once need two
+ *               workspaces.  (It holds one f32 row per output row for the
+ *               sample and the fallback, so it is about the size of the
+ *               logits fp8_paged_mqa_logits would write.)
+ *  opts         as for fp8_paged_mqa_logits_ex (NULL = heuristic).
+ * Six kernels are enqueued on `stream`; no host synchronisation.  Returns
+ * FP8IDX_OK, FP8IDX_ERR_INVALID (bad arguments, workspace too small or
+ * misaligned), FP8IDX_ERR_UNSUPPORTED or FP8IDX_ERR_CUDA.
+ */
+fp8idx_status fp8_paged_mqa_topk(const fp8idx_tensor* q_fp8,
+                                 const fp8idx_tensor* kv_cache,
+                                 const fp8idx_tensor* weights,
+                                 const fp8idx_tensor* context_lens,
+                                 const fp8idx_tensor* block_tables,
+                                 int32_t max_model_len, int32_t k,
+                                 const fp8idx_tensor* indices, void* workspace,
+                                 size_t workspace_bytes,
+                                 const fp8idx_options* opts, void* stream);
+
+/* Bytes of workspace fp8_paged_mqa_topk needs (0 for invalid arguments).
+ * Pure host function. */
+size_t fp8idx_paged_mqa_topk_workspace(int64_t batch, int32_t next_n,
+                                       int32_t max_model_len, int32_t k);
 
 /* Support gates, after the pages' is_supported(num_heads, head_dim,
  * kv_block_size) (aiter PR 5047, Technical Details) and is_supported(

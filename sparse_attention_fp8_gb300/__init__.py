@@ -19,6 +19,8 @@ Entry points (same names as the C ABI):
   fp8_paged_topk(logits, context_lens, next_n, max_model_len, k, indices,
                  stream=None)
   fp8_mqa_topk(logits, cu_seqlen_ks, cu_seqlen_ke, k, indices, stream=None)
+  fp8_paged_mqa_topk(q_fp8, kv_cache, weights, context_lens, block_tables,
+                     max_model_len, k, indices, workspace=None, stream=None)
 """
 from ._native import (  # noqa: F401
     FP8IDX_ERR_CUDA,
@@ -35,10 +37,12 @@ from ._native import (  # noqa: F401
     fp8_mqa_logits_paged,
     fp8_mqa_topk,
     fp8_paged_mqa_logits,
+    fp8_paged_mqa_topk,
     fp8_paged_topk,
     is_supported,
     library,
     library_path,
+    paged_mqa_topk_workspace,
     paged_is_supported,
     plan_paged,
     plan_prefill,

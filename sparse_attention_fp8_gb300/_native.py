@@ -100,6 +100,12 @@ def library():
             lib.fp8_mqa_topk.argtypes = [T, T, T, ctypes.c_int32, T, V]
             lib.fp8_paged_topk_ex.argtypes = [T, T, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, T, P(_Options), V]
             lib.fp8_mqa_topk_ex.argtypes = [T, T, T, ctypes.c_int32, T, P(_Options), V]
+            lib.fp8_paged_mqa_topk.argtypes = [T, T, T, T, T, ctypes.c_int32, ctypes.c_int32, T, V,
+                                               ctypes.c_size_t, P(_Options), V]
+            lib.fp8_paged_mqa_topk.restype = ctypes.c_int
+            lib.fp8idx_paged_mqa_topk_workspace.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                                            ctypes.c_int32]
+            lib.fp8idx_paged_mqa_topk_workspace.restype = ctypes.c_size_t
             for f in ("fp8_paged_mqa_logits", "fp8_paged_mqa_logits_ex", "fp8_mqa_logits", "fp8_mqa_logits_ex",
                       "fp8_mqa_logits_paged", "fp8_paged_topk", "fp8_mqa_topk", "fp8_paged_topk_ex",
                       "fp8_mqa_topk_ex"):
@@ -242,6 +248,35 @@ def fp8_mqa_topk(logits, cu_seqlen_ks, cu_seqlen_ke, k, indices, stream=None, ct
     oc = Options(num_ctas=int(ctas_per_row))._c()
     _check(lib.fp8_mqa_topk_ex(ctypes.byref(lg), ctypes.byref(a), ctypes.byref(b), int(k), ctypes.byref(ix),
                                ctypes.byref(oc), _stream(stream, logits)))
+    return indices
+
+
+def paged_mqa_topk_workspace(batch, next_n, max_model_len, k) -> int:
+    """Bytes of workspace fp8_paged_mqa_topk needs."""
+    return int(library().fp8idx_paged_mqa_topk_workspace(int(batch), int(next_n), int(max_model_len), int(k)))
+
+
+def fp8_paged_mqa_topk(q_fp8, kv_cache, weights, context_lens, block_tables, max_model_len, k, indices,
+                       workspace=None, stream=None, options: Options | None = None):
+    """Decode logits and their per-row top-k in one call (the logits of every
+    row are never written): indices [batch*next_n, k] as fp8_paged_topk gives
+    on the decode logits.  workspace: a uint8 CUDA tensor of at least
+    paged_mqa_topk_workspace(...) bytes (allocated here if None)."""
+    import torch
+    lib = library()
+    B, n = q_fp8.shape[0], q_fp8.shape[1]
+    need = paged_mqa_topk_workspace(B, n, max_model_len, k)
+    if workspace is None:
+        workspace = torch.empty(need + 256, dtype=torch.uint8, device=q_fp8.device)
+    base = workspace.data_ptr()
+    off = (-base) % 256
+    args = [_desc(q_fp8), _desc(kv_cache), _desc(weights), _desc(context_lens), _desc(block_tables)]
+    ix = _desc(indices)
+    oc = options._c() if options is not None else None
+    st = lib.fp8_paged_mqa_topk(*[ctypes.byref(a) for a in args], int(max_model_len), int(k), ctypes.byref(ix),
+                                ctypes.c_void_p(base + off), ctypes.c_size_t(workspace.numel() - off),
+                                ctypes.byref(oc) if oc is not None else None, _stream(stream, q_fp8))
+    _check(st)
     return indices
 
 

@@ -273,16 +273,24 @@ fp8idx_status plan_prefill(int64_t rows, int64_t cols, int32_t heads, int32_t he
 }
 
 // ----------------------------------------------------------------- decode
-fp8idx_status paged_impl(const fp8idx_tensor* q, const fp8idx_tensor* kv, const fp8idx_tensor* w,
-                         const fp8idx_tensor* cl, const fp8idx_tensor* bt, int32_t max_model_len,
-                         const fp8idx_tensor* out, const fp8idx_options* opts, void* stream) {
-  g_last_error.clear();
+// Everything a decode launch needs except its output: the inputs checked,
+// the plan, the tensor maps and the parameter block.
+struct PagedSetup {
+  CUtensorMap tm_q, tm_kv, tm_sc;
+  PagedParams p;
+  fp8idx_plan plan;
+  int heads = 0;
+  bool empty = false;  // nothing to compute (no requests or max_model_len 0)
+};
+
+fp8idx_status paged_setup(const fp8idx_tensor* q, const fp8idx_tensor* kv, const fp8idx_tensor* w,
+                          const fp8idx_tensor* cl, const fp8idx_tensor* bt, int32_t max_model_len,
+                          const fp8idx_options* opts, PagedSetup* S) {
   TRY(check_tensor(q, "q_fp8", FP8IDX_U8, 4));
   TRY(check_tensor(kv, "kv_cache", FP8IDX_U8, 2));
   TRY(check_tensor(w, "weights", FP8IDX_F32, 2));
   TRY(check_tensor(cl, "context_lens", FP8IDX_I32, 1));
   TRY(check_tensor(bt, "block_tables", FP8IDX_I32, 2));
-  TRY(check_tensor(out, "out", FP8IDX_F32, 2));
   const int64_t B = q->shape[0], next_n = q->shape[1], H = q->shape[2], D = q->shape[3];
   if (max_model_len < 0) return fail(FP8IDX_ERR_INVALID, "max_model_len < 0");
   if (!contiguous(q)) return fail(FP8IDX_ERR_INVALID, "q_fp8 must be contiguous");
@@ -292,16 +300,14 @@ fp8idx_status paged_impl(const fp8idx_tensor* q, const fp8idx_tensor* kv, const 
   if (w->shape[0] != B * next_n || w->shape[1] != H) return fail(FP8IDX_ERR_INVALID, "weights must be [batch*next_n, heads]");
   if (bt->shape[0] != B || (bt->shape[1] > 1 && bt->stride[1] != 1) || (B > 1 && bt->stride[0] < bt->shape[1]))
     return fail(FP8IDX_ERR_INVALID, "block_tables must be [batch, max_blocks] with unit inner stride");
-  if (out->shape[0] != B * next_n || out->shape[1] < max_model_len ||
-      (out->shape[1] > 1 && out->stride[1] != 1) || (out->shape[0] > 1 && out->stride[0] < out->shape[1]))
-    return fail(FP8IDX_ERR_INVALID, "out must be [batch*next_n, >=max_model_len] with unit inner stride");
   if (D <= 0 || kv->shape[1] % (D + 4) != 0) return fail(FP8IDX_ERR_INVALID, "kv_cache row is not block_size*(head_dim+4) bytes");
   const int64_t blk = kv->shape[1] / (D + 4);
   if (next_n <= 0 || H <= 0 || blk <= 0) return fail(FP8IDX_ERR_INVALID, "empty next_n/heads/block_size");
   if (!paged_supported((int)H, (int)D, (int)blk, (int)next_n))
     return fail(FP8IDX_ERR_UNSUPPORTED, "decode: heads=%lld head_dim=%lld block_size=%lld next_n=%lld not supported",
                 (long long)H, (long long)D, (long long)blk, (long long)next_n);
-  if (B == 0 || max_model_len == 0) return ok();
+  S->empty = B == 0 || max_model_len == 0;
+  if (S->empty) return ok();
   if (kv->shape[0] < 1) return fail(FP8IDX_ERR_INVALID, "kv_cache has no blocks");
   if (bt->shape[1] < 1) return fail(FP8IDX_ERR_INVALID, "block_tables has no columns");
   if (!aligned16(q->data) || !aligned16(kv->data) || !aligned16(w->data))
@@ -311,40 +317,40 @@ fp8idx_status paged_impl(const fp8idx_tensor* q, const fp8idx_tensor* kv, const 
 
   DeviceInfo dev;
   TRY(device_info(&dev));
-  fp8idx_plan plan;
+  fp8idx_plan& plan = S->plan;
   TRY(plan_paged((int)B, (int)next_n, (int)H, (int)D, (int)blk, max_model_len, dev.sms, dev.smem_optin, opts, &plan));
 
   const int n_cols = (int)(next_n * H);
-  CUtensorMap tm_q, tm_kv, tm_sc;
   {
     const uint64_t dims[2] = {(uint64_t)D, (uint64_t)(B * n_cols)};
     const uint64_t strides[1] = {(uint64_t)D};
     const uint32_t box[2] = {(uint32_t)D, (uint32_t)n_cols};
-    TRY(encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q->data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "q"));
+    TRY(encode(&S->tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q->data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+               "q"));
   }
   if (!plan.gather) {
     // K rows: [block][row][128 B]; scales: [block][blk f32], starting after the block's K rows
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)blk, (uint64_t)kv->shape[0]};
     const uint64_t strides[2] = {(uint64_t)D, (uint64_t)kv->shape[1]};
     const uint32_t box[3] = {(uint32_t)D, (uint32_t)blk, 1u};
-    TRY(encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, kv->data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+    TRY(encode(&S->tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, kv->data, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
                "kv_cache"));
     const uint64_t sdims[2] = {(uint64_t)blk, (uint64_t)kv->shape[0]};
     const uint64_t sstrides[1] = {(uint64_t)kv->shape[1]};
     const uint32_t sbox[2] = {(uint32_t)blk, 1u};
-    TRY(encode(&tm_sc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, static_cast<const uint8_t*>(kv->data) + blk * D, sdims,
+    TRY(encode(&S->tm_sc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, static_cast<const uint8_t*>(kv->data) + blk * D, sdims,
                sstrides, sbox, CU_TENSOR_MAP_SWIZZLE_NONE, "kv_cache scales"));
   } else {
-    tm_kv = tm_q;  // unused by the gather kernel
-    tm_sc = tm_q;
+    S->tm_kv = S->tm_q;  // unused by the gather kernel
+    S->tm_sc = S->tm_q;
   }
-  PagedParams p;
+  PagedParams& p = S->p;
+  std::memset(&p, 0, sizeof(p));
+  p.item_stride = 1;
   p.kv_cache = static_cast<const uint8_t*>(kv->data);
   p.weights = static_cast<const float*>(w->data);
   p.context_lens = static_cast<const int32_t*>(cl->data);
   p.block_tables = static_cast<const int32_t*>(bt->data);
-  p.out = static_cast<float*>(out->data);
-  p.out_stride = out->shape[0] > 1 ? out->stride[0] : out->shape[1];
   p.bt_stride = B > 1 ? bt->stride[0] : bt->shape[1];
   p.num_blocks = kv->shape[0];
   p.batch = (int32_t)B;
@@ -356,9 +362,165 @@ fp8idx_status paged_impl(const fp8idx_tensor* q, const fp8idx_tensor* kv, const 
   p.stages = plan.stages;
   p.sub_tiles = paged_sub_tiles(n_cols, plan.gather != 0);
   p.acc_bufs = paged_acc_buffers(n_cols, p.sub_tiles);
-  cudaError_t e = launch_paged(tm_q, tm_kv, tm_sc, p, (int)H, plan.gather != 0, plan.grid, plan.smem_bytes,
-                               static_cast<cudaStream_t>(stream));
+  S->heads = (int)H;
+  return ok();
+}
+
+fp8idx_status paged_launch(const PagedSetup& S, const PagedParams& p, bool filter, void* stream) {
+  cudaError_t e = launch_paged(S.tm_q, S.tm_kv, S.tm_sc, p, S.heads, S.plan.gather != 0, S.plan.grid,
+                               S.plan.smem_bytes, static_cast<cudaStream_t>(stream), filter);
   if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+fp8idx_status paged_impl(const fp8idx_tensor* q, const fp8idx_tensor* kv, const fp8idx_tensor* w,
+                         const fp8idx_tensor* cl, const fp8idx_tensor* bt, int32_t max_model_len,
+                         const fp8idx_tensor* out, const fp8idx_options* opts, void* stream) {
+  g_last_error.clear();
+  TRY(check_tensor(q, "q_fp8", FP8IDX_U8, 4));
+  TRY(check_tensor(kv, "kv_cache", FP8IDX_U8, 2));
+  TRY(check_tensor(w, "weights", FP8IDX_F32, 2));
+  TRY(check_tensor(cl, "context_lens", FP8IDX_I32, 1));
+  TRY(check_tensor(bt, "block_tables", FP8IDX_I32, 2));
+  TRY(check_tensor(out, "out", FP8IDX_F32, 2));
+  const int64_t B = q->shape[0], next_n = q->shape[1];
+  if (max_model_len < 0) return fail(FP8IDX_ERR_INVALID, "max_model_len < 0");
+  if (out->shape[0] != B * next_n || out->shape[1] < max_model_len ||
+      (out->shape[1] > 1 && out->stride[1] != 1) || (out->shape[0] > 1 && out->stride[0] < out->shape[1]))
+    return fail(FP8IDX_ERR_INVALID, "out must be [batch*next_n, >=max_model_len] with unit inner stride");
+  PagedSetup S;
+  TRY(paged_setup(q, kv, w, cl, bt, max_model_len, opts, &S));
+  if (S.empty) return ok();
+  PagedParams p = S.p;
+  p.out = static_cast<float*>(out->data);
+  p.out_stride = out->shape[0] > 1 ? out->stride[0] : out->shape[1];
+  return paged_launch(S, p, false, stream);
+}
+
+// ----------------------------------------------------- fused decode top-k
+// fp8_paged_mqa_topk: six launches on the caller's stream, none of which
+// writes the logits of every row:
+//   1. the decode kernel on every 16th item of each request, its logits into
+//      the workspace (the threshold sample);
+//   2. per row: reset of the row's state, the threshold;
+//   3. the decode kernel in its filter form: per row the logits above the
+//      threshold (and the positions equal to it) instead of the logits;
+//   4. per row: the exact top-k from the candidates, or the row flagged;
+//   5. the decode kernel over the flagged requests only, all their logits
+//      into the workspace, and 6. the top-k kernel over the flagged rows --
+//      both return at once when no row was flagged.
+size_t paged_topk_workspace(int64_t batch, int64_t next_n, int64_t max_model_len, int32_t k) {
+  return static_cast<size_t>(fused_topk_layout(batch, next_n, max_model_len, k).total);
+}
+
+fp8idx_status paged_topk_impl(const fp8idx_tensor* q, const fp8idx_tensor* kv, const fp8idx_tensor* w,
+                              const fp8idx_tensor* cl, const fp8idx_tensor* bt, int32_t max_model_len, int32_t k,
+                              const fp8idx_tensor* indices, void* workspace, size_t workspace_bytes,
+                              const fp8idx_options* opts, void* stream) {
+  g_last_error.clear();
+  TRY(check_tensor(q, "q_fp8", FP8IDX_U8, 4));
+  TRY(check_tensor(indices, "indices", FP8IDX_I32, 2));
+  const int64_t B = q->shape[0], next_n = q->shape[1], R = B * next_n;
+  if (k < 1 || k > kTopkMaxK) return fail(FP8IDX_ERR_UNSUPPORTED, "top-k: k=%d not in [1, %d]", k, kTopkMaxK);
+  if (max_model_len < 0) return fail(FP8IDX_ERR_INVALID, "max_model_len < 0");
+  if (indices->shape[0] != R || indices->shape[1] != k || (k > 1 && indices->stride[1] != 1) ||
+      (R > 1 && indices->stride[0] < k))
+    return fail(FP8IDX_ERR_INVALID, "indices must be [batch*next_n, k] with unit inner stride");
+  PagedSetup S;
+  TRY(paged_setup(q, kv, w, cl, bt, max_model_len, opts, &S));
+  if (R == 0) return ok();
+  const FusedTopkLayout L = fused_topk_layout(B, next_n, max_model_len, k);
+  if (workspace == nullptr || workspace_bytes < L.total)
+    return fail(FP8IDX_ERR_INVALID, "workspace of %zu bytes, %llu needed (fp8idx_paged_mqa_topk_workspace)",
+                workspace_bytes, (unsigned long long)L.total);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(FP8IDX_ERR_INVALID, "workspace must be 256-byte aligned");
+  if (R >= (1ll << 31) / kTopkMaxCluster) return fail(FP8IDX_ERR_UNSUPPORTED, "top-k: too many rows");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  FusedTopkParams f;
+  std::memset(&f, 0, sizeof(f));
+  f.context_lens = static_cast<const int32_t*>(cl->data);
+  f.rows = (int32_t)R;
+  f.next_n = (int32_t)next_n;
+  f.cols = max_model_len;
+  f.k = k;
+  f.cap = L.cap;
+  f.logits = reinterpret_cast<float*>(ws + L.logits);
+  f.ls = L.ls;
+  f.tw = L.tw;
+  f.thr = reinterpret_cast<float*>(ws + L.thr);
+  f.cnt = reinterpret_cast<uint32_t*>(ws + L.cnt);
+  f.cand_val = reinterpret_cast<const float*>(ws + L.cand_val);
+  f.cand_pos = reinterpret_cast<const int32_t*>(ws + L.cand_pos);
+  f.ties = reinterpret_cast<uint32_t*>(ws + L.ties);
+  f.req_flag = reinterpret_cast<uint32_t*>(ws + L.req_flag);
+  f.row_flag = reinterpret_cast<uint32_t*>(ws + L.row_flag);
+  f.any = reinterpret_cast<uint32_t*>(ws + L.any);
+  f.out = static_cast<int32_t*>(indices->data);
+  f.out_stride = R > 1 ? indices->stride[0] : k;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (S.empty) {  // max_model_len 0: every window is empty
+    f.item_tokens = kTileTokens;
+    cudaError_t e = launch_fused_threshold(f, 0, st);
+    if (e == cudaSuccess) e = launch_fused_select(f, fused_select_smem_bytes(), st);
+    if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "top-k launch: %s", cudaGetErrorString(e));
+    return ok();
+  }
+  f.item_tokens = kTileTokens * S.p.sub_tiles;
+
+  // 1. the sample
+  PagedParams p = S.p;
+  p.out = f.logits;
+  p.out_stride = L.ls;
+  p.item_stride = kFusedSampleStride;
+  TRY(paged_launch(S, p, false, stream));
+  // 2. thresholds
+  cudaError_t e = launch_fused_threshold(f, 0, st);
+  if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "top-k threshold launch: %s", cudaGetErrorString(e));
+  // 3. the filter pass
+  p = S.p;
+  p.out = f.logits;
+  p.out_stride = L.ls;
+  p.thr = f.thr;
+  p.cnt = f.cnt;
+  p.cand_val = reinterpret_cast<float*>(ws + L.cand_val);
+  p.cand_pos = reinterpret_cast<int32_t*>(ws + L.cand_pos);
+  p.ties = f.ties;
+  p.ties_stride = L.tw;
+  p.cap = L.cap;
+  TRY(paged_launch(S, p, true, stream));
+  // 4. the exact selection, or the row flagged
+  e = launch_fused_select(f, fused_select_smem_bytes(), st);
+  if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "top-k select launch: %s", cudaGetErrorString(e));
+  // 5. and 6. the exact fallback for flagged rows
+  p = S.p;
+  p.out = f.logits;
+  p.out_stride = L.ls;
+  p.req_mask = f.req_flag;
+  p.run_flag = f.any;
+  TRY(paged_launch(S, p, false, stream));
+  TopkParams tp;
+  std::memset(&tp, 0, sizeof(tp));
+  tp.mode = 1;
+  tp.k = k;
+  tp.rows = (int32_t)R;
+  tp.context_lens = f.context_lens;
+  tp.cols = max_model_len;
+  tp.next_n = (int32_t)next_n;
+  tp.logits = f.logits;
+  tp.stride = L.ls;
+  tp.out = f.out;
+  tp.out_stride = f.out_stride;
+  tp.vec_ok = 1;  // workspace rows are 16-byte aligned
+  tp.row_mask = f.row_flag;
+  tp.run_flag = f.any;
+  DeviceInfo dev;
+  TRY(device_info(&dev));
+  int cap = kTopkMaxCap;
+  while (cap > 1024 && (int)topk_smem_layout(cap).total > dev.smem_optin) cap >>= 1;
+  tp.cap = cap;
+  e = launch_topk(tp, 1, (int)topk_smem_layout(cap).total, st);
+  if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "top-k fallback launch: %s", cudaGetErrorString(e));
   return ok();
 }
 
@@ -641,6 +803,20 @@ fp8idx_status fp8_mqa_logits_paged(const fp8idx_tensor* q_fp8, const fp8idx_tens
   src.bt = block_tables;
   src.cu = cu_seq_lens;
   return prefill_impl(q_fp8, src, weights, cu_seqlen_ks, cu_seqlen_ke, out, opts, stream);
+}
+
+fp8idx_status fp8_paged_mqa_topk(const fp8idx_tensor* q_fp8, const fp8idx_tensor* kv_cache,
+                                 const fp8idx_tensor* weights, const fp8idx_tensor* context_lens,
+                                 const fp8idx_tensor* block_tables, int32_t max_model_len, int32_t k,
+                                 const fp8idx_tensor* indices, void* workspace, size_t workspace_bytes,
+                                 const fp8idx_options* opts, void* stream) {
+  return paged_topk_impl(q_fp8, kv_cache, weights, context_lens, block_tables, max_model_len, k, indices, workspace,
+                         workspace_bytes, opts, stream);
+}
+
+size_t fp8idx_paged_mqa_topk_workspace(int64_t batch, int32_t next_n, int32_t max_model_len, int32_t k) {
+  if (batch < 0 || next_n < 1 || max_model_len < 0 || k < 1 || k > kTopkMaxK) return 0;
+  return paged_topk_workspace(batch, next_n, max_model_len, k);
 }
 
 fp8idx_status fp8_paged_topk(const fp8idx_tensor* logits, const fp8idx_tensor* context_lens, int32_t next_n,

@@ -35,6 +35,20 @@ struct PagedParams {
   int32_t stages;
   int32_t acc_bufs;   // TMEM accumulator buffers: paged_acc_buffers(n_cols, sub_tiles)
   int32_t sub_tiles;  // 128-token MMA tiles per pipeline item (1 or 2)
+  // Fused top-k passes (all zero / null for a plain logits call):
+  int32_t item_stride;          // request r's items are its items 0, s, 2s, ...: a sample of its window (1: all)
+  const uint32_t* req_mask;     // requests with req_mask[b] == 0 get no items (null: every request)
+  const uint32_t* run_flag;     // if non-null and *run_flag == 0 the launch does nothing
+  // filter epilogue (the FILTER instance): row r's logits above thr[r] are
+  // appended to its candidate list, those equal to it set their bit in the
+  // row's tie bitmap
+  const float* thr;             // [rows]
+  uint32_t* cnt;                // [rows][2]: candidates appended (may exceed cap), unused
+  float* cand_val;              // [rows][cap]
+  int32_t* cand_pos;            // [rows][cap]
+  uint32_t* ties;               // [rows][ties_stride] bitmap over window positions
+  int64_t ties_stride;          // 32-bit words per row
+  int32_t cap;                  // candidate slots per row
 };
 
 // Two epilogue warpgroups take alternate tiles; tensor memory holds 2..16
@@ -155,7 +169,10 @@ struct TopkParams {
   int32_t mode;    // 0 prefill windows, 1 decode windows
   int32_t cap;     // candidates held in shared memory
   int32_t vec_ok;  // every row starts 16-byte aligned: float4 loads inside the windows
+  const uint32_t* row_mask;  // rows with row_mask[r] == 0 are skipped (null: every row)
+  const uint32_t* run_flag;  // if non-null and *run_flag == 0 the launch does nothing
 };
+
 constexpr int kTopkThreads = 512;
 constexpr int kTopkBins = 4096;  // 12-bit radix levels (the last level has 8 bits)
 constexpr int kTopkMaxK = 2048;
@@ -187,6 +204,71 @@ __host__ __device__ inline TopkLayout topk_smem_layout(int cap) {
   return L;
 }
 
+// ------------------------------------------------- fused decode top-k
+// Scratch of fp8_paged_mqa_topk (caller-provided workspace), per call:
+//   logits   [rows][ls] f32   sampled items, and whole rows of the requests that need the exact fallback
+//   thr      [rows] f32       each row's candidate threshold
+//   cnt      [rows][2] u32    candidates above the threshold (may exceed cap), spare
+//   cand_val [rows][cap] f32, cand_pos [rows][cap] i32
+//   ties     [rows][tw] u32   bitmap of window positions whose logit equals the threshold
+//   req_flag [batch] u32, row_flag [rows] u32, any [4] u32   rows left to the fallback
+struct FusedTopkLayout {
+  uint64_t logits, thr, cnt, cand_val, cand_pos, ties, req_flag, row_flag, any, total;
+  int64_t ls, tw;
+  int32_t cap;
+};
+constexpr int kFusedSampleStride = 16;  // the threshold sample: every 16th item of each request
+__host__ __device__ inline int32_t fused_topk_cap(int32_t k) {
+  const int32_t c = 4 * k + 1024;
+  return c < kTopkMaxCap ? c : kTopkMaxCap;
+}
+__host__ __device__ inline FusedTopkLayout fused_topk_layout(int64_t batch, int64_t next_n, int64_t max_model_len,
+                                                             int32_t k) {
+  FusedTopkLayout L;
+  const int64_t rows = batch * next_n;
+  L.ls = (max_model_len + 3) & ~static_cast<int64_t>(3);
+  L.tw = (((max_model_len + 31) / 32) + 3) & ~static_cast<int64_t>(3);
+  L.cap = fused_topk_cap(k);
+  uint64_t off = 0;
+  const auto take = [&](uint64_t bytes) {
+    const uint64_t at = off;
+    off = (off + bytes + 255u) & ~static_cast<uint64_t>(255u);
+    return at;
+  };
+  L.logits = take(static_cast<uint64_t>(rows) * L.ls * 4u);
+  L.thr = take(static_cast<uint64_t>(rows) * 4u);
+  L.cnt = take(static_cast<uint64_t>(rows) * 8u);
+  L.cand_val = take(static_cast<uint64_t>(rows) * L.cap * 4u);
+  L.cand_pos = take(static_cast<uint64_t>(rows) * L.cap * 4u);
+  L.ties = take(static_cast<uint64_t>(rows) * L.tw * 4u);
+  L.req_flag = take(static_cast<uint64_t>(batch) * 4u);
+  L.row_flag = take(static_cast<uint64_t>(rows) * 4u);
+  L.any = take(16u);
+  L.total = off;
+  return L;
+}
+// The per-row passes of the fused top-k around the decode kernel's sample and
+// filter passes: windows of the decode rows (as fp8_paged_topk), k, and the
+// workspace pointers.
+struct FusedTopkParams {
+  const int32_t* context_lens;
+  int32_t rows, next_n, cols, k;  // cols: max_model_len
+  int32_t item_tokens;            // tokens per item of the decode kernel (128 or 256)
+  int32_t cap;
+  float* logits;                  // workspace rows (stride ls)
+  int64_t ls, tw;
+  float* thr;
+  uint32_t* cnt;
+  const float* cand_val;
+  const int32_t* cand_pos;
+  uint32_t* ties;
+  uint32_t* req_flag;
+  uint32_t* row_flag;
+  uint32_t* any;
+  int32_t* out;                   // indices [rows][out_stride]
+  int64_t out_stride;
+};
+
 // Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
 // current device.  The attribute is set once per (kernel, device) and size
 // (cached on the host), not on every launch.
@@ -195,14 +277,26 @@ cudaError_t ensure_dynamic_smem(const void* kernel, int bytes);
 // ------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error.  The tensor maps are encoded
 // by the caller; `heads` selects the template instance.
+// filter: the FILTER instance (candidates and ties instead of stored logits)
 cudaError_t launch_paged(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const CUtensorMap& tm_sc,
-                         const PagedParams& p, int heads, bool gather, int grid, int smem_bytes, cudaStream_t stream);
+                         const PagedParams& p, int heads, bool gather, int grid, int smem_bytes, cudaStream_t stream,
+                         bool filter = false);
 cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_s,
                            const CUtensorMap& tm_w, const CUtensorMap& tm_out, const PrefillParams& p, int heads,
                            int head_dim, bool paged, int grid, int smem_bytes, cudaStream_t stream);
 
 // ctas: CTAs per row (1: one CTA per row; 2..kTopkMaxCluster: one cluster per row)
 cudaError_t launch_topk(const TopkParams& p, int ctas, int smem_bytes, cudaStream_t stream);
+// Fused decode top-k, per row: the threshold from the sampled logits (and
+// the workspace reset), then the exact selection from the candidates (or
+// the row handed to the fallback).  One CTA of kTopkThreads per row.
+cudaError_t launch_fused_threshold(const FusedTopkParams& p, int smem_bytes, cudaStream_t stream);
+// dynamic shared memory of the select kernel: histogram, candidate keys and
+// positions, the chosen positions (sort buffer), the tied positions
+__host__ __device__ constexpr int fused_select_smem_bytes() {
+  return 4 * kTopkBins + 4 * kTopkMaxCap + 4 * kTopkMaxCap + 4 * 2 * kTopkMaxK + 4 * kTopkMaxCap;
+}
+cudaError_t launch_fused_select(const FusedTopkParams& p, int smem_bytes, cudaStream_t stream);
 
 // Launches the watchdog self-test kernel: a bounded wait that nothing
 // satisfies, given up after limit_ns (sets the decode word's self-test bit).

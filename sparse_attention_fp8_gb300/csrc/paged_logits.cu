@@ -99,10 +99,12 @@ __device__ __forceinline__ int32_t clamp_block(int32_t v, int64_t num_blocks) {
 
 }  // namespace
 
-template <int HEADS, bool GATHER>
+template <int HEADS, bool GATHER, bool FILTER>
 __global__ void __launch_bounds__(paged_threads(GATHER), 1)
     paged_logits_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                         const __grid_constant__ CUtensorMap tm_sc, const PagedParams p) {
+  // a launch that is only needed when an earlier one raised the flag
+  if (p.run_flag != nullptr && __ldg(p.run_flag) == 0u) return;
   constexpr int kProdWarps = paged_producer_warps(GATHER);
   constexpr int kMmaWarp = kProdWarps;
   constexpr int kEpiWarp0 = kMmaWarp + 1;
@@ -142,9 +144,12 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
   const int lane = threadIdx.x & 31;
 
   // ---- prologue: per-request tile counts, barriers, tensor memory --------
+  const int IS = p.item_stride;  // items 0, IS, 2*IS, ... of every request (IS > 1: a sample)
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
-    const int64_t c = clamp_ctx(__ldg(p.context_lens + b), p);
-    tp[b + 1] = static_cast<int32_t>((c + ITEM - 1) / ITEM);
+    const bool on = p.req_mask == nullptr || __ldg(p.req_mask + b) != 0u;
+    const int64_t c = on ? clamp_ctx(__ldg(p.context_lens + b), p) : 0;
+    const int64_t items = (c + ITEM - 1) / ITEM;
+    tp[b + 1] = static_cast<int32_t>((items + IS - 1) / IS);
   }
   if (threadIdx.x == 0) {
     tp[0] = 0;
@@ -235,16 +240,19 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
           }
           ctx_eff = clamp_ctx(__ldg(p.context_lens + cur.b), p);
           need_blocks = static_cast<int>((ctx_eff + blk - 1) / blk);
-          chunk = (cur.t * P) & ~31;
+        }
+        const int rt = cur.t * IS;  // the item's index in its request
+        const int first_blk = rt * P;
+        if (it == 0 || cur.t == 0 || IS > 1) {  // (a sample jumps: reload the item's 32-block chunk)
+          chunk = first_blk & ~31;
           tbl_cur = load_table(p, cur.b, chunk + lane, need_blocks);
           tbl_nxt = load_table(p, cur.b, chunk + 32 + lane, need_blocks);
         }
-        const int first_blk = cur.t * P;
         const int32_t id = __shfl_sync(0xffffffffu, tbl_cur, (first_blk - chunk + lane) & 31);
         if ((it & 1) == pw) {
         if (!warp_wait_bounded(empty0 + 8u * st.idx, st.phase ^ 1u, abort_flag, &g_paged_watchdog, kSiteStageEmpty))
           break;
-        const int valid = min(ITEM, static_cast<int>(ctx_eff - static_cast<int64_t>(cur.t) * ITEM));
+        const int valid = min(ITEM, static_cast<int>(ctx_eff - static_cast<int64_t>(rt) * ITEM));
         const int nblk = (valid + blk - 1) / blk;
         const uint32_t full = full0 + 8u * st.idx;
         if (lane == 0) ptx::mbar_arrive_expect_tx(full, nblk * blk_bytes);
@@ -325,12 +333,12 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
           qr.next();
           ++q_issued;
           ctx_eff = clamp_ctx(__ldg(p.context_lens + cur.b), p);
-          const int64_t t0 = static_cast<int64_t>(cur.t) * kTileTokens + pw * 64 + lane;
+          const int64_t t0 = static_cast<int64_t>(cur.t) * IS * kTileTokens + pw * 64 + lane;
           src_a = row_addr(load_table(p, cur.b, t0, ctx_eff));
           src_b = row_addr(load_table(p, cur.b, t0 + 32, ctx_eff));
         }
         if (cur.t + 1 < cur.tiles_b) {  // prefetch the next tile's rows (same request only)
-          const int64_t t1 = static_cast<int64_t>(cur.t + 1) * kTileTokens + pw * 64 + lane;
+          const int64_t t1 = static_cast<int64_t>(cur.t + 1) * IS * kTileTokens + pw * 64 + lane;
           nxt_a = row_addr(load_table(p, cur.b, t1, ctx_eff));
           nxt_b = row_addr(load_table(p, cur.b, t1 + 32, ctx_eff));
         }
@@ -433,6 +441,7 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
       Ring qr{0u, 0u, 2u};
       int32_t ctx = 0;
       const float* w = w_s;
+      float thr_n[8];  // (FILTER) the thresholds of the current request's rows
       for (int it = 0; it < n_items; ++it) {
         if (it == 0 || cur.t == 0) {
           if (!warp_wait_bounded(qf0 + 8u * qr.idx, qr.phase, abort_flag, &g_paged_watchdog, kSiteQFull)) break;
@@ -440,6 +449,11 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
           // the producers' clamped context: positions past what they loaded
           // are never stored, even for inputs that break the precondition
           ctx = static_cast<int32_t>(clamp_ctx(__ldg(p.context_lens + cur.b), p));
+          if constexpr (FILTER) {
+#pragma unroll
+            for (int n = 0; n < 8; ++n)
+              thr_n[n] = n < next_n ? __ldg(p.thr + static_cast<int64_t>(cur.b) * next_n + n) : 0.f;
+          }
         }
         if (kShared || (it & 1) == grp) {
           if (!warp_wait_bounded(full0 + 8u * st.idx, st.phase, abort_flag, &g_paged_watchdog, kSiteStageFull))
@@ -449,7 +463,7 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
           if (lane == 0) ptx::mbar_arrive(empty0 + 8u * st.idx);
           if (!warp_wait_bounded(accf0 + 8u * ac.idx, ac.phase, abort_flag, &g_paged_watchdog, kSiteAccFull)) break;
           ptx::tc_fence_after();
-          const int64_t pos = static_cast<int64_t>(cur.t) * ITEM + k_tile * kTileTokens + row;
+          const int64_t pos = static_cast<int64_t>(cur.t) * IS * ITEM + k_tile * kTileTokens + row;
           const int64_t room = static_cast<int64_t>(ctx) - next_n - pos;  // row n is written iff n + room >= 0
           const bool in_model = pos < p.max_model_len;
           float* out_col = p.out + static_cast<int64_t>(cur.b) * next_n * p.out_stride + pos;
@@ -462,7 +476,30 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
                 if (lane == 0) ptx::mbar_arrive(acce);
               },
               [&](int n, float v) {
-                if (n + room >= 0 && in_model) __stcs(out_col + static_cast<int64_t>(n) * p.out_stride, v * scale);
+                const bool in = n + room >= 0 && in_model;
+                if constexpr (!FILTER) {
+                  if (in) __stcs(out_col + static_cast<int64_t>(n) * p.out_stride, v * scale);
+                } else {
+                  // Candidates of row r: logits above the row's threshold are
+                  // appended (one atomic per warp), logits equal to it set
+                  // their bit in the row's tie bitmap (a warp's 32 tokens are
+                  // one aligned 32-bit word of positions).
+                  const float val = v * scale, t = thr_n[n];
+                  const uint32_t gt = __ballot_sync(0xffffffffu, in && val > t);
+                  const uint32_t eq = __ballot_sync(0xffffffffu, in && val == t);
+                  const int64_t r = static_cast<int64_t>(cur.b) * next_n + n;
+                  if (gt != 0u) {
+                    uint32_t base = 0u;
+                    if (lane == 0) base = atomicAdd(p.cnt + 2 * r, static_cast<uint32_t>(__popc(gt)));
+                    base = __shfl_sync(0xffffffffu, base, 0);
+                    const uint32_t idx = base + static_cast<uint32_t>(__popc(gt & ((1u << lane) - 1u)));
+                    if (in && val > t && idx < static_cast<uint32_t>(p.cap)) {
+                      p.cand_val[r * p.cap + idx] = val;
+                      p.cand_pos[r * p.cap + idx] = static_cast<int32_t>(pos);
+                    }
+                  }
+                  if (eq != 0u && lane == 0) atomicOr(p.ties + r * p.ties_stride + (pos >> 5), eq);
+                }
               });
         }
         st.next();
@@ -490,11 +527,17 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
 }
 
 cudaError_t launch_paged(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const CUtensorMap& tm_sc,
-                         const PagedParams& p, int heads, bool gather, int grid, int smem_bytes, cudaStream_t stream) {
+                         const PagedParams& p, int heads, bool gather, int grid, int smem_bytes, cudaStream_t stream,
+                         bool filter) {
   void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, PagedParams) = nullptr;
-  if (heads == 32) kern = gather ? paged_logits_kernel<32, true> : paged_logits_kernel<32, false>;
-  else if (heads == 64) kern = gather ? paged_logits_kernel<64, true> : paged_logits_kernel<64, false>;
-  else return cudaErrorInvalidValue;
+  if (heads == 32)
+    kern = filter ? (gather ? paged_logits_kernel<32, true, true> : paged_logits_kernel<32, false, true>)
+                  : (gather ? paged_logits_kernel<32, true, false> : paged_logits_kernel<32, false, false>);
+  else if (heads == 64)
+    kern = filter ? (gather ? paged_logits_kernel<64, true, true> : paged_logits_kernel<64, false, true>)
+                  : (gather ? paged_logits_kernel<64, true, false> : paged_logits_kernel<64, false, false>);
+  else
+    return cudaErrorInvalidValue;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem_bytes);
   if (e != cudaSuccess) return e;
   kern<<<grid, paged_threads(gather), smem_bytes, stream>>>(tm_q, tm_kv, tm_sc, p);

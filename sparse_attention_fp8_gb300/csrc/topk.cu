@@ -168,6 +168,9 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, uint8_t* smem_raw)
   const int C = kCluster ? static_cast<int>(cg::this_cluster().num_blocks()) : 1;
   const int crank = kCluster ? static_cast<int>(cg::this_cluster().block_rank()) : 0;
   const int64_t r = blockIdx.x / C;
+  // (every CTA of a row's cluster takes the same branch)
+  if (p.run_flag != nullptr && __ldg(p.run_flag) == 0u) return;
+  if (p.row_mask != nullptr && __ldg(p.row_mask + r) == 0u) return;
   // The row's window [lo, hi).
   int64_t lo = 0, hi = 0;
   if (p.mode == 0) {
@@ -720,6 +723,249 @@ cudaError_t launch_topk(const TopkParams& p, int ctas, int smem_bytes, cudaStrea
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+// ------------------------------------------------ fused decode top-k passes
+//
+// fp8_paged_mqa_topk runs the decode kernel twice: once on every 16th item
+// of each request (the sample, written to the workspace's logits rows), once
+// in its filter form, which keeps only the logits above each row's threshold
+// (and marks those equal to it) instead of writing the logits.  The two
+// per-row kernels below sit before and after the filter pass.
+namespace {
+
+// Row r = b*next_n + n: window [0, W) of the decode logits, W = min(ctx_b -
+// next_n + n + 1, max_model_len) (0 if negative).
+__device__ __forceinline__ int64_t fused_window(const FusedTopkParams& p, int64_t r) {
+  const int64_t b = r / p.next_n, n = r - b * p.next_n;
+  int64_t ctx = __ldg(p.context_lens + b);
+  if (ctx < 0) ctx = 0;
+  int64_t hi = ctx - p.next_n + n + 1;
+  if (hi > p.cols) hi = p.cols;
+  return hi > 0 ? hi : 0;
+}
+
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// The need-th largest of n keys get(i) (1 <= need <= n) and the number of
+// keys above it: three radix levels (12, 12, 8 bits) over block-wide
+// shared-memory histograms.  Every thread of the block calls it.
+template <class Get>
+__device__ uint32_t block_kth_key(Get get, int64_t n, uint32_t need, uint32_t* hist, uint32_t* scan, uint32_t* misc,
+                                  uint32_t* above_out) {
+  const int tid = threadIdx.x;
+  const auto level = [&](int nbins, auto sel, auto bin) {
+    for (int i = tid; i < nbins; i += kT) hist[i] = 0u;
+    __syncthreads();
+    for (int64_t i = tid; i < n; i += kT) {
+      const uint32_t key = get(i);
+      hist_add(hist, sel(key), bin(key));
+    }
+    __syncthreads();
+  };
+  level(kTopkBins, [](uint32_t) { return true; }, [](uint32_t key) { return key >> 20; });
+  find_bin<kTopkBins>(hist, need, scan, misc);
+  const uint32_t b0 = misc[0], a0 = misc[1];
+  __syncthreads();
+  level(kTopkBins, [&](uint32_t key) { return (key >> 20) == b0; }, [](uint32_t key) { return (key >> 8) & 0xFFFu; });
+  find_bin<kTopkBins>(hist, need - a0, scan, misc);
+  const uint32_t pre24 = (b0 << 12) | misc[0], a1 = a0 + misc[1];
+  __syncthreads();
+  level(256, [&](uint32_t key) { return (key >> 8) == pre24; }, [](uint32_t key) { return key & 0xFFu; });
+  find_bin<256>(hist, need - a1, scan, misc);
+  const uint32_t T = (pre24 << 8) | misc[0];
+  *above_out = a1 + misc[1];
+  __syncthreads();
+  return T;
+}
+
+// Ascending sort of a[0, n) in shared memory (bitonic network over the next
+// power of two, padded with INT32_MAX; `a` has room for it).
+__device__ void block_sort_ascending(int32_t* a, int n) {
+  const int tid = threadIdx.x;
+  int P = 1;
+  while (P < n) P <<= 1;
+  for (int i = n + tid; i < P; i += kT) a[i] = 0x7FFFFFFF;
+  __syncthreads();
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < P / 2; i += kT) {
+        const int lo = 2 * i - (i & (stride - 1)), hi = lo + stride;
+        const bool asc = (lo & size) == 0;
+        const int32_t x = a[lo], y = a[hi];
+        if ((x > y) == asc) {
+          a[lo] = y;
+          a[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Order-preserving compaction: thread-owned flags in index order; returns
+// the slot of this thread's element (valid if its flag is set).
+__device__ __forceinline__ uint32_t block_rank(bool flag, uint32_t* scan, uint32_t* total) {
+  return block_scan(flag ? 1u : 0u, scan, total);
+}
+
+}  // namespace
+
+// Per row: reset of the row's per-call state, then the threshold.  The
+// sampled logits of row r are its window positions in items 0, 16, 32, ...
+// of its request.  About mu = k * f of them (f: the sampled fraction of the
+// window) are expected to be among the row's k largest; the threshold is the
+// m-th largest sample with m = mu + 5 sd + 1 (binomial sd), so that the
+// logits above it number about m / f >= k (a shortfall sends the row to the
+// exact fallback) and stay far below the candidate capacity.  A sample that
+// is the whole window gives m = k: the exact k-th largest.
+__global__ void __launch_bounds__(kTopkThreads, 2) fused_threshold_kernel(const FusedTopkParams p) {
+  __shared__ uint32_t hist[kTopkBins];
+  __shared__ uint32_t scan[2 * kWarps];
+  __shared__ uint32_t misc[8];
+  const int64_t r = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int64_t W = fused_window(p, r);
+  if (tid < 2) p.cnt[2 * r + tid] = 0u;
+  if (tid == 0) {
+    p.row_flag[r] = 0u;
+    if (r % p.next_n == 0) p.req_flag[r / p.next_n] = 0u;
+    if (r == 0) p.any[0] = 0u;
+  }
+  for (int64_t i = tid; i < (W + 31) / 32; i += kT) p.ties[r * p.tw + i] = 0u;
+  if (W <= p.k) {
+    if (tid == 0) p.thr[r] = -INFINITY;
+    return;
+  }
+  const int64_t I = p.item_tokens, SI = static_cast<int64_t>(kFusedSampleStride) * I;
+  const int64_t J = (W + SI - 1) / SI;                     // sampled items starting inside the window
+  const int64_t n_s = (J - 1) * I + min(I, W - (J - 1) * SI);
+  const float* row = p.logits + r * p.ls;
+  const auto get = [&](int64_t e) {
+    const int64_t j = e / I;
+    return order_key(row[j * SI + (e - j * I)]);
+  };
+  int64_t m;
+  if (n_s >= W) {
+    m = p.k;
+  } else {
+    const double f = static_cast<double>(n_s) / static_cast<double>(W);
+    const double mu = p.k * f, sd = sqrt(mu * (1.0 - f));
+    m = static_cast<int64_t>(ceil(mu + 5.0 * sd)) + 1;
+  }
+  float t = -INFINITY;
+  if (m <= n_s) {
+    uint32_t above;
+    t = key_value(block_kth_key(get, n_s, static_cast<uint32_t>(m), hist, scan, misc, &above));
+  }
+  if (tid == 0) p.thr[r] = t;
+}
+
+// Per row, after the filter pass: the row's candidates are every logit above
+// its threshold (cnt of them; the first cap stored, in no particular order)
+// and every position whose logit equals it (the tie bitmap).  If the
+// candidates cannot hold the row's k largest -- more above the threshold
+// than were stored, or fewer candidates than k -- the row (and its request)
+// is flagged for the exact fallback and left to it.  Otherwise: the k-th
+// largest candidate key T, every candidate above it, and the lowest
+// positions among those equal to it (positions sorted where more tie than
+// are needed), then the k chosen positions sorted ascending.
+__global__ void __launch_bounds__(kTopkThreads, 1) fused_select_kernel(const FusedTopkParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem_raw);                  // [kTopkBins]
+  uint32_t* keys = hist + kTopkBins;                                        // [cap]
+  int32_t* pos = reinterpret_cast<int32_t*>(keys + kTopkMaxCap);            // [cap]
+  int32_t* sel = pos + kTopkMaxCap;                                         // [2 * kTopkMaxK]
+  int32_t* tie = sel + 2 * kTopkMaxK;                                       // [cap]
+  __shared__ uint32_t scan[2 * kWarps];
+  __shared__ uint32_t misc[8];
+  const int64_t r = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int k = p.k;
+  const int64_t W = fused_window(p, r);
+  int32_t* out_row = p.out + r * p.out_stride;
+  if (W <= k) {
+    for (int j = tid; j < k; j += kT) out_row[j] = j < W ? j : -1;
+    return;
+  }
+  const uint32_t cA = p.cnt[2 * r];
+  // ties: count, and each thread's first tie rank (words in thread order)
+  const int64_t nw = (W + 31) / 32;
+  const int64_t wpt = (nw + kT - 1) / kT;
+  const int64_t w0 = tid * wpt, w1 = min(nw, w0 + wpt);
+  uint32_t mine = 0;
+  for (int64_t w = w0; w < w1; ++w) mine += __popc(p.ties[r * p.tw + w]);
+  uint32_t cE;
+  const uint32_t e_before = block_scan(mine, scan, &cE);
+  if (cA > static_cast<uint32_t>(p.cap) || cA + cE < static_cast<uint32_t>(k)) {
+    if (tid == 0) {
+      p.row_flag[r] = 1u;
+      atomicOr(p.req_flag + r / p.next_n, 1u);
+      atomicOr(p.any, 1u);
+    }
+    return;
+  }
+  for (uint32_t i = tid; i < cA; i += kT) {
+    keys[i] = order_key(p.cand_val[r * p.cap + i]);
+    pos[i] = p.cand_pos[r * p.cap + i];
+  }
+  // the first n_e tie positions, in position order (needed only below k)
+  const uint32_t n_e = cA < static_cast<uint32_t>(k) ? min(cE, static_cast<uint32_t>(k) - cA) : 0u;
+  if (e_before < n_e) {
+    const uint32_t tkey = order_key(p.thr[r]);
+    uint32_t j = e_before;
+    for (int64_t w = w0; w < w1 && j < n_e; ++w) {
+      uint32_t bits = p.ties[r * p.tw + w];
+      while (bits != 0u && j < n_e) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1u;
+        keys[cA + j] = tkey;
+        pos[cA + j] = static_cast<int32_t>(w * 32 + b);
+        ++j;
+      }
+    }
+  }
+  __syncthreads();
+  const int64_t n = static_cast<int64_t>(cA) + n_e;  // >= k
+  uint32_t above;
+  const uint32_t T = block_kth_key([&](int64_t i) { return keys[i]; }, n, static_cast<uint32_t>(k), hist, scan, misc,
+                                   &above);
+  // keys > T into sel[0, above); keys == T into tie[] (all of them)
+  uint32_t n_gt = 0, n_eq = 0;
+  for (int64_t i0 = 0; i0 < n; i0 += kT) {
+    const int64_t i = i0 + tid;
+    const uint32_t key = i < n ? keys[i] : 0u;
+    const bool gt = i < n && key > T, eq = i < n && key == T;
+    uint32_t tg, te;
+    const uint32_t sg = block_rank(gt, scan, &tg);
+    const uint32_t se = block_rank(eq, scan, &te);
+    if (gt) sel[n_gt + sg] = pos[i];
+    if (eq) tie[n_eq + se] = pos[i];
+    n_gt += tg;
+    n_eq += te;
+  }
+  __syncthreads();
+  const uint32_t need_eq = static_cast<uint32_t>(k) - above;
+  if (n_eq > need_eq) block_sort_ascending(tie, static_cast<int>(n_eq));  // the lowest positions win
+  for (uint32_t i = tid; i < need_eq; i += kT) sel[above + i] = tie[i];
+  __syncthreads();
+  block_sort_ascending(sel, k);
+  for (int j = tid; j < k; j += kT) out_row[j] = sel[j];
+}
+
+cudaError_t launch_fused_threshold(const FusedTopkParams& p, int smem_bytes, cudaStream_t stream) {
+  (void)smem_bytes;
+  fused_threshold_kernel<<<p.rows, kTopkThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fused_select(const FusedTopkParams& p, int smem_bytes, cudaStream_t stream) {
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(fused_select_kernel), smem_bytes);
+  if (e != cudaSuccess) return e;
+  fused_select_kernel<<<p.rows, kTopkThreads, smem_bytes, stream>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t read_topk_watchdog(unsigned int* value, bool clear) {

@@ -164,3 +164,13 @@ def test_watchdog_selftest_limit_checked_on_host(lib):
     for bad in (0, -5, 100001):
         assert lib.fp8idx_watchdog_selftest(bad, None) == fp8idx.FP8IDX_ERR_INVALID
         assert b"limit_us" in lib.fp8idx_last_error()
+
+
+def test_fused_topk_workspace_size(lib):
+    """The workspace size is a pure host function: zero for invalid
+    arguments, growing with the rows and the width."""
+    w = fp8idx.paged_mqa_topk_workspace(16, 6, 1048576, 2048)
+    assert w >= 96 * 1048576 * 4  # a logits row per output row for the sample and the fallback
+    assert fp8idx.paged_mqa_topk_workspace(16, 6, 1048576, 0) == 0
+    assert fp8idx.paged_mqa_topk_workspace(16, 6, 1048576, 4096) == 0
+    assert fp8idx.paged_mqa_topk_workspace(2, 1, 1000, 7) < fp8idx.paged_mqa_topk_workspace(4, 1, 1000, 7)
