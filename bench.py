@@ -72,6 +72,11 @@ TOPK_WORKLOADS = {
     "topk_prefill_4x1024": (3, 2048),
 }
 TOPK_METRIC = "top-k of the indexer logits us/call; essential GB/s and % of HBM roofline (1 GB300)"
+# fused decode logits + top-k (fp8_paged_mqa_topk): (config index, k)
+FUSED_WORKLOADS = {
+    "fused_topk_decode_mtp_verify": (2, 2048),
+}
+FUSED_METRIC = "fused indexer logits + top-k us/call; essential GB/s and % of HBM roofline (1 GB300)"
 DEFAULT_WORKLOAD = "decode_mtp_verify"
 L2_FLUSH_BYTES = 512 << 20
 L2_BYTES = 126 << 20  # GB300 L2 (nvidia-smi reports about 126 MiB)
@@ -145,6 +150,8 @@ SHARED_SOURCES = ("api.cpp", "common.cuh", "kernels.h", "ptx.cuh")
 def workload_kernel(workload: str) -> str:
     if workload in TOPK_WORKLOADS:
         return "topk"
+    if workload in FUSED_WORKLOADS:
+        return "decode"  # the filter pass of the decode kernel dominates
     return workloads.CONFIGS[WORKLOADS[workload][0]]["kind"]
 
 
@@ -706,6 +713,118 @@ def run_topk(args, rank, world):
     return line
 
 
+# ------------------------------------------------------------ fused arm
+def run_fused(args, rank, world):
+    """The fused decode logits + top-k call (six launches, the logits of every
+    row never written) on the MTP-verify batch; inputs larger than L2, so
+    calls run back to back (graphs of GRAPH_CALLS calls)."""
+    import torch
+    import sparse_attention_fp8_gb300 as fp8idx
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    idx, k = FUSED_WORKLOADS[args.workload]
+    case = workloads.make_config(idx)
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.Stream(device=dev)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    d = {key: up(getattr(case, key)) for key in ("q", "kv_cache", "weights", "context_lens", "block_tables")}
+    rows = case.batch * case.next_n
+    indices = torch.empty((rows, k), dtype=torch.int32, device=dev)
+    ws = torch.empty(fp8idx.paged_mqa_topk_workspace(case.batch, case.next_n, case.max_model_len, k) + 256,
+                     dtype=torch.uint8, device=dev)
+
+    def call(s=stream):
+        fp8idx.fp8_paged_mqa_topk(d["q"], d["kv_cache"], d["weights"], d["context_lens"], d["block_tables"],
+                                  case.max_model_len, k, indices, workspace=ws, stream=s)
+    b = decode_bytes(case.batch, case.next_n, case.heads, case.context_lens, case.max_model_len, case.block_size)
+    nbytes = {"k": b["k"], "q": b["q"], "w": b["w"], "indices": rows * k * 4,
+              "total": b["k"] + b["q"] + b["w"] + rows * k * 4, "table": b["table"]}
+    with torch.cuda.stream(stream):
+        call()
+    torch.cuda.synchronize()
+    graph_n = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_n, stream=stream):
+        for _ in range(GRAPH_CALLS):
+            call()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup // GRAPH_CALLS)):
+            graph_n.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    n_rep = max(1, args.steps // GRAPH_CALLS)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n_rep):
+            graph_n.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    steps = n_rep * GRAPH_CALLS
+    if time.time() - t0 < 1.0:
+        with torch.cuda.stream(stream):
+            t1 = time.time()
+            while time.time() - t1 < 1.0:
+                for _ in range(10):
+                    graph_n.replay()
+                torch.cuda.synchronize()
+    clocks = ClockSampler.summarize(sampler.stop())
+    clocks["window"] = "timed region + 1 s soak of the same step"
+    total_ms = reduce_max(e0.elapsed_time(e1), world, dev)
+    us_per_call = whole_job_us_per_call(total_ms, steps, world)
+    mean_ms = total_ms / steps
+    # e2e: per-step queries, weights, lengths and tables from pinned memory, indices back
+    step_inputs = ("q", "weights", "context_lens", "block_tables")
+    host_in = {key: torch.from_numpy(np.ascontiguousarray(getattr(case, key))).pin_memory() for key in step_inputs}
+    host_idx = torch.empty((rows, k), dtype=torch.int32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        a0.record(stream)
+        for _ in range(e2e_steps):
+            for key, t in host_in.items():
+                d[key].copy_(t, non_blocking=True)
+            call()
+            host_idx.copy_(indices, non_blocking=True)
+        a1.record(stream)
+    torch.cuda.synchronize()
+    e2e_us = whole_job_us_per_call(reduce_max(a0.elapsed_time(a1), world, dev), e2e_steps, world)
+    hbm_peak = float(peaks["hbm_gbs"])
+    achieved_gbs = nbytes["total"] / (mean_ms * 1e-3) / 1e9
+    return {
+        "metric": FUSED_METRIC, "value": round(us_per_call, 3), "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": round(mean_ms, 6), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 -> i32", "data": "synthetic",
+        "config": {"workload": args.workload, "desc": f"top-{k} per row of the logits of: {case.name}",
+                   "l2": (f"inputs larger than L2: back-to-back calls (graphs of {GRAPH_CALLS} calls), one event "
+                          "pair around the timed region"),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "essential_bytes": nbytes,
+        "essential_gbs": round(achieved_gbs, 1),
+        "roofline_fraction": round(achieved_gbs / hbm_peak, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved_gbs / hbm_peak, 4), "traffic": recorded_traffic(args.workload),
+                     "peak_source": f"{peak_src} hbm_gbs",
+                     "note": "the whole call (six launches) against the bytes of K, Q, weights and indices"},
+        "e2e": {"value": round(e2e_us, 3), "unit": UNIT,
+                "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in host_in.values())),
+                "d2h_bytes_per_step": rows * k * 4,
+                "note": "per-step inputs H2D from pinned memory, call, indices D2H; the paged K cache stays resident"},
+        "gpu_launches": steps * 6,
+        "clocks": clocks,
+        "device_status": "ok" if fp8idx.device_status() == 0 else "watchdog",
+    }
+
+
 # ---------------------------------------------------------- reference arm
 def run_reference_topk(args):
     """Reference arm of a top-k workload: the numpy oracle on a bounded
@@ -740,6 +859,24 @@ def run_reference(args):
     import oracle
     if args.workload in TOPK_WORKLOADS:
         return run_reference_topk(args)
+    if args.workload in FUSED_WORKLOADS:
+        # the oracle logits of the same decode batch (sampled, scaled), plus
+        # the numpy top-k over rows of that length (sampled, scaled)
+        idx, k = FUSED_WORKLOADS[args.workload]
+        a = argparse.Namespace(**vars(args))
+        a.workload = next(w for w, (i, nn) in WORKLOADS.items() if i == idx and nn is None)
+        line = run_reference(a)
+        TOPK_WORKLOADS.setdefault("_fused_topk", (idx, k))
+        a.workload = "_fused_topk"
+        topk_line = run_reference_topk(a)
+        v = line["value"] + topk_line["value"]
+        line.update({"metric": FUSED_METRIC, "value": round(v, 1), "ms_per_step": round(v / 1e3, 3),
+                     "config": {"workload": args.workload, "desc": f"top-{k} per row of the logits of: "
+                                + line["config"]["desc"]}})
+        line["cpu_baseline"]["value"] = round(v, 1)
+        line["cpu_baseline"]["sample"] += "; plus the numpy top-k on 8 random rows per step, scaled"
+        line["e2e"]["value"] = round(v, 1)
+        return line
     idx, case = make_case(args.workload)
     case = contiguous_view(case)
     kind = workloads.CONFIGS[idx]["kind"]
@@ -774,7 +911,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(TOPK_WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(TOPK_WORKLOADS) + sorted(FUSED_WORKLOADS),
+                    default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
@@ -788,7 +926,12 @@ def main(argv=None):
         import torch
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         torch.distributed.init_process_group("nccl")
-    line = run_topk(args, rank, world) if args.workload in TOPK_WORKLOADS else run_ours(args, rank, world)
+    if args.workload in TOPK_WORKLOADS:
+        line = run_topk(args, rank, world)
+    elif args.workload in FUSED_WORKLOADS:
+        line = run_fused(args, rank, world)
+    else:
+        line = run_ours(args, rank, world)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -290,17 +290,16 @@ fp8idx_status fp8_mqa_topk_ex(const fp8idx_tensor* logits,
  * indices[r] is exactly what fp8_paged_topk returns on the logits
  * fp8_paged_mqa_logits writes (same window, tie rule, order and -1 padding).
  *
- * How: the decode kernel first runs on every 16th item (128 or 256 tokens)
+ * How: the decode kernel first runs on every 32nd item (128 or 256 tokens)
  * of each request, and each row's threshold is taken from that sample so
- * that about 1.5k or more of the row's logits lie above it; a second pass of
- * the decode kernel keeps, per row, only the logits above the threshold
- * (up to fp8idx cap = min(4k + 1024, 8192) of them) and a bitmap of the
- * positions equal to it; a per-row kernel then selects the k largest of
- * those exactly.  A row whose candidates cannot be shown to contain its k
- * largest (too few above the threshold, or more than the cap) is recomputed
- * exactly instead: its request's logits are written to the workspace and
- * the top-k kernel selects from them.  The result never depends on which
- * path a row took.
+ * that more than k of the row's logits lie at or above it (about 1.5k for
+ * long windows); a second pass of the decode kernel keeps, per row, only the
+ * logits at or above the threshold (stored at their positions) and a bitmap
+ * of those positions; a per-row kernel then selects the k largest of them
+ * exactly.  A row whose candidates cannot be shown to contain its k largest
+ * (fewer than k, or more than 8192) is recomputed exactly instead: its
+ * request's logits are written to the workspace and the top-k kernel
+ * selects from them.  The result never depends on which path a row took.
  *
  *  q_fp8, kv_cache, weights, context_lens, block_tables, max_model_len
  *               as for fp8_paged_mqa_logits (same support gate).

@@ -400,11 +400,12 @@ fp8idx_status paged_impl(const fp8idx_tensor* q, const fp8idx_tensor* kv, const 
 // ----------------------------------------------------- fused decode top-k
 // fp8_paged_mqa_topk: six launches on the caller's stream, none of which
 // writes the logits of every row:
-//   1. the decode kernel on every 16th item of each request, its logits into
+//   1. the decode kernel on every 32nd item of each request, its logits into
 //      the workspace (the threshold sample);
 //   2. per row: reset of the row's state, the threshold;
-//   3. the decode kernel in its filter form: per row the logits above the
-//      threshold (and the positions equal to it) instead of the logits;
+//   3. the decode kernel in its filter form: per row only the logits at or
+//      above the threshold, with a bitmap of their positions, instead of
+//      every logit;
 //   4. per row: the exact top-k from the candidates, or the row flagged;
 //   5. the decode kernel over the flagged requests only, all their logits
 //      into the workspace, and 6. the top-k kernel over the flagged rows --
@@ -444,15 +445,11 @@ fp8idx_status paged_topk_impl(const fp8idx_tensor* q, const fp8idx_tensor* kv, c
   f.next_n = (int32_t)next_n;
   f.cols = max_model_len;
   f.k = k;
-  f.cap = L.cap;
   f.logits = reinterpret_cast<float*>(ws + L.logits);
   f.ls = L.ls;
   f.tw = L.tw;
   f.thr = reinterpret_cast<float*>(ws + L.thr);
-  f.cnt = reinterpret_cast<uint32_t*>(ws + L.cnt);
-  f.cand_val = reinterpret_cast<const float*>(ws + L.cand_val);
-  f.cand_pos = reinterpret_cast<const int32_t*>(ws + L.cand_pos);
-  f.ties = reinterpret_cast<uint32_t*>(ws + L.ties);
+  f.cand = reinterpret_cast<uint32_t*>(ws + L.cand);
   f.req_flag = reinterpret_cast<uint32_t*>(ws + L.req_flag);
   f.row_flag = reinterpret_cast<uint32_t*>(ws + L.row_flag);
   f.any = reinterpret_cast<uint32_t*>(ws + L.any);
@@ -461,7 +458,7 @@ fp8idx_status paged_topk_impl(const fp8idx_tensor* q, const fp8idx_tensor* kv, c
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (S.empty) {  // max_model_len 0: every window is empty
     f.item_tokens = kTileTokens;
-    cudaError_t e = launch_fused_threshold(f, 0, st);
+    cudaError_t e = launch_fused_threshold(f, fused_threshold_smem_bytes(), st);
     if (e == cudaSuccess) e = launch_fused_select(f, fused_select_smem_bytes(), st);
     if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "top-k launch: %s", cudaGetErrorString(e));
     return ok();
@@ -475,19 +472,15 @@ fp8idx_status paged_topk_impl(const fp8idx_tensor* q, const fp8idx_tensor* kv, c
   p.item_stride = kFusedSampleStride;
   TRY(paged_launch(S, p, false, stream));
   // 2. thresholds
-  cudaError_t e = launch_fused_threshold(f, 0, st);
+  cudaError_t e = launch_fused_threshold(f, fused_threshold_smem_bytes(), st);
   if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "top-k threshold launch: %s", cudaGetErrorString(e));
   // 3. the filter pass
   p = S.p;
   p.out = f.logits;
   p.out_stride = L.ls;
   p.thr = f.thr;
-  p.cnt = f.cnt;
-  p.cand_val = reinterpret_cast<float*>(ws + L.cand_val);
-  p.cand_pos = reinterpret_cast<int32_t*>(ws + L.cand_pos);
-  p.ties = f.ties;
-  p.ties_stride = L.tw;
-  p.cap = L.cap;
+  p.cand_bits = f.cand;
+  p.bits_stride = L.tw;
   TRY(paged_launch(S, p, true, stream));
   // 4. the exact selection, or the row flagged
   e = launch_fused_select(f, fused_select_smem_bytes(), st);

@@ -39,16 +39,12 @@ struct PagedParams {
   int32_t item_stride;          // request r's items are its items 0, s, 2s, ...: a sample of its window (1: all)
   const uint32_t* req_mask;     // requests with req_mask[b] == 0 get no items (null: every request)
   const uint32_t* run_flag;     // if non-null and *run_flag == 0 the launch does nothing
-  // filter epilogue (the FILTER instance): row r's logits above thr[r] are
-  // appended to its candidate list, those equal to it set their bit in the
-  // row's tie bitmap
+  // filter epilogue (the FILTER instance): a logit of row r at or above
+  // thr[r] is stored (at its position in out) and sets its bit in the row's
+  // candidate bitmap
   const float* thr;             // [rows]
-  uint32_t* cnt;                // [rows][2]: candidates appended (may exceed cap), unused
-  float* cand_val;              // [rows][cap]
-  int32_t* cand_pos;            // [rows][cap]
-  uint32_t* ties;               // [rows][ties_stride] bitmap over window positions
-  int64_t ties_stride;          // 32-bit words per row
-  int32_t cap;                  // candidate slots per row
+  uint32_t* cand_bits;          // [rows][bits_stride] bitmaps over window positions
+  int64_t bits_stride;          // 32-bit words per row
 };
 
 // Two epilogue warpgroups take alternate tiles; tensor memory holds 2..16
@@ -206,29 +202,24 @@ __host__ __device__ inline TopkLayout topk_smem_layout(int cap) {
 
 // ------------------------------------------------- fused decode top-k
 // Scratch of fp8_paged_mqa_topk (caller-provided workspace), per call:
-//   logits   [rows][ls] f32   sampled items, and whole rows of the requests that need the exact fallback
+//   logits   [rows][ls] f32   the sampled items, the candidates at their positions,
+//                             and whole rows of the requests that need the exact fallback
 //   thr      [rows] f32       each row's candidate threshold
-//   cnt      [rows][2] u32    candidates above the threshold (may exceed cap), spare
-//   cand_val [rows][cap] f32, cand_pos [rows][cap] i32
-//   ties     [rows][tw] u32   bitmap of window positions whose logit equals the threshold
+//   cand     [rows][tw] u32   bitmap of window positions whose logit is at or above it
 //   req_flag [batch] u32, row_flag [rows] u32, any [4] u32   rows left to the fallback
 struct FusedTopkLayout {
-  uint64_t logits, thr, cnt, cand_val, cand_pos, ties, req_flag, row_flag, any, total;
+  uint64_t logits, thr, cand, req_flag, row_flag, any, total;
   int64_t ls, tw;
-  int32_t cap;
 };
-constexpr int kFusedSampleStride = 16;  // the threshold sample: every 16th item of each request
-__host__ __device__ inline int32_t fused_topk_cap(int32_t k) {
-  const int32_t c = 4 * k + 1024;
-  return c < kTopkMaxCap ? c : kTopkMaxCap;
-}
+constexpr int kFusedSampleStride = 32;  // the threshold sample: every 32nd item of each request
+constexpr int kFusedMaxSample = 16384;  // sampled logits a row's threshold is taken from, at most
 __host__ __device__ inline FusedTopkLayout fused_topk_layout(int64_t batch, int64_t next_n, int64_t max_model_len,
                                                              int32_t k) {
+  (void)k;
   FusedTopkLayout L;
   const int64_t rows = batch * next_n;
   L.ls = (max_model_len + 3) & ~static_cast<int64_t>(3);
   L.tw = (((max_model_len + 31) / 32) + 3) & ~static_cast<int64_t>(3);
-  L.cap = fused_topk_cap(k);
   uint64_t off = 0;
   const auto take = [&](uint64_t bytes) {
     const uint64_t at = off;
@@ -237,10 +228,7 @@ __host__ __device__ inline FusedTopkLayout fused_topk_layout(int64_t batch, int6
   };
   L.logits = take(static_cast<uint64_t>(rows) * L.ls * 4u);
   L.thr = take(static_cast<uint64_t>(rows) * 4u);
-  L.cnt = take(static_cast<uint64_t>(rows) * 8u);
-  L.cand_val = take(static_cast<uint64_t>(rows) * L.cap * 4u);
-  L.cand_pos = take(static_cast<uint64_t>(rows) * L.cap * 4u);
-  L.ties = take(static_cast<uint64_t>(rows) * L.tw * 4u);
+  L.cand = take(static_cast<uint64_t>(rows) * L.tw * 4u);
   L.req_flag = take(static_cast<uint64_t>(batch) * 4u);
   L.row_flag = take(static_cast<uint64_t>(rows) * 4u);
   L.any = take(16u);
@@ -254,14 +242,10 @@ struct FusedTopkParams {
   const int32_t* context_lens;
   int32_t rows, next_n, cols, k;  // cols: max_model_len
   int32_t item_tokens;            // tokens per item of the decode kernel (128 or 256)
-  int32_t cap;
   float* logits;                  // workspace rows (stride ls)
   int64_t ls, tw;
   float* thr;
-  uint32_t* cnt;
-  const float* cand_val;
-  const int32_t* cand_pos;
-  uint32_t* ties;
+  uint32_t* cand;
   uint32_t* req_flag;
   uint32_t* row_flag;
   uint32_t* any;
@@ -291,11 +275,10 @@ cudaError_t launch_topk(const TopkParams& p, int ctas, int smem_bytes, cudaStrea
 // the workspace reset), then the exact selection from the candidates (or
 // the row handed to the fallback).  One CTA of kTopkThreads per row.
 cudaError_t launch_fused_threshold(const FusedTopkParams& p, int smem_bytes, cudaStream_t stream);
-// dynamic shared memory of the select kernel: histogram, candidate keys and
-// positions, the chosen positions (sort buffer), the tied positions
-__host__ __device__ constexpr int fused_select_smem_bytes() {
-  return 4 * kTopkBins + 4 * kTopkMaxCap + 4 * kTopkMaxCap + 4 * 2 * kTopkMaxK + 4 * kTopkMaxCap;
-}
+// dynamic shared memory of the threshold kernel (histogram, sample keys) and
+// of the select kernel (histogram, candidate keys and positions)
+__host__ __device__ constexpr int fused_threshold_smem_bytes() { return 4 * kTopkBins + 4 * kFusedMaxSample; }
+__host__ __device__ constexpr int fused_select_smem_bytes() { return 4 * kTopkBins + 8 * kTopkMaxCap; }
 cudaError_t launch_fused_select(const FusedTopkParams& p, int smem_bytes, cudaStream_t stream);
 
 // Launches the watchdog self-test kernel: a bounded wait that nothing

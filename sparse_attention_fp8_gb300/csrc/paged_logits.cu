@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
       Ring qr{0u, 0u, 2u};
       int32_t ctx = 0;
       const float* w = w_s;
-      float thr_n[8];  // (FILTER) the thresholds of the current request's rows
+      const float* thr_b = p.thr;  // (FILTER) the thresholds of the current request's rows
       for (int it = 0; it < n_items; ++it) {
         if (it == 0 || cur.t == 0) {
           if (!warp_wait_bounded(qf0 + 8u * qr.idx, qr.phase, abort_flag, &g_paged_watchdog, kSiteQFull)) break;
@@ -449,11 +449,7 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
           // the producers' clamped context: positions past what they loaded
           // are never stored, even for inputs that break the precondition
           ctx = static_cast<int32_t>(clamp_ctx(__ldg(p.context_lens + cur.b), p));
-          if constexpr (FILTER) {
-#pragma unroll
-            for (int n = 0; n < 8; ++n)
-              thr_n[n] = n < next_n ? __ldg(p.thr + static_cast<int64_t>(cur.b) * next_n + n) : 0.f;
-          }
+          if constexpr (FILTER) thr_b = p.thr + static_cast<int64_t>(cur.b) * next_n;
         }
         if (kShared || (it & 1) == grp) {
           if (!warp_wait_bounded(full0 + 8u * st.idx, st.phase, abort_flag, &g_paged_watchdog, kSiteStageFull))
@@ -480,25 +476,20 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
                 if constexpr (!FILTER) {
                   if (in) __stcs(out_col + static_cast<int64_t>(n) * p.out_stride, v * scale);
                 } else {
-                  // Candidates of row r: logits above the row's threshold are
-                  // appended (one atomic per warp), logits equal to it set
-                  // their bit in the row's tie bitmap (a warp's 32 tokens are
-                  // one aligned 32-bit word of positions).
-                  const float val = v * scale, t = thr_n[n];
-                  const uint32_t gt = __ballot_sync(0xffffffffu, in && val > t);
-                  const uint32_t eq = __ballot_sync(0xffffffffu, in && val == t);
-                  const int64_t r = static_cast<int64_t>(cur.b) * next_n + n;
-                  if (gt != 0u) {
-                    uint32_t base = 0u;
-                    if (lane == 0) base = atomicAdd(p.cnt + 2 * r, static_cast<uint32_t>(__popc(gt)));
-                    base = __shfl_sync(0xffffffffu, base, 0);
-                    const uint32_t idx = base + static_cast<uint32_t>(__popc(gt & ((1u << lane) - 1u)));
-                    if (in && val > t && idx < static_cast<uint32_t>(p.cap)) {
-                      p.cand_val[r * p.cap + idx] = val;
-                      p.cand_pos[r * p.cap + idx] = static_cast<int32_t>(pos);
-                    }
-                  }
-                  if (eq != 0u && lane == 0) atomicOr(p.ties + r * p.ties_stride + (pos >> 5), eq);
+                  // Candidates of row r: a logit at or above the row's
+                  // threshold sets its bit in the row's bitmap, and a warp
+                  // with any candidate stores all 32 of its logits (one whole
+                  // 128-byte line: no partial-line writes).  A warp's 32
+                  // tokens are one aligned 32-bit word of positions that no
+                  // other warp covers, so lane 0 stores the warp's ballot as
+                  // that word (every word whose first position is in the
+                  // window is written).
+                  const float val = v * scale;
+                  const bool cand = in && val >= __ldg(thr_b + n);
+                  const uint32_t m = __ballot_sync(0xffffffffu, cand);
+                  if (m != 0u && in) __stcs(out_col + static_cast<int64_t>(n) * p.out_stride, val);
+                  if (lane == 0 && in)
+                    p.cand_bits[(static_cast<int64_t>(cur.b) * next_n + n) * p.bits_stride + (pos >> 5)] = m;
                 }
               });
         }

@@ -727,11 +727,12 @@ cudaError_t launch_topk(const TopkParams& p, int ctas, int smem_bytes, cudaStrea
 
 // ------------------------------------------------ fused decode top-k passes
 //
-// fp8_paged_mqa_topk runs the decode kernel twice: once on every 16th item
+// fp8_paged_mqa_topk runs the decode kernel twice: once on every 32nd item
 // of each request (the sample, written to the workspace's logits rows), once
-// in its filter form, which keeps only the logits above each row's threshold
-// (and marks those equal to it) instead of writing the logits.  The two
-// per-row kernels below sit before and after the filter pass.
+// in its filter form, which keeps only the logits at or above each row's
+// threshold (stored at their positions, marked in a bitmap) instead of
+// writing every logit.  The two per-row kernels below sit before and after
+// the filter pass.
 namespace {
 
 // Row r = b*next_n + n: window [0, W) of the decode logits, W = min(ctx_b -
@@ -805,80 +806,89 @@ __device__ void block_sort_ascending(int32_t* a, int n) {
   }
 }
 
-// Order-preserving compaction: thread-owned flags in index order; returns
-// the slot of this thread's element (valid if its flag is set).
-__device__ __forceinline__ uint32_t block_rank(bool flag, uint32_t* scan, uint32_t* total) {
-  return block_scan(flag ? 1u : 0u, scan, total);
-}
-
 }  // namespace
 
 // Per row: reset of the row's per-call state, then the threshold.  The
-// sampled logits of row r are its window positions in items 0, 16, 32, ...
-// of its request.  About mu = k * f of them (f: the sampled fraction of the
-// window) are expected to be among the row's k largest; the threshold is the
-// m-th largest sample with m = mu + 5 sd + 1 (binomial sd), so that the
-// logits above it number about m / f >= k (a shortfall sends the row to the
-// exact fallback) and stay far below the candidate capacity.  A sample that
-// is the whole window gives m = k: the exact k-th largest.
-__global__ void __launch_bounds__(kTopkThreads, 2) fused_threshold_kernel(const FusedTopkParams p) {
-  __shared__ uint32_t hist[kTopkBins];
+// sampled logits of row r are its window positions in items 0, 32, 64, ...
+// of its request (every q-th of those items when there are more than
+// kFusedMaxSample values, q the smallest that fits).  About mu = k * f of
+// them (f: the sampled fraction of the window) are expected among the row's
+// k largest; the threshold is the m-th largest sample with m = mu + 4 sd + 1
+// (binomial sd), so that the logits above it number about m / f >= k (a
+// shortfall sends the row to the exact fallback) and stay far below the
+// candidate capacity.  A sample that is the whole window gives m = k: the
+// exact k-th largest.
+__global__ void __launch_bounds__(kTopkThreads, 1) fused_threshold_kernel(const FusedTopkParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem_raw);  // [kTopkBins]
+  uint32_t* keys = hist + kTopkBins;                      // [kFusedMaxSample]
   __shared__ uint32_t scan[2 * kWarps];
   __shared__ uint32_t misc[8];
   const int64_t r = blockIdx.x;
   const int tid = threadIdx.x;
   const int64_t W = fused_window(p, r);
-  if (tid < 2) p.cnt[2 * r + tid] = 0u;
   if (tid == 0) {
     p.row_flag[r] = 0u;
     if (r % p.next_n == 0) p.req_flag[r / p.next_n] = 0u;
     if (r == 0) p.any[0] = 0u;
   }
-  for (int64_t i = tid; i < (W + 31) / 32; i += kT) p.ties[r * p.tw + i] = 0u;
   if (W <= p.k) {
     if (tid == 0) p.thr[r] = -INFINITY;
     return;
   }
   const int64_t I = p.item_tokens, SI = static_cast<int64_t>(kFusedSampleStride) * I;
-  const int64_t J = (W + SI - 1) / SI;                     // sampled items starting inside the window
-  const int64_t n_s = (J - 1) * I + min(I, W - (J - 1) * SI);
+  const int lgI = I == 256 ? 8 : 7;  // items are 128 or 256 tokens
+  int64_t J = (W + SI - 1) / SI;  // sampled items starting inside the window
+  int64_t q = 1;                  // every q-th of them
+  while (((J + q - 1) / q) * I > kFusedMaxSample) ++q;
+  const int64_t Jq = (J + q - 1) / q, last = (Jq - 1) * q;  // items used; the last one may be partial
+  const int64_t n_s = (Jq - 1) * I + min(I, W - last * SI);
   const float* row = p.logits + r * p.ls;
-  const auto get = [&](int64_t e) {
-    const int64_t j = e / I;
-    return order_key(row[j * SI + (e - j * I)]);
-  };
+  // the sample's keys into shared memory: eight loads in flight per thread
+  for (int64_t e0 = 0; e0 < n_s; e0 += 8 * kT) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t e = e0 + u * kT + tid, j = e >> lgI;
+      v[u] = e < n_s ? row[j * q * SI + (e - (j << lgI))] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t e = e0 + u * kT + tid;
+      if (e < n_s) keys[e] = order_key(v[u]);
+    }
+  }
+  __syncthreads();
   int64_t m;
   if (n_s >= W) {
     m = p.k;
   } else {
     const double f = static_cast<double>(n_s) / static_cast<double>(W);
     const double mu = p.k * f, sd = sqrt(mu * (1.0 - f));
-    m = static_cast<int64_t>(ceil(mu + 5.0 * sd)) + 1;
+    m = static_cast<int64_t>(ceil(mu + 4.0 * sd)) + 1;
   }
   float t = -INFINITY;
   if (m <= n_s) {
     uint32_t above;
-    t = key_value(block_kth_key(get, n_s, static_cast<uint32_t>(m), hist, scan, misc, &above));
+    t = key_value(block_kth_key([&](int64_t i) { return keys[i]; }, n_s, static_cast<uint32_t>(m), hist, scan, misc,
+                                &above));
   }
   if (tid == 0) p.thr[r] = t;
 }
 
-// Per row, after the filter pass: the row's candidates are every logit above
-// its threshold (cnt of them; the first cap stored, in no particular order)
-// and every position whose logit equals it (the tie bitmap).  If the
-// candidates cannot hold the row's k largest -- more above the threshold
-// than were stored, or fewer candidates than k -- the row (and its request)
-// is flagged for the exact fallback and left to it.  Otherwise: the k-th
-// largest candidate key T, every candidate above it, and the lowest
-// positions among those equal to it (positions sorted where more tie than
-// are needed), then the k chosen positions sorted ascending.
+// Per row, after the filter pass: the row's candidates are the positions in
+// its bitmap (their logits, at or above the threshold, stored at those
+// positions of the row).  If they cannot hold the row's k largest -- more
+// than the shared-memory capacity, or fewer than k -- the row (and its
+// request) is flagged for the exact fallback and left to it.  Otherwise the
+// candidates are compacted in position order; the k-th largest key T among
+// them, every candidate above T and the first (k - #above T) equal to T are
+// written in position order.
 __global__ void __launch_bounds__(kTopkThreads, 1) fused_select_kernel(const FusedTopkParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  uint32_t* hist = reinterpret_cast<uint32_t*>(smem_raw);                  // [kTopkBins]
-  uint32_t* keys = hist + kTopkBins;                                        // [cap]
-  int32_t* pos = reinterpret_cast<int32_t*>(keys + kTopkMaxCap);            // [cap]
-  int32_t* sel = pos + kTopkMaxCap;                                         // [2 * kTopkMaxK]
-  int32_t* tie = sel + 2 * kTopkMaxK;                                       // [cap]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem_raw);        // [kTopkBins]
+  uint32_t* keys = hist + kTopkBins;                              // [kTopkMaxCap]
+  int32_t* pos = reinterpret_cast<int32_t*>(keys + kTopkMaxCap);  // [kTopkMaxCap]
   __shared__ uint32_t scan[2 * kWarps];
   __shared__ uint32_t misc[8];
   const int64_t r = blockIdx.x;
@@ -890,16 +900,28 @@ __global__ void __launch_bounds__(kTopkThreads, 1) fused_select_kernel(const Fus
     for (int j = tid; j < k; j += kT) out_row[j] = j < W ? j : -1;
     return;
   }
-  const uint32_t cA = p.cnt[2 * r];
-  // ties: count, and each thread's first tie rank (words in thread order)
+  // the bitmap's count; each thread owns a contiguous run of words, read as
+  // 16-byte vectors (the row's words start 16-byte aligned)
   const int64_t nw = (W + 31) / 32;
-  const int64_t wpt = (nw + kT - 1) / kT;
-  const int64_t w0 = tid * wpt, w1 = min(nw, w0 + wpt);
+  const int64_t nv = (nw + 3) / 4;
+  const int64_t vpt = (nv + kT - 1) / kT;
+  const int64_t v0 = min(nv, tid * vpt), v1 = min(nv, v0 + vpt);
+  const uint4* bits4 = reinterpret_cast<const uint4*>(p.cand + r * p.tw);
+  // (the filter pass writes every word whose first position is in the
+  // window; the words of the last vector past the window are not read)
+  const auto word = [&](int64_t v, int q, const uint4& x) -> uint32_t {
+    const uint32_t w = q == 0 ? x.x : q == 1 ? x.y : q == 2 ? x.z : x.w;
+    return v * 4 + q < nw ? w : 0u;
+  };
   uint32_t mine = 0;
-  for (int64_t w = w0; w < w1; ++w) mine += __popc(p.ties[r * p.tw + w]);
-  uint32_t cE;
-  const uint32_t e_before = block_scan(mine, scan, &cE);
-  if (cA > static_cast<uint32_t>(p.cap) || cA + cE < static_cast<uint32_t>(k)) {
+  for (int64_t v = v0; v < v1; ++v) {
+    const uint4 x = bits4[v];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) mine += __popc(word(v, q, x));
+  }
+  uint32_t cA;
+  const uint32_t before = block_scan(mine, scan, &cA);
+  if (cA > static_cast<uint32_t>(kTopkMaxCap) || cA < static_cast<uint32_t>(k)) {
     if (tid == 0) {
       p.row_flag[r] = 1u;
       atomicOr(p.req_flag + r / p.next_n, 1u);
@@ -907,57 +929,58 @@ __global__ void __launch_bounds__(kTopkThreads, 1) fused_select_kernel(const Fus
     }
     return;
   }
-  for (uint32_t i = tid; i < cA; i += kT) {
-    keys[i] = order_key(p.cand_val[r * p.cap + i]);
-    pos[i] = p.cand_pos[r * p.cap + i];
-  }
-  // the first n_e tie positions, in position order (needed only below k)
-  const uint32_t n_e = cA < static_cast<uint32_t>(k) ? min(cE, static_cast<uint32_t>(k) - cA) : 0u;
-  if (e_before < n_e) {
-    const uint32_t tkey = order_key(p.thr[r]);
-    uint32_t j = e_before;
-    for (int64_t w = w0; w < w1 && j < n_e; ++w) {
-      uint32_t bits = p.ties[r * p.tw + w];
-      while (bits != 0u && j < n_e) {
-        const int b = __ffs(bits) - 1;
-        bits &= bits - 1u;
-        keys[cA + j] = tkey;
-        pos[cA + j] = static_cast<int32_t>(w * 32 + b);
-        ++j;
+  {
+    uint32_t j = before;
+    for (int64_t v = v0; v < v1; ++v) {
+      const uint4 x = bits4[v];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t bits = word(v, q, x);
+        while (bits != 0u) {
+          pos[j++] = static_cast<int32_t>((v * 4 + q) * 32 + __ffs(bits) - 1);
+          bits &= bits - 1u;
+        }
       }
     }
   }
   __syncthreads();
-  const int64_t n = static_cast<int64_t>(cA) + n_e;  // >= k
-  uint32_t above;
-  const uint32_t T = block_kth_key([&](int64_t i) { return keys[i]; }, n, static_cast<uint32_t>(k), hist, scan, misc,
-                                   &above);
-  // keys > T into sel[0, above); keys == T into tie[] (all of them)
-  uint32_t n_gt = 0, n_eq = 0;
-  for (int64_t i0 = 0; i0 < n; i0 += kT) {
-    const int64_t i = i0 + tid;
-    const uint32_t key = i < n ? keys[i] : 0u;
-    const bool gt = i < n && key > T, eq = i < n && key == T;
-    uint32_t tg, te;
-    const uint32_t sg = block_rank(gt, scan, &tg);
-    const uint32_t se = block_rank(eq, scan, &te);
-    if (gt) sel[n_gt + sg] = pos[i];
-    if (eq) tie[n_eq + se] = pos[i];
-    n_gt += tg;
-    n_eq += te;
+  const float* row = p.logits + r * p.ls;
+  for (uint32_t i0 = 0; i0 < cA; i0 += 8 * kT) {  // their logits: eight loads in flight per thread
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint32_t i = i0 + u * kT + tid;
+      v[u] = i < cA ? row[pos[i]] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint32_t i = i0 + u * kT + tid;
+      if (i < cA) keys[i] = order_key(v[u]);
+    }
   }
   __syncthreads();
+  uint32_t above;
+  const uint32_t T = block_kth_key([&](int64_t i) { return keys[i]; }, cA, static_cast<uint32_t>(k), hist, scan,
+                                   misc, &above);
   const uint32_t need_eq = static_cast<uint32_t>(k) - above;
-  if (n_eq > need_eq) block_sort_ascending(tie, static_cast<int>(n_eq));  // the lowest positions win
-  for (uint32_t i = tid; i < need_eq; i += kT) sel[above + i] = tie[i];
-  __syncthreads();
-  block_sort_ascending(sel, k);
-  for (int j = tid; j < k; j += kT) out_row[j] = sel[j];
+  uint32_t n_gt = 0, n_eq = 0;
+  for (uint32_t i0 = 0; i0 < cA; i0 += kT) {  // in position order: slot = kept candidates before
+    const uint32_t i = i0 + tid;
+    const uint32_t key = i < cA ? keys[i] : 0u;
+    const bool gt = i < cA && key > T, eq = i < cA && key == T;
+    uint32_t tot;  // both counts in one scan (16:16; a chunk has kT < 2^16 elements)
+    const uint32_t rk = block_scan((gt ? 0x10000u : 0u) | (eq ? 1u : 0u), scan, &tot);
+    const uint32_t rg = rk >> 16, e_rank = n_eq + (rk & 0xFFFFu);
+    if (gt || (eq && e_rank < need_eq)) out_row[n_gt + rg + (e_rank < need_eq ? e_rank : need_eq)] = pos[i];
+    n_gt += tot >> 16;
+    n_eq += tot & 0xFFFFu;
+  }
 }
 
 cudaError_t launch_fused_threshold(const FusedTopkParams& p, int smem_bytes, cudaStream_t stream) {
-  (void)smem_bytes;
-  fused_threshold_kernel<<<p.rows, kTopkThreads, 0, stream>>>(p);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(fused_threshold_kernel), smem_bytes);
+  if (e != cudaSuccess) return e;
+  fused_threshold_kernel<<<p.rows, kTopkThreads, smem_bytes, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -93,7 +93,8 @@ def test_fused_topk_matches_unfused(fp8idx, name, batch, next_n, heads, mml, blk
 
 def test_fused_topk_all_equal_logits(fp8idx):
     """Every logit 0 (all K scales 0): the threshold equals every value, all
-    positions tie and the lowest k positions win (the tie bitmap)."""
+    positions tie and the lowest k positions win (every position is a
+    candidate, more than the candidate capacity: the exact fallback)."""
     case = workloads.decode_case(3, 2, 32, max_model_len=9000, block_size=64, context_lens=[9000, 3000, 100], seed=4)
     case = scale_tokens(case, lambda b, ctx: (range(ctx), 0.0))
     for k in (1, 100, 2048):
@@ -119,7 +120,7 @@ def test_fused_topk_repeated_keys(fp8idx):
 
 
 def test_fused_topk_misleading_samples(fp8idx):
-    """Sampled items (every 16th) with scales x50: the threshold from the
+    """Sampled items (every 32nd) with scales x50: the threshold from the
     sample sits above almost every other logit, too few candidates pass, and
     the row must take the exact fallback.  Then the opposite: the unsampled
     items x50, the threshold far too low, more candidates than the cap."""
@@ -129,7 +130,7 @@ def test_fused_topk_misleading_samples(fp8idx):
         it = item_tokens(case)
 
         def pick(b, ctx, it=it, boost_sampled=boost_sampled):
-            pos = [p for p in range(ctx) if ((p // it) % 16 == 0) == boost_sampled]
+            pos = [p for p in range(ctx) if ((p // it) % 32 == 0) == boost_sampled]
             return pos, 50.0
         case = scale_tokens(case, pick)
         for k in (512, 2048):
