@@ -333,6 +333,41 @@ fp8idx_status fp8_paged_mqa_topk(const fp8idx_tensor* q_fp8,
 size_t fp8idx_paged_mqa_topk_workspace(int64_t batch, int32_t next_n,
                                        int32_t max_model_len, int32_t k);
 
+/*
+ * fp8_paged_mqa_topk without a workspace argument: the same computation and
+ * result, with its scratch taken from a fixed area inside the library.  The
+ * paper has no counterpart to this entry point; it exists for callers that
+ * cannot allocate device memory -- a serving engine that gives all free
+ * device memory to its KV-cache pool at start-up and allows no allocation
+ * afterwards, a plugin that runs inside a host framework without access to
+ * its allocator, or a latency-critical path on which a cudaMalloc, which can
+ * synchronise the device, is not acceptable.  This call allocates nothing.
+ *
+ *  - The scratch is one static device array of 16 MiB (16777216 bytes) that
+ *    every GPU which loads the library holds until the process exits.  A
+ *    shape whose workspace (fp8idx_paged_mqa_topk_workspace) is larger is
+ *    rejected with FP8IDX_ERR_UNSUPPORTED and a message naming both sizes,
+ *    before anything is launched; such shapes need fp8_paged_mqa_topk.
+ *  - The first call on a device looks up the array's device address on that
+ *    device (cudaGetSymbolAddress) and keeps it; make that first call before
+ *    any stream capture.
+ *  - Every call on a device uses the same array, and it keeps whatever the
+ *    last call left in it; each call resets what it needs.  Calls whose
+ *    kernels overlap on the GPU (other streams, other host threads) race on
+ *    the array and give wrong results: order them on one stream or wait for
+ *    one before starting the next.
+ * Arguments, outputs and statuses as for fp8_paged_mqa_topk.
+ */
+fp8idx_status fp8_paged_mqa_topk_noalloc(const fp8idx_tensor* q_fp8,
+                                         const fp8idx_tensor* kv_cache,
+                                         const fp8idx_tensor* weights,
+                                         const fp8idx_tensor* context_lens,
+                                         const fp8idx_tensor* block_tables,
+                                         int32_t max_model_len, int32_t k,
+                                         const fp8idx_tensor* indices,
+                                         const fp8idx_options* opts,
+                                         void* stream);
+
 /* Support gates, after the pages' is_supported(num_heads, head_dim,
  * kv_block_size) (aiter PR 5047, Technical Details) and is_supported(
  * num_heads, head_dim) (aiter PR 5046, Technical Details): 1 if the shape is

@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libfp8idx.so")
-SOURCES = ["api.cpp", "paged_logits.cu", "mqa_logits.cu", "topk.cu"]
+SOURCES = ["api.cpp", "paged_logits.cu", "mqa_logits.cu", "topk.cu", "noalloc.cu"]
 HEADERS = ["ptx.cuh", "common.cuh", "kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -78,6 +78,10 @@ std::mutex g_smem_attr_mu;
 
 namespace fp8idx {
 
+// Sets the message fp8idx_last_error() returns on this thread (for entry
+// points defined in other translation units).
+void set_last_error_message(const char* msg) { g_last_error = msg; }
+
 cudaError_t ensure_dynamic_smem(const void* kernel, int bytes) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
