@@ -350,7 +350,6 @@ fp8idx_status paged_setup(const fp8idx_tensor* q, const fp8idx_tensor* kv, const
   }
   PagedParams& p = S->p;
   std::memset(&p, 0, sizeof(p));
-  p.item_stride = 1;
   p.kv_cache = static_cast<const uint8_t*>(kv->data);
   p.weights = static_cast<const float*>(w->data);
   p.context_lens = static_cast<const int32_t*>(cl->data);
@@ -370,9 +369,10 @@ fp8idx_status paged_setup(const fp8idx_tensor* q, const fp8idx_tensor* kv, const
   return ok();
 }
 
-fp8idx_status paged_launch(const PagedSetup& S, const PagedParams& p, bool filter, void* stream) {
+// mode: 0 the logits, 1 the fused top-k's filter pass, 2 its sample pass
+fp8idx_status paged_launch(const PagedSetup& S, const PagedParams& p, int mode, void* stream) {
   cudaError_t e = launch_paged(S.tm_q, S.tm_kv, S.tm_sc, p, S.heads, S.plan.gather != 0, S.plan.grid,
-                               S.plan.smem_bytes, static_cast<cudaStream_t>(stream), filter);
+                               S.plan.smem_bytes, static_cast<cudaStream_t>(stream), mode);
   if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
   return ok();
 }
@@ -398,7 +398,7 @@ fp8idx_status paged_impl(const fp8idx_tensor* q, const fp8idx_tensor* kv, const 
   PagedParams p = S.p;
   p.out = static_cast<float*>(out->data);
   p.out_stride = out->shape[0] > 1 ? out->stride[0] : out->shape[1];
-  return paged_launch(S, p, false, stream);
+  return paged_launch(S, p, 0, stream);
 }
 
 // ----------------------------------------------------- fused decode top-k
@@ -473,8 +473,7 @@ fp8idx_status paged_topk_impl(const fp8idx_tensor* q, const fp8idx_tensor* kv, c
   PagedParams p = S.p;
   p.out = f.logits;
   p.out_stride = L.ls;
-  p.item_stride = kFusedSampleStride;
-  TRY(paged_launch(S, p, false, stream));
+  TRY(paged_launch(S, p, 2, stream));
   // 2. thresholds
   cudaError_t e = launch_fused_threshold(f, fused_threshold_smem_bytes(), st);
   if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "top-k threshold launch: %s", cudaGetErrorString(e));
@@ -485,7 +484,7 @@ fp8idx_status paged_topk_impl(const fp8idx_tensor* q, const fp8idx_tensor* kv, c
   p.thr = f.thr;
   p.cand_bits = f.cand;
   p.bits_stride = L.tw;
-  TRY(paged_launch(S, p, true, stream));
+  TRY(paged_launch(S, p, 1, stream));
   // 4. the exact selection, or the row flagged
   e = launch_fused_select(f, fused_select_smem_bytes(), st);
   if (e != cudaSuccess) return fail(FP8IDX_ERR_CUDA, "top-k select launch: %s", cudaGetErrorString(e));
@@ -495,7 +494,7 @@ fp8idx_status paged_topk_impl(const fp8idx_tensor* q, const fp8idx_tensor* kv, c
   p.out_stride = L.ls;
   p.req_mask = f.req_flag;
   p.run_flag = f.any;
-  TRY(paged_launch(S, p, false, stream));
+  TRY(paged_launch(S, p, 0, stream));
   TopkParams tp;
   std::memset(&tp, 0, sizeof(tp));
   tp.mode = 1;

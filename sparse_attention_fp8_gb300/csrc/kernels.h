@@ -36,7 +36,6 @@ struct PagedParams {
   int32_t acc_bufs;   // TMEM accumulator buffers: paged_acc_buffers(n_cols, sub_tiles)
   int32_t sub_tiles;  // 128-token MMA tiles per pipeline item (1 or 2)
   // Fused top-k passes (all zero / null for a plain logits call):
-  int32_t item_stride;          // request r's items are its items 0, s, 2s, ...: a sample of its window (1: all)
   const uint32_t* req_mask;     // requests with req_mask[b] == 0 get no items (null: every request)
   const uint32_t* run_flag;     // if non-null and *run_flag == 0 the launch does nothing
   // filter epilogue (the FILTER instance): a logit of row r at or above
@@ -261,10 +260,11 @@ cudaError_t ensure_dynamic_smem(const void* kernel, int bytes);
 // ------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error.  The tensor maps are encoded
 // by the caller; `heads` selects the template instance.
-// filter: the FILTER instance (candidates and ties instead of stored logits)
+// mode 0: the logits; 1: the fused top-k's filter pass (candidates instead of
+// the logits); 2: the logits of every kFusedSampleStride-th item (its sample)
 cudaError_t launch_paged(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const CUtensorMap& tm_sc,
                          const PagedParams& p, int heads, bool gather, int grid, int smem_bytes, cudaStream_t stream,
-                         bool filter = false);
+                         int mode = 0);
 cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_s,
                            const CUtensorMap& tm_w, const CUtensorMap& tm_out, const PrefillParams& p, int heads,
                            int head_dim, bool paged, int grid, int smem_bytes, cudaStream_t stream);

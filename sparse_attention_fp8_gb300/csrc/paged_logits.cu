@@ -99,10 +99,17 @@ __device__ __forceinline__ int32_t clamp_block(int32_t v, int64_t num_blocks) {
 
 }  // namespace
 
-template <int HEADS, bool GATHER, bool FILTER>
+// MODE: kPlain (the logits), kFilter (the fused top-k's candidates instead
+// of the logits) or kSample (the logits of every kFusedSampleStride-th item
+// of each request).  The item stride is a compile-time constant: a runtime
+// stride slowed the block-size-1 gather by a third.
+enum PagedMode : int { kPlain = 0, kFilter = 1, kSample = 2 };
+
+template <int HEADS, bool GATHER, int MODE>
 __global__ void __launch_bounds__(paged_threads(GATHER), 1)
     paged_logits_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                         const __grid_constant__ CUtensorMap tm_sc, const PagedParams p) {
+  constexpr bool FILTER = MODE == kFilter;
   // a launch that is only needed when an earlier one raised the flag
   if (p.run_flag != nullptr && __ldg(p.run_flag) == 0u) return;
   constexpr int kProdWarps = paged_producer_warps(GATHER);
@@ -144,7 +151,7 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
   const int lane = threadIdx.x & 31;
 
   // ---- prologue: per-request tile counts, barriers, tensor memory --------
-  const int IS = p.item_stride;  // items 0, IS, 2*IS, ... of every request (IS > 1: a sample)
+  constexpr int IS = MODE == kSample ? kFusedSampleStride : 1;  // items 0, IS, 2*IS, ... of every request
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
     const bool on = p.req_mask == nullptr || __ldg(p.req_mask + b) != 0u;
     const int64_t c = on ? clamp_ctx(__ldg(p.context_lens + b), p) : 0;
@@ -517,16 +524,28 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
   }
 }
 
+namespace {
+using PagedKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, PagedParams);
+template <int HEADS, int MODE>
+PagedKernel paged_instance(bool gather) {
+  return gather ? paged_logits_kernel<HEADS, true, MODE> : paged_logits_kernel<HEADS, false, MODE>;
+}
+template <int HEADS>
+PagedKernel paged_instance(bool gather, int mode) {
+  return mode == kFilter ? paged_instance<HEADS, kFilter>(gather)
+         : mode == kSample ? paged_instance<HEADS, kSample>(gather)
+                           : paged_instance<HEADS, kPlain>(gather);
+}
+}  // namespace
+
 cudaError_t launch_paged(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const CUtensorMap& tm_sc,
                          const PagedParams& p, int heads, bool gather, int grid, int smem_bytes, cudaStream_t stream,
-                         bool filter) {
-  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, PagedParams) = nullptr;
+                         int mode) {
+  PagedKernel kern = nullptr;
   if (heads == 32)
-    kern = filter ? (gather ? paged_logits_kernel<32, true, true> : paged_logits_kernel<32, false, true>)
-                  : (gather ? paged_logits_kernel<32, true, false> : paged_logits_kernel<32, false, false>);
+    kern = paged_instance<32>(gather, mode);
   else if (heads == 64)
-    kern = filter ? (gather ? paged_logits_kernel<64, true, true> : paged_logits_kernel<64, false, true>)
-                  : (gather ? paged_logits_kernel<64, true, false> : paged_logits_kernel<64, false, false>);
+    kern = paged_instance<64>(gather, mode);
   else
     return cudaErrorInvalidValue;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem_bytes);
