@@ -114,7 +114,10 @@ __device__ __forceinline__ Unit load_unit(const PrefillParams& p, int u, int num
 
 }  // namespace
 
-template <int HEADS, bool PAGED, int DIM>
+// GATHER (paged K of block size 1 only): the producer gathers token rows
+// with 4-byte copies instead of issuing one TMA per cache block; a separate
+// instance, so that neither producer loop shapes the other's code.
+template <int HEADS, bool PAGED, int DIM, bool GATHER>
 __global__ void __launch_bounds__(prefill_threads(), 1)
     mqa_logits_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_w,
@@ -130,6 +133,7 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
   const int AB = p.acc_bufs;
   const uint32_t acc_cols = kTmemCols / AB;
   static_assert(DIM == 128 || DIM == 64, "head_dim 128 or 64");
+  static_assert(PAGED || !GATHER, "the gather reads a paged cache");
   constexpr int kRow = DIM;                        // bytes per Q/K row
   constexpr int kTileB = kTileTokens * DIM;        // bytes per K tile
   const PrefillSmem L = prefill_smem_layout(N, S, PAGED ? 2 * (p.n_req + 1) : 0, DIM);
@@ -161,7 +165,7 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
     misc[1] = 0u;
     for (int s = 0; s < S; ++s) {
       // TMA: one arrive with the byte count; token gather: every producer lane
-      ptx::mbar_init(full0 + 8u * s, (PAGED && p.block_size == 1) ? 32u : 1u);
+      ptx::mbar_init(full0 + 8u * s, GATHER ? 32u : 1u);
       ptx::mbar_init(empty0 + 8u * s, 1u + 4u);  // MMA commit + the 4 warps that read the tile's scales
     }
     for (int g = 0; g < AB; ++g) {
@@ -249,7 +253,7 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
     // 64-byte swizzle: c ^ ((j >> 1) & 3)), and publishes a tile kLag tiles
     // after issuing it (every lane arrives once its copies have landed).
     constexpr int kLag = 4;
-    const bool gather = PAGED && p.block_size == 1;
+    constexpr bool gather = GATHER;
     int pending = 0;
     Ring pub{0u, 0u, static_cast<uint32_t>(S)};
     const auto publish_all = [&]() {
@@ -260,8 +264,29 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
         pub.next();
       }
     };
+    // Block size 1: this lane's block-table entries of a padded tile (its
+    // tokens 32q + lane; raw, not yet clamped), loaded two computed tiles
+    // ahead of their use so that the loads' latency never stalls the copy
+    // issue.  (For larger blocks the same prefetch measured slower: their
+    // producer issues one TMA per block and is not the bottleneck.)
+    [[maybe_unused]] const auto tile_ids = [&](int j, int32_t (&e)[4]) {
+      const int r = upper_index(tp_s, p.n_req, j);
+      const int t = j - tp_s[r];
+      const int len = cu_s[r + 1] - cu_s[r];
+      const int32_t* bt_row = p.block_tables + static_cast<int64_t>(r) * p.bt_stride;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int tok = t * kTileTokens + 32 * q + lane;
+        e[q] = tok < len ? __ldg(bt_row + min(tok, p.max_blocks - 1)) : 0;
+      }
+    };
+    int32_t ids0[4] = {0, 0, 0, 0}, ids1[4] = {0, 0, 0, 0}, ids2[4] = {0, 0, 0, 0};
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const Unit U = load_unit(p, u, num_rb, n_tiles, ucu, utp);
+      if constexpr (gather) {
+        if (U.n_comp > 0) tile_ids(U.j0, ids0);
+        if (U.n_comp > 1) tile_ids(U.j0 + p.split, ids1);
+      }
       // The Q buffer is freed once the MMA has consumed the unit before the
       // previous one, whose last tiles may still be unpublished.
       if (gather && pending > 0 && !__all_sync(0xffffffffu, ptx::mbar_test_wait(qe0 + 8u * qr.idx, qr.phase ^ 1u)))
@@ -278,6 +303,9 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
       qr.next();
       ++q_issued;
       for (int c = 0, j = U.j0; c < U.n_comp; ++c, j += p.split) {
+        if constexpr (gather) {
+          if (c + 2 < U.n_comp) tile_ids(j + 2 * p.split, ids2);
+        }
         if (!(ok = warp_wait_bounded(empty0 + 8u * st.idx, st.phase ^ 1u, abort_flag, &g_prefill_watchdog,
                                      kSiteStageEmpty)))
           break;
@@ -288,19 +316,15 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
             ptx::tma_load_2d(ptx::smem_u32(k_s + st.idx * kTileB), &tm_k, full, 0, j * kTileTokens);
             ptx::tma_load_1d(ptx::smem_u32(sc_s + st.idx * kTileTokens), &tm_s, full, j * kTileTokens);
           }
-        } else if (gather) {
+        } else if constexpr (gather) {
           // Padded tile j: request r's tokens [128t, 128t + 128); token i's
           // row is block_tables[r][i] (tokens past the request read row 0,
-          // in bounds, and are never stored).
-          const int r = upper_index(tp_s, p.n_req, j);
-          const int t = j - tp_s[r];
-          const int len = cu_s[r + 1] - cu_s[r];
-          const int32_t* bt_row = p.block_tables + static_cast<int64_t>(r) * p.bt_stride;
+          // in bounds, and are never stored); the entries were loaded two
+          // tiles ago (tile_ids).
           const uint8_t* src[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const int tok = t * kTileTokens + 32 * q + lane;
-            int32_t slot = tok < len ? __ldg(bt_row + min(tok, p.max_blocks - 1)) : 0;
+            int32_t slot = ids0[q];
             slot = slot < 0 ? 0 : (slot >= p.num_blocks ? static_cast<int32_t>(p.num_blocks - 1) : slot);
             src[q] = p.kv_cache + static_cast<int64_t>(slot) * (DIM + 4);
           }
@@ -375,9 +399,14 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
         }
         st.next();
         ++issued;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          ids0[q] = ids1[q];
+          ids1[q] = ids2[q];
+        }
       }
     }
-    if (gather) publish_all();  // (copies land before the CTA exits, abort or not)
+    if constexpr (gather) publish_all();  // (copies land before the CTA exits, abort or not)
     if (*abort_flag && lane == 0) {
       for (int c = max(0, issued - S); c < issued && !gather; ++c)
         wait_drain(full0 + 8u * (c % S), (c / S) & 1, &g_prefill_watchdog);
@@ -601,15 +630,19 @@ cudaError_t launch_prefill(const CUtensorMap& tm_q, const CUtensorMap& tm_k, con
                            const CUtensorMap& tm_w, const CUtensorMap& tm_out, const PrefillParams& p, int heads,
                            int head_dim, bool paged, int grid, int smem_bytes, cudaStream_t stream) {
   void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, PrefillParams) = nullptr;
-  if (head_dim == 128) {
-    if (heads == 32) kern = paged ? mqa_logits_kernel<32, true, 128> : mqa_logits_kernel<32, false, 128>;
-    else if (heads == 64) kern = paged ? mqa_logits_kernel<64, true, 128> : mqa_logits_kernel<64, false, 128>;
-    else if (heads == 128) kern = paged ? mqa_logits_kernel<128, true, 128> : mqa_logits_kernel<128, false, 128>;
-  } else if (head_dim == 64) {
-    if (heads == 32) kern = paged ? mqa_logits_kernel<32, true, 64> : mqa_logits_kernel<32, false, 64>;
-    else if (heads == 64) kern = paged ? mqa_logits_kernel<64, true, 64> : mqa_logits_kernel<64, false, 64>;
-    else if (heads == 128) kern = paged ? mqa_logits_kernel<128, true, 64> : mqa_logits_kernel<128, false, 64>;
-  }
+  const bool gather = paged && p.block_size == 1;
+  const auto pick = [&](auto heads_c, auto dim_c) {
+    constexpr int H = decltype(heads_c)::value, D = decltype(dim_c)::value;
+    kern = !paged ? mqa_logits_kernel<H, false, D, false>
+                  : (gather ? mqa_logits_kernel<H, true, D, true> : mqa_logits_kernel<H, true, D, false>);
+  };
+  const auto pick_heads = [&](auto dim_c) {
+    if (heads == 32) pick(IntC<32>{}, dim_c);
+    else if (heads == 64) pick(IntC<64>{}, dim_c);
+    else if (heads == 128) pick(IntC<128>{}, dim_c);
+  };
+  if (head_dim == 128) pick_heads(IntC<128>{});
+  else if (head_dim == 64) pick_heads(IntC<64>{});
   if (kern == nullptr) return cudaErrorInvalidValue;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem_bytes);
   if (e != cudaSuccess) return e;

@@ -308,7 +308,11 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
       const auto row_addr = [&](int32_t slot) -> const uint8_t* {
         return p.kv_cache + static_cast<int64_t>(clamp_block(slot, p.num_blocks)) * (kHeadDim + 4);
       };
-      const uint8_t *src_a = p.kv_cache, *src_b = p.kv_cache, *nxt_a = p.kv_cache, *nxt_b = p.kv_cache;
+      const uint8_t *src_a = p.kv_cache, *src_b = p.kv_cache;
+      // raw table entries of the next two tiles of the request: loaded two
+      // tiles ahead and turned into addresses one tile ahead, so the load's
+      // latency never stalls the copy issue
+      int32_t raw1_a = 0, raw1_b = 0, raw2_a = 0, raw2_b = 0;
       // swizzled position of this lane's 4 bytes in a row whose (row & 7) is e
       uint32_t swz[8];
 #pragma unroll
@@ -343,11 +347,16 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
           const int64_t t0 = static_cast<int64_t>(cur.t) * IS * kTileTokens + pw * 64 + lane;
           src_a = row_addr(load_table(p, cur.b, t0, ctx_eff));
           src_b = row_addr(load_table(p, cur.b, t0 + 32, ctx_eff));
+          if (cur.t + 1 < cur.tiles_b) {
+            const int64_t t1 = t0 + static_cast<int64_t>(IS) * kTileTokens;
+            raw1_a = load_table(p, cur.b, t1, ctx_eff);
+            raw1_b = load_table(p, cur.b, t1 + 32, ctx_eff);
+          }
         }
-        if (cur.t + 1 < cur.tiles_b) {  // prefetch the next tile's rows (same request only)
-          const int64_t t1 = static_cast<int64_t>(cur.t + 1) * IS * kTileTokens + pw * 64 + lane;
-          nxt_a = row_addr(load_table(p, cur.b, t1, ctx_eff));
-          nxt_b = row_addr(load_table(p, cur.b, t1 + 32, ctx_eff));
+        if (cur.t + 2 < cur.tiles_b) {  // the rows two tiles ahead (same request only)
+          const int64_t t2 = static_cast<int64_t>(cur.t + 2) * IS * kTileTokens + pw * 64 + lane;
+          raw2_a = load_table(p, cur.b, t2, ctx_eff);
+          raw2_b = load_table(p, cur.b, t2 + 32, ctx_eff);
         }
         if (!warp_wait_bounded(empty0 + 8u * st.idx, st.phase ^ 1u, abort_flag, &g_paged_watchdog, kSiteStageEmpty))
           break;
@@ -371,8 +380,10 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
           pub.next();
           --pending;
         }
-        src_a = nxt_a;
-        src_b = nxt_b;
+        src_a = row_addr(raw1_a);  // (past the request's last tile: replaced at the next request)
+        src_b = row_addr(raw1_b);
+        raw1_a = raw2_a;
+        raw1_b = raw2_b;
         cur.advance();
       }
       ptx::cp_async_wait<0>();
@@ -448,7 +459,12 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
       Ring qr{0u, 0u, 2u};
       int32_t ctx = 0;
       const float* w = w_s;
-      const float* thr_b = p.thr;  // (FILTER) the thresholds of the current request's rows
+      // (FILTER) the thresholds of the current request's rows, in registers:
+      // the emit below indexes them with compile-time row numbers
+      constexpr int kRows = NCH / (HEADS / 32);
+      float thr_r[kRows > 0 ? kRows : 1];
+#pragma unroll
+      for (int n = 0; n < kRows; ++n) thr_r[n] = 0.f;
       for (int it = 0; it < n_items; ++it) {
         if (it == 0 || cur.t == 0) {
           if (!warp_wait_bounded(qf0 + 8u * qr.idx, qr.phase, abort_flag, &g_paged_watchdog, kSiteQFull)) break;
@@ -456,7 +472,10 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
           // the producers' clamped context: positions past what they loaded
           // are never stored, even for inputs that break the precondition
           ctx = static_cast<int32_t>(clamp_ctx(__ldg(p.context_lens + cur.b), p));
-          if constexpr (FILTER) thr_b = p.thr + static_cast<int64_t>(cur.b) * next_n;
+          if constexpr (FILTER) {
+#pragma unroll
+            for (int n = 0; n < kRows; ++n) thr_r[n] = __ldg(p.thr + static_cast<int64_t>(cur.b) * next_n + n);
+          }
         }
         if (kShared || (it & 1) == grp) {
           if (!warp_wait_bounded(full0 + 8u * st.idx, st.phase, abort_flag, &g_paged_watchdog, kSiteStageFull))
@@ -492,7 +511,7 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
                   // that word (every word whose first position is in the
                   // window is written).
                   const float val = v * scale;
-                  const bool cand = in && val >= __ldg(thr_b + n);
+                  const bool cand = in && val >= thr_r[n];
                   const uint32_t m = __ballot_sync(0xffffffffu, cand);
                   if (m != 0u && in) __stcs(out_col + static_cast<int64_t>(n) * p.out_stride, val);
                   if (lane == 0 && in)
