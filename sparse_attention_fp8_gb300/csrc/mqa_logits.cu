@@ -494,6 +494,18 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
           const bool mine = (ci & 1) == grp;
           ++ci;
           if (mine) {
+            // the tile's output columns first: this work then overlaps the
+            // waits instead of delaying the accumulator's release
+            int n = col0 + row;
+            bool col_ok = n < p.cols;
+            if constexpr (PAGED) {  // padded tile -> the request's output columns; padding is not written
+              const int j = U.j0 + c * p.split;
+              const int r = upper_index(tp_s, p.n_req, j);
+              const int local = (j - tp_s[r]) * kTileTokens + row;
+              n = cu_s[r] + local;
+              col_ok = local < cu_s[r + 1] - cu_s[r] && n < p.cols;
+            }
+            float* const out_col = out_block + n;
             if (!(ok = warp_wait_bounded(full0 + 8u * st.idx, st.phase, abort_flag, &g_prefill_watchdog,
                                          kSiteStageFull)))
               break;
@@ -505,16 +517,6 @@ __global__ void __launch_bounds__(prefill_threads(), 1)
               break;
             ptx::tc_fence_after();
             const uint32_t taddr = tmem + ac.idx * acc_cols + (static_cast<uint32_t>(quad * 32) << 16);
-            int n = col0 + row;
-            bool col_ok = n < p.cols;
-            if constexpr (PAGED) {  // padded tile -> the request's output columns; padding is not written
-              const int j = U.j0 + c * p.split;
-              const int r = upper_index(tp_s, p.n_req, j);
-              const int local = (j - tp_s[r]) * kTileTokens + row;
-              n = cu_s[r] + local;
-              col_ok = local < cu_s[r + 1] - cu_s[r] && n < p.cols;
-            }
-            float* const out_col = out_block + n;
             const uint32_t acce = acce0 + 8u * ac.idx;
             reduce_rows<HEADS, NCH>(
                 taddr, w,
