@@ -65,7 +65,7 @@ __host__ __device__ constexpr int paged_acc_buffers(int n_cols, int sub_tiles = 
 }
 
 // Roles: producer warp(s), one MMA warp, kEpiGroups epilogue warpgroups.
-__host__ __device__ constexpr int paged_producer_warps(bool gather) { return 2; }
+__host__ __device__ constexpr int paged_producer_warps(bool gather) { return gather ? 2 : 1; }
 __host__ __device__ constexpr int paged_threads(bool gather) {
   return 32 * (paged_producer_warps(gather) + 1 + 4 * kEpiGroups);
 }

@@ -8,28 +8,31 @@
 //                          * kv_scale_b[p]       for p <= ctx_b - next_n + n,
 // with K_b[p] and its scale read from the paged cache through block_tables.
 //
-// Design (one persistent CTA per SM, warp-specialised, 11 warps):
+// Design (one persistent CTA per SM, warp-specialised, 10 warps; 11 for
+// block size 1):
 //  * Work items are (request b, T consecutive 128-token tiles): T = 2 when
 //    next_n*heads <= 128 (one barrier round trip per 256 tokens), else 1.
 //    Each CTA takes one contiguous range of the flattened item list, found on
 //    the device from context_lens (a prefix sum in shared memory), so no host
 //    synchronisation is needed and every CTA gets the same number of items
 //    (+-1).
-//  * Producer warps 0-1 take alternate items: per item one 3-D TMA per cache
-//    block for the K rows (view [block][row][128 B], 128-byte swizzle) and one
-//    2-D TMA (or, for 16-token blocks, a bulk copy) per block for its scales,
-//    into a ring of shared-memory stages; block-table entries are prefetched
-//    32 blocks ahead.  For block size 1 (co-packed 132-byte tokens, only
-//    4-byte aligned) each producer warp gathers 64 tokens of a tile with
-//    4-byte cp.async into the same swizzled layout instead.  Warp 0 also
-//    loads each request's Q block and weights into one of two buffers.
-//  * MMA warp 2: the K tile is the A operand (M = 128 tokens) and the
+//  * Producer warp 0: per item one 3-D TMA per cache block for the K rows
+//    (view [block][row][128 B], 128-byte swizzle) and one 2-D TMA (or, for
+//    16-token blocks, a bulk copy) per block for its scales, into a ring of
+//    shared-memory stages; block-table entries are prefetched 32 blocks
+//    ahead.  (One warp: a second one walking the same items only took issue
+//    slots from the epilogue warps on its sub-partition.)  For block size 1
+//    (co-packed 132-byte tokens, only 4-byte aligned) producer warps 0-1 each
+//    gather 64 tokens of a tile with 4-byte cp.async into the same swizzled
+//    layout instead.  Warp 0 also loads each request's Q block and weights
+//    into one of two buffers.
+//  * MMA warp (after the producers): the K tile is the A operand (M = 128 tokens) and the
 //    request's whole Q block [next_n*heads, 128] is the B operand, so
 //    N = next_n*heads: one K tile feeds every speculative row in one
 //    tcgen05.mma chain (the fold of next_n into the MMA asked for in aiter
 //    issue 5477, The ask).  Four K=32 e4m3 MMAs accumulate in f32 in tensor
 //    memory, which holds 2..16 accumulators (as many as 512 columns allow).
-//  * Epilogue warpgroups (warps 3-10): with two tiles per item group g reads
+//  * Epilogue warpgroups (the last 8 warps): with two tiles per item group g reads
 //    tile g of every item; with one, the groups take alternate items.  Thread
 //    = token (TMEM lane): read the token's scale and free the stage, then
 //    reduce the accumulator's 32-column chunks (common.cuh reduce_rows: loads
@@ -222,9 +225,10 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
     int issued = 0, q_issued = 0;
     int64_t ctx_eff = 0;
     if constexpr (!GATHER) {
-      // Two producer warps take alternate items; both walk every item to keep
-      // the ring and the block-table prefetch in step.  Warp 0 also loads Q.
-      const int pw = warp;              // 0..1
+      // With several producer warps each would take every kProdWarps-th item
+      // and all walk every item to keep the ring and the block-table prefetch
+      // in step; one warp is used (it also loads Q).
+      const int pw = warp;              // 0 .. kProdWarps-1
       const int blk = p.block_size;     // 16, 32, 64 or 128
       const int P = ITEM / blk;         // cache blocks per item (divides 32)
       const uint32_t blk_bytes = static_cast<uint32_t>(blk) * (kHeadDim + 4);
@@ -256,7 +260,7 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
           tbl_nxt = load_table(p, cur.b, chunk + 32 + lane, need_blocks);
         }
         const int32_t id = __shfl_sync(0xffffffffu, tbl_cur, (first_blk - chunk + lane) & 31);
-        if ((it & 1) == pw) {
+        if (it % kProdWarps == pw) {
         if (!warp_wait_bounded(empty0 + 8u * st.idx, st.phase ^ 1u, abort_flag, &g_paged_watchdog, kSiteStageEmpty))
           break;
         const int valid = min(ITEM, static_cast<int>(ctx_eff - static_cast<int64_t>(rt) * ITEM));
@@ -288,7 +292,7 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
       }
       if (*abort_flag && lane == 0) {  // let issued copies land before the CTA exits
         for (int it = max(0, issued - S); it < issued; ++it)
-          if ((it & 1) == pw) wait_drain(full0 + 8u * (it % S), (it / S) & 1, &g_paged_watchdog);
+          if (it % kProdWarps == pw) wait_drain(full0 + 8u * (it % S), (it / S) & 1, &g_paged_watchdog);
         for (int sg = max(0, q_issued - 2); sg < q_issued; ++sg)
           wait_drain(qf0 + 8u * (sg & 1), (sg >> 1) & 1, &g_paged_watchdog);
       }
