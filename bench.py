@@ -504,6 +504,23 @@ def run_ours(args, rank, world):
     e2e_ms = reduce_max(e0.elapsed_time(e1), world, dev)
     e2e_us = whole_job_us_per_call(e2e_ms, e2e_steps, world)
 
+    # Eager calls (no graph), back to back: the host cost of one public-API
+    # call (binding, validation, tensor maps, launch) and the device time per
+    # call when every call is launched on its own.
+    n_eager = 200
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        ea.record(stream)
+        h0 = time.perf_counter()
+        for _ in range(n_eager):
+            call()
+        host_us = (time.perf_counter() - h0) / n_eager * 1e6
+        eb.record(stream)
+    torch.cuda.synchronize()
+    eager = {"host_us_per_call": round(host_us, 2), "device_us_per_call": round(ea.elapsed_time(eb) * 1e3 / n_eager, 2),
+             "calls": n_eager, "note": "eager back-to-back calls through the public API, no graph"}
+
     status = fp8idx.device_status()
     hbm_peak = float(peaks["hbm_gbs"])
     fp8_peak = 2.0 * float(peaks["bf16_tflops"])  # nominal fp8:bf16 dense ratio 2
@@ -543,6 +560,7 @@ def run_ours(args, rank, world):
                         + ("the paged K cache stays resident" if kind == "decode" or args.workload in PAGED_PREFILL
                            else "")},
         "gpu_launches": args.steps,
+        "eager": eager,
         "clocks": clocks,
         "device_status": "ok" if status == 0 else f"watchdog {status}",
     }

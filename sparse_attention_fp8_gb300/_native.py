@@ -5,6 +5,7 @@ import ctypes
 import dataclasses
 import os
 import re
+import struct
 import threading
 
 from . import _build
@@ -26,8 +27,18 @@ class Fp8IdxError(RuntimeError):
 
 
 class _Tensor(ctypes.Structure):
+    """fp8idx_tensor as a ctypes structure (tests build descriptors by hand)."""
     _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
                 ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+# fp8idx_tensor packed in one call (data, dtype, ndim, shape[4], stride[4]):
+# the descriptors of a call are bytes objects handed to the library as
+# pointers, which costs a third of filling ctypes structures field by field.
+_TENSOR_PACK = struct.Struct("=qii4q4q")
+assert _TENSOR_PACK.size == ctypes.sizeof(_Tensor)
+_PAD = (0, 0, 0, 0)
+_dtype_codes = None
 
 
 class _Options(ctypes.Structure):
@@ -89,7 +100,7 @@ def library():
                                   "or python sparse_attention_fp8_gb300/_build.py")
             lib = ctypes.CDLL(path)
             P = ctypes.POINTER
-            T = P(_Tensor)
+            T = ctypes.c_void_p  # const fp8idx_tensor*: a packed descriptor, or byref(_Tensor)
             V = ctypes.c_void_p
             lib.fp8_paged_mqa_logits.argtypes = [T, T, T, T, T, ctypes.c_int32, T, V]
             lib.fp8_paged_mqa_logits_ex.argtypes = [T, T, T, T, T, ctypes.c_int32, T, P(_Options), V]
@@ -146,27 +157,29 @@ def _check(status: int):
         raise Fp8IdxError(status, msg.decode() if msg else "")
 
 
-def _desc(t) -> _Tensor:
-    """torch tensor -> descriptor (no copy; the tensor must outlive the call)."""
-    import torch
-    dt = {torch.uint8: _U8, torch.float8_e4m3fn: _U8, torch.float32: _F32, torch.int32: _I32}.get(t.dtype)
+def _desc(t) -> bytes:
+    """torch tensor -> packed fp8idx_tensor (no copy of the data; the tensor
+    must outlive the call)."""
+    global _dtype_codes
+    if _dtype_codes is None:
+        import torch
+        _dtype_codes = {torch.uint8: _U8, torch.float8_e4m3fn: _U8, torch.float32: _F32, torch.int32: _I32}
+    dt = _dtype_codes.get(t.dtype)
     if dt is None:
         raise TypeError(f"unsupported dtype {t.dtype}")
-    if t.dim() > 4:
+    shape = t.shape
+    n = len(shape)
+    if n > 4:
         raise ValueError("at most 4 dimensions")
-    d = _Tensor()
-    d.data = t.data_ptr()
-    d.dtype = dt
-    d.ndim = t.dim()
-    for i in range(t.dim()):
-        d.shape[i] = t.shape[i]
-        d.stride[i] = t.stride(i)
-    return d
+    return _TENSOR_PACK.pack(t.data_ptr(), dt, n, *shape, *_PAD[n:], *t.stride(), *_PAD[n:])
 
 
 def _stream(stream, like):
     import torch
     if stream is None:
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)  # the current stream's handle, no object
+        if raw is not None:
+            return ctypes.c_void_p(raw(like.get_device()))
         return ctypes.c_void_p(torch.cuda.current_stream(like.device).cuda_stream)
     if isinstance(stream, int):
         return ctypes.c_void_p(stream)
@@ -180,12 +193,11 @@ def fp8_paged_mqa_logits(q_fp8, kv_cache, weights, context_lens, block_tables, m
     args = [_desc(q_fp8), _desc(kv_cache), _desc(weights), _desc(context_lens), _desc(block_tables)]
     o = _desc(out)
     s = _stream(stream, q_fp8)
-    refs = [ctypes.byref(a) for a in args]
     if options is None:
-        st = lib.fp8_paged_mqa_logits(*refs, int(max_model_len), ctypes.byref(o), s)
+        st = lib.fp8_paged_mqa_logits(*args, int(max_model_len), o, s)
     else:
         oc = options._c()
-        st = lib.fp8_paged_mqa_logits_ex(*refs, int(max_model_len), ctypes.byref(o), ctypes.byref(oc), s)
+        st = lib.fp8_paged_mqa_logits_ex(*args, int(max_model_len), o, ctypes.byref(oc), s)
     _check(st)
     return out
 
@@ -201,12 +213,11 @@ def fp8_mqa_logits(q_fp8, k_fp8, kv_scale, weights, cu_seqlen_ks, cu_seqlen_ke, 
             _desc(cu_seqlen_ke)]
     o = _desc(out)
     s = _stream(stream, q_fp8)
-    refs = [ctypes.byref(a) for a in args]
     if options is None:
-        st = lib.fp8_mqa_logits(*refs, ctypes.byref(o), s)
+        st = lib.fp8_mqa_logits(*args, o, s)
     else:
         oc = options._c()
-        st = lib.fp8_mqa_logits_ex(*refs, ctypes.byref(o), ctypes.byref(oc), s)
+        st = lib.fp8_mqa_logits_ex(*args, o, ctypes.byref(oc), s)
     _check(st)
     return out
 
@@ -222,8 +233,7 @@ def fp8_mqa_logits_paged(q_fp8, kv_cache, block_tables, cu_seq_lens, weights, cu
             _desc(cu_seqlen_ks), _desc(cu_seqlen_ke)]
     o = _desc(out)
     oc = options._c() if options is not None else None
-    st = lib.fp8_mqa_logits_paged(*[ctypes.byref(a) for a in args], ctypes.byref(o),
-                                  ctypes.byref(oc) if oc is not None else None, _stream(stream, q_fp8))
+    st = lib.fp8_mqa_logits_paged(*args, o, ctypes.byref(oc) if oc is not None else None, _stream(stream, q_fp8))
     _check(st)
     return out
 
@@ -236,8 +246,8 @@ def fp8_paged_topk(logits, context_lens, next_n, max_model_len, k, indices, stre
     lib = library()
     lg, cl, ix = _desc(logits), _desc(context_lens), _desc(indices)
     oc = Options(num_ctas=int(ctas_per_row))._c()
-    _check(lib.fp8_paged_topk_ex(ctypes.byref(lg), ctypes.byref(cl), int(next_n), int(max_model_len), int(k),
-                                 ctypes.byref(ix), ctypes.byref(oc), _stream(stream, logits)))
+    _check(lib.fp8_paged_topk_ex(lg, cl, int(next_n), int(max_model_len), int(k), ix, ctypes.byref(oc),
+                                 _stream(stream, logits)))
     return indices
 
 
@@ -246,8 +256,7 @@ def fp8_mqa_topk(logits, cu_seqlen_ks, cu_seqlen_ke, k, indices, stream=None, ct
     lib = library()
     lg, a, b, ix = _desc(logits), _desc(cu_seqlen_ks), _desc(cu_seqlen_ke), _desc(indices)
     oc = Options(num_ctas=int(ctas_per_row))._c()
-    _check(lib.fp8_mqa_topk_ex(ctypes.byref(lg), ctypes.byref(a), ctypes.byref(b), int(k), ctypes.byref(ix),
-                               ctypes.byref(oc), _stream(stream, logits)))
+    _check(lib.fp8_mqa_topk_ex(lg, a, b, int(k), ix, ctypes.byref(oc), _stream(stream, logits)))
     return indices
 
 
@@ -273,7 +282,7 @@ def fp8_paged_mqa_topk(q_fp8, kv_cache, weights, context_lens, block_tables, max
     args = [_desc(q_fp8), _desc(kv_cache), _desc(weights), _desc(context_lens), _desc(block_tables)]
     ix = _desc(indices)
     oc = options._c() if options is not None else None
-    st = lib.fp8_paged_mqa_topk(*[ctypes.byref(a) for a in args], int(max_model_len), int(k), ctypes.byref(ix),
+    st = lib.fp8_paged_mqa_topk(*args, int(max_model_len), int(k), ix,
                                 ctypes.c_void_p(base + off), ctypes.c_size_t(workspace.numel() - off),
                                 ctypes.byref(oc) if oc is not None else None, _stream(stream, q_fp8))
     _check(st)

@@ -31,14 +31,14 @@ def noalloc_call(fp8idx, d, case, k, indices):
     from sparse_attention_fp8_gb300 import _native
     lib = fp8idx.library()
     fn = lib.fp8_paged_mqa_topk_noalloc
-    T = ctypes.POINTER(_native._Tensor)
+    T = ctypes.c_void_p  # const fp8idx_tensor*: the binding's packed descriptors
     fn.argtypes = [T, T, T, T, T, ctypes.c_int32, ctypes.c_int32, T, ctypes.POINTER(_native._Options),
                    ctypes.c_void_p]
     fn.restype = ctypes.c_int
     descs = [_native._desc(d[key]) for key in ("q", "kv_cache", "weights", "context_lens", "block_tables")]
     ix = _native._desc(indices)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    return fn(*[ctypes.byref(x) for x in descs], case.max_model_len, k, ctypes.byref(ix), None, stream)
+    return fn(*descs, case.max_model_len, k, ix, None, stream)
 
 
 def with_workspace(fp8idx, d, case, k):
