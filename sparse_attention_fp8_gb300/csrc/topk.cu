@@ -305,9 +305,10 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, uint8_t* smem_raw)
   };
 
   // ---- sources: the slice in global memory, or candidates in shared memory
-  const auto smem_hist = [&](int64_t n_c, auto sel, auto bin) {
-    for (int64_t i0 = 0; i0 < n_c; i0 += kT) {
-      const int64_t i = i0 + tid;
+  const auto smem_hist = [&](int64_t n_c64, auto sel, auto bin) {
+    const int n_c = static_cast<int>(n_c64);  // at most cap
+    for (int i0 = 0; i0 < n_c; i0 += kT) {
+      const int i = i0 + tid;
       const uint32_t key = i < n_c ? sh.cand_key[i] : 0u;
       hist_add(sh.hist, i < n_c && sel(key), bin(key));
     }
@@ -320,29 +321,30 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, uint8_t* smem_raw)
   // elements of each predicate before it in position order.  Counts per
   // chunk go through one 16-entry scan of warp totals (double-buffered, one
   // barrier per chunk).
-  const auto smem_get = [&](int64_t e, uint32_t& key, int32_t& pos) {
+  const auto smem_get = [&](int e, uint32_t& key, int32_t& pos) {
     key = sh.cand_key[e];
     pos = sh.cand_pos[e];
   };
-  const auto global_get = [&](int64_t e, uint32_t& key, int32_t& pos) {
+  const auto global_get = [&](int e, uint32_t& key, int32_t& pos) {
     key = order_key(__ldg(row_base + slo + e));
     pos = static_cast<int32_t>(slo + e);
   };
   // Two independent counts per element (packed 16:16 per chunk: a chunk has
   // kT*kPer < 2^16 elements), starting from done_a / done_b.
-  const auto ordered2 = [&](int64_t n, auto get, auto pred_a, auto pred_b, auto place, uint32_t done_a,
+  const auto ordered2 = [&](int64_t n64, auto get, auto pred_a, auto pred_b, auto place, uint32_t done_a,
                             uint32_t done_b) {
+    const int n = static_cast<int>(n64);  // a window or slice: fewer than 2^31 columns
     const int lane = tid & 31, warp = tid >> 5;
     const uint32_t lt = (1u << lane) - 1u;
     int parity = 0;
-    for (int64_t c0 = 0; c0 < n; c0 += static_cast<int64_t>(kT) * kPer) {
-      const int64_t wbase = c0 + static_cast<int64_t>(warp) * 32 * kPer;
+    for (int c0 = 0; c0 < n; c0 += kT * kPer) {
+      const int wbase = c0 + warp * 32 * kPer;
       uint32_t keys[kPer], ba[kPer], bb[kPer];
       int32_t pos[kPer];
       uint32_t wa = 0, wb = 0;
 #pragma unroll
       for (int j = 0; j < kPer; ++j) {
-        const int64_t e = wbase + j * 32 + lane;
+        const int e = wbase + j * 32 + lane;
         const bool in = e < n;
         keys[j] = 0u;
         pos[j] = 0;
@@ -463,19 +465,23 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, uint8_t* smem_raw)
       wait_bounded(sh.bar, 0u, abort_flag, &g_topk_watchdog, kSiteStageFull);
       if (*abort_flag && tid == 0) wait_drain(sh.bar, 0u, &g_topk_watchdog);
     }
-    for (int64_t i0 = 0; i0 < Ls; i0 += static_cast<int64_t>(kT) * 4) {
+    // (32-bit offsets: a slice here holds at most cap values, positions are below 2^31)
+    const int Ls32 = static_cast<int>(Ls), slo32 = static_cast<int>(slo);
+    const int a1r = static_cast<int>(a1 - slo);  // the staged part is [0, a1r) of the slice
+    const float* ring_s = sh.ring + (slo - b0);
+    for (int i0 = 0; i0 < Ls32; i0 += kT * 4) {
       float v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int64_t i = i0 + u * kT + tid, pos = slo + i;
-        v[u] = i >= Ls ? 0.f : (staged && pos < a1) ? sh.ring[pos - b0] : __ldg(row_base + pos);
+        const int i = i0 + u * kT + tid;
+        v[u] = i >= Ls32 ? 0.f : (staged && i < a1r) ? ring_s[i] : __ldg(row_base + slo32 + i);
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int64_t i = i0 + u * kT + tid;
-        if (i < Ls) {
+        const int i = i0 + u * kT + tid;
+        if (i < Ls32) {
           sh.cand_key[i] = order_key(v[u]);
-          sh.cand_pos[i] = static_cast<int32_t>(slo + i);
+          sh.cand_pos[i] = slo32 + i;
         }
       }
     }
@@ -497,17 +503,22 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, uint8_t* smem_raw)
   const int64_t ns = (L + S - 1) / S;  // samples lo + jS of the whole window: <= cap
   const int64_t j_lo = (slo - lo + S - 1) / S, j_hi = (shi - lo + S - 1) / S;  // this slice's samples
   const int64_t ns_c = j_hi - j_lo;
-  for (int64_t j0 = 0; j0 < ns_c; j0 += static_cast<int64_t>(kT) * 16) {  // all of a cap-8192 sample in flight
-    float v[16];
+  {
+    // (32-bit offsets: positions are below 2^31)
+    const int ns32 = static_cast<int>(ns_c), S32 = static_cast<int>(S);
+    const float* samp = row_base + lo + j_lo * S;
+    for (int j0 = 0; j0 < ns32; j0 += kT * 16) {  // all of a cap-8192 sample in flight
+      float v[16];
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const int64_t j = j0 + u * kT + tid;
-      v[u] = j < ns_c ? __ldg(row_base + lo + (j_lo + j) * S) : 0.f;
-    }
+      for (int u = 0; u < 16; ++u) {
+        const int j = j0 + u * kT + tid;
+        v[u] = j < ns32 ? __ldg(samp + j * S32) : 0.f;
+      }
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const int64_t j = j0 + u * kT + tid;
-      if (j < ns_c) sh.cand_key[j] = order_key(v[u]);
+      for (int u = 0; u < 16; ++u) {
+        const int j = j0 + u * kT + tid;
+        if (j < ns32) sh.cand_key[j] = order_key(v[u]);
+      }
     }
   }
   __syncthreads();
@@ -780,30 +791,6 @@ __device__ uint32_t block_kth_key(Get get, int64_t n, uint32_t need, uint32_t* h
   *above_out = a1 + misc[1];
   __syncthreads();
   return T;
-}
-
-// Ascending sort of a[0, n) in shared memory (bitonic network over the next
-// power of two, padded with INT32_MAX; `a` has room for it).
-__device__ void block_sort_ascending(int32_t* a, int n) {
-  const int tid = threadIdx.x;
-  int P = 1;
-  while (P < n) P <<= 1;
-  for (int i = n + tid; i < P; i += kT) a[i] = 0x7FFFFFFF;
-  __syncthreads();
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < P / 2; i += kT) {
-        const int lo = 2 * i - (i & (stride - 1)), hi = lo + stride;
-        const bool asc = (lo & size) == 0;
-        const int32_t x = a[lo], y = a[hi];
-        if ((x > y) == asc) {
-          a[lo] = y;
-          a[hi] = x;
-        }
-      }
-      __syncthreads();
-    }
-  }
 }
 
 }  // namespace

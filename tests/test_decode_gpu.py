@@ -82,6 +82,22 @@ def test_decode_planner_overrides(fp8idx, oracle_impl, opts):
     assert_rows_close(gpu, ref, written=decode_window_mask(case), what=str(opts))
 
 
+@pytest.mark.parametrize("num_ctas", [1, 2, 5, 0])
+def test_decode_block1_table_prefetch_edges(fp8idx, oracle_impl, num_ctas):
+    """Block size 1: each producer lane loads its block-table entries two
+    tiles ahead of their use.  Requests of 1 token to 5 tiles, one exactly a
+    tile long, and CTA ranges that start inside a request (num_ctas) cover
+    every case of that look-ahead: a request shorter than the look-ahead,
+    the last tiles of a request, and a range that begins mid-request."""
+    ctx = [1, 129, 256, 257, 383, 130, 2, 640]
+    case = workloads.decode_case(len(ctx), 2, 32, max_model_len=640, block_size=1, context_lens=ctx, seed=71,
+                                 poison=True, extra_blocks=3)
+    opts = fp8idx.Options(num_ctas=num_ctas) if num_ctas else None
+    gpu = run_decode(fp8idx, case, options=opts).cpu().numpy()
+    ref = oracle_decode(oracle_impl, case)
+    assert_rows_close(gpu, ref, written=decode_window_mask(case), what=f"blk1 num_ctas={num_ctas}")
+
+
 def test_decode_config0(fp8idx, oracle_impl):
     case = workloads.make_config(0)
     gpu = run_decode(fp8idx, case).cpu().numpy()
