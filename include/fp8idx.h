@@ -125,7 +125,8 @@ typedef struct {
  *  block_tables [batch, max_blocks] I32, contiguous rows (stride[0] >=
  *               max_blocks, stride[1] == 1); entry j of row b is the physical
  *               block holding tokens [j*block_size, (j+1)*block_size).
- *  max_model_len  output width.
+ *  max_model_len  output width, at most 2^31 - 512 (UNSUPPORTED above: the
+ *               kernel keeps positions in 32-bit registers).
  *  out          [batch*next_n, >= max_model_len] F32, stride[1] == 1,
  *               stride[0] >= max_model_len.
  * Supported (fp8idx_paged_is_supported): head_dim 128; heads 32 or 64;

@@ -297,6 +297,9 @@ fp8idx_status paged_setup(const fp8idx_tensor* q, const fp8idx_tensor* kv, const
   TRY(check_tensor(bt, "block_tables", FP8IDX_I32, 2));
   const int64_t B = q->shape[0], next_n = q->shape[1], H = q->shape[2], D = q->shape[3];
   if (max_model_len < 0) return fail(FP8IDX_ERR_INVALID, "max_model_len < 0");
+  if (max_model_len > kMaxModelLen)
+    return fail(FP8IDX_ERR_UNSUPPORTED, "max_model_len %d > %d (positions are kept in 32 bits)", max_model_len,
+                kMaxModelLen);
   if (!contiguous(q)) return fail(FP8IDX_ERR_INVALID, "q_fp8 must be contiguous");
   if (!contiguous(kv)) return fail(FP8IDX_ERR_INVALID, "kv_cache must be contiguous");
   if (!contiguous(w)) return fail(FP8IDX_ERR_INVALID, "weights must be contiguous");

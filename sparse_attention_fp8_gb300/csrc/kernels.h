@@ -50,6 +50,9 @@ struct PagedParams {
 // accumulators (512 columns in buffers of the smallest power of two >=
 // n_cols), so the MMA warp can run that many tiles ahead of the epilogue.
 constexpr int kEpiGroups = 2;
+// Decode positions (and a tile past them) stay below 2^31: the epilogue keeps
+// them in 32-bit registers.
+constexpr int32_t kMaxModelLen = 0x7FFFFE00;
 constexpr int kMaxAccBufs = 16;
 __host__ __device__ constexpr int pow2_cols(int n_cols) {
   return n_cols <= 32 ? 32 : n_cols <= 64 ? 64 : n_cols <= 128 ? 128 : 256;

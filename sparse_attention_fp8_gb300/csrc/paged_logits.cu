@@ -489,8 +489,9 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
           if (lane == 0) ptx::mbar_arrive(empty0 + 8u * st.idx);
           if (!warp_wait_bounded(accf0 + 8u * ac.idx, ac.phase, abort_flag, &g_paged_watchdog, kSiteAccFull)) break;
           ptx::tc_fence_after();
-          const int64_t pos = static_cast<int64_t>(cur.t) * IS * ITEM + k_tile * kTileTokens + row;
-          const int64_t room = static_cast<int64_t>(ctx) - next_n - pos;  // row n is written iff n + room >= 0
+          // (32-bit: positions and context lengths are below 2^31)
+          const int pos = cur.t * IS * ITEM + k_tile * kTileTokens + row;
+          const int room = ctx - next_n - pos;  // row n is written iff n + room >= 0
           const bool in_model = pos < p.max_model_len;
           float* out_col = p.out + static_cast<int64_t>(cur.b) * next_n * p.out_stride + pos;
           const uint32_t acce = acce0 + 8u * ac.idx;

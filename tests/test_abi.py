@@ -127,6 +127,17 @@ def test_validation_rejects_before_touching_the_device(lib):
     assert st == fp8idx.FP8IDX_ERR_INVALID
 
 
+def test_max_model_len_bound(lib):
+    """Decode positions are kept in 32-bit registers: max_model_len above
+    2^31 - 512 is UNSUPPORTED, reported by the host checks (fake pointers)."""
+    B, n, H, D = 2, 2, 32, 128
+    big = 0x7FFFFE01
+    R = ctypes.byref
+    st = lib.fp8_paged_mqa_logits(R(_t(0, (B, n, H, D))), R(_t(0, (4, 64 * (D + 4)))), R(_t(1, (B * n, H))),
+                                  R(_t(2, (B,))), R(_t(2, (B, 2))), big, R(_t(1, (B * n, big))), None)
+    assert st == fp8idx.FP8IDX_ERR_UNSUPPORTED and b"32 bits" in lib.fp8idx_last_error()
+
+
 def test_misaligned_pointers_rejected(lib):
     """Operands read by TMA or bulk copies must be 16-byte aligned: an
     address 4 bytes off returns INVALID from the host checks, before any
