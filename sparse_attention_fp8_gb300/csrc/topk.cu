@@ -765,13 +765,13 @@ __device__ __forceinline__ float key_value(uint32_t key) {
 // keys above it: three radix levels (12, 12, 8 bits) over block-wide
 // shared-memory histograms.  Every thread of the block calls it.
 template <class Get>
-__device__ uint32_t block_kth_key(Get get, int64_t n, uint32_t need, uint32_t* hist, uint32_t* scan, uint32_t* misc,
+__device__ uint32_t block_kth_key(Get get, int n, uint32_t need, uint32_t* hist, uint32_t* scan, uint32_t* misc,
                                   uint32_t* above_out) {
   const int tid = threadIdx.x;
   const auto level = [&](int nbins, auto sel, auto bin) {
     for (int i = tid; i < nbins; i += kT) hist[i] = 0u;
     __syncthreads();
-    for (int64_t i = tid; i < n; i += kT) {
+    for (int i = tid; i < n; i += kT) {
       const uint32_t key = get(i);
       hist_add(hist, sel(key), bin(key));
     }
@@ -832,17 +832,22 @@ __global__ void __launch_bounds__(kTopkThreads, 1) fused_threshold_kernel(const 
   const int64_t n_s = (Jq - 1) * I + min(I, W - last * SI);
   const float* row = p.logits + r * p.ls;
   // the sample's keys into shared memory: eight loads in flight per thread
-  for (int64_t e0 = 0; e0 < n_s; e0 += 8 * kT) {
-    float v[8];
+  {
+    // (32-bit offsets: the sample holds at most kFusedMaxSample values, the
+    // row's positions are below 2^31)
+    const int n32 = static_cast<int>(n_s), qSI = static_cast<int>(q * SI);
+    for (int e0 = 0; e0 < n32; e0 += 8 * kT) {
+      float v[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int64_t e = e0 + u * kT + tid, j = e >> lgI;
-      v[u] = e < n_s ? row[j * q * SI + (e - (j << lgI))] : 0.f;
-    }
+      for (int u = 0; u < 8; ++u) {
+        const int e = e0 + u * kT + tid, j = e >> lgI;
+        v[u] = e < n32 ? row[j * qSI + (e - (j << lgI))] : 0.f;
+      }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int64_t e = e0 + u * kT + tid;
-      if (e < n_s) keys[e] = order_key(v[u]);
+      for (int u = 0; u < 8; ++u) {
+        const int e = e0 + u * kT + tid;
+        if (e < n32) keys[e] = order_key(v[u]);
+      }
     }
   }
   __syncthreads();
@@ -857,7 +862,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) fused_threshold_kernel(const 
   float t = -INFINITY;
   if (m <= n_s) {
     uint32_t above;
-    t = key_value(block_kth_key([&](int64_t i) { return keys[i]; }, n_s, static_cast<uint32_t>(m), hist, scan, misc,
+    t = key_value(block_kth_key([&](int i) { return keys[i]; }, static_cast<int>(n_s), static_cast<uint32_t>(m), hist, scan, misc,
                                 &above));
   }
   if (tid == 0) p.thr[r] = t;
@@ -889,19 +894,20 @@ __global__ void __launch_bounds__(kTopkThreads, 1) fused_select_kernel(const Fus
   }
   // the bitmap's count; each thread owns a contiguous run of words, read as
   // 16-byte vectors (the row's words start 16-byte aligned)
-  const int64_t nw = (W + 31) / 32;
-  const int64_t nv = (nw + 3) / 4;
-  const int64_t vpt = (nv + kT - 1) / kT;
-  const int64_t v0 = min(nv, tid * vpt), v1 = min(nv, v0 + vpt);
+  // (32-bit offsets: positions are below 2^31)
+  const int nw = static_cast<int>((W + 31) / 32);
+  const int nv = (nw + 3) / 4;
+  const int vpt = (nv + kT - 1) / kT;
+  const int v0 = min(nv, tid * vpt), v1 = min(nv, v0 + vpt);
   const uint4* bits4 = reinterpret_cast<const uint4*>(p.cand + r * p.tw);
   // (the filter pass writes every word whose first position is in the
   // window; the words of the last vector past the window are not read)
-  const auto word = [&](int64_t v, int q, const uint4& x) -> uint32_t {
+  const auto word = [&](int v, int q, const uint4& x) -> uint32_t {
     const uint32_t w = q == 0 ? x.x : q == 1 ? x.y : q == 2 ? x.z : x.w;
     return v * 4 + q < nw ? w : 0u;
   };
   uint32_t mine = 0;
-  for (int64_t v = v0; v < v1; ++v) {
+  for (int v = v0; v < v1; ++v) {
     const uint4 x = bits4[v];
 #pragma unroll
     for (int q = 0; q < 4; ++q) mine += __popc(word(v, q, x));
@@ -918,7 +924,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) fused_select_kernel(const Fus
   }
   {
     uint32_t j = before;
-    for (int64_t v = v0; v < v1; ++v) {
+    for (int v = v0; v < v1; ++v) {
       const uint4 x = bits4[v];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -947,7 +953,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) fused_select_kernel(const Fus
   }
   __syncthreads();
   uint32_t above;
-  const uint32_t T = block_kth_key([&](int64_t i) { return keys[i]; }, cA, static_cast<uint32_t>(k), hist, scan,
+  const uint32_t T = block_kth_key([&](int i) { return keys[i]; }, static_cast<int>(cA), static_cast<uint32_t>(k), hist, scan,
                                    misc, &above);
   const uint32_t need_eq = static_cast<uint32_t>(k) - above;
   uint32_t n_gt = 0, n_eq = 0;
