@@ -16,7 +16,9 @@
 //  * Radix select of the k-th largest key T: three levels of histograms
 //    (12, 12, 8 bits of the key; plain shared atomics).
 //  * A window of at most `cap` values is brought into shared memory by one
-//    bulk copy and selected there.  A longer one is sampled with a stride S
+//    bulk copy straight into the key array, converted to keys in place while
+//    the first radix level is counted, and selected there (positions
+//    implicit).  A longer one is sampled with a stride S
 //    (at most cap samples); the sample's (2k/S + 32)-th largest key is a
 //    lower threshold, and the values above it (about 2k + 32S of them) are
 //    compacted into shared memory, in position order, for the exact select:
@@ -27,10 +29,12 @@
 //    every candidate at its final slot).  If the kept count falls outside
 //    [k, cap] (adversarial or heavily tied rows), the levels and the
 //    selection re-read the window from global memory instead.
-//  * Selection: an ordered pass keeps every key above the k-th key T and the
-//    first (k - #above) keys equal to T in position order (block-wide
-//    prefix sums), so ties resolve to the lowest positions, and writes the
-//    kept positions straight to the output in position order.
+//  * Selection: every key above the k-th key T and the first (k - #above)
+//    keys equal to T in position order are kept, so ties resolve to the
+//    lowest positions, and written straight to the output in position
+//    order: with one CTA per row each thread marks a run of consecutive keys
+//    and one packed block scan places the runs; in a cluster an ordered pass
+//    with warp ballots and block-wide prefix sums.
 // Rows far too few to fill the GPU (the host's rule: at most a quarter of
 // the SM count) with long windows are each split over a thread-block cluster
 // of C CTAs instead (or as many as the caller asks for): every step
@@ -305,14 +309,15 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, uint8_t* smem_raw)
   };
 
   // ---- sources: the slice in global memory, or candidates in shared memory
-  const auto smem_hist = [&](int64_t n_c64, auto sel, auto bin) {
+  const auto smem_hist_at = [&](const uint32_t* src, int64_t n_c64, auto sel, auto bin) {
     const int n_c = static_cast<int>(n_c64);  // at most cap
     for (int i0 = 0; i0 < n_c; i0 += kT) {
       const int i = i0 + tid;
-      const uint32_t key = i < n_c ? sh.cand_key[i] : 0u;
+      const uint32_t key = i < n_c ? src[i] : 0u;
       hist_add(sh.hist, i < n_c && sel(key), bin(key));
     }
   };
+  const auto smem_hist = [&](int64_t n_c64, auto sel, auto bin) { smem_hist_at(sh.cand_key, n_c64, sel, bin); };
   // Ordered passes: element e of a source is (key, position); a chunk is
   // kT*kPer elements, warp w takes the chunk's w-th run of 32*kPer, step j
   // of the run one element per lane (consecutive lanes, consecutive
@@ -383,10 +388,14 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, uint8_t* smem_raw)
   // ---- the `need`-th largest key T of the cluster's source and #keys > T,
   // three radix levels (12, 12 and 8 bits of the key)
   // (levels = 2: T is the lower edge of the 24-bit bin holding that key)
+  // (level1_done: the caller has already counted every key's top 12 bits
+  // into the zeroed histogram)
   const auto radix_select = [&](auto hist_pass, uint32_t need, uint32_t* T_out, uint32_t* above_out,
-                                int levels = 3) {
-    zero_level(kTopkBins);
-    hist_pass([](uint32_t) { return true; }, [](uint32_t key) { return key >> 20; });
+                                int levels = 3, bool level1_done = false) {
+    if (!level1_done) {
+      zero_level(kTopkBins);
+      hist_pass([](uint32_t) { return true; }, [](uint32_t key) { return key >> 20; });
+    }
     __syncthreads();
     combine(kTopkBins);
     find_bin<kTopkBins>(sh.hsum, need, sh.scan, sh.misc);
@@ -445,49 +454,93 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, uint8_t* smem_raw)
         gt0, eq0);
   };
 
+  // Selection of a window (one CTA per row) whose keys sit in shared memory
+  // at kb[0, n) in position order, key i at position pos_of(i): thread t
+  // takes the run [t*m, t*m + m) (m odd, so
+  // the lanes of a warp read different banks), one pass marks its keys > T
+  // and == T in two bit masks, one packed block scan gives every run its
+  // counts before it, and the run's kept positions are written in order.
+  const auto select_runs = [&](const uint32_t* kb, int n, auto pos_of, uint32_t T, uint32_t above) {
+    const uint32_t need_eq = static_cast<uint32_t>(k) - above;
+    const int m = ((n + kT - 1) / kT) | 1;  // at most cap / kT + 1 <= 17
+    const int e0 = tid * m, e1 = min(n, e0 + m);
+    uint32_t mgt = 0u, meq = 0u;
+    for (int e = e0; e < e1; ++e) {
+      const uint32_t key = kb[e];
+      mgt |= (key > T ? 1u : 0u) << (e - e0);
+      meq |= (key == T ? 1u : 0u) << (e - e0);
+    }
+    uint32_t tot;  // both counts in one scan (16:16; a slice has fewer than 2^16 keys)
+    const uint32_t ex = block_scan((static_cast<uint32_t>(__popc(mgt)) << 16) | static_cast<uint32_t>(__popc(meq)),
+                                   sh.scan, &tot);
+    (void)tot;
+    uint32_t n_gt = ex >> 16, n_eq = ex & 0xFFFFu;
+    for (uint32_t keep = mgt | meq; keep != 0u; keep &= keep - 1u) {
+      const int j = __ffs(keep) - 1;
+      if ((mgt >> j) & 1u) {
+        out_row[n_gt + (n_eq < need_eq ? n_eq : need_eq)] = pos_of(e0 + j);
+        ++n_gt;
+      } else {
+        if (n_eq < need_eq) out_row[n_gt + n_eq] = pos_of(e0 + j);
+        ++n_eq;
+      }
+    }
+  };
+
   uint32_t T = 0, above = 0;
   if ((L + C - 1) / C + 4 <= p.cap) {
-    // Short windows: each slice into its CTA's shared memory (keys and
-    // positions in position order), then everything runs there.  Aligned
-    // rows: one bulk copy of [slo rounded down to 4, shi rounded down to 4)
-    // into the ring, the last (at most 3) values by plain loads.
+    // Short windows: each slice into its CTA's shared memory, then
+    // everything runs there.  Aligned rows: one bulk copy of [slo rounded
+    // down to 4, shi rounded down to 4) straight into the key array, the
+    // last (at most 3) values by plain loads; the keys are converted in
+    // place while the first radix level is counted, and the positions are
+    // implicit (key i of the slice is position slo + i).
     const int64_t b0 = slo & ~static_cast<int64_t>(3), a1 = shi & ~static_cast<int64_t>(3);
     const bool staged = vec && a1 > b0;
+    // (32-bit offsets: a slice here holds at most cap - 4 values, positions are below 2^31)
+    const int Ls32 = static_cast<int>(Ls), slo32 = static_cast<int>(slo);
+    const int a1r = static_cast<int>(a1 - slo);  // the staged part is [0, a1r) of the slice
+    uint32_t* const kbase = sh.cand_key + (staged ? static_cast<int>(slo - b0) : 0);
+    zero_level(kTopkBins);
     if (staged) {
       if (tid == 0) {
         ptx::fence_proxy_async_smem();
         const uint32_t bytes = static_cast<uint32_t>((a1 - b0) * 4);
         ptx::mbar_arrive_expect_tx(sh.bar, bytes);
-        ptx::bulk_g2s(ptx::smem_u32(sh.ring), row_base + b0, bytes, sh.bar);
+        ptx::bulk_g2s(ptx::smem_u32(sh.cand_key), row_base + b0, bytes, sh.bar);
       }
       // bounded: a wait that runs out flags the watchdog; in-flight bytes
-      // land before the ring is reused
+      // land before the array is reused
       wait_bounded(sh.bar, 0u, abort_flag, &g_topk_watchdog, kSiteStageFull);
       if (*abort_flag && tid == 0) wait_drain(sh.bar, 0u, &g_topk_watchdog);
     }
-    // (32-bit offsets: a slice here holds at most cap values, positions are below 2^31)
-    const int Ls32 = static_cast<int>(Ls), slo32 = static_cast<int>(slo);
-    const int a1r = static_cast<int>(a1 - slo);  // the staged part is [0, a1r) of the slice
-    const float* ring_s = sh.ring + (slo - b0);
     for (int i0 = 0; i0 < Ls32; i0 += kT * 4) {
       float v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int i = i0 + u * kT + tid;
-        v[u] = i >= Ls32 ? 0.f : (staged && i < a1r) ? ring_s[i] : __ldg(row_base + slo32 + i);
+        v[u] = i >= Ls32 ? 0.f : (staged && i < a1r) ? __uint_as_float(kbase[i]) : __ldg(row_base + slo32 + i);
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int i = i0 + u * kT + tid;
         if (i < Ls32) {
-          sh.cand_key[i] = order_key(v[u]);
-          sh.cand_pos[i] = slo32 + i;
+          const uint32_t key = order_key(v[u]);
+          kbase[i] = key;
+          hist_add(sh.hist, true, key >> 20);
         }
       }
     }
-    __syncthreads();
-    radix_select([&](auto sel, auto bin) { smem_hist(Ls, sel, bin); }, static_cast<uint32_t>(k), &T, &above);
-    select(Ls, smem_get, T, above);
+    radix_select([&](auto sel, auto bin) { smem_hist_at(kbase, Ls, sel, bin); }, static_cast<uint32_t>(k), &T,
+                 &above, 3, true);
+    if constexpr (!kCluster) {
+      select_runs(kbase, Ls32, [&](int e) { return slo32 + e; }, T, above);
+    } else {
+      select(Ls, [&](int e, uint32_t& key, int32_t& pos) {
+        key = kbase[e];
+        pos = slo32 + e;
+      }, T, above);
+    }
     return;
   }
 
@@ -694,7 +747,10 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, uint8_t* smem_raw)
   if (cnt.all >= static_cast<uint32_t>(k) && cnt.max <= static_cast<uint32_t>(p.cap)) {
     // Every key >= the k-th largest is a candidate, in position order.
     radix_select([&](auto sel, auto bin) { smem_hist(n_c, sel, bin); }, static_cast<uint32_t>(k), &T, &above);
-    select(n_c, smem_get, T, above);
+    if constexpr (!kCluster)
+      select_runs(sh.cand_key, static_cast<int>(n_c), [&](int e) { return sh.cand_pos[e]; }, T, above);
+    else
+      select(n_c, smem_get, T, above);
   } else {
     radix_select(window_hist, static_cast<uint32_t>(k), &T, &above);
     select(Ls, global_get, T, above);
