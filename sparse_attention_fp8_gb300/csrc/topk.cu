@@ -150,6 +150,40 @@ __device__ __forceinline__ void find_bin(const uint32_t* hist, uint32_t need, ui
   __syncthreads();
 }
 
+// Writes the positions of every key > T and of the first need_eq keys == T
+// among kb[0, n) (keys in position order, key i at position pos_of(i)) to
+// out_row in position order.  Thread t takes the run [t*m, t*m + m) (m
+// odd, so the lanes of a warp read different banks), marks its keys > T and
+// == T in two bit masks in one pass, one packed block scan gives every run
+// its counts before it, and the run's kept positions are written in order.
+// n <= 31 * kT.  Every thread of the block calls it.
+template <class PosOf>
+__device__ __forceinline__ void write_kept_runs(const uint32_t* kb, int n, PosOf pos_of, uint32_t T,
+                                                uint32_t need_eq, int32_t* out_row, uint32_t* scan) {
+  const int m = ((n + kT - 1) / kT) | 1;
+  const int e0 = threadIdx.x * m, e1 = min(n, e0 + m);
+  uint32_t mgt = 0u, meq = 0u;
+  for (int e = e0; e < e1; ++e) {
+    const uint32_t key = kb[e];
+    mgt |= (key > T ? 1u : 0u) << (e - e0);
+    meq |= (key == T ? 1u : 0u) << (e - e0);
+  }
+  uint32_t tot;  // both counts in one scan (16:16; fewer than 2^16 keys)
+  const uint32_t ex = block_scan((static_cast<uint32_t>(__popc(mgt)) << 16) | static_cast<uint32_t>(__popc(meq)),
+                                 scan, &tot);
+  uint32_t n_gt = ex >> 16, n_eq = ex & 0xFFFFu;
+  for (uint32_t keep = mgt | meq; keep != 0u; keep &= keep - 1u) {
+    const int j = __ffs(keep) - 1;
+    if ((mgt >> j) & 1u) {
+      out_row[n_gt + (n_eq < need_eq ? n_eq : need_eq)] = pos_of(e0 + j);
+      ++n_gt;
+    } else {
+      if (n_eq < need_eq) out_row[n_gt + n_eq] = pos_of(e0 + j);
+      ++n_eq;
+    }
+  }
+}
+
 }  // namespace
 
 // One row's selection by C CTAs: one CTA, or (kCluster) the C CTAs of a
@@ -455,36 +489,9 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, uint8_t* smem_raw)
   };
 
   // Selection of a window (one CTA per row) whose keys sit in shared memory
-  // at kb[0, n) in position order, key i at position pos_of(i): thread t
-  // takes the run [t*m, t*m + m) (m odd, so
-  // the lanes of a warp read different banks), one pass marks its keys > T
-  // and == T in two bit masks, one packed block scan gives every run its
-  // counts before it, and the run's kept positions are written in order.
+  // in position order (write_kept_runs).
   const auto select_runs = [&](const uint32_t* kb, int n, auto pos_of, uint32_t T, uint32_t above) {
-    const uint32_t need_eq = static_cast<uint32_t>(k) - above;
-    const int m = ((n + kT - 1) / kT) | 1;  // at most cap / kT + 1 <= 17
-    const int e0 = tid * m, e1 = min(n, e0 + m);
-    uint32_t mgt = 0u, meq = 0u;
-    for (int e = e0; e < e1; ++e) {
-      const uint32_t key = kb[e];
-      mgt |= (key > T ? 1u : 0u) << (e - e0);
-      meq |= (key == T ? 1u : 0u) << (e - e0);
-    }
-    uint32_t tot;  // both counts in one scan (16:16; a slice has fewer than 2^16 keys)
-    const uint32_t ex = block_scan((static_cast<uint32_t>(__popc(mgt)) << 16) | static_cast<uint32_t>(__popc(meq)),
-                                   sh.scan, &tot);
-    (void)tot;
-    uint32_t n_gt = ex >> 16, n_eq = ex & 0xFFFFu;
-    for (uint32_t keep = mgt | meq; keep != 0u; keep &= keep - 1u) {
-      const int j = __ffs(keep) - 1;
-      if ((mgt >> j) & 1u) {
-        out_row[n_gt + (n_eq < need_eq ? n_eq : need_eq)] = pos_of(e0 + j);
-        ++n_gt;
-      } else {
-        if (n_eq < need_eq) out_row[n_gt + n_eq] = pos_of(e0 + j);
-        ++n_eq;
-      }
-    }
+    write_kept_runs(kb, n, pos_of, T, static_cast<uint32_t>(k) - above, out_row, sh.scan);
   };
 
   uint32_t T = 0, above = 0;
@@ -1011,19 +1018,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1) fused_select_kernel(const Fus
   uint32_t above;
   const uint32_t T = block_kth_key([&](int i) { return keys[i]; }, static_cast<int>(cA), static_cast<uint32_t>(k), hist, scan,
                                    misc, &above);
-  const uint32_t need_eq = static_cast<uint32_t>(k) - above;
-  uint32_t n_gt = 0, n_eq = 0;
-  for (uint32_t i0 = 0; i0 < cA; i0 += kT) {  // in position order: slot = kept candidates before
-    const uint32_t i = i0 + tid;
-    const uint32_t key = i < cA ? keys[i] : 0u;
-    const bool gt = i < cA && key > T, eq = i < cA && key == T;
-    uint32_t tot;  // both counts in one scan (16:16; a chunk has kT < 2^16 elements)
-    const uint32_t rk = block_scan((gt ? 0x10000u : 0u) | (eq ? 1u : 0u), scan, &tot);
-    const uint32_t rg = rk >> 16, e_rank = n_eq + (rk & 0xFFFFu);
-    if (gt || (eq && e_rank < need_eq)) out_row[n_gt + rg + (e_rank < need_eq ? e_rank : need_eq)] = pos[i];
-    n_gt += tot >> 16;
-    n_eq += tot & 0xFFFFu;
-  }
+  write_kept_runs(keys, static_cast<int>(cA), [&](int e) { return pos[e]; }, T, static_cast<uint32_t>(k) - above,
+                  out_row, scan);
 }
 
 cudaError_t launch_fused_threshold(const FusedTopkParams& p, int smem_bytes, cudaStream_t stream) {
