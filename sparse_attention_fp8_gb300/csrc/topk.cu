@@ -829,7 +829,7 @@ __device__ __forceinline__ float key_value(uint32_t key) {
 // shared-memory histograms.  Every thread of the block calls it.
 template <class Get>
 __device__ uint32_t block_kth_key(Get get, int n, uint32_t need, uint32_t* hist, uint32_t* scan, uint32_t* misc,
-                                  uint32_t* above_out) {
+                                  uint32_t* above_out, bool lower_edge_24 = false) {
   const int tid = threadIdx.x;
   const auto level = [&](int nbins, auto sel, auto bin) {
     for (int i = tid; i < nbins; i += kT) hist[i] = 0u;
@@ -848,6 +848,10 @@ __device__ uint32_t block_kth_key(Get get, int n, uint32_t need, uint32_t* hist,
   find_bin<kTopkBins>(hist, need - a0, scan, misc);
   const uint32_t pre24 = (b0 << 12) | misc[0], a1 = a0 + misc[1];
   __syncthreads();
+  if (lower_edge_24) {  // the lower edge of the 24-bit bin holding that key (a lower bound of it)
+    *above_out = a1;
+    return pre24 << 8;
+  }
   level(256, [&](uint32_t key) { return (key >> 8) == pre24; }, [](uint32_t key) { return key & 0xFFu; });
   find_bin<256>(hist, need - a1, scan, misc);
   const uint32_t T = (pre24 << 8) | misc[0];
@@ -925,8 +929,13 @@ __global__ void __launch_bounds__(kTopkThreads, 1) fused_threshold_kernel(const 
   float t = -INFINITY;
   if (m <= n_s) {
     uint32_t above;
-    t = key_value(block_kth_key([&](int i) { return keys[i]; }, static_cast<int>(n_s), static_cast<uint32_t>(m), hist, scan, misc,
-                                &above));
+    // (a threshold from a part of the window need only be a lower bound of
+    // the m-th largest sample: two radix levels, the lower edge of its
+    // 24-bit bin; a whole-window sample gives the exact k-th largest)
+    uint32_t tk = block_kth_key([&](int i) { return keys[i]; }, static_cast<int>(n_s), static_cast<uint32_t>(m), hist,
+                                scan, misc, &above, n_s < W);
+    const uint32_t k_ninf = order_key(-INFINITY);  // (the edge of the bin holding -inf is a NaN pattern)
+    t = key_value(tk > k_ninf ? tk : k_ninf);
   }
   if (tid == 0) p.thr[r] = t;
 }
