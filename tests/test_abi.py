@@ -127,6 +127,24 @@ def test_validation_rejects_before_touching_the_device(lib):
     assert st == fp8idx.FP8IDX_ERR_INVALID
 
 
+def test_descriptor_packing():
+    """The binding packs each tensor into fp8idx_tensor bytes in one call:
+    the same layout as the ctypes structure (pointer, dtype, ndim, shape[4],
+    stride[4]), unused dimensions zero, strides in elements."""
+    import torch
+    t = torch.empty((3, 5, 7), dtype=torch.float32)[:, ::2, :]
+    d = _native._Tensor.from_buffer_copy(_native._desc(t))
+    assert d.data == t.data_ptr() and d.dtype == 1 and d.ndim == 3
+    assert list(d.shape) == [3, 3, 7, 0] and list(d.stride) == [35, 14, 1, 0]
+    u = torch.empty(16, dtype=torch.uint8)
+    d = _native._Tensor.from_buffer_copy(_native._desc(u))
+    assert d.dtype == 0 and d.ndim == 1 and list(d.shape) == [16, 0, 0, 0] and list(d.stride) == [1, 0, 0, 0]
+    with pytest.raises(TypeError):
+        _native._desc(torch.empty(4, dtype=torch.float64))
+    with pytest.raises(ValueError):
+        _native._desc(torch.empty((1, 1, 1, 1, 1), dtype=torch.float32))
+
+
 def test_max_model_len_bound(lib):
     """Decode positions are kept in 32-bit registers: max_model_len above
     2^31 - 512 is UNSUPPORTED, reported by the host checks (fake pointers)."""
