@@ -1025,8 +1025,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1) fused_select_kernel(const Fus
   }
   __syncthreads();
   uint32_t above;
-  const uint32_t T = block_kth_key([&](int i) { return keys[i]; }, static_cast<int>(cA), static_cast<uint32_t>(k), hist, scan,
-                                   misc, &above);
+  const uint32_t T = block_kth_key([&](int i) { return keys[i]; }, static_cast<int>(cA), static_cast<uint32_t>(k), hist,
+                                   scan, misc, &above);
   write_kept_runs(keys, static_cast<int>(cA), [&](int e) { return pos[e]; }, T, static_cast<uint32_t>(k) - above,
                   out_row, scan);
 }
