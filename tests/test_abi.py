@@ -154,6 +154,12 @@ def test_max_model_len_bound(lib):
     st = lib.fp8_paged_mqa_logits(R(_t(0, (B, n, H, D))), R(_t(0, (4, 64 * (D + 4)))), R(_t(1, (B * n, H))),
                                   R(_t(2, (B,))), R(_t(2, (B, 2))), big, R(_t(1, (B * n, big))), None)
     assert st == fp8idx.FP8IDX_ERR_UNSUPPORTED and b"32 bits" in lib.fp8idx_last_error()
+    # the fused decode top-k shares the decode set-up (and its bound)
+    k = 8
+    st = lib.fp8_paged_mqa_topk(R(_t(0, (B, n, H, D))), R(_t(0, (4, 64 * (D + 4)))), R(_t(1, (B * n, H))),
+                                R(_t(2, (B,))), R(_t(2, (B, 2))), big, k, R(_t(2, (B * n, k))),
+                                ctypes.c_void_p(0x100000), ctypes.c_size_t(1 << 40), None, None)
+    assert st == fp8idx.FP8IDX_ERR_UNSUPPORTED and b"32 bits" in lib.fp8idx_last_error()
 
 
 def test_misaligned_pointers_rejected(lib):
