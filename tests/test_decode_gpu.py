@@ -98,6 +98,27 @@ def test_decode_block1_table_prefetch_edges(fp8idx, oracle_impl, num_ctas):
     assert_rows_close(gpu, ref, written=decode_window_mask(case), what=f"blk1 num_ctas={num_ctas}")
 
 
+@pytest.mark.parametrize("blk", [64, 1])
+def test_decode_max_batch(fp8idx, oracle_impl, blk):
+    """The largest batch a call accepts (4096 requests: the per-request tile
+    prefix lives in shared memory and the planner trims the ring for it),
+    with short ragged contexts (0 to 300 tokens), against the oracle on every
+    row; one request more is UNSUPPORTED."""
+    B = 4096
+    rng = np.random.default_rng(91)
+    ctx = rng.integers(0, 301, size=B)
+    ctx[:3] = [0, 1, 300]
+    case = workloads.decode_case(B, 2, 32, max_model_len=320, block_size=blk, context_lens=ctx, seed=91)
+    gpu = run_decode(fp8idx, case).cpu().numpy()
+    ref = oracle_decode(oracle_impl, case)
+    assert_rows_close(gpu, ref, written=decode_window_mask(case), what=f"batch {B} blk{blk}")
+    if blk == 64:
+        big = workloads.decode_case(B + 1, 1, 32, max_model_len=64, block_size=64, context_lens=[64] * (B + 1), seed=92)
+        with pytest.raises(fp8idx.Fp8IdxError) as e:
+            run_decode(fp8idx, big)
+        assert e.value.status == fp8idx.FP8IDX_ERR_UNSUPPORTED
+
+
 def test_decode_config0(fp8idx, oracle_impl):
     case = workloads.make_config(0)
     gpu = run_decode(fp8idx, case).cpu().numpy()
