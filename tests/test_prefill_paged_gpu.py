@@ -72,6 +72,29 @@ def test_paged_prefill_many_small_requests(fp8idx, oracle_impl, split):
                       what=f"small requests split {split}")
 
 
+@pytest.mark.parametrize("blk", [16, 1])
+def test_paged_prefill_max_requests(fp8idx, oracle_impl, blk):
+    """The largest request count a call accepts (4096: the request offsets
+    and the padded tile prefix live in shared memory), requests of 0 to 7
+    tokens with 0 or 1 query rows, against the oracle on every row; one
+    request more is UNSUPPORTED."""
+    R = 4096
+    rng = np.random.default_rng(17)
+    lens = rng.integers(0, 8, R)
+    rows = np.minimum(lens, rng.integers(0, 2, R))
+    case = workloads.paged_prefill_case(lens, rows, 32, block_size=blk, seed=18)
+    k, s = gathered(case)
+    gpu = run_paged(fp8idx, case)
+    assert_rows_close(gpu, oracle_impl.mqa_logits(case.q, k, s, case.weights, case.ks, case.ke),
+                      what=f"{R} requests blk{blk}")
+    if blk == 16:
+        lens2 = np.ones(R + 1, np.int64)
+        big = workloads.paged_prefill_case(lens2, lens2, 32, block_size=16, seed=19)
+        with pytest.raises(fp8idx.Fp8IdxError) as e:
+            run_paged(fp8idx, big)
+        assert e.value.status == fp8idx.FP8IDX_ERR_UNSUPPORTED
+
+
 def test_paged_prefill_no_clean_and_overrides(fp8idx, oracle_impl):
     case = workloads.paged_prefill_case([900, 257], [70, 40], 32, block_size=64, seed=11, poison=True)
     k, s = gathered(case)
