@@ -57,6 +57,28 @@ def test_mqa_topk_window_modes(fp8idx, mode, k):
     assert np.array_equal(gpu_mqa_topk(fp8idx, logits, ks, ke, k), want), f"{mode} k={k}"
 
 
+@pytest.mark.parametrize("k", [512, 2048])
+def test_mqa_topk_short_long_boundary(fp8idx, k):
+    """Windows on both sides of the length where the selection moves from
+    the whole window in shared memory (at most 8188 values: bulk copy into
+    the key array, per-thread runs of up to 17 keys) to the sampled
+    threshold and candidate compaction, starting at every offset modulo 4
+    (the staged copy's 0-3 value lead-in)."""
+    rng = np.random.default_rng(k)
+    lens = [k + 1, 8183, 8187, 8188, 8189, 8192, 8193, 12000, 16384]
+    m, n = len(lens) * 4, 20000
+    ks = np.zeros(m, np.int32)
+    ke = np.zeros(m, np.int32)
+    for i, L in enumerate(lens):
+        for off in range(4):
+            s0 = int(rng.integers(0, n - L - 4)) // 4 * 4 + off
+            ks[4 * i + off], ke[4 * i + off] = s0, s0 + L
+    logits = rng.normal(size=(m, n)).astype(np.float32)
+    logits[:, ::17] = np.round(logits[:, ::17], 1)  # some exact ties
+    want = T.topk_rows(logits, *T.prefill_windows(ks, ke, n), k)
+    assert np.array_equal(gpu_mqa_topk(fp8idx, logits, ks, ke, k), want), f"k={k}"
+
+
 @pytest.mark.parametrize("levels", [1, 3, 50, 4000])
 def test_mqa_topk_ties(fp8idx, levels):
     """Few distinct values: the top radix bin holds more candidates than
