@@ -32,9 +32,11 @@
 //  * Selection: every key above the k-th key T and the first (k - #above)
 //    keys equal to T in position order are kept, so ties resolve to the
 //    lowest positions, and written straight to the output in position
-//    order: with one CTA per row each thread marks a run of consecutive keys
-//    and one packed block scan places the runs; in a cluster an ordered pass
-//    with warp ballots and block-wide prefix sums.
+//    order: with one CTA per row each thread takes a run of consecutive
+//    keys, marks the run's keys above the 24-bit prefix while counting the
+//    third radix level over it (only keys with that prefix are compared with
+//    T afterwards), and one packed block scan places the runs; in a cluster
+//    an ordered pass with warp ballots and block-wide prefix sums.
 // Rows far too few to fill the GPU (the host's rule: at most a quarter of
 // the SM count) with long windows are each split over a thread-block cluster
 // of C CTAs instead (or as many as the caller asks for): every step
@@ -157,17 +159,11 @@ __device__ __forceinline__ void find_bin(const uint32_t* hist, uint32_t need, ui
 // == T in two bit masks in one pass, one packed block scan gives every run
 // its counts before it, and the run's kept positions are written in order.
 // n <= 31 * kT.  Every thread of the block calls it.
+// The writing half of write_kept_runs: this thread's run starts at key e0,
+// bit j of mgt / meq marks its key e0 + j as > T / == T.
 template <class PosOf>
-__device__ __forceinline__ void write_kept_runs(const uint32_t* kb, int n, PosOf pos_of, uint32_t T,
-                                                uint32_t need_eq, int32_t* out_row, uint32_t* scan) {
-  const int m = ((n + kT - 1) / kT) | 1;
-  const int e0 = threadIdx.x * m, e1 = min(n, e0 + m);
-  uint32_t mgt = 0u, meq = 0u;
-  for (int e = e0; e < e1; ++e) {
-    const uint32_t key = kb[e];
-    mgt |= (key > T ? 1u : 0u) << (e - e0);
-    meq |= (key == T ? 1u : 0u) << (e - e0);
-  }
+__device__ __forceinline__ void write_kept_masks(uint32_t mgt, uint32_t meq, int e0, PosOf pos_of, uint32_t need_eq,
+                                                 int32_t* out_row, uint32_t* scan) {
   uint32_t tot;  // both counts in one scan (16:16; fewer than 2^16 keys)
   const uint32_t ex = block_scan((static_cast<uint32_t>(__popc(mgt)) << 16) | static_cast<uint32_t>(__popc(meq)),
                                  scan, &tot);
@@ -182,6 +178,20 @@ __device__ __forceinline__ void write_kept_runs(const uint32_t* kb, int n, PosOf
       ++n_eq;
     }
   }
+}
+
+template <class PosOf>
+__device__ __forceinline__ void write_kept_runs(const uint32_t* kb, int n, PosOf pos_of, uint32_t T,
+                                                uint32_t need_eq, int32_t* out_row, uint32_t* scan) {
+  const int m = ((n + kT - 1) / kT) | 1;
+  const int e0 = threadIdx.x * m, e1 = min(n, e0 + m);
+  uint32_t mgt = 0u, meq = 0u;
+  for (int e = e0; e < e1; ++e) {
+    const uint32_t key = kb[e];
+    mgt |= (key > T ? 1u : 0u) << (e - e0);
+    meq |= (key == T ? 1u : 0u) << (e - e0);
+  }
+  write_kept_masks(mgt, meq, e0, pos_of, need_eq, out_row, scan);
 }
 
 }  // namespace
@@ -488,10 +498,51 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, uint8_t* smem_raw)
         gt0, eq0);
   };
 
-  // Selection of a window (one CTA per row) whose keys sit in shared memory
-  // in position order (write_kept_runs).
-  const auto select_runs = [&](const uint32_t* kb, int n, auto pos_of, uint32_t T, uint32_t above) {
-    write_kept_runs(kb, n, pos_of, T, static_cast<uint32_t>(k) - above, out_row, sh.scan);
+  // One CTA per row, keys kb[0, n) in shared memory in position order:
+  // the exact selection written to the output.  The first two radix levels
+  // as in radix_select (the first already counted when level1_done); the
+  // third is counted over each thread's run of keys while the run's keys
+  // above the 24-bit prefix are marked, so that only the run's keys with
+  // that prefix are compared with T once it is known, and the runs are
+  // written (write_kept_masks) without a further pass.
+  const auto exact_runs = [&](const uint32_t* kb, int n, auto pos_of, bool level1_done) {
+    if (!level1_done) {
+      zero_level(kTopkBins);
+      smem_hist_at(kb, n, [](uint32_t) { return true; }, [](uint32_t key) { return key >> 20; });
+    }
+    __syncthreads();
+    find_bin<kTopkBins>(sh.hist, static_cast<uint32_t>(k), sh.scan, sh.misc);
+    const uint32_t b0 = sh.misc[0], a0 = sh.misc[1];
+    zero_level(kTopkBins);
+    smem_hist_at(kb, n, [&](uint32_t key) { return (key >> 20) == b0; },
+                 [](uint32_t key) { return (key >> 8) & 0xFFFu; });
+    __syncthreads();
+    find_bin<kTopkBins>(sh.hist, static_cast<uint32_t>(k) - a0, sh.scan, sh.misc);
+    const uint32_t pre24 = (b0 << 12) | sh.misc[0], a1c = a0 + sh.misc[1];
+    zero_level(256);
+    const int m = ((n + kT - 1) / kT) | 1;  // odd: the lanes of a warp read different banks
+    const int e0 = tid * m, e1 = min(n, e0 + m);
+    uint32_t mgt = 0u, mcand = 0u;
+    for (int e = e0; e < e1; ++e) {
+      const uint32_t key = kb[e], pre = key >> 8;
+      mgt |= (pre > pre24 ? 1u : 0u) << (e - e0);
+      if (pre == pre24) {
+        mcand |= 1u << (e - e0);
+        atomicAdd(sh.hist + (key & 0xFFu), 1u);
+      }
+    }
+    __syncthreads();
+    find_bin<256>(sh.hist, static_cast<uint32_t>(k) - a1c, sh.scan, sh.misc);
+    const uint32_t Tk = (pre24 << 8) | sh.misc[0];
+    const uint32_t above_k = a1c + sh.misc[1];
+    uint32_t meq = 0u;
+    for (uint32_t c = mcand; c != 0u; c &= c - 1u) {
+      const int j = __ffs(c) - 1;
+      const uint32_t key = kb[e0 + j];
+      mgt |= (key > Tk ? 1u : 0u) << j;
+      meq |= (key == Tk ? 1u : 0u) << j;
+    }
+    write_kept_masks(mgt, meq, e0, pos_of, static_cast<uint32_t>(k) - above_k, out_row, sh.scan);
   };
 
   uint32_t T = 0, above = 0;
@@ -538,11 +589,11 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, uint8_t* smem_raw)
         }
       }
     }
-    radix_select([&](auto sel, auto bin) { smem_hist_at(kbase, Ls, sel, bin); }, static_cast<uint32_t>(k), &T,
-                 &above, 3, true);
     if constexpr (!kCluster) {
-      select_runs(kbase, Ls32, [&](int e) { return slo32 + e; }, T, above);
+      exact_runs(kbase, Ls32, [&](int e) { return slo32 + e; }, true);
     } else {
+      radix_select([&](auto sel, auto bin) { smem_hist_at(kbase, Ls, sel, bin); }, static_cast<uint32_t>(k), &T,
+                   &above, 3, true);
       select(Ls, [&](int e, uint32_t& key, int32_t& pos) {
         key = kbase[e];
         pos = slo32 + e;
@@ -753,11 +804,12 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, uint8_t* smem_raw)
   exchange2(n_c, 0u, cnt, unused);
   if (cnt.all >= static_cast<uint32_t>(k) && cnt.max <= static_cast<uint32_t>(p.cap)) {
     // Every key >= the k-th largest is a candidate, in position order.
-    radix_select([&](auto sel, auto bin) { smem_hist(n_c, sel, bin); }, static_cast<uint32_t>(k), &T, &above);
-    if constexpr (!kCluster)
-      select_runs(sh.cand_key, static_cast<int>(n_c), [&](int e) { return sh.cand_pos[e]; }, T, above);
-    else
+    if constexpr (!kCluster) {
+      exact_runs(sh.cand_key, static_cast<int>(n_c), [&](int e) { return sh.cand_pos[e]; }, false);
+    } else {
+      radix_select([&](auto sel, auto bin) { smem_hist(n_c, sel, bin); }, static_cast<uint32_t>(k), &T, &above);
       select(n_c, smem_get, T, above);
+    }
   } else {
     radix_select(window_hist, static_cast<uint32_t>(k), &T, &above);
     select(Ls, global_get, T, above);
