@@ -33,10 +33,11 @@
 //    keys equal to T in position order are kept, so ties resolve to the
 //    lowest positions, and written straight to the output in position
 //    order: with one CTA per row each thread takes a run of consecutive
-//    keys, marks the run's keys above the 24-bit prefix while counting the
-//    third radix level over it (only keys with that prefix are compared with
-//    T afterwards), and one packed block scan places the runs; in a cluster
-//    an ordered pass with warp ballots and block-wide prefix sums.
+//    keys, marks the run's keys above the first level's bin while counting
+//    the second level over it (only the bin's keys are visited by the third
+//    level and compared with T afterwards), and one packed block scan places
+//    the runs; in a cluster an ordered pass with warp ballots and block-wide
+//    prefix sums.
 // Rows far too few to fill the GPU (the host's rule: at most a quarter of
 // the SM count) with long windows are each split over a thread-block cluster
 // of C CTAs instead (or as many as the caller asks for): every step
@@ -499,12 +500,12 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, uint8_t* smem_raw)
   };
 
   // One CTA per row, keys kb[0, n) in shared memory in position order:
-  // the exact selection written to the output.  The first two radix levels
-  // as in radix_select (the first already counted when level1_done); the
-  // third is counted over each thread's run of keys while the run's keys
-  // above the 24-bit prefix are marked, so that only the run's keys with
-  // that prefix are compared with T once it is known, and the runs are
-  // written (write_kept_masks) without a further pass.
+  // the exact selection written to the output.  The first radix level as in
+  // radix_select (already counted when level1_done); the second is counted
+  // over each thread's run of keys while the run's keys above the first
+  // level's bin are marked as kept and the bin's keys as open; the third
+  // level and the final comparison with T visit only the open keys, and the
+  // runs are written (write_kept_masks) without a further pass.
   const auto exact_runs = [&](const uint32_t* kb, int n, auto pos_of, bool level1_done) {
     if (!level1_done) {
       zero_level(kTopkBins);
@@ -513,21 +514,32 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, uint8_t* smem_raw)
     __syncthreads();
     find_bin<kTopkBins>(sh.hist, static_cast<uint32_t>(k), sh.scan, sh.misc);
     const uint32_t b0 = sh.misc[0], a0 = sh.misc[1];
+    const int m = ((n + kT - 1) / kT) | 1;  // odd: the lanes of a warp read different banks
+    const int e0 = tid * m, e1 = min(n, e0 + m);
+    // second level over the run: keys above the first level's bin are kept
+    // whatever T is; the bin's own keys are marked for the later levels
     zero_level(kTopkBins);
-    smem_hist_at(kb, n, [&](uint32_t key) { return (key >> 20) == b0; },
-                 [](uint32_t key) { return (key >> 8) & 0xFFFu; });
+    uint32_t mgt = 0u, mbin = 0u;
+    for (int e = e0; e < e1; ++e) {
+      const uint32_t key = kb[e], pre = key >> 20;
+      mgt |= (pre > b0 ? 1u : 0u) << (e - e0);
+      if (pre == b0) {
+        mbin |= 1u << (e - e0);
+        atomicAdd(sh.hist + ((key >> 8) & 0xFFFu), 1u);
+      }
+    }
     __syncthreads();
     find_bin<kTopkBins>(sh.hist, static_cast<uint32_t>(k) - a0, sh.scan, sh.misc);
     const uint32_t pre24 = (b0 << 12) | sh.misc[0], a1c = a0 + sh.misc[1];
+    // third level over the marked keys only
     zero_level(256);
-    const int m = ((n + kT - 1) / kT) | 1;  // odd: the lanes of a warp read different banks
-    const int e0 = tid * m, e1 = min(n, e0 + m);
-    uint32_t mgt = 0u, mcand = 0u;
-    for (int e = e0; e < e1; ++e) {
-      const uint32_t key = kb[e], pre = key >> 8;
-      mgt |= (pre > pre24 ? 1u : 0u) << (e - e0);
+    uint32_t mcand = 0u;
+    for (uint32_t c = mbin; c != 0u; c &= c - 1u) {
+      const int j = __ffs(c) - 1;
+      const uint32_t key = kb[e0 + j], pre = key >> 8;
+      mgt |= (pre > pre24 ? 1u : 0u) << j;
       if (pre == pre24) {
-        mcand |= 1u << (e - e0);
+        mcand |= 1u << j;
         atomicAdd(sh.hist + (key & 0xFFu), 1u);
       }
     }
