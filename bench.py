@@ -6,10 +6,12 @@ default workload is the MTP-verify decode batch (batch 16, next_n 6, 32 heads,
 131072-token contexts, max_model_len 1048576, KV block size 64) -- the shape
 the indexer pages quote their decode figure on.  Other workloads:
 --workload {decode_b1, decode_ragged, decode_mtp_verify, decode_mtp_verify_n1,
-prefill_4x1024, decode_blk1, prefill_paged_4x1024 (the prefill shape with K read
-from a paged cache, block 64), prefill_2048x65536, prefill_1024x131072 (the
-prefill page's other real chunk shapes)}, and the top-k consumer of the logits (k = 2048)
-on two of those shapes: --workload {topk_decode_mtp_verify, topk_prefill_4x1024}.
+prefill_4x1024, decode_blk1, prefill_paged_4x1024 and prefill_paged_blk1_4x1024
+(the prefill shape with K read from a paged cache, block 64 or the co-packed
+block-1 cache), prefill_2048x65536, prefill_1024x131072 (the prefill page's
+other real chunk shapes)}, the top-k consumer of the logits (k = 2048) on two
+of those shapes: --workload {topk_decode_mtp_verify, topk_prefill_4x1024}, and
+the fused decode logits + top-k: --workload fused_topk_decode_mtp_verify.
 
 Prints ONE JSON line (rank 0):
   value      = us per call (all ranks' calls / max-over-ranks device time),
@@ -61,10 +63,11 @@ WORKLOADS = {
     "prefill_4x1024": (3, None),
     "decode_blk1": (4, None),
     "prefill_paged_4x1024": (3, None),  # config 3 with K in a paged cache (block 64), gathered in the kernel
+    "prefill_paged_blk1_4x1024": (3, None),  # the same with the co-packed block-size-1 cache
     "prefill_2048x65536": (5, None),
     "prefill_1024x131072": (6, None),
 }
-PAGED_PREFILL = {"prefill_paged_4x1024"}
+PAGED_PREFILL = {"prefill_paged_4x1024": 64, "prefill_paged_blk1_4x1024": 1}  # workload -> cache block size
 # top-k consumer workloads: (config index, k); the logits are the library's
 # own output for that configuration, produced before the timed region
 TOPK_WORKLOADS = {
@@ -266,8 +269,9 @@ def make_case(workload):
         c = workloads.CONFIGS[idx]
         lens = [c["n"] // c["requests"]] * c["requests"]
         rows = [c["m"] // c["requests"]] * c["requests"]
-        return idx, workloads.paged_prefill_case(lens, rows, c["heads"], block_size=64, seed=1000 + idx,
-                                                 name=c["desc"] + ", K paged (block 64)")
+        blk = PAGED_PREFILL[workload]
+        return idx, workloads.paged_prefill_case(lens, rows, c["heads"], block_size=blk, seed=1000 + idx,
+                                                 name=c["desc"] + f", K paged (block {blk})")
     return idx, workloads.make_config(idx, next_n=next_n)
 
 
