@@ -336,6 +336,21 @@ def cpu_baseline(case, kind, units, budget_s=12.0, seed=0):
             "sample": f"{n} random in-window logits of {units} ({t:.1f} s), scaled to the whole workload"}
 
 
+def run_conditions(workload, world, nbytes=None):
+    """The config keys that say how a workload's calls are timed (the same in
+    both arms, so that their configs compare equal)."""
+    if workload in TOPK_WORKLOADS:
+        l2 = "flushed before every call (512 MB written, then read back)"
+    elif workload in FUSED_WORKLOADS:
+        l2 = f"inputs larger than L2: back-to-back calls (graphs of {GRAPH_CALLS} calls), one event pair around the timed region"
+    else:
+        input_bytes = int(nbytes["total"] - nbytes["out"])
+        l2 = (f"inputs ({input_bytes / 1e6:.0f} MB per call) larger than L2: back-to-back calls "
+              f"(graphs of {GRAPH_CALLS} calls), one event pair around the timed region"
+              if input_bytes > L2_BYTES else "flushed before every call (512 MB written, then read back)")
+    return {"l2": l2, "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args, rank, world):
     import torch
@@ -546,11 +561,7 @@ def run_ours(args, rank, world):
         "metric": METRIC, "value": round(us_per_call, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(mean_ms, 6), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32", "data": "synthetic",
-        "config": {"workload": args.workload, "desc": case.name,
-                   "l2": (f"inputs ({input_bytes / 1e6:.0f} MB per call) larger than L2: back-to-back calls "
-                          f"(graphs of {GRAPH_CALLS} calls), one event pair around the timed region"
-                          if back_to_back else "flushed before every call (512 MB written, then read back)"),
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": {"workload": args.workload, "desc": case.name, **run_conditions(args.workload, world, nbytes)},
         "median_us": round(median_us, 3),
         "l2_flushed_median_us": round(flushed_us, 3) if flushed_us is not None else round(median_us, 3),
         "essential_bytes": nbytes, "fp8_flops": flops,
@@ -712,8 +723,7 @@ def run_topk(args, rank, world):
         "warmup": args.warmup, "ms_per_step": round(mean_ms, 6), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32 -> i32", "data": "synthetic (logits of the library's kernel)",
         "config": {"workload": args.workload, "desc": f"top-{k} per row of: {case.name}",
-                   "l2": "flushed before every call (512 MB written, then read back)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   **run_conditions(args.workload, world)},
         "median_us": round(median_us, 3),
         "essential_bytes": nbytes,
         "essential_gbs": round(achieved_gbs, 1),
@@ -827,9 +837,7 @@ def run_fused(args, rank, world):
         "warmup": args.warmup, "ms_per_step": round(mean_ms, 6), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 -> i32", "data": "synthetic",
         "config": {"workload": args.workload, "desc": f"top-{k} per row of the logits of: {case.name}",
-                   "l2": (f"inputs larger than L2: back-to-back calls (graphs of {GRAPH_CALLS} calls), one event "
-                          "pair around the timed region"),
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   **run_conditions(args.workload, world)},
         "essential_bytes": nbytes,
         "essential_gbs": round(achieved_gbs, 1),
         "roofline_fraction": round(achieved_gbs / hbm_peak, 4),
@@ -870,7 +878,8 @@ def run_reference_topk(args):
         "impl": "reference", "metric": TOPK_METRIC, "value": round(v, 1), "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v / 1e3, 3), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32 -> i32", "data": "synthetic",
-        "config": {"workload": args.workload, "desc": f"top-{k} per row of: {case.name}"},
+        "config": {"workload": args.workload, "desc": f"top-{k} per row of: {case.name}",
+                   **run_conditions(args.workload, int(os.environ.get("WORLD_SIZE", "1")))},
         "cpu_baseline": {"value": round(v, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": "8 random rows per step, scaled to all rows"},
         "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -894,12 +903,14 @@ def run_reference(args):
         v = line["value"] + topk_line["value"]
         line.update({"metric": FUSED_METRIC, "value": round(v, 1), "ms_per_step": round(v / 1e3, 3),
                      "config": {"workload": args.workload, "desc": f"top-{k} per row of the logits of: "
-                                + line["config"]["desc"]}})
+                                + line["config"]["desc"],
+                                **run_conditions(args.workload, int(os.environ.get("WORLD_SIZE", "1")))}})
         line["cpu_baseline"]["value"] = round(v, 1)
         line["cpu_baseline"]["sample"] += "; plus the numpy top-k on 8 random rows per step, scaled"
         line["e2e"]["value"] = round(v, 1)
         return line
     idx, case = make_case(args.workload)
+    nbytes, _, _ = case_bytes_flops(idx, case)
     case = contiguous_view(case)
     kind = workloads.CONFIGS[idx]["kind"]
     _, _, units = case_bytes_flops(idx, case)
@@ -920,7 +931,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v / 1e3, 3), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "desc": case.name},
+        "config": {"workload": args.workload, "desc": case.name,
+                   **run_conditions(args.workload, int(os.environ.get("WORLD_SIZE", "1")), nbytes)},
         "cpu_baseline": {"value": round(v, 1), "unit": UNIT, "cores": o.max_threads(), "kind": "oracle",
                          "sample": f"{n_elems} random in-window logits per step of {units}, scaled"},
         "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
