@@ -19,8 +19,10 @@
 //    bulk copy straight into the key array, converted to keys in place while
 //    the first radix level is counted, and selected there (positions
 //    implicit).  A longer one is sampled with a stride S
-//    (at most cap samples); the sample's (2k/S + 32)-th largest key is a
-//    lower threshold, and the values above it (about 2k + 32S of them) are
+//    (at most cap samples); the sample's (k/S + 5 sqrt(k/S) + 16)-th
+//    largest key is a lower threshold (about six standard deviations of the
+//    sampled rank above k/S), and the values above it (about that rank
+//    times S: 3.2K for k = 2048 at S = 16) are
 //    compacted into shared memory, in position order, for the exact select:
 //    in one pass every warp appends the candidates of its own segment of the
 //    window, in order, to its own share of the candidate arrays (no block
@@ -616,9 +618,11 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, uint8_t* smem_raw)
 
   // Long windows.  A stride sample of at most cap values (stride S over
   // the whole window, each CTA loading the samples in its slice) estimates a
-  // lower threshold t_low: the (2k/S + 32)-th largest sample key (rounded
-  // down to its 24-bit bin), so about 2k + 32S window values lie above it
-  // (many standard deviations from both k and cap for the strides used).
+  // lower threshold t_low: the (k/S + 5 sqrt(k/S) + 16)-th largest sample
+  // key (rounded down to its 24-bit bin).  About k/S samples lie above the
+  // true k-th value, give or take sqrt(k/S), so the rank sits about six of
+  // those deviations above it, and about rank * S window values lie above
+  // t_low (3.2K for k = 2048 at S = 16, 2.6K at S = 4: well inside cap).
   // The values >= t_low are then compacted into shared memory; if fewer than
   // k pass in the cluster, or more than cap in one CTA, the exact radix
   // select runs over the window instead.
@@ -646,7 +650,10 @@ __device__ __forceinline__ void topk_row(const TopkParams& p, uint8_t* smem_raw)
   }
   __syncthreads();
   {
-    const int64_t want = 2 * static_cast<int64_t>(k) / S + 32;
+    // the sample's count above the true k-th value is about k/S with a
+    // standard deviation of about sqrt(k/S): keep about six of them as margin
+    const float kS = static_cast<float>(k) / static_cast<float>(S);
+    const int64_t want = static_cast<int64_t>(kS + 5.0f * sqrtf(kS)) + 16;
     const uint32_t rank = static_cast<uint32_t>(want < ns ? want : ns);
     radix_select([&](auto sel, auto bin) { smem_hist(ns_c, sel, bin); }, rank, &T, &above, 2);
   }
