@@ -406,6 +406,20 @@ const char* fp8idx_last_error(void);
  * (it copies the word back), so it does not belong inside a captured graph. */
 fp8idx_status fp8idx_device_status(int32_t clear);
 
+/* The device address of page-locked host memory, so that a host buffer can
+ * be the output of fp8_paged_mqa_logits or of the top-k calls (whose kernels
+ * write their results with plain stores): the results then go straight into
+ * host memory while the kernel runs (on Grace-Blackwell over NVLink-C2C),
+ * with no separate device-to-host copy.  Inputs, and the prefill output
+ * (written partly by TMA stores), stay in device memory.
+ * host_ptr: an address inside an allocation made by cudaHostAlloc /
+ * cudaMallocHost or registered with cudaHostRegister.  FP8IDX_OK with
+ * *device_ptr set; FP8IDX_ERR_INVALID if an argument is null or host_ptr is
+ * not page-locked host memory; FP8IDX_ERR_UNSUPPORTED if the memory is not
+ * mapped into the current device's address space.  Neither synchronises nor
+ * allocates. */
+fp8idx_status fp8idx_host_mapped_pointer(const void* host_ptr, void** device_ptr);
+
 /* Test hook for the watchdog above.  Enqueues one small kernel that waits,
  * through the same bounded wait as every pipeline stage, on a shared-memory
  * barrier that nothing ever arrives on, and gives up after limit_us

@@ -135,6 +135,8 @@ def library():
             lib.fp8idx_last_error.restype = ctypes.c_char_p
             lib.fp8idx_device_status.argtypes = [ctypes.c_int32]
             lib.fp8idx_device_status.restype = ctypes.c_int
+            lib.fp8idx_host_mapped_pointer.argtypes = [V, P(ctypes.c_void_p)]
+            lib.fp8idx_host_mapped_pointer.restype = ctypes.c_int
             lib.fp8idx_version.restype = ctypes.c_int32
             lib.fp8idx_watchdog_selftest.argtypes = [ctypes.c_int32, ctypes.c_void_p]
             lib.fp8idx_watchdog_selftest.restype = ctypes.c_int
@@ -157,9 +159,19 @@ def _check(status: int):
         raise Fp8IdxError(status, msg.decode() if msg else "")
 
 
-def _desc(t) -> bytes:
-    """torch tensor -> packed fp8idx_tensor (no copy of the data; the tensor
-    must outlive the call)."""
+def _host_mapped(t) -> int:
+    """Device address of a pinned host tensor (an output the kernel writes
+    straight into host memory)."""
+    if not t.is_pinned():
+        raise ValueError("a host output must be a pinned (page-locked) tensor")
+    dev = ctypes.c_void_p()
+    _check(library().fp8idx_host_mapped_pointer(ctypes.c_void_p(t.data_ptr()), ctypes.byref(dev)))
+    return dev.value
+
+
+def _pack(t, ptr: int) -> bytes:
+    """Packs tensor t's dtype, shape and strides with data address ptr into
+    fp8idx_tensor bytes."""
     global _dtype_codes
     if _dtype_codes is None:
         import torch
@@ -171,7 +183,18 @@ def _desc(t) -> bytes:
     n = len(shape)
     if n > 4:
         raise ValueError("at most 4 dimensions")
-    return _TENSOR_PACK.pack(t.data_ptr(), dt, n, *shape, *_PAD[n:], *t.stride(), *_PAD[n:])
+    return _TENSOR_PACK.pack(ptr, dt, n, *shape, *_PAD[n:], *t.stride(), *_PAD[n:])
+
+
+def _desc(t, out: bool = False) -> bytes:
+    """torch tensor -> packed fp8idx_tensor (no copy of the data; the tensor
+    must outlive the call).  Inputs are CUDA tensors; an output (out=True) may
+    also be a pinned host tensor, passed by its device mapping."""
+    if t.is_cuda:
+        return _pack(t, t.data_ptr())
+    if not out:
+        raise ValueError("inputs must be CUDA tensors")
+    return _pack(t, _host_mapped(t))
 
 
 def _stream(stream, like):
@@ -188,10 +211,12 @@ def _stream(stream, like):
 
 def fp8_paged_mqa_logits(q_fp8, kv_cache, weights, context_lens, block_tables, max_model_len, out,
                          stream=None, options: Options | None = None):
-    """Decode logits into ``out`` (only the causal windows are written)."""
+    """Decode logits into ``out`` (only the causal windows are written).
+    ``out`` may be a pinned host tensor: the kernel then writes the logits
+    straight into host memory."""
     lib = library()
     args = [_desc(q_fp8), _desc(kv_cache), _desc(weights), _desc(context_lens), _desc(block_tables)]
-    o = _desc(out)
+    o = _desc(out, out=True)
     s = _stream(stream, q_fp8)
     if options is None:
         st = lib.fp8_paged_mqa_logits(*args, int(max_model_len), o, s)
@@ -244,7 +269,7 @@ def fp8_paged_topk(logits, context_lens, next_n, max_model_len, k, indices, stre
     past the window.  ctas_per_row: 0 = heuristic, 1..8 = fixed (the result
     does not depend on it)."""
     lib = library()
-    lg, cl, ix = _desc(logits), _desc(context_lens), _desc(indices)
+    lg, cl, ix = _desc(logits), _desc(context_lens), _desc(indices, out=True)
     oc = Options(num_ctas=int(ctas_per_row))._c()
     _check(lib.fp8_paged_topk_ex(lg, cl, int(next_n), int(max_model_len), int(k), ix, ctypes.byref(oc),
                                  _stream(stream, logits)))
@@ -254,7 +279,7 @@ def fp8_paged_topk(logits, context_lens, next_n, max_model_len, k, indices, stre
 def fp8_mqa_topk(logits, cu_seqlen_ks, cu_seqlen_ke, k, indices, stream=None, ctas_per_row: int = 0):
     """Prefill top-k over the windows [ks, ke) (same rule, order and padding)."""
     lib = library()
-    lg, a, b, ix = _desc(logits), _desc(cu_seqlen_ks), _desc(cu_seqlen_ke), _desc(indices)
+    lg, a, b, ix = _desc(logits), _desc(cu_seqlen_ks), _desc(cu_seqlen_ke), _desc(indices, out=True)
     oc = Options(num_ctas=int(ctas_per_row))._c()
     _check(lib.fp8_mqa_topk_ex(lg, a, b, int(k), ix, ctypes.byref(oc), _stream(stream, logits)))
     return indices
@@ -280,7 +305,7 @@ def fp8_paged_mqa_topk(q_fp8, kv_cache, weights, context_lens, block_tables, max
     base = workspace.data_ptr()
     off = (-base) % 256
     args = [_desc(q_fp8), _desc(kv_cache), _desc(weights), _desc(context_lens), _desc(block_tables)]
-    ix = _desc(indices)
+    ix = _desc(indices, out=True)
     oc = options._c() if options is not None else None
     st = lib.fp8_paged_mqa_topk(*args, int(max_model_len), int(k), ix,
                                 ctypes.c_void_p(base + off), ctypes.c_size_t(workspace.numel() - off),

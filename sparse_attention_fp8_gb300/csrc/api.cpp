@@ -879,6 +879,23 @@ fp8idx_status fp8idx_plan_prefill(int64_t rows, int64_t cols, int32_t heads, int
 
 const char* fp8idx_last_error(void) { return g_last_error.c_str(); }
 
+fp8idx_status fp8idx_host_mapped_pointer(const void* host_ptr, void** device_ptr) {
+  g_last_error.clear();
+  if (host_ptr == nullptr || device_ptr == nullptr) return fail(FP8IDX_ERR_INVALID, "host_mapped_pointer: null argument");
+  cudaPointerAttributes a;
+  std::memset(&a, 0, sizeof(a));
+  const cudaError_t e = cudaPointerGetAttributes(&a, host_ptr);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(FP8IDX_ERR_INVALID, "host_mapped_pointer: %s", cudaGetErrorString(e));
+  }
+  if (a.type != cudaMemoryTypeHost) return fail(FP8IDX_ERR_INVALID, "host_mapped_pointer: not page-locked host memory");
+  if (a.devicePointer == nullptr)
+    return fail(FP8IDX_ERR_UNSUPPORTED, "host_mapped_pointer: the memory is not mapped into the device");
+  *device_ptr = a.devicePointer;
+  return ok();
+}
+
 fp8idx_status fp8idx_device_status(int32_t clear) {
   g_last_error.clear();
   unsigned int a = 0, b = 0, c = 0;

@@ -133,16 +133,30 @@ def test_descriptor_packing():
     stride[4]), unused dimensions zero, strides in elements."""
     import torch
     t = torch.empty((3, 5, 7), dtype=torch.float32)[:, ::2, :]
-    d = _native._Tensor.from_buffer_copy(_native._desc(t))
-    assert d.data == t.data_ptr() and d.dtype == 1 and d.ndim == 3
+    d = _native._Tensor.from_buffer_copy(_native._pack(t, 4096))
+    assert d.data == 4096 and d.dtype == 1 and d.ndim == 3
     assert list(d.shape) == [3, 3, 7, 0] and list(d.stride) == [35, 14, 1, 0]
     u = torch.empty(16, dtype=torch.uint8)
-    d = _native._Tensor.from_buffer_copy(_native._desc(u))
+    d = _native._Tensor.from_buffer_copy(_native._pack(u, u.data_ptr()))
+    assert d.data == u.data_ptr()
     assert d.dtype == 0 and d.ndim == 1 and list(d.shape) == [16, 0, 0, 0] and list(d.stride) == [1, 0, 0, 0]
     with pytest.raises(TypeError):
-        _native._desc(torch.empty(4, dtype=torch.float64))
+        _native._pack(torch.empty(4, dtype=torch.float64), 0)
     with pytest.raises(ValueError):
-        _native._desc(torch.empty((1, 1, 1, 1, 1), dtype=torch.float32))
+        _native._pack(torch.empty((1, 1, 1, 1, 1), dtype=torch.float32), 0)
+    # host tensors: never as inputs; as outputs only pinned (checked before any call)
+    with pytest.raises(ValueError, match="inputs must be CUDA"):
+        _native._desc(torch.empty(4, dtype=torch.float32))
+    with pytest.raises(ValueError, match="pinned"):
+        _native._desc(torch.empty(4, dtype=torch.float32), out=True)
+
+
+def test_host_mapped_pointer_arguments(lib):
+    """The host-mapping query rejects null arguments before any CUDA call."""
+    dev = ctypes.c_void_p()
+    assert lib.fp8idx_host_mapped_pointer(None, ctypes.byref(dev)) == fp8idx.FP8IDX_ERR_INVALID
+    assert lib.fp8idx_host_mapped_pointer(ctypes.c_void_p(4096), None) == fp8idx.FP8IDX_ERR_INVALID
+    assert b"null" in lib.fp8idx_last_error()
 
 
 def test_max_model_len_bound(lib):

@@ -119,6 +119,27 @@ def test_decode_max_batch(fp8idx, oracle_impl, blk):
         assert e.value.status == fp8idx.FP8IDX_ERR_UNSUPPORTED
 
 
+def test_decode_into_pinned_host_memory(fp8idx):
+    """A pinned host tensor as the output: the kernel writes the windows
+    straight into host memory (through its device mapping), bit for bit what
+    it writes into device memory, and leaves the rest untouched."""
+    case = workloads.decode_case(3, 2, 32, max_model_len=700, block_size=64, context_lens=[700, 300, 5], seed=5,
+                                 poison=True, extra_blocks=1)
+    dev = run_decode(fp8idx, case).cpu().numpy()
+    host = torch.full(dev.shape, float("nan"), dtype=torch.float32).pin_memory()
+    d = to_device(case)
+    fp8idx.fp8_paged_mqa_logits(d["q"], d["kv_cache"], d["weights"], d["context_lens"], d["block_tables"],
+                                case.max_model_len, host)
+    torch.cuda.synchronize()
+    assert np.array_equal(host.numpy(), dev, equal_nan=True)
+    with pytest.raises(ValueError, match="pinned"):
+        fp8idx.fp8_paged_mqa_logits(d["q"], d["kv_cache"], d["weights"], d["context_lens"], d["block_tables"],
+                                    case.max_model_len, torch.empty(dev.shape, dtype=torch.float32))
+    with pytest.raises(ValueError, match="inputs must be CUDA"):
+        fp8idx.fp8_paged_mqa_logits(d["q"].cpu(), d["kv_cache"], d["weights"], d["context_lens"], d["block_tables"],
+                                    case.max_model_len, host)
+
+
 def test_decode_config0(fp8idx, oracle_impl):
     case = workloads.make_config(0)
     gpu = run_decode(fp8idx, case).cpu().numpy()

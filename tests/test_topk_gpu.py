@@ -138,6 +138,27 @@ def test_paged_topk_ragged(fp8idx, ctas):
         assert np.array_equal(gpu_paged_topk(fp8idx, logits, ctx, next_n, mml, k, ctas), want), f"k={k}"
 
 
+def test_topk_into_pinned_host_memory(fp8idx):
+    """Pinned host index buffers: the kernels write the indices straight into
+    host memory, the same as into device memory."""
+    rng = np.random.default_rng(12)
+    batch, next_n, mml, k = 5, 2, 20000, 512
+    ctx = np.array([0, 3, 700, 12000, 20000], dtype=np.int32)
+    logits = rng.normal(size=(batch * next_n, mml)).astype(np.float32)
+    want = gpu_paged_topk(fp8idx, logits, ctx, next_n, mml, k)
+    host = torch.full((batch * next_n, k), -7, dtype=torch.int32).pin_memory()
+    fp8idx.fp8_paged_topk(torch.from_numpy(logits).cuda(), torch.from_numpy(ctx).cuda(), next_n, mml, k, host)
+    torch.cuda.synchronize()
+    assert np.array_equal(host.numpy(), want)
+    ks, ke = T.decode_windows(ctx, next_n, mml)
+    want = gpu_mqa_topk(fp8idx, logits, ks.astype(np.int32), ke.astype(np.int32), k)
+    host.fill_(-7)
+    fp8idx.fp8_mqa_topk(torch.from_numpy(logits).cuda(), torch.from_numpy(ks.astype(np.int32)).cuda(),
+                        torch.from_numpy(ke.astype(np.int32)).cuda(), k, host)
+    torch.cuda.synchronize()
+    assert np.array_equal(host.numpy(), want)
+
+
 def test_topk_more_rows_than_sms(fp8idx):
     """More rows than SMs (several waves of CTAs, two per SM): short, long,
     tied and empty windows."""
