@@ -513,13 +513,14 @@ __global__ void __launch_bounds__(paged_threads(GATHER), 1)
                   // 128-byte line: no partial-line writes).  A warp's 32
                   // tokens are one aligned 32-bit word of positions that no
                   // other warp covers, so lane 0 stores the warp's ballot as
-                  // that word (every word whose first position is in the
-                  // window is written).
+                  // that word when it is not zero (the threshold pass
+                  // cleared the bitmap over the window of every row it
+                  // reads).
                   const float val = v * scale;
                   const bool cand = in && val >= thr_r[n];
                   const uint32_t m = __ballot_sync(0xffffffffu, cand);
                   if (m != 0u && in) __stcs(out_col + static_cast<int64_t>(n) * p.out_stride, val);
-                  if (lane == 0 && in)
+                  if (lane == 0 && m != 0u)
                     p.cand_bits[(static_cast<int64_t>(cur.b) * next_n + n) * p.bits_stride + (pos >> 5)] = m;
                 }
               });

@@ -961,6 +961,14 @@ __global__ void __launch_bounds__(kTopkThreads, 1) fused_threshold_kernel(const 
     if (tid == 0) p.thr[r] = -INFINITY;
     return;
   }
+  {
+    // The row's candidate bitmap, cleared for the filter pass, which then
+    // stores only the words that hold a candidate (the row's words start
+    // 16-byte aligned; positions are below 2^31).
+    const int nv = static_cast<int>((W + 127) / 128);
+    uint4* b4 = reinterpret_cast<uint4*>(p.cand + r * p.tw);
+    for (int v = tid; v < nv; v += kT) b4[v] = make_uint4(0u, 0u, 0u, 0u);
+  }
   const int64_t I = p.item_tokens, SI = static_cast<int64_t>(kFusedSampleStride) * I;
   const int lgI = I == 256 ? 8 : 7;  // items are 128 or 256 tokens
   int64_t J = (W + SI - 1) / SI;  // sampled items starting inside the window
