@@ -2,13 +2,15 @@
 claim on the CPU (numpy; no kernel code involved).
 
 A window of L values longer than the candidate capacity C is sampled with
-stride S = ceil(L / C); the (2k/S + 32)-th largest sample key, rounded down
+stride S = ceil(L / C); the (k/S + 5 sqrt(k/S) + 16)-th largest sample key
+(the rank computed in f32 and truncated, as the kernel does), rounded down
 to its 24-bit radix bin, is a lower threshold; the values at or above it are
-the candidates, and the fast path needs k <= #candidates <= C.  About
-2k + 32S values should pass, many standard deviations from both bounds for
-independent values -- this test measures that over the shapes the kernel
-meets (decode windows of 131072, prefill windows up to 65536, k 512 and
-2048) and a few value distributions.
+the candidates, and the fast path needs k <= #candidates <= C.  The sample
+holds about k/S values above the true k-th, give or take sqrt(k/S), so
+about rank * S values should pass, several standard deviations from both
+bounds for independent values -- this test measures that over the shapes the
+kernel meets (decode windows of 131072, prefill windows up to 65536, k 512
+and 2048) and a few value distributions.
 """
 import numpy as np
 import pytest
@@ -26,9 +28,10 @@ def candidates(vals, k):
     S = -(-L // CAP)
     keys = order_keys(vals)
     sample = keys[::S]
-    rank = min(2 * k // S + 32, sample.size)
+    kS = np.float32(k) / np.float32(S)
+    rank = min(int(kS + np.float32(5.0) * np.sqrt(kS)) + 16, sample.size)
     t = np.sort(sample)[::-1][rank - 1] & np.uint32(0xFFFFFF00)
-    return int(np.count_nonzero(keys >= t)), 2 * k + 32 * S
+    return int(np.count_nonzero(keys >= t)), rank * S
 
 
 DISTS = {
@@ -50,8 +53,25 @@ def test_candidate_count_within_bounds(dist, L, k):
     counts = np.array(counts)
     assert counts.min() >= k, (dist, L, k, counts.min())
     assert counts.max() <= CAP, (dist, L, k, counts.max())
-    # the spread leaves room on both sides: at least 4 standard deviations
+    # the spread leaves room on both sides: at least 3 standard deviations
+    # of the observed candidate counts (which also carry the spread of the
+    # threshold sample's own gaps)
     sd = max(counts.std(), 1.0)
-    assert counts.mean() - 4 * sd >= k and counts.mean() + 4 * sd <= CAP, (dist, L, k, counts.mean(), sd)
-    # and the mean lands near the design's 2k + 32S
+    assert counts.mean() - 3 * sd >= k and counts.mean() + 4 * sd <= CAP, (dist, L, k, counts.mean(), sd)
+    # and the mean lands near the design's rank * S
     assert 0.6 * expect <= counts.mean() <= 1.6 * expect, (dist, L, k, counts.mean(), expect)
+
+
+@pytest.mark.parametrize("L,k", [(131072, 2048), (131072, 512), (65536, 2048), (16384, 2048), (8200, 2048),
+                                 (1 << 20, 2048), (1 << 20, 512)])
+def test_fallback_probability(L, k):
+    """The fast path misses only if the stride sample holds at least `rank`
+    of the window's k largest values: for independent values that count is
+    Binomial(k, 1/S), and the rank leaves it below 1e-6 (the exact fallback
+    keeps the result right either way)."""
+    from scipy.stats import binom
+    S = -(-L // CAP)
+    kS = np.float32(k) / np.float32(S)
+    rank = int(kS + np.float32(5.0) * np.sqrt(kS)) + 16
+    assert binom.sf(rank - 1, k, 1.0 / S) < 1e-6, (L, k, S, rank)
+    assert rank * S <= CAP, (L, k, S, rank)  # the expected candidates fit the shared-memory capacity
