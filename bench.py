@@ -24,8 +24,12 @@ Prints ONE JSON line (rank 0):
   roofline   = the dominant kernel's algorithmic bytes / its mean duration
                against the measured HBM copy bandwidth.
   e2e        = the same call driven from pinned host memory: per-step inputs
-               copied host->device and the written logits copied back, all
-               inside the timed region.
+               copied host->device and the results back on the host, all
+               inside the timed region.  Decode writes its logits straight
+               into a pinned host output (e2e.copy_back: the same with a
+               device output and the written columns copied back); prefill
+               copies its logits back; the top-k workloads copy the indices
+               back.
   cpu_baseline = the CPU oracle (fp64, OpenMP) on a bounded random sample of
                the same workload's logits, scaled to the whole workload.
 --impl reference times that oracle alone as the reference arm.
