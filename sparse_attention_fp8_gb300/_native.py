@@ -194,6 +194,8 @@ def _desc(t, out: bool = False) -> bytes:
         return _pack(t, t.data_ptr())
     if not out:
         raise ValueError("inputs must be CUDA tensors")
+    if t.numel() == 0:  # nothing is written: no address needed
+        return _pack(t, 0)
     return _pack(t, _host_mapped(t))
 
 

@@ -149,6 +149,8 @@ def test_descriptor_packing():
         _native._desc(torch.empty(4, dtype=torch.float32))
     with pytest.raises(ValueError, match="pinned"):
         _native._desc(torch.empty(4, dtype=torch.float32), out=True)
+    d = _native._Tensor.from_buffer_copy(_native._desc(torch.empty((0, 4), dtype=torch.int32), out=True))
+    assert d.data is None and list(d.shape) == [0, 4, 0, 0]  # an empty host output needs no mapping
 
 
 def test_host_mapped_pointer_arguments(lib):
